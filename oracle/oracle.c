@@ -1,0 +1,435 @@
+/*
+ * oracle.c -- plain, slow, unsharded CPU reference for the tensor-parallel
+ * MLP block and the vocabulary-parallel cross-entropy.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the library's product path links,
+ * loads or calls this file; only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg do. It shares no code, header or constant with
+ * the CUDA library.
+ *
+ * Arithmetic: every input arrives as float64 (the callers widen the exact
+ * bf16 or fp32 values that the GPU also reads); every sum, product, exp, log
+ * and erf is done in double precision, in the plain order of the definition.
+ * The matrix products are written out as loops; the only parallelism is an
+ * OpenMP split over independent output rows, which does not change any sum.
+ *
+ * Layout: row-major everywhere. X, Z, dX, dZ, H, dH are [T, h]; A, dA are
+ * [h, f]; B, dB are [f, h]; U, Y are [T, f]; E, dE are [v_pad, h].
+ *
+ * Sources (page title, then section):
+ *   [MF]  "Tensor Parallelism and Pipeline Parallelism: Mathematical
+ *         Foundations of Megatron-LM 1D Slicing ..." (llms.blog):
+ *         "Column-Parallel Linear Layer", "Row-Parallel Linear Layer",
+ *         "Conjugate Communication Operators".
+ *   [LIT] "LIT-022: Megatron-LM: Training Multi-Billion Parameter Language
+ *         Models Using Model Parallelism" (anthology digest): "Key takeaways".
+ *   [LEC] "Cutting a Model Into Pieces" (lecture 3): "Megatron-LM: cutting
+ *         inside the layer".
+ *   [DEP] "Megatron-LM, in depth" (aicassindra): "Failure modes".
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   - GeLU is the exact erf form x * Phi(x); its derivative Phi(x) + x phi(x).
+ *   - The row-parallel bias bB is added once, after the shard sum.
+ *   - The backward is the chain rule of the forward; f* sums the per-shard
+ *     input gradients, g* hands the same dZ to every shard.
+ *   - Cross-entropy is the textbook softmax cross-entropy over the real ids
+ *     [0, v_valid); padded ids take no part in the max or the sum of exps
+ *     and get a zero gradient.
+ *   - The gradient returned is that of grad_scale * sum_t loss_t.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef M_PI
+#define M_PI 3.14159265358979323846
+#endif
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* GeLU(x) = x * Phi(x), Phi the standard normal CDF written with erf.
+ * [LIT] key takeaways (GeLU between the two GEMMs); [LEC] Y = GeLU(XA). */
+double oracle_gelu(double x)
+{
+    return x * 0.5 * (1.0 + erf(x / sqrt(2.0)));
+}
+
+/* d/dx [x Phi(x)] = Phi(x) + x phi(x), phi the standard normal density. */
+double oracle_gelu_grad(double x)
+{
+    double Phi = 0.5 * (1.0 + erf(x / sqrt(2.0)));
+    double phi = exp(-0.5 * x * x) / sqrt(2.0 * M_PI);
+    return Phi + x * phi;
+}
+
+/* ------------------------------------------------------------------------ */
+/* MLP forward, unsharded: U = X A + bA, Y = GeLU(U), Z = Y B + bB.
+ * [LEC] Y = GeLU(X A), Z = Y B. bA, bB may be NULL (zero). U, Y, Z may be
+ * NULL when the caller does not want them. */
+void oracle_mlp_forward(int64_t T, int64_t h, int64_t f,
+                        const double *X, const double *A, const double *bA,
+                        const double *B, const double *bB,
+                        double *U, double *Y, double *Z)
+{
+    int64_t t;
+#pragma omp parallel for schedule(static)
+    for (t = 0; t < T; t++) {
+        double *u = (double *)malloc(sizeof(double) * (size_t)f);
+        double *y = (double *)malloc(sizeof(double) * (size_t)f);
+        for (int64_t j = 0; j < f; j++)
+            u[j] = bA ? bA[j] : 0.0;
+        for (int64_t k = 0; k < h; k++) {
+            double x = X[t * h + k];
+            for (int64_t j = 0; j < f; j++)
+                u[j] += x * A[k * f + j];
+        }
+        for (int64_t j = 0; j < f; j++)
+            y[j] = oracle_gelu(u[j]);
+        if (Z) {
+            for (int64_t n = 0; n < h; n++)
+                Z[t * h + n] = bB ? bB[n] : 0.0;
+            for (int64_t j = 0; j < f; j++) {
+                double yj = y[j];
+                for (int64_t n = 0; n < h; n++)
+                    Z[t * h + n] += yj * B[j * h + n];
+            }
+        }
+        if (U) memcpy(U + t * f, u, sizeof(double) * (size_t)f);
+        if (Y) memcpy(Y + t * f, y, sizeof(double) * (size_t)f);
+        free(u);
+        free(y);
+    }
+}
+
+/* MLP backward, unsharded, by the chain rule of oracle_mlp_forward for the
+ * upstream gradient dZ:
+ *   dB = Y^T dZ,  dbB = sum_t dZ,  dY = dZ B^T,  dU = dY (.) GeLU'(U),
+ *   dA = X^T dU,  dbA = sum_t dU,  dX = dU A^T.
+ * The oracle recomputes U and Y itself from X, A, bA. Any output may be NULL.
+ */
+void oracle_mlp_backward(int64_t T, int64_t h, int64_t f,
+                         const double *X, const double *A, const double *bA,
+                         const double *B, const double *dZ,
+                         double *dX, double *dA, double *dbA,
+                         double *dB, double *dbB)
+{
+    double *U = (double *)malloc(sizeof(double) * (size_t)(T * f));
+    double *Y = (double *)malloc(sizeof(double) * (size_t)(T * f));
+    double *dU = (double *)malloc(sizeof(double) * (size_t)(T * f));
+    oracle_mlp_forward(T, h, f, X, A, bA, B, NULL, U, Y, NULL);
+
+    int64_t t, j, k, n;
+    /* dY = dZ B^T, then dU = dY (.) GeLU'(U) */
+#pragma omp parallel for schedule(static)
+    for (t = 0; t < T; t++) {
+        for (int64_t jj = 0; jj < f; jj++) {
+            double acc = 0.0;
+            for (int64_t nn = 0; nn < h; nn++)
+                acc += dZ[t * h + nn] * B[jj * h + nn];
+            dU[t * f + jj] = acc * oracle_gelu_grad(U[t * f + jj]);
+        }
+    }
+    if (dX) {
+        /* dX = dU A^T */
+#pragma omp parallel for schedule(static)
+        for (t = 0; t < T; t++) {
+            for (int64_t kk = 0; kk < h; kk++) {
+                double acc = 0.0;
+                for (int64_t jj = 0; jj < f; jj++)
+                    acc += dU[t * f + jj] * A[kk * f + jj];
+                dX[t * h + kk] = acc;
+            }
+        }
+    }
+    if (dA) {
+        /* dA = X^T dU */
+#pragma omp parallel for schedule(static)
+        for (k = 0; k < h; k++) {
+            for (int64_t jj = 0; jj < f; jj++)
+                dA[k * f + jj] = 0.0;
+            for (int64_t tt = 0; tt < T; tt++) {
+                double x = X[tt * h + k];
+                for (int64_t jj = 0; jj < f; jj++)
+                    dA[k * f + jj] += x * dU[tt * f + jj];
+            }
+        }
+    }
+    if (dB) {
+        /* dB = Y^T dZ */
+#pragma omp parallel for schedule(static)
+        for (j = 0; j < f; j++) {
+            for (int64_t nn = 0; nn < h; nn++)
+                dB[j * h + nn] = 0.0;
+            for (int64_t tt = 0; tt < T; tt++) {
+                double y = Y[tt * f + j];
+                for (int64_t nn = 0; nn < h; nn++)
+                    dB[j * h + nn] += y * dZ[tt * h + nn];
+            }
+        }
+    }
+    if (dbA) {
+        for (j = 0; j < f; j++) {
+            double acc = 0.0;
+            for (t = 0; t < T; t++)
+                acc += dU[t * f + j];
+            dbA[j] = acc;
+        }
+    }
+    if (dbB) {
+        for (n = 0; n < h; n++) {
+            double acc = 0.0;
+            for (t = 0; t < T; t++)
+                acc += dZ[t * h + n];
+            dbB[n] = acc;
+        }
+    }
+    free(U);
+    free(Y);
+    free(dU);
+}
+
+/* Selected columns j of the weight gradients, from the same definitions:
+ * dA[:, j] = X^T dU[:, j], dbA[j] = sum_t dU[t, j], dB[j, :] = Y[:, j]^T dZ,
+ * with U[:, j] = X A[:, j] + bA[j], dU[:, j] = (dZ B[j, :]^T) (.) GeLU'(U[:, j]).
+ * Column j needs only O(T h) work, which makes full-size spot checks cheap.
+ * Outputs: dA_cols [h][ncols], dbA_cols [ncols], dB_rows [ncols][h]. */
+void oracle_mlp_backward_cols(int64_t T, int64_t h, int64_t f,
+                              const double *X, const double *A, const double *bA,
+                              const double *B, const double *dZ,
+                              int64_t ncols, const int64_t *cols,
+                              double *dA_cols, double *dbA_cols, double *dB_rows)
+{
+    int64_t c;
+#pragma omp parallel for schedule(dynamic)
+    for (c = 0; c < ncols; c++) {
+        int64_t j = cols[c];
+        double *u = (double *)malloc(sizeof(double) * (size_t)T);
+        double *du = (double *)malloc(sizeof(double) * (size_t)T);
+        for (int64_t t = 0; t < T; t++) {
+            double acc = bA ? bA[j] : 0.0;
+            for (int64_t k = 0; k < h; k++)
+                acc += X[t * h + k] * A[k * f + j];
+            u[t] = acc;
+            double dy = 0.0;
+            for (int64_t n = 0; n < h; n++)
+                dy += dZ[t * h + n] * B[j * h + n];
+            du[t] = dy * oracle_gelu_grad(acc);
+        }
+        double sb = 0.0;
+        for (int64_t t = 0; t < T; t++)
+            sb += du[t];
+        dbA_cols[c] = sb;
+        for (int64_t k = 0; k < h; k++) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < T; t++)
+                acc += X[t * h + k] * du[t];
+            dA_cols[k * ncols + c] = acc;
+        }
+        for (int64_t n = 0; n < h; n++) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < T; t++)
+                acc += oracle_gelu(u[t]) * dZ[t * h + n];
+            dB_rows[c * h + n] = acc;
+        }
+        free(u);
+        free(du);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* The sharded restatement of the same block, for t shards, written the way
+ * the pages partition it. [MF] "Column-Parallel Linear Layer": A = [A_1 ..
+ * A_t] by columns, Y_i = GeLU(X A_i) per shard with no exchange; [MF]
+ * "Row-Parallel Linear Layer": B = [B_1; ..; B_t] by rows, Z_i = Y_i B_i and
+ * Z = sum_i Z_i (the forward operator g); bias bA split with A's columns, bB
+ * added once after the sum. The backward follows [MF] "Conjugate
+ * Communication Operators": g* passes dZ unchanged to every shard, each shard
+ * forms its own dB_i, dU_i, dA_i and partial dX_i, and f* sums the dX_i.
+ * Used only to pin that the partition reproduces the unsharded block.
+ * Requires f % t == 0. */
+void oracle_mlp_sharded(int64_t T, int64_t h, int64_t f, int t,
+                        const double *X, const double *A, const double *bA,
+                        const double *B, const double *bB, const double *dZ,
+                        double *Z, double *dX, double *dA, double *dB)
+{
+    int64_t fs = f / t;
+    double *Zi = (double *)malloc(sizeof(double) * (size_t)(T * h));
+    double *dXi = (double *)malloc(sizeof(double) * (size_t)(T * h));
+    double *Ai = (double *)malloc(sizeof(double) * (size_t)(h * fs));
+    double *bAi = (double *)malloc(sizeof(double) * (size_t)fs);
+    double *Bi = (double *)malloc(sizeof(double) * (size_t)(fs * h));
+    double *dAi = (double *)malloc(sizeof(double) * (size_t)(h * fs));
+    double *dBi = (double *)malloc(sizeof(double) * (size_t)(fs * h));
+    for (int64_t e = 0; e < T * h; e++) {
+        Z[e] = 0.0;
+        dX[e] = 0.0;
+    }
+    for (int i = 0; i < t; i++) {
+        /* shard i's slices: columns [i fs, (i+1) fs) of A and bA, rows of B */
+        for (int64_t k = 0; k < h; k++)
+            for (int64_t j = 0; j < fs; j++)
+                Ai[k * fs + j] = A[k * f + (int64_t)i * fs + j];
+        for (int64_t j = 0; j < fs; j++)
+            bAi[j] = bA ? bA[(int64_t)i * fs + j] : 0.0;
+        memcpy(Bi, B + (int64_t)i * fs * h, sizeof(double) * (size_t)(fs * h));
+        /* forward of shard i (partial Z_i, no bias), then g: Z += Z_i */
+        oracle_mlp_forward(T, h, fs, X, Ai, bAi, Bi, NULL, NULL, NULL, Zi);
+        for (int64_t e = 0; e < T * h; e++)
+            Z[e] += Zi[e];
+        /* backward of shard i under g* (dZ unchanged), then f*: dX += dX_i */
+        oracle_mlp_backward(T, h, fs, X, Ai, bAi, Bi, dZ, dXi, dAi, NULL, dBi, NULL);
+        for (int64_t e = 0; e < T * h; e++)
+            dX[e] += dXi[e];
+        for (int64_t k = 0; k < h; k++)
+            for (int64_t j = 0; j < fs; j++)
+                dA[k * f + (int64_t)i * fs + j] = dAi[k * fs + j];
+        memcpy(dB + (int64_t)i * fs * h, dBi, sizeof(double) * (size_t)(fs * h));
+    }
+    /* bB enters once, after the sum over shards */
+    for (int64_t tt = 0; tt < T; tt++)
+        for (int64_t n = 0; n < h; n++)
+            Z[tt * h + n] += bB ? bB[n] : 0.0;
+    free(Zi);
+    free(dXi);
+    free(Ai);
+    free(bAi);
+    free(Bi);
+    free(dAi);
+    free(dBi);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Softmax cross-entropy over the logits l = H E^T, unsharded. [LIT] key
+ * takeaways: the logit GEMM is fused with the cross-entropy loss. For token
+ * t over the real ids j < v_valid:
+ *   lse_t  = log sum_j exp(l_tj)        (written with the max subtracted)
+ *   loss_t = lse_t - l_{t, target_t}
+ *   dl_tj  = grad_scale * (exp(l_tj - lse_t) - [j == target_t]),  0 for j >= v_valid
+ *   dH = dl E,  dE = dl^T H  (rows j >= v_valid of dE are zero).
+ * loss, lse: [T]. dH [T, h] and dE [v_pad, h] may be NULL. A target outside
+ * [0, v_valid) makes the loss of that token NaN. */
+void oracle_ce(int64_t T, int64_t h, int64_t v_pad, int64_t v_valid,
+               const double *H, const double *E, const int32_t *targets,
+               double grad_scale, double *loss, double *lse,
+               double *dH, double *dE)
+{
+    double *dl = NULL;
+    if (dE)
+        dl = (double *)malloc(sizeof(double) * (size_t)(T * v_valid));
+    int64_t t;
+#pragma omp parallel for schedule(dynamic)
+    for (t = 0; t < T; t++) {
+        double *l = (double *)malloc(sizeof(double) * (size_t)v_valid);
+        for (int64_t j = 0; j < v_valid; j++) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < h; k++)
+                acc += H[t * h + k] * E[j * h + k];
+            l[j] = acc;
+        }
+        double m = -INFINITY;
+        for (int64_t j = 0; j < v_valid; j++)
+            if (l[j] > m) m = l[j];
+        double S = 0.0;
+        for (int64_t j = 0; j < v_valid; j++)
+            S += exp(l[j] - m);
+        double L = m + log(S);
+        int32_t y = targets[t];
+        int ok = (y >= 0 && (int64_t)y < v_valid);
+        lse[t] = L;
+        loss[t] = ok ? L - l[y] : NAN;
+        if (dH || dE) {
+            for (int64_t j = 0; j < v_valid; j++)
+                l[j] = grad_scale * (exp(l[j] - L) - (j == (int64_t)y ? 1.0 : 0.0));
+            if (dH) {
+                for (int64_t k = 0; k < h; k++)
+                    dH[t * h + k] = 0.0;
+                for (int64_t j = 0; j < v_valid; j++) {
+                    double d = l[j];
+                    for (int64_t k = 0; k < h; k++)
+                        dH[t * h + k] += d * E[j * h + k];
+                }
+            }
+            if (dE)
+                memcpy(dl + t * v_valid, l, sizeof(double) * (size_t)v_valid);
+        }
+        free(l);
+    }
+    if (dE) {
+        int64_t j;
+#pragma omp parallel for schedule(static)
+        for (j = 0; j < v_pad; j++) {
+            for (int64_t k = 0; k < h; k++)
+                dE[j * h + k] = 0.0;
+            if (j >= v_valid) continue;
+            for (int64_t tt = 0; tt < T; tt++) {
+                double d = dl[tt * v_valid + j];
+                for (int64_t k = 0; k < h; k++)
+                    dE[j * h + k] += d * H[tt * h + k];
+            }
+        }
+        free(dl);
+    }
+}
+
+/* The vocabulary-parallel form of the same loss, written the way the digest
+ * describes the fusion ([LIT] key takeaways): E is split by rows into t shards
+ * of v_pad / t ids; shard i computes its own logits and reduces them, per
+ * token, to three numbers -- its max m_i over its real ids, its sum
+ * s_i = sum exp(l - m_i), and the target logit if it owns the target. Only
+ * these per-token numbers are combined:
+ *   m = max_i m_i,  S = sum_i s_i exp(m_i - m),  loss = m + log S - tau.
+ * A shard holding only padded ids has m_i = -inf, s_i = 0 and takes no part.
+ * Outputs: m_shard, s_shard [t][T], tau [T], loss [T]. */
+void oracle_ce_sharded(int64_t T, int64_t h, int64_t v_pad, int64_t v_valid, int t,
+                       const double *H, const double *E, const int32_t *targets,
+                       double *m_shard, double *s_shard, double *tau, double *loss)
+{
+    int64_t vs = v_pad / t;
+    int64_t tok;
+#pragma omp parallel for schedule(dynamic)
+    for (tok = 0; tok < T; tok++) {
+        double *l = (double *)malloc(sizeof(double) * (size_t)vs);
+        int32_t y = targets[tok];
+        tau[tok] = NAN;
+        for (int i = 0; i < t; i++) {
+            int64_t lo = (int64_t)i * vs, hi = lo + vs;
+            if (hi > v_valid) hi = v_valid; /* padded ids are not logits */
+            double m = -INFINITY, s = 0.0;
+            for (int64_t j = lo; j < hi; j++) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < h; k++)
+                    acc += H[tok * h + k] * E[j * h + k];
+                l[j - lo] = acc;
+                if (acc > m) m = acc;
+            }
+            for (int64_t j = lo; j < hi; j++)
+                s += exp(l[j - lo] - m);
+            if ((int64_t)y >= lo && (int64_t)y < hi)
+                tau[tok] = l[y - lo];
+            m_shard[(int64_t)i * T + tok] = m;
+            s_shard[(int64_t)i * T + tok] = s;
+        }
+        double M = -INFINITY;
+        for (int i = 0; i < t; i++)
+            if (m_shard[(int64_t)i * T + tok] > M) M = m_shard[(int64_t)i * T + tok];
+        double S = 0.0;
+        for (int i = 0; i < t; i++) {
+            double si = s_shard[(int64_t)i * T + tok];
+            if (si > 0.0)
+                S += si * exp(m_shard[(int64_t)i * T + tok] - M);
+        }
+        loss[tok] = M + log(S) - tau[tok];
+        free(l);
+    }
+}

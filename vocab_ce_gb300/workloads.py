@@ -1,0 +1,153 @@
+"""Workload table and seeded synthetic inputs.
+
+This module holds the five workloads this library is measured and tested on
+and the seeded generators that draw their inputs. It holds none of the
+method's arithmetic: no GEMM, no GeLU, no softmax. Both the CUDA path (through
+the tests and ``bench.py``) and the CPU oracle (through the tests) consume the
+arrays made here, so that the two sides see bit-identical inputs.
+
+Recipe (every workload):
+
+* Activations X, H and the upstream gradient dZ are N(0, 1).
+* Weights A, B, E are N(0, 0.02) -- the initialisation stated on the
+  Megatron-LM digest page ("Key takeaways", initialisation bullet). B is the
+  weight that feeds the residual, so it is further scaled by 1/sqrt(2N), N
+  counting the attention and MLP blocks of the model the shapes come from.
+* Biases are zero (a bias pin in the tests sets them non-zero explicitly).
+* Targets are uniform over the real (unpadded) vocabulary ids [0, v_valid).
+* bf16 workloads draw fp32 normals and round them to bf16 (round to nearest
+  even); the fp32 workload keeps the fp32 draws.
+
+Each tensor has its own generator, seeded with ``seed * 16 + slot`` where the
+slot is fixed per tensor name, so drawing one tensor never shifts another.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, Optional
+
+import torch
+
+# fixed generator slot per tensor
+_SLOTS = {"X": 1, "A": 2, "B": 3, "dZ": 4, "H": 5, "E": 6, "targets": 7}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One workload: token count, widths, shard count and input statistics."""
+
+    name: str
+    T: int                 # tokens = b * s
+    h: int                 # hidden width
+    f: int                 # MLP inner width (0: no MLP in this workload)
+    v_valid: int           # real vocabulary size (0: no CE in this workload)
+    v_pad: int             # padded vocabulary (a multiple of 128 * t)
+    t: int                 # tensor-parallel shards laid out on the one GPU
+    dtype: str             # "bf16" or "f32"
+    n_blocks: int          # attention + MLP blocks, for the 1/sqrt(2N) scaling of B
+    b: int = 0
+    s: int = 0
+    weight_std: float = 0.02
+
+    @property
+    def b_scale(self) -> float:
+        return 1.0 / math.sqrt(2.0 * self.n_blocks)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+
+# The five workloads. Shapes follow the pages: the 8.3B GPT-2-style model of
+# the Megatron-LM digest (hidden 3072, 72 layers, vocabulary 50,257 padded to
+# 51,200 at 8-way), the 70B decoder of the in-depth page's worked example
+# (hidden 8192, 80 layers, sequence 4096), and a 128,256-token vocabulary
+# padded to a multiple of 128 * t.
+WORKLOADS: Dict[str, Workload] = {
+    "tiny": Workload("tiny", T=32, h=64, f=256, v_valid=512, v_pad=512, t=2,
+                     dtype="f32", n_blocks=2, b=2, s=16),
+    "gpt8b": Workload("gpt8b", T=8192, h=3072, f=12288, v_valid=50257, v_pad=51200,
+                      t=8, dtype="bf16", n_blocks=144, b=8, s=1024),
+    "mlp70b": Workload("mlp70b", T=4096, h=8192, f=32768, v_valid=0, v_pad=0, t=8,
+                       dtype="bf16", n_blocks=160, b=1, s=4096),
+    "ce128k": Workload("ce128k", T=16384, h=8192, f=0, v_valid=128256, v_pad=129024,
+                       t=8, dtype="bf16", n_blocks=160, b=4, s=4096),
+}
+
+# shard-count sweep over the 8.3B MLP shapes
+SWEEP_T = (1, 2, 4, 8, 16)
+
+
+def sweep_workload(t: int) -> Workload:
+    base = WORKLOADS["gpt8b"]
+    return dataclasses.replace(base, name=f"sweep_t{t}", t=t, v_valid=0, v_pad=0)
+
+
+def custom(name: str, T: int, h: int, f: int, v_valid: int, v_pad: int, t: int,
+           dtype: str = "bf16", n_blocks: int = 2) -> Workload:
+    """A workload of arbitrary shape with the same input statistics."""
+    return Workload(name, T=T, h=h, f=f, v_valid=v_valid, v_pad=v_pad, t=t,
+                    dtype=dtype, n_blocks=n_blocks)
+
+
+def _gen(device, seed: int, slot: str) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 16 + _SLOTS[slot])
+    return g
+
+
+def _normal(shape, std, dtype, device, seed, slot):
+    g = _gen(device, seed, slot)
+    x = torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
+    if std != 1.0:
+        x.mul_(std)
+    return x.to(dtype)
+
+
+def mlp_inputs(w: Workload, seed: int = 0, device="cpu") -> Dict[str, torch.Tensor]:
+    """X [T,h], A [h,f], B [f,h] (dtype), bA [f], bB [h] (fp32 zeros), dZ [T,h]."""
+    dt = w.torch_dtype
+    return {
+        "X": _normal((w.T, w.h), 1.0, dt, device, seed, "X"),
+        "A": _normal((w.h, w.f), w.weight_std, dt, device, seed, "A"),
+        "B": _normal((w.f, w.h), w.weight_std * w.b_scale, dt, device, seed, "B"),
+        "bA": torch.zeros(w.f, dtype=torch.float32, device=device),
+        "bB": torch.zeros(w.h, dtype=torch.float32, device=device),
+        "dZ": _normal((w.T, w.h), 1.0, dt, device, seed, "dZ"),
+    }
+
+
+def ce_inputs(w: Workload, seed: int = 0, device="cpu") -> Dict[str, torch.Tensor]:
+    """H [T,h], E [v_pad,h] (dtype), targets [T] int32 uniform over [0, v_valid)."""
+    dt = w.torch_dtype
+    g = _gen(device, seed, "targets")
+    targets = torch.randint(0, w.v_valid, (w.T,), generator=g, device=device,
+                            dtype=torch.int64).to(torch.int32)
+    return {
+        "H": _normal((w.T, w.h), 1.0, dt, device, seed, "H"),
+        "E": _normal((w.v_pad, w.h), w.weight_std, dt, device, seed, "E"),
+        "targets": targets,
+    }
+
+
+def sample_indices(n: int, k: int, seed: int = 0, include_edges: bool = True) -> torch.Tensor:
+    """k distinct indices in [0, n), sorted; the first and last index included."""
+    k = min(k, n)
+    g = torch.Generator().manual_seed(seed + 12345)
+    idx = torch.randperm(n, generator=g)[:k]
+    if include_edges and k >= 2:
+        idx[0] = 0
+        idx[1] = n - 1
+        idx = torch.unique(idx)
+    return torch.sort(idx).values
+
+
+def to_f32_numpy(x: torch.Tensor):
+    """Exact widening of bf16/fp32 data to a contiguous fp32 numpy array."""
+    return x.detach().to("cpu").to(torch.float32).contiguous().numpy()
+
+
+def maybe_int32_numpy(x: Optional[torch.Tensor]):
+    return None if x is None else x.detach().to("cpu").to(torch.int32).contiguous().numpy()
