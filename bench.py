@@ -1,0 +1,507 @@
+#!/usr/bin/env python
+"""Benchmark: tensor-parallel MLP block forward+backward and fused
+vocabulary-parallel cross-entropy forward+backward, all t shards on one GPU.
+
+One step = one pass of the whole path over one batch of synthetic inputs
+resident in HBM: tp_mlp_forward, tp_mlp_backward, vocab_parallel_ce (loss,
+dH, dE). The default workload is the 8.3B-shaped block (T = 8192 tokens,
+h = 3072, f = 12288, vocabulary 50,257 padded to 51,200, t = 8).
+
+Printed (rank 0, one JSON line): whole-job TFLOP/s over the step (MLP
+12 T h f + CE 8 T h v_pad FLOPs, the CE count including the logit recompute
+that unmaterialised logits require), the MLP TFLOP/s and CE tokens/s parts,
+the end-to-end figure through the Python API from pinned host buffers, the
+roofline of the dominant kernel, SM clocks during the timed region, and the
+CPU oracle timed on a bounded sample on this host.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W]
+                       [--impl ours|reference] [--workload gpt8b|mlp70b|ce128k|sweep]
+Multi-GPU (one process per GPU under torchrun): every rank runs its own
+independent batch (data parallel, weak scaling); there is no collective on
+the data path, only a barrier and a max over ranks of the elapsed time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from vocab_ce_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "TP-MLP fwd+bwd TFLOP/s and fused vocab-parallel CE tokens/s vs roofline, 1 GB300"
+UNIT = "TFLOP/s"
+# fallbacks only if the generated MEASURED_PEAKS.json is absent
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# tokens the CPU oracle processes per timed sample
+CPU_SAMPLE_TOKENS = {"gpt8b": 64, "mlp70b": 16, "ce128k": 8, "sweep": 64}
+REF_STEP_TOKENS = {"gpt8b": 8, "mlp70b": 4, "ce128k": 2, "sweep": 8}
+
+
+# ---------------------------------------------------------------------- setup
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=["gpt8b", "mlp70b", "ce128k", "sweep"], default="gpt8b")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def flops(w):
+    mlp = 12.0 * w.T * w.h * w.f if w.f else 0.0
+    ce = 8.0 * w.T * w.h * w.v_pad if w.v_pad else 0.0
+    return mlp, ce
+
+
+def workload_config(w, name):
+    desc = {
+        "gpt8b": "8.3B-shaped block: MLP fwd+bwd + fused vocab-parallel CE fwd+bwd",
+        "mlp70b": "70B-shaped MLP fwd+bwd",
+        "ce128k": "vocab-parallel fused logit GEMM + CE fwd+bwd, 128,256-token vocabulary",
+        "sweep": "shard-count sweep of the 8.3B MLP fwd+bwd",
+    }[name]
+    cfg = {"workload": f"{desc}: T={w.T} (b={w.b}, s={w.s}), h={w.h}", "T": w.T, "h": w.h, "t": w.t,
+           "seed": 0, "inputs": "seeded synthetic (workloads.py recipe), resident in HBM"}
+    if w.f:
+        cfg["f"] = w.f
+    if w.v_pad:
+        cfg.update(v_valid=w.v_valid, v_pad=w.v_pad)
+    return cfg
+
+
+# ---------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device, enabled=True):
+        self.proc = None
+        self.path = None
+        if not enabled:
+            return
+        sel = []
+        try:
+            uuid = torch.cuda.get_device_properties(device).uuid
+            sel = ["-i", "GPU-" + str(uuid)]
+        except Exception:
+            pass
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "50"] + sel, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------- traffic from committed ncu summaries
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("gemm.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "vocab_ce_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel, workload):
+    """dram bytes per launch recorded in profiles/ for this kernel and workload,
+    if the GEMM source has not changed since the capture; else None."""
+    d = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(d):
+        return None
+    src = kernel_source_hash()
+    for fn in sorted(os.listdir(d)):
+        if not fn.endswith((".md", ".txt")):
+            continue
+        text = open(os.path.join(d, fn)).read()
+        for m in re.finditer(r"traffic_per_launch\s+kernel=(\S+)\s+workload=(\S+)\s+bytes=(\d+)\s+source=(\w+)",
+                             text):
+            if m.group(1) == kernel and m.group(2) == workload and m.group(4) == src:
+                return int(m.group(3))
+    return None
+
+
+# ---------------------------------------------------------------------- the step
+class Step:
+    def __init__(self, w, dev, seed):
+        import vocab_ce_gb300 as tp
+
+        self.tp = tp
+        self.w = w
+        self.dev = dev
+        self.mi = wl.mlp_inputs(w, seed=seed, device=dev) if w.f else None
+        self.ci = wl.ce_inputs(w, seed=seed, device=dev) if w.v_pad else None
+        T, h, f = w.T, w.h, w.f
+        bf = torch.bfloat16
+        self.out = {}
+        if w.f:
+            self.fo = {k: torch.empty(s, dtype=bf, device=dev) for k, s in (("Z", (T, h)), ("U", (T, f)), ("Y", (T, f)))}
+            self.bo = {"dX": torch.empty((T, h), dtype=bf, device=dev), "dA": torch.empty((h, f), dtype=bf, device=dev),
+                       "dB": torch.empty((f, h), dtype=bf, device=dev),
+                       "dbA": torch.empty(f, dtype=torch.float32, device=dev),
+                       "dbB": torch.empty(h, dtype=torch.float32, device=dev)}
+            self.mws = torch.empty(max(1, tp.mlp_workspace_bytes(T, h, f, w.t)), dtype=torch.uint8, device=dev)
+        if w.v_pad:
+            self.co = {"loss": torch.empty(T, dtype=torch.float32, device=dev),
+                       "lse": torch.empty(T, dtype=torch.float32, device=dev),
+                       "dH": torch.empty((T, h), dtype=bf, device=dev),
+                       "dE": torch.empty((w.v_pad, h), dtype=bf, device=dev)}
+            self.cws = torch.empty(tp.ce_workspace_bytes(T, h, w.v_pad, w.t), dtype=torch.uint8, device=dev)
+
+    def mlp(self, mi=None):
+        mi = mi or self.mi
+        tp, w = self.tp, self.w
+        fo = tp.tp_mlp_forward(mi["X"], mi["A"], mi["B"], w.t, mi["bA"], mi["bB"], out=self.fo)
+        tp.tp_mlp_backward(mi["dZ"], mi["X"], mi["A"], mi["B"], fo["U"], fo["Y"], w.t, out=self.bo, ws=self.mws)
+
+    def ce(self, ci=None):
+        ci = ci or self.ci
+        return self.tp.vocab_parallel_ce(ci["H"], ci["E"], ci["targets"], self.w.v_valid, self.w.t, grad_scale=1.0,
+                                         out=self.co, ws=self.cws)
+
+    def run(self, mi=None, ci=None):
+        if self.w.f:
+            self.mlp(mi)
+        if self.w.v_pad:
+            self.ce(ci)
+
+
+def input_bytes(step):
+    b = 0
+    for d in (step.mi, step.ci):
+        if d:
+            b += sum(v.numel() * v.element_size() for v in d.values())
+    return b
+
+
+# ---------------------------------------------------------------------- CPU oracle
+def oracle_sample(w, mi, ci, n_tokens):
+    """Host copies of the first n_tokens tokens plus the full weights, as float64."""
+    import numpy as np
+
+    def f64(x):
+        return x.detach().float().cpu().numpy().astype(np.float64)
+
+    s = {}
+    if mi is not None:
+        s.update(X=f64(mi["X"][:n_tokens]), dZ=f64(mi["dZ"][:n_tokens]), A=f64(mi["A"]), B=f64(mi["B"]),
+                 bA=f64(mi["bA"]), bB=f64(mi["bB"]))
+    if ci is not None:
+        s.update(H=f64(ci["H"][:n_tokens]), E=f64(ci["E"]),
+                 y=ci["targets"][:n_tokens].cpu().numpy().astype(np.int32))
+    return s
+
+
+def oracle_step(w, s):
+    import oracle
+
+    if "X" in s:
+        oracle.mlp_forward(s["X"], s["A"], s["bA"], s["B"], s["bB"])
+        oracle.mlp_backward(s["X"], s["A"], s["bA"], s["B"], s["dZ"])
+    if "H" in s:
+        oracle.ce(s["H"], s["E"], s["y"], w.v_valid, grad_scale=1.0)
+
+
+def oracle_rate(w, s, n_tokens, reps=1):
+    """(TFLOP/s in the bench's FLOP convention, seconds per rep)."""
+    mlp, ce = flops(w)
+    work = (mlp + ce) / w.T * n_tokens
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_step(w, s)
+    dt = (time.perf_counter() - t0) / reps
+    return work / dt / 1e12, dt
+
+
+# ---------------------------------------------------------------------- arms
+def run_reference(args, w, name):
+    import oracle
+
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    oracle.build()
+    n = REF_STEP_TOKENS[name]
+    mi = wl.mlp_inputs(w, seed=0) if w.f else None
+    ci = wl.ce_inputs(w, seed=0) if w.v_pad else None
+    s = oracle_sample(w, mi, ci, n)
+    for _ in range(args.warmup):
+        oracle_step(w, s)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(w, s)
+        times.append(time.perf_counter() - t0)
+    dt = sum(times) / len(times)
+    mlp, ce = flops(w)
+    value = (mlp + ce) / w.T * n / dt / 1e12
+    sample = f"first {n} of {w.T} tokens at full h, f, v per step (weights in full), fp64 oracle"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, name),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w, name):
+    ws, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    import vocab_ce_gb300 as tp
+
+    step = Step(w, dev, seed=rank)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        step.run()
+    torch.cuda.synchronize()
+    assert tp.device_status() == 0, "device status after warm-up"
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    # ---------------- timed region (device-resident inputs)
+    mlp_fl, ce_fl = flops(w)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(dev, enabled=not args.no_clocks)
+    barrier()
+    torch.cuda.synchronize()
+    tp.profile_enable(True)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        if w.f:
+            step.mlp()
+        ev[i][1].record(stream)
+        if w.v_pad:
+            step.ce()
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    kernels = tp.profile_read()
+    tp.profile_enable(False)
+    clk = clocks.stop()
+    assert tp.device_status() == 0, "device status after the timed region"
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if ws > 1:
+        import torch.distributed as dist
+
+        tmax = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tmax.item())
+    ms_step = elapsed_ms / args.steps
+    mlp_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / args.steps
+    ce_ms = sum(b.elapsed_time(c) for _, b, c in ev) / args.steps
+    value = ws * (mlp_fl + ce_fl) / (ms_step * 1e-3) / 1e12
+
+    pk, pk_src = peaks()
+    # ---------------- roofline of the dominant kernel
+    dominant = max(kernels.items(), key=lambda kv: kv[1]["ms"]) if kernels else None
+    roof = None
+    if dominant:
+        kname, kd = dominant
+        kflops = kernel_flops_per_step(kname, w)
+        launches_per_step = kd["launches"] / args.steps
+        per_launch = kflops / launches_per_step if kflops and launches_per_step else None
+        avg_ms = kd["ms"] / kd["launches"]
+        if per_launch:
+            achieved = per_launch / (avg_ms * 1e-3) / 1e12
+            roof = {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": pk["bf16_tflops_sustained"],
+                    "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"],
+                    "peak_kind": f"{pk_src} sustained bf16 (kernel timed inside a long step)",
+                    "frac_of_burst_peak": achieved / pk["bf16_tflops"],
+                    "flops_per_launch": per_launch, "avg_launch_ms": avg_ms,
+                    "traffic": traffic_from_profiles(kname, name)}
+    gpu_launches = int(sum(k["launches"] for k in kernels.values()))
+    per_kernel = {k: {"launches": v["launches"], "ms_per_step": v["ms"] / args.steps,
+                      "tflops": (kernel_flops_per_step(k, w) / (v["ms"] / args.steps * 1e-3) / 1e12)
+                      if kernel_flops_per_step(k, w) else None}
+                  for k, v in sorted(kernels.items(), key=lambda kv: -kv[1]["ms"])}
+
+    # ---------------- end to end: pinned host inputs -> device, the step, loss -> host
+    e2e = None
+    if not args.no_e2e:
+        host = {}
+        for src in (step.mi, step.ci):
+            if src:
+                for k, v in src.items():
+                    host[k] = v.cpu().pin_memory()
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        loss_host = torch.empty(w.T, dtype=torch.float32).pin_memory() if w.v_pad else None
+        z_host = torch.empty((w.T, w.h), dtype=torch.bfloat16).pin_memory() if not w.v_pad else None
+
+        def e2e_step():
+            for k, v in host.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            mi = {k: dev_in[k] for k in ("X", "A", "B", "bA", "bB", "dZ")} if w.f else None
+            ci = {k: dev_in[k] for k in ("H", "E", "targets")} if w.v_pad else None
+            step.run(mi, ci)
+            if w.v_pad:
+                loss_host.copy_(step.co["loss"], non_blocking=True)
+            else:
+                z_host.copy_(step.fo["Z"], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e_ms = a.elapsed_time(b)
+        if ws > 1:
+            import torch.distributed as dist
+
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = (loss_host.numel() * 4) if w.v_pad else z_host.numel() * 2
+        e2e = {"value": ws * (mlp_fl + ce_fl) / (e_ms / args.steps * 1e-3) / 1e12, "unit": UNIT,
+               "ms_per_step": e_ms / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "path": "vocab_ce_gb300 Python API -> C ABI; inputs copied from pinned host memory every step"}
+
+    # ---------------- CPU oracle baseline (rank 0 at N = 1 only)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        n = CPU_SAMPLE_TOKENS[name]
+        s = oracle_sample(w, step.mi, step.ci, n)
+        rate, sec = oracle_rate(w, s, n)
+        cpu = {"value": rate, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"first {n} of {w.T} tokens through the full step (MLP fwd+bwd, CE fwd+bwd with dH and dE) "
+                         f"at full h, f, v; {sec:.1f} s; same FLOP-per-token convention as value"}
+
+    if rank != 0:
+        return 0
+    ws_bytes = input_bytes(step)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {**workload_config(w, name), "parallelism": f"t={w.t} shards on each GPU; dp{ws} (independent batches)",
+                       "l2": f"no flush: inputs alone are {ws_bytes / 1e9:.2f} GB per step, > 129 MB L2"},
+            "parts": {"mlp_tflops": (mlp_fl / (mlp_ms * 1e-3) / 1e12) if w.f else None, "mlp_ms": mlp_ms if w.f else None,
+                      "ce_tokens_per_s": (w.T / (ce_ms * 1e-3)) if w.v_pad else None,
+                      "ce_tflops": (ce_fl / (ce_ms * 1e-3) / 1e12) if w.v_pad else None, "ce_ms": ce_ms if w.v_pad else None,
+                      "mlp_frac_of_peak": ((mlp_fl / (mlp_ms * 1e-3) / 1e12) / pk["bf16_tflops_sustained"]) if w.f else None,
+                      "ce_frac_of_roofline": ((ce_fl / (ce_ms * 1e-3) / 1e12) / pk["bf16_tflops_sustained"]) if w.v_pad else None},
+            "roofline": roof, "kernels": per_kernel, "gpu_launches": gpu_launches,
+            "e2e": e2e, "cpu_baseline": cpu, "clocks": clk}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def kernel_flops_per_step(name, w):
+    T, h, f, vp = w.T, w.h, w.f, w.v_pad
+    table = {
+        "mlp_fwd_gemm1_bias_gelu": 2.0 * T * h * f, "mlp_fwd_gemm2_shard_sum": 2.0 * T * f * h,
+        "mlp_bwd_dY_gelu_grad": 2.0 * T * h * f, "mlp_bwd_dB": 2.0 * T * f * h, "mlp_bwd_dA": 2.0 * T * h * f,
+        "mlp_bwd_dX_shard_sum": 2.0 * T * f * h,
+        "ce_fwd_logits_stats": 2.0 * T * h * vp, "ce_bwd_logits_dl": 2.0 * T * h * vp,
+        "ce_bwd_dE": 2.0 * T * h * vp, "ce_bwd_dH_shard_sum": 2.0 * T * h * vp,
+    }
+    return table.get(name)
+
+
+def main():
+    args = parse_args()
+    name = args.workload
+    if name == "sweep":
+        rc = 0
+        for t in wl.SWEEP_T:
+            rc |= (run_reference if args.impl == "reference" else run_ours)(args, wl.sweep_workload(t), name)
+        return rc
+    w = wl.WORKLOADS[name]
+    return run_reference(args, w, name) if args.impl == "reference" else run_ours(args, w, name)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

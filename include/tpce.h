@@ -1,0 +1,212 @@
+/*
+ * tpce.h -- C ABI of libtpce: Megatron-style 1D tensor-parallel MLP block and
+ * vocabulary-parallel fused cross-entropy, with all t shards on one GPU.
+ *
+ * The partition follows "Tensor Parallelism and Pipeline Parallelism:
+ * Mathematical Foundations of Megatron-LM 1D Slicing ..." (llms.blog),
+ * sections "Column-Parallel Linear Layer", "Row-Parallel Linear Layer" and
+ * "Conjugate Communication Operators", and "Cutting a Model Into Pieces"
+ * (lecture 3), section "Megatron-LM: cutting inside the layer":
+ *
+ *   A = [A_1 .. A_t] split by columns, Y_i = GeLU(X A_i + bA_i) per shard
+ *   with no exchange; B = [B_1; ..; B_t] split by rows, Z_i = Y_i B_i, and
+ *   the forward operator g sums Z = sum_i Z_i (+ bB once). Backward: g*
+ *   hands dZ to every shard unchanged, f* sums the per-shard dX_i.
+ *
+ * The fused logit GEMM + cross-entropy follows "LIT-022: Megatron-LM:
+ * Training Multi-Billion Parameter Language Models Using Model Parallelism"
+ * (anthology digest), "Key takeaways": each vocabulary shard reduces its
+ * logits to per-token statistics, so b*s numbers are combined instead of
+ * b*s*v logits. The vocabulary is padded to a multiple of 128 * t (same
+ * bullet, and "Megatron-LM, in depth", section "Failure modes").
+ *
+ * On one GPU the shard index is a coordinate of the kernels' tile grid and
+ * every sum over shards (g, f*, the statistics exchange, the dH sum) is done
+ * on the device: in the tensor-core accumulator or in a reduction kernel.
+ * There is no collective.
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the
+ *    library never allocates device memory and never frees a pointer.
+ *  - Row-major layouts. X, Z, dX, dZ, H, dH: [T, h]. A, dA: [h, f].
+ *    B, dB: [f, h]. U, Y (saved activations): [T, f]. E, dE: [v_pad, h].
+ *    Shard i is the column block A[:, i f/t : (i+1) f/t], the row block
+ *    B[i f/t : (i+1) f/t, :] and the row block E[i v_pad/t : (i+1) v_pad/t, :];
+ *    the unsharded tensors are passed and t selects the partition.
+ *  - dtype TPCE_BF16: X, A, B, Z, U, Y, dZ, dX, dA, dB, H, E, dH, dE are bf16,
+ *    accumulation is fp32. Biases and bias gradients are always fp32.
+ *  - Every tensor pointer must be 16-byte aligned; h must be a multiple of 8.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream). Shape and alignment checks run on the host before any
+ *    launch; a failed check launches nothing.
+ *  - Gradients are written, not accumulated.
+ *  - Errors are returned as tpce_status; nothing is thrown across the ABI.
+ *    Problems only the device can see (a target id out of range, a bounded
+ *    wait inside a kernel that ran out) are recorded in a device status word
+ *    that tpce_device_status() reads.
+ */
+#ifndef TPCE_H
+#define TPCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TPCE_BF16 = 0,   /* bf16 tensors, fp32 accumulate */
+    TPCE_F32 = 1     /* fp32 tensors (not supported by this build: TPCE_ERR_UNSUPPORTED) */
+} tpce_dtype;
+
+typedef enum {
+    TPCE_OK = 0,
+    TPCE_ERR_INVALID = 1,      /* null pointer, bad dtype, target id out of range */
+    TPCE_ERR_SHAPE = 2,        /* sizes violate the partition rules */
+    TPCE_ERR_ALIGN = 3,        /* a pointer is not 16-byte aligned */
+    TPCE_ERR_WORKSPACE = 4,    /* workspace missing or smaller than the query says */
+    TPCE_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
+    TPCE_ERR_TIMEOUT = 6,      /* a bounded wait inside a kernel gave up */
+    TPCE_ERR_UNSUPPORTED = 7   /* valid request this build does not implement */
+} tpce_status;
+
+/* Human-readable name of a status. Never NULL. */
+const char *tpce_status_string(tpce_status s);
+
+/* Library ABI version (major * 100 + minor). */
+int tpce_version(void);
+
+/* Description of the last failure a call made on this host thread returned
+ * (the failing CUDA call or check and its error name). Empty if none. The
+ * text stays valid until the next failing call on the same thread. Setting
+ * the environment variable TPCE_SYNC_CHECK=1 makes the library synchronise
+ * after every kernel launch, so that an execution error is attributed to the
+ * kernel that raised it (debugging aid; slow). */
+const char *tpce_last_error(void);
+
+/* ---------------------------------------------------------------------------
+ * Vocabulary padding rule: the smallest multiple of divisor * t that is
+ * >= v (divisor 128 is Megatron's default; 50,257 -> 51,200 at t = 8). Source:
+ * LIT-022 digest, "Key takeaways" (vocabulary padded so each slice is a
+ * multiple of 128); "Megatron-LM, in depth", "Failure modes" (rounded up to a
+ * multiple of the divisor times TP). Returns -1 if v < 0, t < 1 or
+ * divisor < 1.
+ * ------------------------------------------------------------------------- */
+int64_t tpce_pad_vocab(int64_t v, int t, int divisor);
+
+/* ---------------------------------------------------------------------------
+ * Workspace sizes in bytes (0 when none is needed). The caller allocates at
+ * least this much device memory, 256-byte aligned, and passes it with its
+ * size. The contents need not be initialised and are garbage afterwards.
+ * tpce_mlp_workspace_bytes covers both tp_mlp_forward (which needs none) and
+ * tp_mlp_backward. tpce_ce_workspace_bytes depends on whether gradients are
+ * requested (with_grads != 0): the forward keeps per-token statistics only;
+ * the backward adds a bounded bf16 scratch for one vocabulary chunk of
+ * logit gradients and, when there is more than one chunk, an fp32 [T, h]
+ * accumulator for dH. Returns 0 for invalid shapes.
+ * ------------------------------------------------------------------------- */
+size_t tpce_mlp_workspace_bytes(int64_t T, int64_t h, int64_t f, int t, int dtype);
+size_t tpce_ce_workspace_bytes(int64_t T, int64_t h, int64_t v_pad, int t, int dtype,
+                               int with_grads);
+
+/* ---------------------------------------------------------------------------
+ * tp_mlp_forward -- the tensor-parallel MLP block, forward.
+ *   U = X A + bA,  Y = GeLU(U)   (column-parallel GEMM1; per shard i the
+ *                                 columns of A_i; GeLU needs no exchange)
+ *   Z = sum_i Y_i B_i + bB       (row-parallel GEMM2; g = sum over shards,
+ *                                 done in the accumulator; bB added once)
+ * GeLU is the exact form x * Phi(x) (Phi via erf).
+ * Inputs:  X [T, h], A [h, f], B [f, h]; bA [f] and bB [h] fp32, may be NULL
+ *          (zero bias).
+ * Outputs: Z [T, h]; U [T, f] and Y [T, f] are written for the backward.
+ * Shapes:  T >= 0 (T == 0 is a no-op and every pointer may then be NULL),
+ *          h >= 8 and h % 8 == 0, t >= 1, f % t == 0 and (f / t) % 64 == 0.
+ * Workspace: none (ws may be NULL, ws_bytes 0).
+ * ------------------------------------------------------------------------- */
+tpce_status tp_mlp_forward(const void *X, const void *A, const float *bA,
+                           const void *B, const float *bB,
+                           int64_t T, int64_t h, int64_t f, int t, int dtype,
+                           void *Z, void *U, void *Y,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * tp_mlp_backward -- gradients of the block for the upstream gradient dZ.
+ * Chain rule of tp_mlp_forward, with the conjugate operators of the
+ * Mathematical Foundations page: g* gives dZ to every shard,
+ *   dB_i = Y_i^T dZ,  dY_i = dZ B_i^T,  dU_i = dY_i (.) GeLU'(U_i),
+ *   dA_i = X^T dU_i,  dbA_i = sum_tokens dU_i,  dbB = sum_tokens dZ,
+ * and f* sums the shard partials  dX = sum_i dU_i A_i^T  (in the accumulator).
+ * Inputs:  dZ [T, h], X [T, h], A [h, f], B [f, h], and the U [T, f] and
+ *          Y [T, f] that tp_mlp_forward wrote for the same X, A, bA.
+ * Outputs: dX [T, h], dA [h, f], dB [f, h]; dbA [f] and dbB [h] fp32, may be
+ *          NULL (not computed).
+ * Shapes:  as tp_mlp_forward. T == 0 writes zero weight/bias gradients; the
+ *          token-dimension pointers (dZ, X, U, Y, dX) may then be NULL.
+ * Workspace: tpce_mlp_workspace_bytes(T, h, f, t, dtype) bytes (holds dU).
+ * ------------------------------------------------------------------------- */
+tpce_status tp_mlp_backward(const void *dZ, const void *X, const void *A, const void *B,
+                            const void *U, const void *Y,
+                            int64_t T, int64_t h, int64_t f, int t, int dtype,
+                            void *dX, void *dA, float *dbA, void *dB, float *dbB,
+                            void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * vocab_parallel_ce -- logit GEMM fused with softmax cross-entropy, the
+ * vocabulary split into t shards of v_pad / t rows of E.
+ * Forward, per shard i and token r (the logits l = H E_i^T stay in fp32
+ * registers and are never written to memory):
+ *   m_i = max of l over the shard's real ids (< v_valid),
+ *   s_i = sum exp(l - m_i) over them, tau = l[target] in the owning shard.
+ * Only (m_i, s_i) and tau are combined across shards:
+ *   m = max_i m_i,  S = sum_i s_i exp(m_i - m),  lse = m + ln S,
+ *   loss = lse - tau.
+ * Backward (dH and/or dE requested), with dl = grad_scale * (softmax - onehot)
+ * on real ids and 0 on padded ids, recomputing the logits chunk by chunk:
+ *   dE_i = dl_i^T H   (each shard's own rows, no exchange; padded rows = 0)
+ *   dH   = sum_i dl_i E_i   (sum over shards on the device)
+ * grad_scale is the upstream dLoss per token (1 for the sum, 1/T for the mean).
+ * Inputs:  H [T, h], E [v_pad, h], targets [T] int32 in [0, v_valid).
+ * Outputs: loss [T] fp32; lse [T] fp32 may be NULL; dH [T, h] and dE
+ *          [v_pad, h] may be NULL (a NULL pair is the forward-only call).
+ * Shapes:  T >= 0, h % 8 == 0, t >= 1, v_pad % t == 0, (v_pad / t) % 128 == 0,
+ *          1 <= v_valid <= v_pad. T == 0 writes dE = 0 (if requested); H,
+ *          targets and loss may then be NULL.
+ * Errors:  a target outside [0, v_valid) gives a NaN loss for that token and
+ *          TPCE_ERR_INVALID in the device status word.
+ * Workspace: tpce_ce_workspace_bytes(T, h, v_pad, t, dtype, dH||dE) bytes.
+ * ------------------------------------------------------------------------- */
+tpce_status vocab_parallel_ce(const void *H, const void *E, const int32_t *targets,
+                              int64_t T, int64_t h, int64_t v_pad, int64_t v_valid, int t,
+                              float grad_scale, int dtype,
+                              float *loss, float *lse, void *dH, void *dE,
+                              void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Device status word. Kernels record the first device-side failure (a
+ * TPCE_ERR_* code in the low 8 bits, detail above) instead of trapping.
+ * tpce_device_status synchronises `stream`, reads the word of the current
+ * device, clears it when clear != 0, and returns its status code
+ * (TPCE_ERR_CUDA if the synchronisation itself fails). *detail, if not NULL,
+ * receives the raw word.
+ * ------------------------------------------------------------------------- */
+tpce_status tpce_device_status(void *stream, int clear, uint32_t *detail);
+
+/* ---------------------------------------------------------------------------
+ * Kernel timing. While enabled, every kernel the library launches is
+ * bracketed by two CUDA events recorded on the launch stream.
+ * tpce_profile_enable(1) starts a fresh record (0 stops recording).
+ * tpce_profile_count() waits for the recorded events, aggregates them by
+ * kernel name and returns the number of distinct names (-1 on error).
+ * tpce_profile_get(i, ...) returns entry i of that aggregate: the kernel's
+ * name (static storage), number of launches and total milliseconds.
+ * ------------------------------------------------------------------------- */
+tpce_status tpce_profile_enable(int on);
+int tpce_profile_count(void);
+tpce_status tpce_profile_get(int i, const char **name, int64_t *launches, double *total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPCE_H */

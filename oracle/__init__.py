@@ -67,6 +67,8 @@ def _load():
         lib.oracle_mlp_backward.argtypes = [I64, I64, I64, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_mlp_backward_cols.restype = None
         lib.oracle_mlp_backward_cols.argtypes = [I64, I64, I64, P, P, P, P, P, I64, P, P, P, P]
+        lib.oracle_bias_grad.restype = None
+        lib.oracle_bias_grad.argtypes = [I64, I64, P, P]
         lib.oracle_mlp_sharded.restype = None
         lib.oracle_mlp_sharded.argtypes = [I64, I64, I64, ctypes.c_int, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_ce.restype = None
@@ -136,6 +138,15 @@ def mlp_backward_cols(X, A, bA, B, dZ, cols) -> Dict[str, np.ndarray]:
     _load().oracle_mlp_backward_cols(T, h, f, _ptr(X), _ptr(A), _ptr(bA), _ptr(B), _ptr(dZ),
                                      n, _ptr(cols), _ptr(dA), _ptr(dbA), _ptr(dB))
     return {"dA": dA, "dbA": dbA, "dB": dB}
+
+
+def bias_grad(dZ) -> np.ndarray:
+    """dbB = sum over tokens of dZ."""
+    dZ = _f64(dZ)
+    T, h = dZ.shape
+    out = np.empty((h,))
+    _load().oracle_bias_grad(T, h, _ptr(dZ), _ptr(out))
+    return out
 
 
 def mlp_sharded(X, A, bA, B, bB, dZ, t: int) -> Dict[str, np.ndarray]:

@@ -214,12 +214,17 @@ void oracle_mlp_backward_cols(int64_t T, int64_t h, int64_t f,
 #pragma omp parallel for schedule(dynamic)
     for (c = 0; c < ncols; c++) {
         int64_t j = cols[c];
+        double *a = (double *)malloc(sizeof(double) * (size_t)h);   /* A[:, j] */
         double *u = (double *)malloc(sizeof(double) * (size_t)T);
         double *du = (double *)malloc(sizeof(double) * (size_t)T);
+        double *da = (double *)calloc((size_t)h, sizeof(double));
+        double *db = (double *)calloc((size_t)h, sizeof(double));
+        for (int64_t k = 0; k < h; k++)
+            a[k] = A[k * f + j];
         for (int64_t t = 0; t < T; t++) {
             double acc = bA ? bA[j] : 0.0;
             for (int64_t k = 0; k < h; k++)
-                acc += X[t * h + k] * A[k * f + j];
+                acc += X[t * h + k] * a[k];
             u[t] = acc;
             double dy = 0.0;
             for (int64_t n = 0; n < h; n++)
@@ -230,20 +235,35 @@ void oracle_mlp_backward_cols(int64_t T, int64_t h, int64_t f,
         for (int64_t t = 0; t < T; t++)
             sb += du[t];
         dbA_cols[c] = sb;
-        for (int64_t k = 0; k < h; k++) {
-            double acc = 0.0;
-            for (int64_t t = 0; t < T; t++)
-                acc += X[t * h + k] * du[t];
-            dA_cols[k * ncols + c] = acc;
+        /* dA[k, j] = sum_t X[t, k] du[t] and dB[j, n] = sum_t Y[t, j] dZ[t, n],
+         * each sum taken over t in order */
+        for (int64_t t = 0; t < T; t++) {
+            double y = oracle_gelu(u[t]);
+            for (int64_t k = 0; k < h; k++)
+                da[k] += X[t * h + k] * du[t];
+            for (int64_t n = 0; n < h; n++)
+                db[n] += y * dZ[t * h + n];
         }
-        for (int64_t n = 0; n < h; n++) {
-            double acc = 0.0;
-            for (int64_t t = 0; t < T; t++)
-                acc += oracle_gelu(u[t]) * dZ[t * h + n];
-            dB_rows[c * h + n] = acc;
-        }
+        for (int64_t k = 0; k < h; k++)
+            dA_cols[k * ncols + c] = da[k];
+        memcpy(dB_rows + c * h, db, sizeof(double) * (size_t)h);
+        free(a);
         free(u);
         free(du);
+        free(da);
+        free(db);
+    }
+}
+
+/* dbB = sum_t dZ[t, :] -- the row-parallel bias gradient on its own, the same
+ * definition oracle_mlp_backward uses. Out: dbB [h]. */
+void oracle_bias_grad(int64_t T, int64_t h, const double *dZ, double *dbB)
+{
+    for (int64_t n = 0; n < h; n++) {
+        double acc = 0.0;
+        for (int64_t t = 0; t < T; t++)
+            acc += dZ[t * h + n];
+        dbB[n] = acc;
     }
 }
 

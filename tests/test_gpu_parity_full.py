@@ -1,0 +1,108 @@
+"""GPU parity at the full workload sizes, in the launch configuration the
+benchmark times.
+
+The oracle cannot redo a full-size GEMM in plain fp64 loops in seconds, so it
+checks outputs it can compute one by one: every row of Z, U, Y, dX, loss, lse
+and dH belongs to one token, so 64 sampled tokens (first and last included)
+are recomputed from their own rows; a column j of dA / dbA and a row j of dB
+need only O(T h) work, so 32 sampled j are recomputed over all tokens; dbB is
+the token sum of dZ, recomputed in full. dE needs the softmax of every token,
+so it is checked in full on a run over the first tokens at the full h and v.
+The shard sweep checks that t = 1 and t = 16 give bit-identical outputs at
+full size.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import vocab_ce_gb300 as tp
+from vocab_ce_gb300 import workloads as wl
+from _parity import assert_loss, assert_rel, gpu_or_skip
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+N_ROWS = 64
+N_COLS = 32
+
+
+def _host(x):
+    return x.detach().cpu()
+
+
+def check_mlp_full(w, dev, seed=0):
+    mi = wl.mlp_inputs(w, seed=seed, device=dev)
+    fwd = tp.tp_mlp_forward(mi["X"], mi["A"], mi["B"], w.t, mi["bA"], mi["bB"])
+    bwd = tp.tp_mlp_backward(mi["dZ"], mi["X"], mi["A"], mi["B"], fwd["U"], fwd["Y"], w.t)
+    assert tp.device_status() == 0
+    rows = wl.sample_indices(w.T, N_ROWS, seed=seed)
+    cols = wl.sample_indices(w.f, N_COLS, seed=seed + 1)
+    X, A, B, dZ = (_host(mi[k]) for k in ("X", "A", "B", "dZ"))
+    bA, bB = _host(mi["bA"]), _host(mi["bB"])
+    of = oracle.mlp_forward(X[rows], A, bA, B, bB)
+    ob = oracle.mlp_backward(X[rows], A, bA, B, dZ[rows], want=("dX",))
+    for k in ("U", "Y", "Z"):
+        assert_rel(k, _host(fwd[k])[rows], of[k])
+    assert_rel("dX", _host(bwd["dX"])[rows], ob["dX"])
+    oc = oracle.mlp_backward_cols(X, A, bA, B, dZ, cols)
+    assert_rel("dA[:, cols]", _host(bwd["dA"])[:, cols], oc["dA"])
+    assert_rel("dbA[cols]", _host(bwd["dbA"])[cols], oc["dbA"])
+    assert_rel("dB[cols, :]", _host(bwd["dB"])[cols, :], oc["dB"])
+    assert_rel("dbB", _host(bwd["dbB"]), oracle.bias_grad(dZ))
+    return mi, fwd, bwd
+
+
+def check_ce_full(w, dev, seed=0, de_tokens=48):
+    ci = wl.ce_inputs(w, seed=seed, device=dev)
+    ci["targets"][0] = 0
+    ci["targets"][1] = w.v_valid - 1
+    gs = 1.0 / w.T
+    out = tp.vocab_parallel_ce(ci["H"], ci["E"], ci["targets"], w.v_valid, w.t, grad_scale=gs)
+    assert tp.device_status() == 0
+    H, E, y = _host(ci["H"]), _host(ci["E"]), _host(ci["targets"]).numpy()
+    rows = wl.sample_indices(w.T, N_ROWS, seed=seed)
+    ref = oracle.ce(H[rows], E, y[rows], w.v_valid, grad_scale=gs, want_dE=False)
+    assert_loss("loss", _host(out["loss"])[rows], ref["loss"])
+    assert_loss("lse", _host(out["lse"])[rows], ref["lse"])
+    assert_rel("dH", _host(out["dH"])[rows], ref["dH"])
+    assert torch.count_nonzero(out["dE"][w.v_valid:]).item() == 0
+    # dE in full on the first de_tokens tokens, same h and vocabulary
+    sub = tp.vocab_parallel_ce(ci["H"][:de_tokens].contiguous(), ci["E"], ci["targets"][:de_tokens].contiguous(),
+                               w.v_valid, w.t, grad_scale=1.0)
+    assert tp.device_status() == 0
+    ref2 = oracle.ce(H[:de_tokens], E, y[:de_tokens], w.v_valid, grad_scale=1.0)
+    assert_rel("dE", sub["dE"], ref2["dE"])
+    assert_loss("loss (sub)", sub["loss"], ref2["loss"])
+    return out
+
+
+def test_gpt8b_block_full_size():
+    dev = gpu_or_skip()
+    w = wl.WORKLOADS["gpt8b"]
+    check_mlp_full(w, dev)
+    check_ce_full(w, dev, de_tokens=128)
+
+
+def test_mlp70b_full_size():
+    dev = gpu_or_skip()
+    check_mlp_full(wl.WORKLOADS["mlp70b"], dev)
+
+
+def test_ce128k_full_size():
+    dev = gpu_or_skip()
+    check_ce_full(wl.WORKLOADS["ce128k"], dev, de_tokens=32)
+
+
+def test_shard_sweep_full_size_bit_identical():
+    dev = gpu_or_skip()
+    outs = {}
+    for t in (1, 16):
+        w = wl.sweep_workload(t)
+        mi = wl.mlp_inputs(w, seed=0, device=dev)
+        fwd = tp.tp_mlp_forward(mi["X"], mi["A"], mi["B"], w.t, mi["bA"], mi["bB"])
+        bwd = tp.tp_mlp_backward(mi["dZ"], mi["X"], mi["A"], mi["B"], fwd["U"], fwd["Y"], w.t)
+        outs[t] = {"Z": fwd["Z"], **bwd}
+    assert tp.device_status() == 0
+    for k in outs[1]:
+        assert torch.equal(outs[1][k], outs[16][k]), k

@@ -1,0 +1,174 @@
+"""GPU parity, small and medium sizes: every output element compared with the
+fp64 CPU oracle on the same seeded inputs, through the C ABI.
+
+Cases span several tiles in every dimension and ragged tails (T, h, N not
+multiples of the 128 x 256 tile; vocabulary shards that are odd multiples of
+128; shards made only of padded ids).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import vocab_ce_gb300 as tp
+from vocab_ce_gb300 import workloads as wl
+from _parity import assert_loss, assert_rel, gpu_or_skip
+
+pytestmark = pytest.mark.gpu
+
+
+def _biases(w, seed):
+    g = torch.Generator().manual_seed(1000 + seed)
+    return (0.1 * torch.randn(w.f, generator=g)).float(), (0.1 * torch.randn(w.h, generator=g)).float()
+
+
+def run_mlp(w, dev, seed=0, nonzero_bias=True):
+    mi = wl.mlp_inputs(w, seed=seed)
+    if nonzero_bias:
+        mi["bA"], mi["bB"] = _biases(w, seed)
+    g = {k: v.to(dev) for k, v in mi.items()}
+    fwd = tp.tp_mlp_forward(g["X"], g["A"], g["B"], w.t, g["bA"], g["bB"])
+    bwd = tp.tp_mlp_backward(g["dZ"], g["X"], g["A"], g["B"], fwd["U"], fwd["Y"], w.t)
+    assert tp.device_status() == 0
+    return mi, fwd, bwd
+
+
+MLP_CASES = {
+    # name: (T, h, f, t)
+    "tiny_shape_bf16": (32, 64, 256, 2),
+    "ragged": (333, 200, 384, 2),
+    "multi_tile": (640, 512, 1024, 4),
+    "one_token": (1, 64, 128, 2),
+}
+
+
+@pytest.mark.parametrize("case", list(MLP_CASES))
+def test_mlp_matches_oracle(case):
+    dev = gpu_or_skip()
+    T, h, f, t = MLP_CASES[case]
+    w = wl.custom(case, T=T, h=h, f=f, v_valid=0, v_pad=0, t=t)
+    mi, fwd, bwd = run_mlp(w, dev)
+    of = oracle.mlp_forward(mi["X"], mi["A"], mi["bA"], mi["B"], mi["bB"])
+    ob = oracle.mlp_backward(mi["X"], mi["A"], mi["bA"], mi["B"], mi["dZ"])
+    for k in ("U", "Y", "Z"):
+        assert_rel(k, fwd[k], of[k])
+    for k in ("dX", "dA", "dB", "dbA", "dbB"):
+        assert_rel(k, bwd[k], ob[k])
+
+
+def test_mlp_shard_count_does_not_change_results():
+    # Z = sum_i Y_i B_i equals the unsharded product for every t; on one GPU the
+    # shards are tile coordinates, so the results agree bit for bit.
+    dev = gpu_or_skip()
+    base = None
+    for t in (1, 2, 4, 8, 16):
+        w = wl.custom(f"t{t}", T=512, h=256, f=1024, v_valid=0, v_pad=0, t=t)
+        mi, fwd, bwd = run_mlp(w, dev)
+        cur = {**{k: fwd[k].cpu() for k in ("Z", "Y")}, **{k: v.cpu() for k, v in bwd.items()}}
+        if base is None:
+            base = cur
+            of = oracle.mlp_forward(mi["X"], mi["A"], mi["bA"], mi["B"], mi["bB"])
+            ob = oracle.mlp_backward(mi["X"], mi["A"], mi["bA"], mi["B"], mi["dZ"])
+            assert_rel("Z", fwd["Z"], of["Z"])
+            assert_rel("dX", bwd["dX"], ob["dX"])
+        else:
+            for k in base:
+                assert torch.equal(base[k], cur[k]), f"t={t}: {k} differs from t=1"
+
+
+CE_CASES = {
+    # name: (T, h, v_pad, v_valid, t)
+    "tiny_shape_bf16": (32, 64, 512, 512, 2),
+    "ragged_bn128": (333, 200, 768, 700, 2),          # shard = 384 ids: 128-wide tiles
+    "padded_shards": (130, 96, 2048, 1800, 16),       # shard 15 holds only padding
+    "single_shard": (257, 128, 1024, 1000, 1),        # t = 1: the unsharded loss
+    "multi_tile": (600, 320, 4096, 4000, 4),
+}
+
+
+@pytest.mark.parametrize("case", list(CE_CASES))
+def test_ce_matches_oracle(case):
+    dev = gpu_or_skip()
+    T, h, v_pad, v_valid, t = CE_CASES[case]
+    assert tp.pad_vocab(v_valid, t) <= v_pad
+    w = wl.custom(case, T=T, h=h, f=0, v_valid=v_valid, v_pad=v_pad, t=t)
+    ci = wl.ce_inputs(w, seed=0)
+    ci["targets"][0] = 0
+    ci["targets"][-1] = v_valid - 1
+    g = {k: v.to(dev) for k, v in ci.items()}
+    gs = 1.0 / T
+    out = tp.vocab_parallel_ce(g["H"], g["E"], g["targets"], v_valid, t, grad_scale=gs)
+    assert tp.device_status() == 0
+    ref = oracle.ce(ci["H"], ci["E"], ci["targets"].numpy(), v_valid, grad_scale=gs)
+    assert_loss("loss", out["loss"], ref["loss"])
+    assert_loss("lse", out["lse"], ref["lse"])
+    assert_rel("dH", out["dH"], ref["dH"])
+    assert_rel("dE", out["dE"], ref["dE"])
+    # padded vocabulary rows get exactly zero gradient
+    assert torch.count_nonzero(out["dE"][v_valid:]).item() == 0
+    # the sharded statistics restatement of the oracle agrees with the loss too
+    sh = oracle.ce_sharded(ci["H"], ci["E"], ci["targets"].numpy(), v_valid, t)
+    assert_loss("loss vs sharded oracle", out["loss"], sh["loss"])
+
+
+def test_ce_forward_only_and_single_gradients():
+    dev = gpu_or_skip()
+    T, h, v_pad, v_valid, t = 200, 128, 1024, 1000, 4
+    w = wl.custom("fo", T=T, h=h, f=0, v_valid=v_valid, v_pad=v_pad, t=t)
+    ci = wl.ce_inputs(w, seed=3)
+    g = {k: v.to(dev) for k, v in ci.items()}
+    ref = oracle.ce(ci["H"], ci["E"], ci["targets"].numpy(), v_valid, grad_scale=1.0)
+    fo = tp.vocab_parallel_ce(g["H"], g["E"], g["targets"], v_valid, t, grads=False)
+    assert "dH" not in fo and "dE" not in fo
+    assert_loss("loss", fo["loss"], ref["loss"])
+    only_dh = tp.vocab_parallel_ce(g["H"], g["E"], g["targets"], v_valid, t, want_dE=False)
+    assert_rel("dH", only_dh["dH"], ref["dH"])
+    only_de = tp.vocab_parallel_ce(g["H"], g["E"], g["targets"], v_valid, t, want_dH=False)
+    assert_rel("dE", only_de["dE"], ref["dE"])
+    assert tp.device_status() == 0
+
+
+def test_ce_closed_form_zero_embedding():
+    # E = 0 on the real ids: loss = ln(v_valid) for every token, dH = 0
+    dev = gpu_or_skip()
+    T, h, v_pad, v_valid, t = 256, 64, 2048, 2000, 8
+    H = torch.randn(T, h).to(torch.bfloat16).to(dev)
+    E = torch.zeros(v_pad, h, dtype=torch.bfloat16, device=dev)
+    E[v_valid:] = 3.0  # padded rows must not enter
+    y = torch.randint(0, v_valid, (T,), dtype=torch.int32, device=dev)
+    out = tp.vocab_parallel_ce(H, E, y, v_valid, t)
+    assert tp.device_status() == 0
+    assert_loss("loss", out["loss"], np.full(T, np.log(v_valid)))
+    assert torch.count_nonzero(out["dH"]).item() == 0
+
+
+def test_empty_token_batch():
+    dev = gpu_or_skip()
+    h, f, t = 64, 256, 2
+    X = torch.empty(0, h, dtype=torch.bfloat16, device=dev)
+    A = torch.randn(h, f, device=dev).to(torch.bfloat16)
+    B = torch.randn(f, h, device=dev).to(torch.bfloat16)
+    fwd = tp.tp_mlp_forward(X, A, B, t)
+    assert fwd["Z"].shape == (0, h)
+    bwd = tp.tp_mlp_backward(X, X, A, B, fwd["U"], fwd["Y"], t)
+    assert torch.count_nonzero(bwd["dA"]).item() == 0 and torch.count_nonzero(bwd["dB"]).item() == 0
+    assert torch.count_nonzero(bwd["dbA"]).item() == 0
+    E = torch.randn(512, h, device=dev).to(torch.bfloat16)
+    ce = tp.vocab_parallel_ce(X, E, torch.empty(0, dtype=torch.int32, device=dev), 500, 2)
+    assert ce["loss"].numel() == 0 and torch.count_nonzero(ce["dE"]).item() == 0
+    assert tp.device_status() == 0
+
+
+def test_out_of_range_target_is_reported():
+    dev = gpu_or_skip()
+    T, h, v_pad, v_valid, t = 64, 64, 512, 500, 2
+    H = torch.randn(T, h, device=dev).to(torch.bfloat16)
+    E = torch.randn(v_pad, h, device=dev).to(torch.bfloat16)
+    y = torch.randint(0, v_valid, (T,), dtype=torch.int32, device=dev)
+    y[5] = v_valid  # a padded id is not a valid target
+    out = tp.vocab_parallel_ce(H, E, y, v_valid, t, grads=False)
+    assert tp.device_status() == 1  # TPCE_ERR_INVALID, then cleared
+    loss = out["loss"].cpu()
+    assert torch.isnan(loss[5]) and torch.isfinite(loss[:5]).all()
+    assert tp.device_status() == 0

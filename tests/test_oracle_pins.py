@@ -141,6 +141,18 @@ def test_mlp_backward_matches_finite_differences():
         assert np.abs(fd - grads[name]).max() < 1e-7 * scale, name
 
 
+def test_bias_grad_is_token_sum():
+    # dbB of the block equals the column sums of dZ: with B = 0 the loss
+    # sum(dZ * Z) is sum(dZ * bB), whose gradient in bB is sum_t dZ
+    T, h, f = 6, 5, 4
+    r = rng(16)
+    dZ = r.standard_normal((T, h))
+    g = oracle.mlp_backward(r.standard_normal((T, h)), r.standard_normal((h, f)), None,
+                            np.zeros((f, h)), dZ)
+    np.testing.assert_allclose(oracle.bias_grad(dZ), g["dbB"], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(oracle.bias_grad(np.ones((T, h))), np.full(h, float(T)), atol=0)
+
+
 def test_mlp_backward_cols_match_full_backward():
     T, h, f = 5, 6, 10
     r = rng(5)

@@ -1,0 +1,14 @@
+"""vocab_ce_gb300 -- Megatron-style 1D tensor-parallel MLP block and
+vocabulary-parallel fused cross-entropy, all t shards on one GB300 (sm_103a).
+
+The compute lives in the CUDA library ``lib/libtpce.so`` (C ABI in
+``include/tpce.h``); this package only marshals torch tensors to it.
+"""
+
+from .api import (TpceError, ce_workspace_bytes, device_status, device_status_detail,
+                  mlp_workspace_bytes, pad_vocab, profile_enable, profile_read, tp_mlp_backward,
+                  tp_mlp_forward, vocab_parallel_ce)
+
+__all__ = ["TpceError", "ce_workspace_bytes", "device_status", "device_status_detail",
+           "mlp_workspace_bytes", "pad_vocab", "profile_enable", "profile_read", "tp_mlp_backward",
+           "tp_mlp_forward", "vocab_parallel_ce"]

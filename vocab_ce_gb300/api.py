@@ -1,0 +1,189 @@
+"""Python face of libtpce: the same calls as the C ABI, on torch tensors.
+
+Only argument marshalling happens here (checking devices and dtypes,
+allocating outputs and workspace with torch, passing raw pointers and the
+current CUDA stream). Every arithmetic step runs in the library's kernels.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Dict, Optional
+
+import torch
+
+from ._lib import TPCE_BF16, TPCE_F32, TpceError, check, lib
+
+_DT = {torch.bfloat16: TPCE_BF16, torch.float32: TPCE_F32}
+
+
+def _ptr(x: Optional[torch.Tensor]):
+    return None if x is None else ctypes.c_void_p(x.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(x: torch.Tensor, name: str, dtype=None, shape=None):
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (row-major)")
+    if dtype is not None and x.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {x.dtype}")
+    if shape is not None and tuple(x.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(x.shape)}")
+
+
+def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]) -> Optional[torch.Tensor]:
+    if nbytes == 0:
+        return ws
+    if ws is not None and ws.numel() * ws.element_size() >= nbytes:
+        return ws
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def pad_vocab(v: int, t: int, divisor: int = 128) -> int:
+    """Smallest multiple of divisor * t that is >= v (Megatron's vocabulary padding)."""
+    r = lib().tpce_pad_vocab(v, t, divisor)
+    if r < 0:
+        raise ValueError("pad_vocab: v >= 0, t >= 1 and divisor >= 1 required")
+    return int(r)
+
+
+def mlp_workspace_bytes(T: int, h: int, f: int, t: int, dtype=torch.bfloat16) -> int:
+    return int(lib().tpce_mlp_workspace_bytes(T, h, f, t, _DT[dtype]))
+
+
+def ce_workspace_bytes(T: int, h: int, v_pad: int, t: int, grads: bool = True, dtype=torch.bfloat16) -> int:
+    return int(lib().tpce_ce_workspace_bytes(T, h, v_pad, t, _DT[dtype], 1 if grads else 0))
+
+
+def tp_mlp_forward(X: torch.Tensor, A: torch.Tensor, B: torch.Tensor, t: int,
+                   bA: Optional[torch.Tensor] = None, bB: Optional[torch.Tensor] = None,
+                   out: Optional[Dict[str, torch.Tensor]] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """Z = sum_i GeLU(X A_i + bA_i) B_i + bB over t shards; returns Z, U, Y."""
+    T, h = X.shape
+    f = A.shape[1]
+    dt = X.dtype
+    for name, x, shp in (("X", X, (T, h)), ("A", A, (h, f)), ("B", B, (f, h))):
+        _need(x, name, dt, shp)
+    for name, b, n in (("bA", bA, f), ("bB", bB, h)):
+        if b is not None:
+            _need(b, name, torch.float32, (n,))
+    out = dict(out or {})
+    Z = out.get("Z") if out.get("Z") is not None else torch.empty((T, h), dtype=dt, device=X.device)
+    U = out.get("U") if out.get("U") is not None else torch.empty((T, f), dtype=dt, device=X.device)
+    Y = out.get("Y") if out.get("Y") is not None else torch.empty((T, f), dtype=dt, device=X.device)
+    st = lib().tp_mlp_forward(_ptr(X), _ptr(A), _ptr(bA), _ptr(B), _ptr(bB), T, h, f, t, _DT[dt],
+                              _ptr(Z), _ptr(U), _ptr(Y), None, 0, _stream(stream))
+    check(st, "tp_mlp_forward")
+    return {"Z": Z, "U": U, "Y": Y}
+
+
+def tp_mlp_backward(dZ: torch.Tensor, X: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                    U: torch.Tensor, Y: torch.Tensor, t: int, bias_grads: bool = True,
+                    out: Optional[Dict[str, torch.Tensor]] = None, ws: Optional[torch.Tensor] = None,
+                    stream=None) -> Dict[str, torch.Tensor]:
+    """dX (f* sum over shards), dA, dB and optionally dbA, dbB."""
+    T, h = X.shape
+    f = A.shape[1]
+    dt = X.dtype
+    for name, x, shp in (("dZ", dZ, (T, h)), ("X", X, (T, h)), ("A", A, (h, f)), ("B", B, (f, h)),
+                         ("U", U, (T, f)), ("Y", Y, (T, f))):
+        _need(x, name, dt, shp)
+    out = dict(out or {})
+    dev = X.device
+
+    def get(k, shp, d):
+        return out.get(k) if out.get(k) is not None else torch.empty(shp, dtype=d, device=dev)
+
+    dX, dA, dB = get("dX", (T, h), dt), get("dA", (h, f), dt), get("dB", (f, h), dt)
+    dbA = get("dbA", (f,), torch.float32) if bias_grads else None
+    dbB = get("dbB", (h,), torch.float32) if bias_grads else None
+    nbytes = mlp_workspace_bytes(T, h, f, t, dt) if T > 0 else 0
+    w = _workspace(nbytes, dev, ws)
+    st = lib().tp_mlp_backward(_ptr(dZ), _ptr(X), _ptr(A), _ptr(B), _ptr(U), _ptr(Y), T, h, f, t, _DT[dt],
+                               _ptr(dX), _ptr(dA), _ptr(dbA), _ptr(dB), _ptr(dbB), _ptr(w),
+                               0 if w is None else w.numel() * w.element_size(), _stream(stream))
+    check(st, "tp_mlp_backward")
+    res = {"dX": dX, "dA": dA, "dB": dB}
+    if bias_grads:
+        res.update(dbA=dbA, dbB=dbB)
+    return res
+
+
+def vocab_parallel_ce(H: torch.Tensor, E: torch.Tensor, targets: torch.Tensor, v_valid: int, t: int,
+                      grad_scale: float = 1.0, grads: bool = True, want_dH: bool = True, want_dE: bool = True,
+                      out: Optional[Dict[str, torch.Tensor]] = None, ws: Optional[torch.Tensor] = None,
+                      stream=None) -> Dict[str, torch.Tensor]:
+    """Per-token loss and lse; with grads, dH and dE of grad_scale * sum(loss)."""
+    T, h = H.shape
+    v_pad = E.shape[0]
+    dt = H.dtype
+    _need(H, "H", dt, (T, h))
+    _need(E, "E", dt, (v_pad, h))
+    _need(targets, "targets", torch.int32, (T,))
+    out = dict(out or {})
+    dev = H.device
+    loss = out.get("loss") if out.get("loss") is not None else torch.empty(T, dtype=torch.float32, device=dev)
+    lse = out.get("lse") if out.get("lse") is not None else torch.empty(T, dtype=torch.float32, device=dev)
+    dH = dE = None
+    if grads and want_dH:
+        dH = out.get("dH") if out.get("dH") is not None else torch.empty((T, h), dtype=dt, device=dev)
+    if grads and want_dE:
+        dE = out.get("dE") if out.get("dE") is not None else torch.empty((v_pad, h), dtype=dt, device=dev)
+    with_g = dH is not None or dE is not None
+    nbytes = ce_workspace_bytes(T, h, v_pad, t, with_g, dt) if T > 0 else 0
+    w = _workspace(nbytes, dev, ws)
+    st = lib().vocab_parallel_ce(_ptr(H), _ptr(E), _ptr(targets), T, h, v_pad, v_valid, t, float(grad_scale),
+                                 _DT[dt], _ptr(loss), _ptr(lse), _ptr(dH), _ptr(dE), _ptr(w),
+                                 0 if w is None else w.numel() * w.element_size(), _stream(stream))
+    check(st, "vocab_parallel_ce")
+    res = {"loss": loss, "lse": lse}
+    if dH is not None:
+        res["dH"] = dH
+    if dE is not None:
+        res["dE"] = dE
+    return res
+
+
+def device_status(clear: bool = True, stream=None) -> int:
+    """Synchronise and return the device status word's code (0 = OK)."""
+    detail = ctypes.c_uint32(0)
+    return int(lib().tpce_device_status(_stream(stream), 1 if clear else 0, ctypes.byref(detail)))
+
+
+def device_status_detail(clear: bool = True, stream=None):
+    detail = ctypes.c_uint32(0)
+    code = int(lib().tpce_device_status(_stream(stream), 1 if clear else 0, ctypes.byref(detail)))
+    return code, int(detail.value)
+
+
+def profile_enable(on: bool = True) -> None:
+    check(lib().tpce_profile_enable(1 if on else 0), "tpce_profile_enable")
+
+
+def profile_read() -> Dict[str, Dict[str, float]]:
+    """Per-kernel launches and total ms recorded since profile_enable(True)."""
+    L = lib()
+    n = L.tpce_profile_count()
+    if n < 0:
+        raise TpceError(5, "tpce_profile_count")
+    res = {}
+    for i in range(n):
+        name = ctypes.c_char_p()
+        launches = ctypes.c_int64()
+        ms = ctypes.c_double()
+        check(L.tpce_profile_get(i, ctypes.byref(name), ctypes.byref(launches), ctypes.byref(ms)),
+              "tpce_profile_get")
+        res[name.value.decode()] = {"launches": int(launches.value), "ms": float(ms.value)}
+    return res
+
+
+__all__ = ["TpceError", "pad_vocab", "mlp_workspace_bytes", "ce_workspace_bytes", "tp_mlp_forward",
+           "tp_mlp_backward", "vocab_parallel_ce", "device_status", "device_status_detail",
+           "profile_enable", "profile_read"]

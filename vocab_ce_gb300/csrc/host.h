@@ -1,0 +1,63 @@
+// host.h -- host-side pieces shared by the translation units of libtpce:
+// device status word, SM count, kernel timing, TMA tensor maps, validation
+// helpers and the column-sum kernels used for the bias gradients.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "tpce.h"
+
+namespace tpce {
+
+// address of the device status word on the current device (null on failure)
+uint32_t *device_error_word();
+// number of SMs of the current device (0 on failure)
+int num_sms();
+
+// RAII kernel timer: when profiling is on, records an event pair around the
+// launches made during its lifetime on `stream` and files them under `name`.
+class KernelTimer {
+   public:
+    KernelTimer(const char *name, cudaStream_t stream);
+    ~KernelTimer();
+    KernelTimer(const KernelTimer &) = delete;
+    KernelTimer &operator=(const KernelTimer &) = delete;
+
+   private:
+    const char *name_;
+    cudaStream_t stream_;
+    cudaEvent_t start_ = nullptr;
+};
+
+// 2-D bf16 tensor map with 128-byte swizzle: `inner` contiguous elements per
+// row (row pitch `ld` elements), `outer` rows, box {box_inner, box_outer}.
+bool make_tmap_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t ld,
+                    uint32_t box_inner, uint32_t box_outer);
+
+// fp32 column sums out[n] = sum_r X[r, n] of a bf16 [R, N] matrix (row pitch
+// ld), through a partial buffer of colsum_partial_floats(R, N) floats.
+size_t colsum_partial_floats(int64_t R, int64_t N);
+tpce_status colsum_bf16(const void *X, int64_t R, int64_t N, int64_t ld, float *out, float *partial,
+                        cudaStream_t s);
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline tpce_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TPCE_OK : TPCE_ERR_CUDA; }
+
+// Record a description of a failure for tpce_last_error() (per host thread)
+// and return `st`.
+tpce_status fail(tpce_status st, const char *fmt, ...);
+tpce_status fail_cuda(cudaError_t e, const char *what);
+// cudaGetLastError after a launch, recorded under the kernel's name
+tpce_status check_launch(const char *name);
+// when the environment sets TPCE_SYNC_CHECK=1, every launch is followed by a
+// stream synchronisation so that a failing kernel is named by check_launch
+bool sync_check_enabled();
+
+}  // namespace tpce

@@ -1,0 +1,349 @@
+// runtime.cu -- status codes, the vocabulary padding rule, the device status
+// word, kernel timing, TMA tensor-map encoding, SM count, and the column-sum
+// kernels for the bias gradients.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "host.h"
+
+namespace tpce {
+
+// ------------------------------------------------------------------ status word
+// First device-side failure of any kernel of this library on this device.
+__device__ uint32_t g_error_word;
+
+uint32_t *device_error_word() {
+    static std::mutex mu;
+    static uint32_t *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> g(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<uint32_t *>(p);
+    }
+    return addr[dev];
+}
+
+int num_sms() {
+    static std::mutex mu;
+    static int count[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> g(mu);
+    if (!count[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        count[dev] = n;
+    }
+    return count[dev];
+}
+
+// ------------------------------------------------------------------ error text
+namespace {
+thread_local char g_last_error[512] = "";
+}
+
+tpce_status fail(tpce_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+tpce_status fail_cuda(cudaError_t e, const char *what) {
+    return fail(TPCE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool sync_check_enabled() {
+    static int on = -1;
+    if (on < 0) {
+        const char *v = getenv("TPCE_SYNC_CHECK");
+        on = (v && v[0] == '1') ? 1 : 0;
+    }
+    return on == 1;
+}
+
+tpce_status check_launch(const char *name) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e, name);
+    if (sync_check_enabled()) {
+        e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return fail_cuda(e, name);
+    }
+    return TPCE_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool make_tmap_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t ld,
+                    uint32_t box_inner, uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (!fn || inner == 0 || outer == 0 || !aligned16(base) || (ld * 2) % 16 != 0) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ profiling
+namespace {
+struct Rec {
+    const char *name;
+    int dev;
+    cudaEvent_t a, b;
+};
+struct Agg {
+    const char *name;
+    int64_t launches;
+    double ms;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<Rec> g_recs;
+std::vector<Agg> g_agg;
+std::map<int, std::vector<cudaEvent_t>> g_pool;
+
+cudaEvent_t take_event(int dev) {
+    auto &v = g_pool[dev];
+    if (!v.empty()) {
+        cudaEvent_t e = v.back();
+        v.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+void release_records() {
+    for (auto &r : g_recs) {
+        if (r.a) g_pool[r.dev].push_back(r.a);
+        if (r.b) g_pool[r.dev].push_back(r.b);
+    }
+    g_recs.clear();
+}
+}  // namespace
+
+KernelTimer::KernelTimer(const char *name, cudaStream_t stream) : name_(name), stream_(stream) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    if (!g_prof_on) return;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    start_ = take_event(dev);
+    if (start_ && cudaEventRecord(start_, stream_) != cudaSuccess) {
+        g_pool[dev].push_back(start_);
+        start_ = nullptr;
+    }
+}
+
+KernelTimer::~KernelTimer() {
+    if (!start_) return;
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaEvent_t end = take_event(dev);
+    if (!end || cudaEventRecord(end, stream_) != cudaSuccess) {
+        g_pool[dev].push_back(start_);
+        if (end) g_pool[dev].push_back(end);
+        return;
+    }
+    g_recs.push_back({name_, dev, start_, end});
+}
+
+// ------------------------------------------------------------------ column sums
+// Stage 1: block (x, y) sums rows [y*rows_per, (y+1)*rows_per) of 256 columns
+// starting at 256*x; each lane owns 8 adjacent columns (one 16-byte load per
+// row), the 8 warps stride over the rows, and shared memory combines the warps.
+__global__ void __launch_bounds__(256) colsum_stage1(const __nv_bfloat16 *__restrict__ X, int64_t R, int64_t N,
+                                                     int64_t ld, int64_t rows_per, float *__restrict__ part) {
+    __shared__ float red[8][256];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 256 + lane * 8;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * rows_per;
+    const int64_t r1 = min(R, r0 + rows_per);
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (c0 < N) {
+        for (int64_t r = r0 + warp; r < r1; r += 8) {
+            uint4 u = __ldg(reinterpret_cast<const uint4 *>(X + r * ld + c0));
+            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float2 f = __bfloat1622float2(h[i]);
+                acc[2 * i] += f.x;
+                acc[2 * i + 1] += f.y;
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) red[warp][lane * 8 + i] = acc[i];
+    __syncthreads();
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+    if (c < N) {
+        float s = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) s += red[w][threadIdx.x];
+        part[static_cast<int64_t>(blockIdx.y) * N + c] = s;
+    }
+}
+
+// Stage 2: out[c] = sum over the S partial rows.
+__global__ void colsum_stage2(const float *__restrict__ part, int S, int64_t N, float *__restrict__ out) {
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (c >= N) return;
+    float s = 0.0f;
+    for (int i = 0; i < S; ++i) s += part[static_cast<int64_t>(i) * N + c];
+    out[c] = s;
+}
+
+static int colsum_splits(int64_t R, int64_t N) {
+    const int64_t col_blocks = (N + 255) / 256;
+    int64_t S = (2 * 152 + col_blocks - 1) / col_blocks;
+    S = std::max<int64_t>(1, std::min<int64_t>(S, 64));
+    S = std::min<int64_t>(S, std::max<int64_t>(1, R));
+    return static_cast<int>(S);
+}
+
+size_t colsum_partial_floats(int64_t R, int64_t N) { return static_cast<size_t>(colsum_splits(R, N)) * N; }
+
+tpce_status colsum_bf16(const void *X, int64_t R, int64_t N, int64_t ld, float *out, float *partial,
+                        cudaStream_t s) {
+    if (N <= 0) return TPCE_OK;
+    if (R <= 0) return cuda_status(cudaMemsetAsync(out, 0, sizeof(float) * N, s));
+    const int S = colsum_splits(R, N);
+    const int64_t rows_per = (R + S - 1) / S;
+    {
+        KernelTimer t("colsum_stage1", s);
+        dim3 grid(static_cast<unsigned>((N + 255) / 256), static_cast<unsigned>(S));
+        colsum_stage1<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(X), R, N, ld, rows_per, partial);
+        if (check_launch("colsum_stage1") != TPCE_OK) return TPCE_ERR_CUDA;
+    }
+    {
+        KernelTimer t("colsum_stage2", s);
+        colsum_stage2<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(partial, S, N, out);
+        if (check_launch("colsum_stage2") != TPCE_OK) return TPCE_ERR_CUDA;
+    }
+    return TPCE_OK;
+}
+
+}  // namespace tpce
+
+// ====================================================================== C ABI
+using namespace tpce;
+
+extern "C" const char *tpce_status_string(tpce_status s) {
+    switch (s) {
+        case TPCE_OK: return "TPCE_OK";
+        case TPCE_ERR_INVALID: return "TPCE_ERR_INVALID";
+        case TPCE_ERR_SHAPE: return "TPCE_ERR_SHAPE";
+        case TPCE_ERR_ALIGN: return "TPCE_ERR_ALIGN";
+        case TPCE_ERR_WORKSPACE: return "TPCE_ERR_WORKSPACE";
+        case TPCE_ERR_CUDA: return "TPCE_ERR_CUDA";
+        case TPCE_ERR_TIMEOUT: return "TPCE_ERR_TIMEOUT";
+        case TPCE_ERR_UNSUPPORTED: return "TPCE_ERR_UNSUPPORTED";
+    }
+    return "TPCE_ERR_UNKNOWN";
+}
+
+extern "C" int tpce_version(void) { return 100; }
+
+extern "C" const char *tpce_last_error(void) { return g_last_error; }
+
+extern "C" int64_t tpce_pad_vocab(int64_t v, int t, int divisor) {
+    if (v < 0 || t < 1 || divisor < 1) return -1;
+    const int64_t m = static_cast<int64_t>(divisor) * t;
+    return (v + m - 1) / m * m;
+}
+
+extern "C" tpce_status tpce_device_status(void *stream, int clear, uint32_t *detail) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TPCE_ERR_CUDA;
+    uint32_t *w = device_error_word();
+    if (!w) return TPCE_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return TPCE_ERR_CUDA;
+    if (clear && cudaMemset(w, 0, sizeof(uint32_t)) != cudaSuccess) return TPCE_ERR_CUDA;
+    if (detail) *detail = v;
+    const uint32_t code = v & 0xffu;
+    return code <= TPCE_ERR_UNSUPPORTED ? static_cast<tpce_status>(code) : TPCE_ERR_INVALID;
+}
+
+extern "C" tpce_status tpce_profile_enable(int on) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    release_records();
+    g_agg.clear();
+    g_prof_on = on != 0;
+    return TPCE_OK;
+}
+
+extern "C" int tpce_profile_count(void) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    std::vector<Agg> agg;
+    int bad = 0;
+    for (auto &r : g_recs) {
+        float ms = 0.0f;
+        if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) {
+            ++bad;
+            continue;
+        }
+        auto it = std::find_if(agg.begin(), agg.end(),
+                               [&](const Agg &x) { return std::string(x.name) == std::string(r.name); });
+        if (it == agg.end())
+            agg.push_back({r.name, 1, ms});
+        else {
+            it->launches += 1;
+            it->ms += ms;
+        }
+    }
+    release_records();
+    // keep aggregating across calls until the next tpce_profile_enable
+    for (auto &a : agg) {
+        auto it = std::find_if(g_agg.begin(), g_agg.end(),
+                               [&](const Agg &x) { return std::string(x.name) == std::string(a.name); });
+        if (it == g_agg.end())
+            g_agg.push_back(a);
+        else {
+            it->launches += a.launches;
+            it->ms += a.ms;
+        }
+    }
+    return bad ? -1 : static_cast<int>(g_agg.size());
+}
+
+extern "C" tpce_status tpce_profile_get(int i, const char **name, int64_t *launches, double *total_ms) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    if (i < 0 || i >= static_cast<int>(g_agg.size())) return TPCE_ERR_INVALID;
+    if (name) *name = g_agg[i].name;
+    if (launches) *launches = g_agg[i].launches;
+    if (total_ms) *total_ms = g_agg[i].ms;
+    return TPCE_OK;
+}
