@@ -46,7 +46,7 @@ UNIT = "TFLOP/s"
 # fallbacks only if the generated MEASURED_PEAKS.json is absent
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # tokens the CPU oracle processes per timed sample
-CPU_SAMPLE_TOKENS = {"gpt8b": 64, "mlp70b": 16, "ce128k": 8, "sweep": 64}
+CPU_SAMPLE_TOKENS = {"gpt8b": 512, "mlp70b": 192, "ce128k": 96, "sweep": 512}
 REF_STEP_TOKENS = {"gpt8b": 8, "mlp70b": 4, "ce128k": 2, "sweep": 8}
 
 
