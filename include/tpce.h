@@ -183,6 +183,36 @@ tpce_status vocab_parallel_ce(const void *H, const void *E, const int32_t *targe
                               void *ws, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * vocab_parallel_ce_loss_static -- the forward of vocab_parallel_ce (loss and
+ * optionally lse, no gradients) that allocates nothing and needs no
+ * workspace. The pages have no counterpart to this call; it exists for
+ * callers that cannot call cudaMalloc, such as a plugin inside a host
+ * framework whose memory planner owns every device buffer and forbids
+ * allocations it did not plan, or a latency-critical path that must not risk
+ * the implicit device synchronisation of an allocation.
+ * The caller passes inputs and outputs exactly as for vocab_parallel_ce with
+ * dH = dE = NULL. The per-tile statistics live instead in a static device
+ * array of TPCE_CE_STATIC_SCRATCH_BYTES bytes inside the library, which every
+ * GPU that loads the library holds until the process exits. It must hold
+ * n_tiles * T * 8 bytes plus T * 4 (plus another T * 4 when lse is NULL),
+ * rounded up to 256 each, where n_tiles = v_pad / 256 when (v_pad / t) is a
+ * multiple of 256 and v_pad / 128 otherwise; larger requests return
+ * TPCE_ERR_WORKSPACE with the sizes in tpce_last_error(), before any launch.
+ * The first call on a device, with that device current, looks up the array's
+ * device address (cudaGetSymbolAddress) and caches it; make that first call
+ * before any stream capture. All calls share the one array and it keeps the
+ * last call's contents (nothing in it needs clearing: a call writes every
+ * entry it reads); calls whose kernels overlap on the GPU race on it, so
+ * order them on one stream or with events.
+ * Errors as vocab_parallel_ce.
+ * ------------------------------------------------------------------------- */
+#define TPCE_CE_STATIC_SCRATCH_BYTES (16u << 20)
+
+tpce_status vocab_parallel_ce_loss_static(const void *H, const void *E, const int32_t *targets,
+                                          int64_t T, int64_t h, int64_t v_pad, int64_t v_valid,
+                                          int t, int dtype, float *loss, float *lse, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Device status word. Kernels record the first device-side failure (a
  * TPCE_ERR_* code in the low 8 bits, detail above) instead of trapping.
  * tpce_device_status synchronises `stream`, reads the word of the current

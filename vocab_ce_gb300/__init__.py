@@ -7,8 +7,8 @@ The compute lives in the CUDA library ``lib/libtpce.so`` (C ABI in
 
 from .api import (TpceError, ce_workspace_bytes, device_status, device_status_detail,
                   mlp_workspace_bytes, pad_vocab, profile_enable, profile_read, tp_mlp_backward,
-                  tp_mlp_forward, vocab_parallel_ce)
+                  tp_mlp_forward, vocab_parallel_ce, vocab_parallel_ce_loss_static)
 
 __all__ = ["TpceError", "ce_workspace_bytes", "device_status", "device_status_detail",
            "mlp_workspace_bytes", "pad_vocab", "profile_enable", "profile_read", "tp_mlp_backward",
-           "tp_mlp_forward", "vocab_parallel_ce"]
+           "tp_mlp_forward", "vocab_parallel_ce", "vocab_parallel_ce_loss_static"]

@@ -151,6 +151,33 @@ def vocab_parallel_ce(H: torch.Tensor, E: torch.Tensor, targets: torch.Tensor, v
     return res
 
 
+CE_STATIC_SCRATCH_BYTES = 16 << 20  # TPCE_CE_STATIC_SCRATCH_BYTES in include/tpce.h
+
+
+def vocab_parallel_ce_loss_static(H: torch.Tensor, E: torch.Tensor, targets: torch.Tensor, v_valid: int, t: int,
+                                  loss: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                                  stream=None) -> Dict[str, torch.Tensor]:
+    """Forward-only fused CE into caller-provided loss (and lse) buffers, with
+    the library's static device scratch instead of a workspace: for callers
+    that cannot allocate device memory. Nothing is allocated here either."""
+    T, h = H.shape
+    v_pad = E.shape[0]
+    dt = H.dtype
+    _need(H, "H", dt, (T, h))
+    _need(E, "E", dt, (v_pad, h))
+    _need(targets, "targets", torch.int32, (T,))
+    _need(loss, "loss", torch.float32, (T,))
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (T,))
+    st = lib().vocab_parallel_ce_loss_static(_ptr(H), _ptr(E), _ptr(targets), T, h, v_pad, v_valid, t, _DT[dt],
+                                             _ptr(loss), _ptr(lse), _stream(stream))
+    check(st, "vocab_parallel_ce_loss_static")
+    res = {"loss": loss}
+    if lse is not None:
+        res["lse"] = lse
+    return res
+
+
 def device_status(clear: bool = True, stream=None) -> int:
     """Synchronise and return the device status word's code (0 = OK)."""
     detail = ctypes.c_uint32(0)
@@ -185,5 +212,5 @@ def profile_read() -> Dict[str, Dict[str, float]]:
 
 
 __all__ = ["TpceError", "pad_vocab", "mlp_workspace_bytes", "ce_workspace_bytes", "tp_mlp_forward",
-           "tp_mlp_backward", "vocab_parallel_ce", "device_status", "device_status_detail",
+           "tp_mlp_backward", "vocab_parallel_ce", "vocab_parallel_ce_loss_static", "device_status", "device_status_detail",
            "profile_enable", "profile_read"]

@@ -1,0 +1,109 @@
+// ce_static.cu -- vocab_parallel_ce_loss_static: the forward of the fused
+// vocabulary-parallel cross-entropy (loss and lse, no gradients) with its
+// scratch in a static device array instead of a caller-provided workspace.
+//
+// Who needs it: a caller that cannot call cudaMalloc -- for instance a plugin
+// running inside a host framework whose memory planner owns every device
+// buffer and forbids allocations it did not plan, or a latency-critical path
+// that must not risk the implicit device synchronisation a cudaMalloc may
+// perform. Such a caller still passes its inputs and outputs; everything
+// else the call needs lives in the static array below.
+//
+// The scratch is a file-scope __device__ array of TPCE_CE_STATIC_SCRATCH_BYTES
+// bytes: every GPU that loads this library holds it until the process exits.
+// Host code cannot use the array's name as a device address (on the host it
+// names a host-side stand-in), so the first call on each device, with that
+// device current, asks the runtime for the array's device address with
+// cudaGetSymbolAddress and caches it; that first call should therefore come
+// before any stream capture. All calls share the one array: two calls whose
+// kernels overlap on the GPU (different streams, no ordering) race on it.
+// Nothing in it needs clearing between calls: every statistic the combine
+// kernel reads is written earlier in the same call.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "ce_common.cuh"
+#include "gemm_launch.cuh"
+#include "host.h"
+
+namespace tpce {
+
+static __device__ __align__(256) unsigned char g_ce_static_scratch[TPCE_CE_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+// The array's device address on the current device, looked up once per device.
+tpce_status static_scratch_address(uint8_t **out) {
+    static std::mutex mu;
+    static void *addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "vocab_parallel_ce_loss_static: cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(TPCE_ERR_CUDA, "vocab_parallel_ce_loss_static: device %d out of range", dev);
+    std::lock_guard<std::mutex> g(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_ce_static_scratch);
+        if (e != cudaSuccess) return fail_cuda(e, "vocab_parallel_ce_loss_static: cudaGetSymbolAddress");
+        addr[dev] = p;
+    }
+    *out = static_cast<uint8_t *>(addr[dev]);
+    return TPCE_OK;
+}
+
+}  // namespace
+}  // namespace tpce
+
+using namespace tpce;
+
+extern "C" tpce_status vocab_parallel_ce_loss_static(const void *H, const void *E, const int32_t *targets, int64_t T,
+                                                     int64_t h, int64_t v_pad, int64_t v_valid, int t, int dtype,
+                                                     float *loss, float *lse, void *stream) {
+    tpce_status st = check_ce_shape(T, h, v_pad, v_valid, t, dtype);
+    if (st != TPCE_OK) return st;
+    if (T == 0) return TPCE_OK;
+    if (!H || !E || !targets || !loss) return TPCE_ERR_INVALID;
+    if (!aligned16(H) || !aligned16(E)) return TPCE_ERR_ALIGN;
+    for (const void *p : {static_cast<const void *>(targets), static_cast<const void *>(loss),
+                          static_cast<const void *>(lse)})
+        if (reinterpret_cast<uintptr_t>(p) & 3u) return TPCE_ERR_ALIGN;
+
+    // scratch layout: per-tile (max, sumexp) [n_tiles][T], target logit [T], lse [T] if not an output
+    const int64_t vs = v_pad / t;
+    const int bn = (vs % 256 == 0) ? 256 : 128;  // a tile never straddles two shards
+    const int64_t n_tiles = v_pad / bn;
+    const size_t stats_bytes = round_up(static_cast<size_t>(n_tiles) * T * sizeof(float2), 256);
+    const size_t tau_bytes = round_up(static_cast<size_t>(T) * sizeof(float), 256);
+    const size_t lse_bytes = lse ? 0 : tau_bytes;
+    const size_t need = stats_bytes + tau_bytes + lse_bytes;
+    if (need > TPCE_CE_STATIC_SCRATCH_BYTES)
+        return fail(TPCE_ERR_WORKSPACE,
+                    "vocab_parallel_ce_loss_static: T=%lld and %lld vocabulary tiles need %zu bytes of scratch; "
+                    "the static scratch holds %u",
+                    static_cast<long long>(T), static_cast<long long>(n_tiles), need,
+                    static_cast<unsigned>(TPCE_CE_STATIC_SCRATCH_BYTES));
+    uint8_t *base = nullptr;
+    st = static_scratch_address(&base);
+    if (st != TPCE_OK) return st;
+    float2 *stats = reinterpret_cast<float2 *>(base);
+    float *tau = reinterpret_cast<float *>(base + stats_bytes);
+    float *lse_buf = lse ? lse : reinterpret_cast<float *>(base + stats_bytes + tau_bytes);
+    uint32_t *err = device_error_word();
+    if (!err) return fail(TPCE_ERR_CUDA, "vocab_parallel_ce_loss_static: device status word");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int Ti = static_cast<int>(T), hi = static_cast<int>(h), vpi = static_cast<int>(v_pad);
+    const int vvi = static_cast<int>(v_valid);
+
+    Operand a{H, T, h, h};      // K-major [T, h]
+    Operand b{E, v_pad, h, h};  // K-major: N = v_pad rows, K = h columns
+    EpiCeStats::Params ep{stats, tau, targets, T, vvi, 0, 0};
+    st = bn == 256 ? launch_gemm<256, false, false, EpiCeStats>("ce_static_logits_stats", a, b, Ti, vpi, hi, 0, 0, 0,
+                                                                 0, ep, s, /*timed=*/false)
+                   : launch_gemm<128, false, false, EpiCeStats>("ce_static_logits_stats", a, b, Ti, vpi, hi, 0, 0, 0,
+                                                                 0, ep, s, /*timed=*/false);
+    if (st != TPCE_OK) return st;
+    ce_combine_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, s>>>(
+        stats, tau, targets, T, t, static_cast<int>(n_tiles / t), vvi, loss, lse_buf, err);
+    return check_launch("ce_static_combine");
+}

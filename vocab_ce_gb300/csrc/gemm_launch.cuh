@@ -47,7 +47,7 @@ inline tpce_status set_smem_attr(K kern, uint32_t bytes, bool (&done)[64], std::
 template <int BN, bool A_MN, bool B_MN, class Epi>
 tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, int M, int N, int K, int a_off_mn,
                         int a_off_k, int b_off_mn, int b_off_k, const typename Epi::Params &ep,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool timed = true) {
     using Cfg = TileCfg<BN>;
     if (M <= 0 || N <= 0 || K <= 0) return TPCE_ERR_SHAPE;
     CUtensorMap ta, tb;
@@ -80,7 +80,7 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, in
     if (sms <= 0 || err == nullptr) return fail(TPCE_ERR_CUDA, "device query failed (%s)", name);
     const int64_t tiles = static_cast<int64_t>(s.tiles_m) * s.tiles_n;
     const int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
-    KernelTimer timer(name, stream);
+    KernelTimer timer(timed ? name : nullptr, stream);
     kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(ta, tb, s, ep, err);
     return check_launch(name);
 }

@@ -20,6 +20,7 @@ int num_sms();
 
 // RAII kernel timer: when profiling is on, records an event pair around the
 // launches made during its lifetime on `stream` and files them under `name`.
+// A null name makes it inert.
 class KernelTimer {
    public:
     KernelTimer(const char *name, cudaStream_t stream);

@@ -156,6 +156,7 @@ void release_records() {
 }  // namespace
 
 KernelTimer::KernelTimer(const char *name, cudaStream_t stream) : name_(name), stream_(stream) {
+    if (!name_) return;  // an untimed launch
     std::lock_guard<std::mutex> g(g_prof_mu);
     if (!g_prof_on) return;
     int dev = 0;
