@@ -34,7 +34,10 @@
  *    B[i f/t : (i+1) f/t, :] and the row block E[i v_pad/t : (i+1) v_pad/t, :];
  *    the unsharded tensors are passed and t selects the partition.
  *  - dtype TPCE_BF16: X, A, B, Z, U, Y, dZ, dX, dA, dB, H, E, dH, dE are bf16,
- *    accumulation is fp32. Biases and bias gradients are always fp32.
+ *    accumulation is fp32. dtype TPCE_F32: the same tensors are fp32 and the
+ *    tensor cores read them as tf32 (10-bit mantissa), fp32 accumulate; this
+ *    path stages transposed copies of some operands in the workspace. Biases
+ *    and bias gradients are always fp32.
  *  - Every tensor pointer must be 16-byte aligned; h must be a multiple of 8.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream). Shape and alignment checks run on the host before any
@@ -57,7 +60,7 @@ extern "C" {
 
 typedef enum {
     TPCE_BF16 = 0,   /* bf16 tensors, fp32 accumulate */
-    TPCE_F32 = 1     /* fp32 tensors (not supported by this build: TPCE_ERR_UNSUPPORTED) */
+    TPCE_F32 = 1     /* fp32 tensors, multiplied as tf32 on the tensor cores, fp32 accumulate */
 } tpce_dtype;
 
 typedef enum {
@@ -107,6 +110,8 @@ int64_t tpce_pad_vocab(int64_t v, int t, int divisor);
  * accumulator for dH. Returns 0 for invalid shapes.
  * ------------------------------------------------------------------------- */
 size_t tpce_mlp_workspace_bytes(int64_t T, int64_t h, int64_t f, int t, int dtype);
+/* (the MLP query covers both calls of one dtype; TPCE_F32 adds transposed
+ * copies of A, B, Y, dZ, X and dU) */
 size_t tpce_ce_workspace_bytes(int64_t T, int64_t h, int64_t v_pad, int t, int dtype,
                                int with_grads);
 
@@ -122,7 +127,8 @@ size_t tpce_ce_workspace_bytes(int64_t T, int64_t h, int64_t v_pad, int t, int d
  * Outputs: Z [T, h]; U [T, f] and Y [T, f] are written for the backward.
  * Shapes:  T >= 0 (T == 0 is a no-op and every pointer may then be NULL),
  *          h >= 8 and h % 8 == 0, t >= 1, f % t == 0 and (f / t) % 64 == 0.
- * Workspace: none (ws may be NULL, ws_bytes 0).
+ * Workspace: none for TPCE_BF16 (ws may be NULL, ws_bytes 0); for TPCE_F32,
+ *          tpce_mlp_workspace_bytes(T, h, f, t, TPCE_F32) bytes.
  * ------------------------------------------------------------------------- */
 tpce_status tp_mlp_forward(const void *X, const void *A, const float *bA,
                            const void *B, const float *bB,

@@ -77,8 +77,16 @@ def test_workspace_sizes(L):
     fwd = tp.ce_workspace_bytes(T, h, vp, t, grads=False)
     bwd = tp.ce_workspace_bytes(T, h, vp, t, grads=True)
     assert fwd < 0.02 * T * vp * 2
+    # the dl scratch holds at most half the vocabulary and at most 1 GiB
     assert bwd <= 2 ** 30 + T * h * 4 + fwd + 4096
-    assert bwd < 0.3 * T * vp * 2
+    assert bwd < 0.5 * T * vp * 2
+    # the 8.3B block: 4 of 8 shards per chunk
+    T2, h2, vp2 = 8192, 3072, 51200
+    b2 = tp.ce_workspace_bytes(T2, h2, vp2, 8, grads=True) - tp.ce_workspace_bytes(T2, h2, vp2, 8, grads=False)
+    assert b2 <= T2 * (vp2 // 2) * 2 + T2 * h2 * 4 + 1024
+    # fp32 adds transposed operand copies: A^T, B^T, Y^T, dZ^T, X^T, dU^T
+    T, h, f = 32, 64, 256
+    assert tp.mlp_workspace_bytes(T, h, f, 2, dtype=__import__("torch").float32) >= 4 * (T * f + 2 * f * h + 2 * f * T + 2 * h * T)
     # invalid shapes give 0
     assert L.tpce_mlp_workspace_bytes(10, 64, 100, 3, 0) == 0
     assert L.tpce_ce_workspace_bytes(10, 64, 1000, 8, 0, 1) == 0
@@ -100,7 +108,7 @@ def test_mlp_validation(L):
     assert mlp_fwd(L, T=-1) == 2
     assert mlp_fwd(L, X=MISALIGNED) == 3
     assert mlp_fwd(L, X=None) == 1
-    assert mlp_fwd(L, dtype=1) == 7                    # fp32 not in this build
+    assert mlp_fwd(L, dtype=1) == 4                    # the fp32 (tf32) forward needs its workspace
     assert mlp_fwd(L, dtype=5) == 1
     assert mlp_fwd(L, T=0) == 0                        # empty batch: nothing to do
     # backward with T > 0 and no workspace

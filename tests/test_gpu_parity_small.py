@@ -35,19 +35,67 @@ def run_mlp(w, dev, seed=0, nonzero_bias=True):
 
 
 MLP_CASES = {
-    # name: (T, h, f, t)
-    "tiny_shape_bf16": (32, 64, 256, 2),
-    "ragged": (333, 200, 384, 2),
-    "multi_tile": (640, 512, 1024, 4),
-    "one_token": (1, 64, 128, 2),
+    # name: (T, h, f, t, dtype)
+    "tiny_shape_bf16": (32, 64, 256, 2, "bf16"),
+    "ragged": (333, 200, 384, 2, "bf16"),
+    "multi_tile": (640, 512, 1024, 4, "bf16"),
+    "one_token": (1, 64, 128, 2, "bf16"),
+    "wide_n_tiles": (1000, 1536, 3072, 8, "bf16"),   # picks 192-wide tiles
+    "ragged_f32": (333, 200, 384, 2, "f32"),
+    "multi_tile_f32": (300, 256, 512, 4, "f32"),
 }
+
+
+def test_tiny_config_fp32_matches_oracle():
+    # the tiny workload as specified: fp32 tensors (tf32 tensor-core path), t = 2
+    dev = gpu_or_skip()
+    w = wl.WORKLOADS["tiny"]
+    assert w.dtype == "f32"
+    mi, fwd, bwd = run_mlp(w, dev)
+    assert fwd["Z"].dtype == torch.float32
+    of = oracle.mlp_forward(mi["X"], mi["A"], mi["bA"], mi["B"], mi["bB"])
+    ob = oracle.mlp_backward(mi["X"], mi["A"], mi["bA"], mi["B"], mi["dZ"])
+    for k in ("U", "Y", "Z"):
+        assert_rel(k, fwd[k], of[k])
+    for k in ("dX", "dA", "dB", "dbA", "dbB"):
+        assert_rel(k, bwd[k], ob[k])
+    ci = wl.ce_inputs(w, seed=0)
+    g = {k: v.to(dev) for k, v in ci.items()}
+    out = tp.vocab_parallel_ce(g["H"], g["E"], g["targets"], w.v_valid, w.t, grad_scale=1.0)
+    assert tp.device_status() == 0
+    ref = oracle.ce(ci["H"], ci["E"], ci["targets"].numpy(), w.v_valid, grad_scale=1.0)
+    assert_loss("loss", out["loss"], ref["loss"])
+    assert_rel("dH", out["dH"], ref["dH"])
+    assert_rel("dE", out["dE"], ref["dE"])
+
+
+def test_gelu_and_derivative_evaluation_error_fp32():
+    # GeLU and GeLU' on the device (erf by Abramowitz & Stegun 7.1.26, error
+    # <= 1.5e-7) checked at their own accuracy through the fp32 API: with
+    # A = B = I, bA = 0 and dZ = 1, a single token gives U = tf32(X), Y =
+    # GeLU(U) and dbA = dY (.) GeLU'(U) = GeLU'(U) exactly up to the device
+    # evaluation of the two functions.
+    dev = gpu_or_skip()
+    h = f = 256
+    X = torch.linspace(-7.0, 7.0, h, dtype=torch.float32).reshape(1, h).to(dev)
+    I = torch.eye(h, dtype=torch.float32, device=dev)
+    fwd = tp.tp_mlp_forward(X, I, I, 2)
+    bwd = tp.tp_mlp_backward(torch.ones(1, h, device=dev), X, I, I, fwd["U"], fwd["Y"], 2)
+    assert tp.device_status() == 0
+    U = fwd["U"].double().cpu().numpy()[0]
+    Y = fwd["Y"].double().cpu().numpy()[0]
+    dU = bwd["dbA"].double().cpu().numpy()
+    gelu = np.array([oracle.gelu(u) for u in U])
+    dgelu = np.array([oracle.gelu_grad(u) for u in U])
+    assert np.abs(Y - gelu).max() <= 1e-6 * max(1.0, np.abs(U).max())
+    assert np.abs(dU - dgelu).max() <= 1e-6
 
 
 @pytest.mark.parametrize("case", list(MLP_CASES))
 def test_mlp_matches_oracle(case):
     dev = gpu_or_skip()
-    T, h, f, t = MLP_CASES[case]
-    w = wl.custom(case, T=T, h=h, f=f, v_valid=0, v_pad=0, t=t)
+    T, h, f, t, dtype = MLP_CASES[case]
+    w = wl.custom(case, T=T, h=h, f=f, v_valid=0, v_pad=0, t=t, dtype=dtype)
     mi, fwd, bwd = run_mlp(w, dev)
     of = oracle.mlp_forward(mi["X"], mi["A"], mi["bA"], mi["B"], mi["bB"])
     ob = oracle.mlp_backward(mi["X"], mi["A"], mi["bA"], mi["B"], mi["dZ"])
@@ -78,21 +126,24 @@ def test_mlp_shard_count_does_not_change_results():
 
 
 CE_CASES = {
-    # name: (T, h, v_pad, v_valid, t)
-    "tiny_shape_bf16": (32, 64, 512, 512, 2),
-    "ragged_bn128": (333, 200, 768, 700, 2),          # shard = 384 ids: 128-wide tiles
-    "padded_shards": (130, 96, 2048, 1800, 16),       # shard 15 holds only padding
-    "single_shard": (257, 128, 1024, 1000, 1),        # t = 1: the unsharded loss
-    "multi_tile": (600, 320, 4096, 4000, 4),
+    # name: (T, h, v_pad, v_valid, t, dtype)
+    "tiny_shape_bf16": (32, 64, 512, 512, 2, "bf16"),
+    "ragged_bn128": (333, 200, 768, 700, 2, "bf16"),          # shard = 384 ids: 128-wide tiles
+    "padded_shards": (130, 96, 2048, 1800, 16, "bf16"),       # shard 15 holds only padding
+    "single_shard": (257, 128, 1024, 1000, 1, "bf16"),        # t = 1: the unsharded loss
+    "multi_tile": (600, 320, 4096, 4000, 4, "bf16"),
+    "wide_h": (700, 1536, 3072, 3000, 4, "bf16"),             # dE / dH pick 192-wide tiles
+    "ragged_f32": (333, 200, 768, 700, 2, "f32"),
+    "padded_shards_f32": (130, 96, 2048, 1800, 16, "f32"),
 }
 
 
 @pytest.mark.parametrize("case", list(CE_CASES))
 def test_ce_matches_oracle(case):
     dev = gpu_or_skip()
-    T, h, v_pad, v_valid, t = CE_CASES[case]
+    T, h, v_pad, v_valid, t, dtype = CE_CASES[case]
     assert tp.pad_vocab(v_valid, t) <= v_pad
-    w = wl.custom(case, T=T, h=h, f=0, v_valid=v_valid, v_pad=v_pad, t=t)
+    w = wl.custom(case, T=T, h=h, f=0, v_valid=v_valid, v_pad=v_pad, t=t, dtype=dtype)
     ci = wl.ce_inputs(w, seed=0)
     ci["targets"][0] = 0
     ci["targets"][-1] = v_valid - 1

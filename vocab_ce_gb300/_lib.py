@@ -10,7 +10,9 @@ import ctypes
 import os
 import threading
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libtpce.so")
+# the in-tree build; TPCE_LIBRARY may name another build of the same library
+LIB_PATH = os.environ.get("TPCE_LIBRARY") or os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib",
+                                                           "libtpce.so")
 
 STATUS = {
     0: "TPCE_OK", 1: "TPCE_ERR_INVALID", 2: "TPCE_ERR_SHAPE", 3: "TPCE_ERR_ALIGN",

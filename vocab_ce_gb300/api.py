@@ -64,7 +64,8 @@ def ce_workspace_bytes(T: int, h: int, v_pad: int, t: int, grads: bool = True, d
 
 def tp_mlp_forward(X: torch.Tensor, A: torch.Tensor, B: torch.Tensor, t: int,
                    bA: Optional[torch.Tensor] = None, bB: Optional[torch.Tensor] = None,
-                   out: Optional[Dict[str, torch.Tensor]] = None, stream=None) -> Dict[str, torch.Tensor]:
+                   out: Optional[Dict[str, torch.Tensor]] = None, ws: Optional[torch.Tensor] = None,
+                   stream=None) -> Dict[str, torch.Tensor]:
     """Z = sum_i GeLU(X A_i + bA_i) B_i + bB over t shards; returns Z, U, Y."""
     T, h = X.shape
     f = A.shape[1]
@@ -78,8 +79,12 @@ def tp_mlp_forward(X: torch.Tensor, A: torch.Tensor, B: torch.Tensor, t: int,
     Z = out.get("Z") if out.get("Z") is not None else torch.empty((T, h), dtype=dt, device=X.device)
     U = out.get("U") if out.get("U") is not None else torch.empty((T, f), dtype=dt, device=X.device)
     Y = out.get("Y") if out.get("Y") is not None else torch.empty((T, f), dtype=dt, device=X.device)
+    w = None
+    if dt == torch.float32 and T > 0:  # the tf32 path stages transposed operands
+        w = _workspace(mlp_workspace_bytes(T, h, f, t, dt), X.device, ws)
     st = lib().tp_mlp_forward(_ptr(X), _ptr(A), _ptr(bA), _ptr(B), _ptr(bB), T, h, f, t, _DT[dt],
-                              _ptr(Z), _ptr(U), _ptr(Y), None, 0, _stream(stream))
+                              _ptr(Z), _ptr(U), _ptr(Y), _ptr(w),
+                              0 if w is None else w.numel() * w.element_size(), _stream(stream))
     check(st, "tp_mlp_forward")
     return {"Z": Z, "U": U, "Y": Y}
 

@@ -38,16 +38,21 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= _deps_mtime():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    os.makedirs(LIB_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=None, out_path: str = None,
+          build_dir: str = None) -> str:
+    """Compile and link libtpce.so (default: in-tree). extra_flags are added to
+    every nvcc compile (e.g. -DTPCE_EPI_WARPS=8 tuning knobs)."""
+    lib_path = out_path or LIB_PATH
+    bdir = build_dir or BUILD_DIR
+    if not force and os.path.exists(lib_path) and os.path.getmtime(lib_path) >= _deps_mtime():
+        return lib_path
+    os.makedirs(bdir, exist_ok=True)
+    os.makedirs(os.path.dirname(lib_path), exist_ok=True)
     exe = nvcc()
     flags = NVCC_FLAGS + list(extra_flags or [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
         cmd = [exe] + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r
@@ -59,13 +64,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
             sys.stderr.write(r.stdout + r.stderr)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr}")
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [exe] + ARCH + ["-shared", "-o", tmp] + [obj for _, obj, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stderr)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

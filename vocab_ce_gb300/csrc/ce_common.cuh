@@ -18,13 +18,14 @@ namespace {
 constexpr int64_t kMaxDim = INT_MAX - 1024;  // kernel coordinates are 32-bit
 
 tpce_status check_ce_shape(int64_t T, int64_t h, int64_t v_pad, int64_t v_valid, int t, int dtype) {
-    if (dtype == TPCE_F32) return TPCE_ERR_UNSUPPORTED;
-    if (dtype != TPCE_BF16) return TPCE_ERR_INVALID;
+    if (dtype != TPCE_BF16 && dtype != TPCE_F32) return TPCE_ERR_INVALID;
     if (T < 0 || h < 8 || t < 1 || v_pad < 1) return TPCE_ERR_SHAPE;
     if (T > kMaxDim || h > kMaxDim || v_pad > kMaxDim) return TPCE_ERR_SHAPE;
     if (h % 8 != 0) return TPCE_ERR_SHAPE;
     if (v_pad % t != 0 || (v_pad / t) % 128 != 0) return TPCE_ERR_SHAPE;  // 128-multiple shards
     if (v_valid < 1 || v_valid > v_pad) return TPCE_ERR_SHAPE;
+    // the fp32 path transposes [T, *] and [v_pad, *] matrices with 32-row blocks in grid.y
+    if (dtype == TPCE_F32 && ((T + 31) / 32 > 65535 || (v_pad + 31) / 32 > 65535)) return TPCE_ERR_SHAPE;
     return TPCE_OK;
 }
 

@@ -71,7 +71,8 @@ extern "C" tpce_status vocab_parallel_ce_loss_static(const void *H, const void *
 
     // scratch layout: per-tile (max, sumexp) [n_tiles][T], target logit [T], lse [T] if not an output
     const int64_t vs = v_pad / t;
-    const int bn = (vs % 256 == 0) ? 256 : 128;  // a tile never straddles two shards
+    const bool f32 = dtype == TPCE_F32;
+    const int bn = (!f32 && vs % 256 == 0) ? 256 : 128;  // a tile never straddles two shards
     const int64_t n_tiles = v_pad / bn;
     const size_t stats_bytes = round_up(static_cast<size_t>(n_tiles) * T * sizeof(float2), 256);
     const size_t tau_bytes = round_up(static_cast<size_t>(T) * sizeof(float), 256);
@@ -97,11 +98,16 @@ extern "C" tpce_status vocab_parallel_ce_loss_static(const void *H, const void *
 
     Operand a{H, T, h, h};      // K-major [T, h]
     Operand b{E, v_pad, h, h};  // K-major: N = v_pad rows, K = h columns
-    EpiCeStats::Params ep{stats, tau, targets, T, vvi, 0, 0};
-    st = bn == 256 ? launch_gemm<256, false, false, EpiCeStats>("ce_static_logits_stats", a, b, Ti, vpi, hi, 0, 0, 0,
-                                                                 0, ep, s, /*timed=*/false)
-                   : launch_gemm<128, false, false, EpiCeStats>("ce_static_logits_stats", a, b, Ti, vpi, hi, 0, 0, 0,
-                                                                 0, ep, s, /*timed=*/false);
+    EpiCeStats::Params ep{stats, tau, targets, T, vvi, 0, 0, bn};
+    if (f32)
+        st = launch_gemm<float, 128, false, false, EpiCeStats>("ce_static_logits_stats", a, b, nullptr, Ti, vpi, hi, 0, 0, 0,
+                                                               0, ep, s, /*timed=*/false);
+    else if (bn == 256)
+        st = launch_gemm<__nv_bfloat16, 256, false, false, EpiCeStats>("ce_static_logits_stats", a, b, nullptr, Ti,
+                                                                       vpi, hi, 0, 0, 0, 0, ep, s, /*timed=*/false);
+    else
+        st = launch_gemm<__nv_bfloat16, 128, false, false, EpiCeStats>("ce_static_logits_stats", a, b, nullptr, Ti, vpi, hi,
+                                                                       0, 0, 0, 0, ep, s, /*timed=*/false);
     if (st != TPCE_OK) return st;
     ce_combine_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, s>>>(
         stats, tau, targets, T, t, static_cast<int>(n_tiles / t), vvi, loss, lse_buf, err);

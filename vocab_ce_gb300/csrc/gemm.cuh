@@ -1,22 +1,25 @@
 // gemm.cuh -- the tensor-core GEMM behind every contraction of the block.
 //
-// D[M, N] = sum_k A[m, k] B[k, n] with bf16 operands and an fp32 accumulator
-// in tensor memory, followed by a fused epilogue. One persistent CTA per SM
-// walks the output tiles; inside a CTA the work is split by warp:
+// D[M, N] = sum_k A[m, k] B[k, n] with an fp32 accumulator in tensor memory,
+// followed by a fused epilogue. Operands are bf16 (tcgen05.mma kind::f16) or
+// fp32 read as tf32 (kind::tf32). One persistent CTA per SM walks the output
+// tiles; inside a CTA the work is split by warp:
 //
-//   warp 0      TMA producer: streams 128x64 A and BNx64 B tiles into a ring
-//               of shared-memory stages (128-byte swizzle).
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN, K=16)
-//               into one of two TMEM accumulators; it also owns the TMEM
-//               allocation.
+//   warp 0      TMA producer: streams 128-row A and BN-row B tiles, 128 bytes
+//               of K per row, into a ring of shared-memory stages (128-byte
+//               swizzle).
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN) into
+//               one of two TMEM accumulators; the warp owns the TMEM allocation.
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (one row per thread),
-//               apply the fused epilogue, store to global memory, and hand the
-//               accumulator back, so the next tile's MMAs overlap this tile's
-//               epilogue.
+//               apply the fused epilogue, stage each 32x32 output chunk in
+//               swizzled shared memory and write it with a TMA bulk tensor
+//               store (or reduce-add), then hand the accumulator back, so the
+//               next tile's MMAs overlap this tile's epilogue.
 //
-// Operands can be K-major (rows of the contraction dimension contiguous) or
+// bf16 operands can be K-major (the contraction dimension contiguous) or
 // MN-major (the output dimension contiguous): the transposed operands of the
 // backward GEMMs (Y^T dZ, X^T dU, dl^T H) are read in place, no transpose pass.
+// tf32 operands are K-major.
 //
 // The tile grid's N coordinate of the column-parallel GEMMs is the
 // concatenation of the t shards' column ranges, and the K loop of the
@@ -28,6 +31,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "ptx.cuh"
 
@@ -36,28 +40,37 @@ namespace tpce {
 // state (a kernel instantiated in two units is two device functions).
 namespace {
 
-constexpr int kBM = 128;           // tile rows (TMEM lanes)
-constexpr int kBK = 64;            // bf16 elements per 128-byte swizzle row
-constexpr int kUmmaK = 16;         // K of one tcgen05.mma kind::f16
-constexpr int kThreads = 192;      // 6 warps
-constexpr uint32_t kMnBlockBytes = 64 * kBK * 2;   // one 64-wide MN block of an MN-major tile
+// Epilogue warps of the heavy epilogues (4: one per TMEM lane quarter; 8: two
+// per quarter, splitting the columns). Build-time tuning knob.
+#ifndef TPCE_EPI_WARPS
+#define TPCE_EPI_WARPS 4
+#endif
+constexpr int kHeavyEpiWarps = TPCE_EPI_WARPS;
 
-template <int BN>
-struct TileCfg {
-    static constexpr int kStages = BN == 256 ? 4 : 6;
-    static constexpr uint32_t kABytes = kBM * kBK * 2;
-    static constexpr uint32_t kBBytes = BN * kBK * 2;
-    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-    static constexpr uint32_t kTmemCols = 2 * BN;           // two accumulators
-    static constexpr uint32_t kBarrierBytes = 256;
-    static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 + kBarrierBytes;
+constexpr int kBM = 128;                 // tile rows (TMEM lanes)
+constexpr uint32_t kRowBytes = 128;      // K bytes per smem row = one 128-byte swizzle span
+constexpr uint32_t kMnBlockBytes = 64 * kRowBytes;  // one 64-wide MN block of a bf16 MN-major tile (64 K rows)
+
+template <typename ElemT>
+struct ElemTraits;
+template <>
+struct ElemTraits<__nv_bfloat16> {
+    static constexpr int kBK = 64;       // elements of K per stage
+    static constexpr int kUmmaK = 16;    // K of one tcgen05.mma kind::f16
+    static constexpr uint32_t kFmt = 1;  // bf16
+};
+template <>
+struct ElemTraits<float> {
+    static constexpr int kBK = 32;
+    static constexpr int kUmmaK = 8;     // K of one tcgen05.mma kind::tf32
+    static constexpr uint32_t kFmt = 2;  // tf32
 };
 
 // Problem description shared by every role of the kernel.
 struct GemmShape {
     int M, N, K;               // output rows, output columns, contraction length
     int tiles_m, tiles_n;      // ceil(M / 128), ceil(N / BN)
-    int k_blocks;              // ceil(K / 64)
+    int k_blocks;              // ceil(K / BK)
     int group_m;               // rasterisation: tiles_m are walked in groups of this many
     int a_off_mn, a_off_k;     // coordinate offsets of the A operand inside its tensor map
     int b_off_mn, b_off_k;     // same for B
@@ -74,24 +87,14 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmShape &s, int &m
 }
 
 // --------------------------------------------------------------------------
-// bf16 helpers for the epilogues
+// 8-element loads for the epilogues (16- or 32-byte aligned)
 // --------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// store 8 consecutive values as bf16 (16 bytes, aligned)
-__device__ __forceinline__ void store_bf16x8(__nv_bfloat16 *p, const float *v) {
-    uint4 u;
-    u.x = pack_bf16x2(v[0], v[1]);
-    u.y = pack_bf16x2(v[2], v[3]);
-    u.z = pack_bf16x2(v[4], v[5]);
-    u.w = pack_bf16x2(v[6], v[7]);
-    *reinterpret_cast<uint4 *>(p) = u;
-}
-
-__device__ __forceinline__ void load_bf16x8(const __nv_bfloat16 *p, float *v) {
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float *v) {
     uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
     const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
@@ -101,119 +104,199 @@ __device__ __forceinline__ void load_bf16x8(const __nv_bfloat16 *p, float *v) {
         v[2 * i + 1] = f.y;
     }
 }
+__device__ __forceinline__ void load8(const float *p, float *v) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
 
-// GeLU(u) = u Phi(u), Phi(u) = (1 + erf(u / sqrt 2)) / 2
+// 32 bias values starting at column n (zeros where absent); N % 8 == 0, so
+// every 8-column group is entirely inside or outside [0, N).
+__device__ __forceinline__ void load_bias32(const float *bias, int n, int N, float *b) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (bias && n + 8 * q < N) {
+            load8(bias + n + 8 * q, b + 8 * q);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) b[8 * q + i] = 0.0f;
+        }
+    }
+}
+
+// Standard normal CDF Phi(u) = (1 + erf(u / sqrt 2)) / 2, with erf taken from
+// Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26:
+// for z >= 0, erf(z) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) e^{-z^2},
+// t = 1 / (1 + p z), |error| <= 1.5e-7. With z = |u| / sqrt 2 the factor
+// e^{-z^2} = e^{-u^2 / 2} is also the Gaussian density's exponent, so GeLU'
+// reuses it. `g` receives e^{-u^2 / 2}.
+__device__ __forceinline__ float normal_cdf(float u, float &g) {
+    constexpr float p = 0.3275911f;
+    constexpr float a1 = 0.254829592f, a2 = -0.284496736f, a3 = 1.421413741f, a4 = -1.453152027f,
+                    a5 = 1.061405429f;
+    const float z = fabsf(u) * 0.70710678118654752440f;
+    const float t = __fdividef(1.0f, fmaf(p, z, 1.0f));
+    g = __expf(-0.5f * u * u);
+    const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, a5, a4), a3), a2), a1);
+    const float erf_z = 1.0f - poly * g;  // erf(|u| / sqrt 2)
+    return 0.5f + 0.5f * copysignf(erf_z, u);
+}
+// GeLU(u) = u Phi(u)
 __device__ __forceinline__ float gelu_f(float u) {
-    return 0.5f * u * (1.0f + erff(u * 0.70710678118654752440f));
+    float g;
+    return u * normal_cdf(u, g);
 }
-// GeLU'(u) = Phi(u) + u phi(u), phi(u) = exp(-u^2 / 2) / sqrt(2 pi)
+// GeLU'(u) = Phi(u) + u phi(u), phi(u) = e^{-u^2 / 2} / sqrt(2 pi)
 __device__ __forceinline__ float gelu_grad_f(float u) {
-    const float Phi = 0.5f * (1.0f + erff(u * 0.70710678118654752440f));
-    const float phi = 0.39894228040143267794f * __expf(-0.5f * u * u);
-    return Phi + u * phi;
+    float g;
+    const float Phi = normal_cdf(u, g);
+    return fmaf(u * 0.39894228040143267794f, g, Phi);
 }
 
 // --------------------------------------------------------------------------
-// Epilogues. `apply` runs in each of the 128 epilogue threads for one tile:
-// `row` is the thread's global output row, `n0` the tile's first output
-// column, `taddr` the TMEM address of the thread's warp quarter of the
-// accumulator. Every thread of a warp executes the TMEM loads (they are
-// warp-collective); only rows < M and columns < N are stored.
+// Output staging. An epilogue warp writes each 32-row x 32-column chunk of an
+// output into a shared-memory buffer, one row per lane, swizzled exactly as
+// the TMA store of that buffer expects (bf16: 64-byte rows, 64-byte swizzle;
+// fp32: 128-byte rows, 128-byte swizzle); one lane then stores the chunk with
+// a TMA bulk tensor store, which writes whole lines, clips the tensor's ragged
+// edges and runs asynchronously.
 // --------------------------------------------------------------------------
-
-// GEMM1 epilogue: U = acc + bA, Y = GeLU(U); both stored bf16.
-struct EpiBiasGelu {
-    struct Params {
-        __nv_bfloat16 *U;
-        __nv_bfloat16 *Y;
-        const float *bias;  // [N] or null
-        int64_t ld;
-    };
-    template <int BN>
-    __device__ static void apply(const Params &p, const GemmShape &s, int row, int n0, uint32_t taddr) {
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            ptx::tmem_ld32(taddr + c * 32, v);
-            const int nc = n0 + c * 32;
-            if (row >= s.M || nc >= s.N) continue;
+template <typename OutT>
+struct Stage;
+template <>
+struct Stage<__nv_bfloat16> {
+    static constexpr uint32_t kBytes = 32 * 64;
+    static constexpr int kSwizzle = 64;
+    // 16-byte piece j of row r lives at piece j ^ ((r >> 1) & 3)
+    __device__ static void write(uint8_t *buf, int r, const float *v) {
+        uint8_t *row = buf + r * 64;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int n = nc + q * 8;
-                if (n >= s.N) break;
-                float u[8], y[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) u[i] = v[q * 8 + i] + (p.bias ? __ldg(p.bias + n + i) : 0.0f);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) y[i] = gelu_f(u[i]);
-                store_bf16x8(p.U + static_cast<int64_t>(row) * p.ld + n, u);
-                store_bf16x8(p.Y + static_cast<int64_t>(row) * p.ld + n, y);
-            }
+        for (int j = 0; j < 4; ++j) {
+            uint4 u;
+            u.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+            u.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+            u.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+            u.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+            *reinterpret_cast<uint4 *>(row + ((j ^ ((r >> 1) & 3)) << 4)) = u;
         }
     }
 };
+template <>
+struct Stage<float> {
+    static constexpr uint32_t kBytes = 32 * 128;
+    static constexpr int kSwizzle = 128;
+    // 16-byte piece j of row r lives at piece j ^ (r & 7)
+    __device__ static void write(uint8_t *buf, int r, const float *v) {
+        uint8_t *row = buf + r * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4 *>(row + ((j ^ (r & 7)) << 4)) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+};
 
-// Plain epilogue: out = acc (+ bias), bf16.
-struct EpiStore {
+// --------------------------------------------------------------------------
+// Epilogues. Each turns the fp32 accumulator values of one 32-column chunk of
+// the thread's output row into kOuts output chunks (stored by the kernel), or
+// reduces them itself (kOuts = 0). begin/end run once per tile and row.
+// `live` is false for rows >= M or chunks at columns >= N: such values are
+// never stored, and the epilogue must not read memory for them.
+// --------------------------------------------------------------------------
+struct NoRow {};
+
+// GEMM1 epilogue: U = acc + bA, Y = GeLU(U).
+template <typename OutT>
+struct EpiBiasGelu {
+    static constexpr int kWarps = kHeavyEpiWarps;
+    static constexpr int kOuts = 2;
+    using Out = OutT;
+    using Row = NoRow;
     struct Params {
-        __nv_bfloat16 *out;
         const float *bias;  // [N] or null
-        int64_t ld;
     };
-    template <int BN>
-    __device__ static void apply(const Params &p, const GemmShape &s, int row, int n0, uint32_t taddr) {
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            ptx::tmem_ld32(taddr + c * 32, v);
-            const int nc = n0 + c * 32;
-            if (row >= s.M || nc >= s.N) continue;
+    __device__ static int mode(const Params &) { return 0; }
+    __device__ static Row begin(const Params &, int, bool) { return {}; }
+    __device__ static void chunk(const Params &p, Row &, int, int n, int N, bool, float (&v)[32],
+                                 float (&o)[kOuts][32]) {
+        float b[32];
+        load_bias32(p.bias, n, N, b);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int n = nc + q * 8;
-                if (n >= s.N) break;
-                float o[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) o[i] = v[q * 8 + i] + (p.bias ? __ldg(p.bias + n + i) : 0.0f);
-                store_bf16x8(p.out + static_cast<int64_t>(row) * p.ld + n, o);
-            }
+        for (int i = 0; i < 32; ++i) {
+            o[0][i] = v[i] + b[i];
+            o[1][i] = gelu_f(o[0][i]);
         }
     }
+    __device__ static void end(const Params &, Row &, int, int, bool) {}
+};
+
+// Plain epilogue: out = acc (+ bias).
+template <typename OutT>
+struct EpiStore {
+    static constexpr int kWarps = kHeavyEpiWarps;
+    static constexpr int kOuts = 1;
+    using Out = OutT;
+    using Row = NoRow;
+    struct Params {
+        const float *bias;  // [N] or null
+    };
+    __device__ static int mode(const Params &) { return 0; }
+    __device__ static Row begin(const Params &, int, bool) { return {}; }
+    __device__ static void chunk(const Params &p, Row &, int, int n, int N, bool, float (&v)[32],
+                                 float (&o)[kOuts][32]) {
+        float b[32];
+        load_bias32(p.bias, n, N, b);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[0][i] = v[i] + b[i];
+    }
+    __device__ static void end(const Params &, Row &, int, int, bool) {}
 };
 
 // dY epilogue of the backward: dU = acc (.) GeLU'(U), U read from the saved activations.
+template <typename OutT>
 struct EpiGeluGrad {
+    static constexpr int kWarps = kHeavyEpiWarps;
+    static constexpr int kOuts = 1;
+    using Out = OutT;
+    using Row = NoRow;
     struct Params {
-        __nv_bfloat16 *dU;
-        const __nv_bfloat16 *U;
+        const OutT *U;
         int64_t ld;
     };
-    template <int BN>
-    __device__ static void apply(const Params &p, const GemmShape &s, int row, int n0, uint32_t taddr) {
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            ptx::tmem_ld32(taddr + c * 32, v);
-            const int nc = n0 + c * 32;
-            if (row >= s.M || nc >= s.N) continue;
+    __device__ static int mode(const Params &) { return 0; }
+    __device__ static Row begin(const Params &, int, bool) { return {}; }
+    __device__ static void chunk(const Params &p, Row &, int row, int n, int N, bool live, float (&v)[32],
+                                 float (&o)[kOuts][32]) {
+        float u[32];
+        const OutT *src = p.U + static_cast<int64_t>(row) * p.ld + n;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int n = nc + q * 8;
-                if (n >= s.N) break;
-                float u[8], d[8];
-                load_bf16x8(p.U + static_cast<int64_t>(row) * p.ld + n, u);
+        for (int q = 0; q < 4; ++q) {
+            if (live && n + 8 * q < N) {
+                load8(src + 8 * q, u + 8 * q);
+            } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) d[i] = v[q * 8 + i] * gelu_grad_f(u[i]);
-                store_bf16x8(p.dU + static_cast<int64_t>(row) * p.ld + n, d);
+                for (int i = 0; i < 8; ++i) u[8 * q + i] = 0.0f;
             }
         }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[0][i] = v[i] * gelu_grad_f(u[i]);
     }
+    __device__ static void end(const Params &, Row &, int, int, bool) {}
 };
 
 // CE pass 1: logits of one vocabulary tile, reduced per token to (max, sum of
 // exp(l - max)) over the real ids, plus the target logit where the target
-// falls in this tile. The logits never leave the registers.
+// falls in this tile. The logits never leave the registers. One warp per TMEM
+// lane quarter, so each thread sees its token's whole tile row.
 struct EpiCeStats {
+    static constexpr int kWarps = 4;
+    static constexpr int kOuts = 0;
+    using Out = float;
+    struct Row {
+        int tgt;
+        float m, sum, tau;
+        bool has_tau;
+    };
     struct Params {
         float2 *stats;          // [n_tiles_total][T]: (max, sumexp) per tile and token
         float *tau;             // [T] target logit
@@ -222,145 +305,148 @@ struct EpiCeStats {
         int v_valid;
         int n_base;             // vocabulary id of GEMM column 0
         int tile_base;          // global tile index of GEMM tile column 0
+        int bn;                 // tile width
     };
-    template <int BN>
-    __device__ static void apply(const Params &p, const GemmShape &s, int row, int n0, uint32_t taddr) {
-        const bool live = row < s.M;
-        const int tgt = live ? __ldg(p.targets + row) : -1;
-        float m = -INFINITY, sum = 0.0f, tau = 0.0f;
-        bool has_tau = false;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            ptx::tmem_ld32(taddr + c * 32, v);
-            const int g0 = p.n_base + n0 + c * 32;   // vocabulary id of v[0]
-            const int nvalid = min(32, p.v_valid - g0);  // ids < v_valid are real
-            if (nvalid > 0) {
-                float cm = -INFINITY;
+    __device__ static int mode(const Params &) { return 0; }
+    __device__ static Row begin(const Params &p, int row, bool live) {
+        return Row{live ? __ldg(p.targets + row) : -1, -INFINITY, 0.0f, 0.0f, false};
+    }
+    __device__ static void chunk(const Params &p, Row &r, int, int n, int, bool, float (&v)[32],
+                                 float (&)[1][32]) {
+        const int g0 = p.n_base + n;                 // vocabulary id of v[0]
+        const int nvalid = min(32, p.v_valid - g0);  // ids < v_valid are real
+        if (nvalid > 0) {
+            float cm = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i < nvalid) cm = fmaxf(cm, v[i]);
-                const float nm = fmaxf(m, cm);
-                float acc = sum * __expf(m - nm);
+            for (int i = 0; i < 32; ++i)
+                if (i < nvalid) cm = fmaxf(cm, v[i]);
+            const float nm = fmaxf(r.m, cm);
+            float acc = r.sum * __expf(r.m - nm);
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i < nvalid) acc += __expf(v[i] - nm);
-                sum = acc;
-                m = nm;
-            }
-            const int tl = tgt - g0;
-            if (tl >= 0 && tl < 32) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i == tl) tau = v[i];
-                has_tau = true;
-            }
+            for (int i = 0; i < 32; ++i)
+                if (i < nvalid) acc += __expf(v[i] - nm);
+            r.sum = acc;
+            r.m = nm;
         }
-        if (live) {
-            const int tile = p.tile_base + n0 / BN;
-            p.stats[static_cast<int64_t>(tile) * p.T + row] = make_float2(m, sum);
-            if (has_tau) p.tau[row] = tau;
+        const int tl = r.tgt - g0;
+        if (tl >= 0 && tl < 32) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i == tl) r.tau = v[i];
+            r.has_tau = true;
         }
+    }
+    __device__ static void end(const Params &p, Row &r, int row, int n0, bool live) {
+        if (!live) return;
+        const int tile = p.tile_base + n0 / p.bn;
+        p.stats[static_cast<int64_t>(tile) * p.T + row] = make_float2(r.m, r.sum);
+        if (r.has_tau) p.tau[row] = r.tau;
     }
 };
 
 // CE pass 2, first GEMM: recomputed logits -> dl = g (exp(l - lse) - onehot),
-// zero on padded ids, stored bf16 into the chunk scratch.
+// zero on padded ids.
+template <typename OutT>
 struct EpiCeDlogits {
+    static constexpr int kWarps = kHeavyEpiWarps;
+    static constexpr int kOuts = 1;
+    using Out = OutT;
+    struct Row {
+        float lse;
+        int tgt;
+    };
     struct Params {
-        __nv_bfloat16 *dl;      // [T][ld] chunk scratch
-        int64_t ld;
         const float *lse;       // [T]
         const int32_t *targets; // [T]
         float grad_scale;
         int v_valid;
         int n_base;             // vocabulary id of GEMM column 0
     };
-    template <int BN>
-    __device__ static void apply(const Params &p, const GemmShape &s, int row, int n0, uint32_t taddr) {
-        const bool live = row < s.M;
-        const float L = live ? __ldg(p.lse + row) : 0.0f;
-        const int tgt = live ? __ldg(p.targets + row) : -1;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            ptx::tmem_ld32(taddr + c * 32, v);
-            const int nc = n0 + c * 32;
-            if (!live || nc >= s.N) continue;
-            const int g0 = p.n_base + nc;
+    __device__ static int mode(const Params &) { return 0; }
+    __device__ static Row begin(const Params &p, int row, bool live) {
+        return Row{live ? __ldg(p.lse + row) : 0.0f, live ? __ldg(p.targets + row) : -1};
+    }
+    __device__ static void chunk(const Params &p, Row &r, int, int n, int, bool, float (&v)[32],
+                                 float (&o)[kOuts][32]) {
+        const int g0 = p.n_base + n;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int n = nc + q * 8;
-                if (n >= s.N) break;
-                float d[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int g = g0 + q * 8 + i;
-                    const float pr = __expf(v[q * 8 + i] - L);
-                    d[i] = g < p.v_valid ? p.grad_scale * (pr - (g == tgt ? 1.0f : 0.0f)) : 0.0f;
-                }
-                store_bf16x8(p.dl + static_cast<int64_t>(row) * p.ld + n, d);
-            }
+        for (int i = 0; i < 32; ++i) {
+            const int g = g0 + i;
+            const float pr = __expf(v[i] - r.lse);
+            o[0][i] = g < p.v_valid ? p.grad_scale * (pr - (g == r.tgt ? 1.0f : 0.0f)) : 0.0f;
         }
     }
+    __device__ static void end(const Params &, Row &, int, int, bool) {}
 };
 
-// fp32 accumulation across launches (dH summed over vocabulary chunks):
-// mode 0: acc = v; 1: acc += v; 2: out = bf16(acc + v); 3: out = bf16(v).
-struct EpiAccF32 {
+// fp32 output stored (mode 0) or added element-wise into global memory by the
+// TMA reduction (mode 1): dH summed over vocabulary chunks, in chunk order.
+struct EpiF32Accumulate {
+    static constexpr int kWarps = kHeavyEpiWarps;
+    static constexpr int kOuts = 1;
+    using Out = float;
+    using Row = NoRow;
     struct Params {
-        float *acc;             // [M][ld] fp32
-        __nv_bfloat16 *out;     // [M][ld] bf16
-        int64_t ld;
-        int mode;
+        int add;  // 0: store, 1: add into the existing values
     };
-    template <int BN>
-    __device__ static void apply(const Params &p, const GemmShape &s, int row, int n0, uint32_t taddr) {
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            ptx::tmem_ld32(taddr + c * 32, v);
-            const int nc = n0 + c * 32;
-            if (row >= s.M || nc >= s.N) continue;
+    __device__ static int mode(const Params &p) { return p.add; }
+    __device__ static Row begin(const Params &, int, bool) { return {}; }
+    __device__ static void chunk(const Params &, Row &, int, int, int, bool, float (&v)[32],
+                                 float (&o)[kOuts][32]) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int n = nc + q * 8;
-                if (n >= s.N) break;
-                const int64_t off = static_cast<int64_t>(row) * p.ld + n;
-                float o[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) o[i] = v[q * 8 + i];
-                if (p.mode == 1 || p.mode == 2) {
-                    const float4 a0 = *reinterpret_cast<const float4 *>(p.acc + off);
-                    const float4 a1 = *reinterpret_cast<const float4 *>(p.acc + off + 4);
-                    o[0] += a0.x; o[1] += a0.y; o[2] += a0.z; o[3] += a0.w;
-                    o[4] += a1.x; o[5] += a1.y; o[6] += a1.z; o[7] += a1.w;
-                }
-                if (p.mode <= 1) {
-                    *reinterpret_cast<float4 *>(p.acc + off) = make_float4(o[0], o[1], o[2], o[3]);
-                    *reinterpret_cast<float4 *>(p.acc + off + 4) = make_float4(o[4], o[5], o[6], o[7]);
-                } else {
-                    store_bf16x8(p.out + off, o);
-                }
-            }
-        }
+        for (int i = 0; i < 32; ++i) o[0][i] = v[i];
     }
+    __device__ static void end(const Params &, Row &, int, int, bool) {}
+};
+
+// --------------------------------------------------------------------------
+// Shared-memory plan of one instantiation: operand stages, then output
+// staging (per epilogue warp: kOuts outputs x 2 buffers), then barriers.
+// --------------------------------------------------------------------------
+constexpr uint32_t kSmemMax = 232448;  // opt-in dynamic shared memory per block
+
+template <int BN, class Epi>
+struct KernelCfg {
+    static_assert(BN == 128 || BN == 192 || BN == 256, "tile width");
+    static constexpr uint32_t kABytes = kBM * kRowBytes;
+    static constexpr uint32_t kBBytes = BN * kRowBytes;
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kStagingBytes =
+        static_cast<uint32_t>(Epi::kWarps) * Epi::kOuts * 2 * Stage<typename Epi::Out>::kBytes;
+    static constexpr uint32_t kBarrierBytes = 256;
+    static constexpr uint32_t kFree = kSmemMax - 1024 - kBarrierBytes - kStagingBytes;
+    static constexpr int kStages = (kFree / kStageBytes) > 6 ? 6 : static_cast<int>(kFree / kStageBytes);
+    static_assert(kStages >= 3, "too few pipeline stages");
+    static constexpr uint32_t kTmemCols = BN == 128 ? 256 : 512;  // two accumulators, power of two
+    static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024 + kBarrierBytes;
 };
 
 // --------------------------------------------------------------------------
 // The kernel
 // --------------------------------------------------------------------------
-template <int BN, bool A_MN, bool B_MN, class Epi>
-__global__ void __launch_bounds__(kThreads, 1)
+template <typename ElemT, int BN, bool A_MN, bool B_MN, class Epi>
+__global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
                    const GemmShape shp, const typename Epi::Params ep, uint32_t *err) {
-    using C = TileCfg<BN>;
+    using C = KernelCfg<BN, Epi>;
+    using ET = ElemTraits<ElemT>;
+    using OutT = typename Epi::Out;
+    static_assert(std::is_same<ElemT, __nv_bfloat16>::value || (!A_MN && !B_MN),
+                  "tf32 operands are K-major");
+    static_assert(Epi::kWarps == 4 || Epi::kWarps == 8, "epilogue warps");
     constexpr int S = C::kStages;
-    constexpr uint32_t kIdesc = ptx::idesc_bf16(kBM, BN, A_MN, B_MN);
+    constexpr int kBK = ET::kBK;
+    constexpr int kUmmaK = ET::kUmmaK;
+    constexpr uint32_t kIdesc = ptx::idesc_f32acc(kBM, BN, ET::kFmt, A_MN, B_MN);
+    constexpr int kGroups = Epi::kWarps / 4;  // epilogue warps per TMEM lane quarter
+    constexpr int kChunks = BN / 32;
+    constexpr int kOuts = Epi::kOuts;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * C::kStageBytes);
+    uint8_t *staging = smem + S * C::kStageBytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(staging + C::kStagingBytes);
     uint64_t *empty = full + S;
     uint64_t *tfull = empty + S;
     uint64_t *tempty = tfull + 2;
@@ -378,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&tfull[i], 1);
-            ptx::mbar_init(&tempty[i], 4);
+            ptx::mbar_init(&tempty[i], Epi::kWarps);
         }
         ptx::mbar_init(drain, 1);
         *abort_flag = 0;
@@ -468,11 +554,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sb = sa + C::kABytes;
 #pragma unroll
                     for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                        const uint64_t ad = A_MN ? ptx::sdesc_sw128(sa + kk * (kUmmaK * 128), kMnBlockBytes, 1024)
-                                                 : ptx::sdesc_sw128(sa + kk * (kUmmaK * 2), 16, 1024);
-                        const uint64_t bd = B_MN ? ptx::sdesc_sw128(sb + kk * (kUmmaK * 128), kMnBlockBytes, 1024)
-                                                 : ptx::sdesc_sw128(sb + kk * (kUmmaK * 2), 16, 1024);
-                        ptx::mma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        // K-major: step 32 bytes inside the swizzled row; MN-major:
+                        // step kUmmaK whole rows (kUmmaK * 128 bytes)
+                        const uint64_t ad = A_MN ? ptx::sdesc_sw128(sa + kk * (kUmmaK * kRowBytes), kMnBlockBytes, 1024)
+                                                 : ptx::sdesc_sw128(sa + kk * 32, 16, 1024);
+                        const uint64_t bd = B_MN ? ptx::sdesc_sw128(sb + kk * (kUmmaK * kRowBytes), kMnBlockBytes, 1024)
+                                                 : ptx::sdesc_sw128(sb + kk * 32, 16, 1024);
+                        if constexpr (std::is_same<ElemT, float>::value)
+                            ptx::mma_tf32(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        else
+                            ptx::mma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     ptx::mma_commit(&empty[stage]);
                     if (++stage == S) {
@@ -491,8 +582,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------ epilogue warps
-        const int quarter = warp & 3;  // TMEM lanes this warp may access
-        const int row_in_tile = quarter * 32 + lane;
+        const int ew = warp - 2;                 // epilogue warp index
+        const int quarter = warp & 3;            // TMEM lanes this warp may access
+        const int group = ew / 4;                // which share of the tile's columns
+        const int c0 = group * kChunks / kGroups;
+        const int c1 = (group + 1) * kChunks / kGroups;
+        uint8_t *my_stage = staging + ew * (kOuts * 2 * Stage<OutT>::kBytes);
+        const CUtensorMap *tmC[2] = {&tmC0, &tmC1};
+        int chunk_ctr = 0;
+        bool prev_stored = false;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -503,13 +601,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
-            Epi::template apply<BN>(ep, shp, mb * kBM + row_in_tile, nb * BN, taddr);
+            const int row0 = mb * kBM + quarter * 32;  // first output row of this warp
+            const int row = row0 + lane;
+            const int n0 = nb * BN;
+            typename Epi::Row rs = Epi::begin(ep, row, row < shp.M);
+#pragma unroll 1
+            for (int c = c0; c < c1; ++c) {
+                float v[32];
+                ptx::tmem_ld32(taddr + c * 32, v);
+                const int n = n0 + c * 32;
+                const bool col_live = n < shp.N;
+                float o[kOuts > 0 ? kOuts : 1][32];
+                Epi::chunk(ep, rs, row, n, shp.N, row < shp.M && col_live, v, o);
+                if constexpr (kOuts > 0) {
+                    const int buf = chunk_ctr & 1;
+                    // the buffer's previous store (two chunks ago) must have read it
+                    if (lane == 0) {
+                        if (prev_stored)
+                            ptx::bulk_wait_read<1>();
+                        else
+                            ptx::bulk_wait_read<0>();
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < kOuts; ++k)
+                        Stage<OutT>::write(my_stage + (2 * k + buf) * Stage<OutT>::kBytes, lane, o[k]);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    const bool do_store = col_live && row0 < shp.M;
+                    if (lane == 0 && do_store) {
+#pragma unroll
+                        for (int k = 0; k < kOuts; ++k) {
+                            const uint8_t *src = my_stage + (2 * k + buf) * Stage<OutT>::kBytes;
+                            if (Epi::mode(ep) == 1)
+                                ptx::tma_reduce_add_2d(tmC[k], src, n, row0);
+                            else
+                                ptx::tma_store_2d(tmC[k], src, n, row0);
+                        }
+                        ptx::bulk_commit();
+                    }
+                    prev_stored = do_store;
+                    ++chunk_ctr;
+                }
+            }
+            Epi::end(ep, rs, row, n0, row < shp.M);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
+        // every output this warp staged has been written before the CTA exits
+        if (kOuts > 0 && lane == 0) ptx::bulk_wait_all();
+        __syncwarp();
     }
 
     ptx::tc_fence_before();

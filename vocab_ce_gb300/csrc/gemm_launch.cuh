@@ -1,16 +1,16 @@
 // gemm_launch.cuh -- host-side launch of tc_gemm_kernel: tensor maps, tile
-// grid, rasterisation and the persistent grid size.
+// width, rasterisation and the persistent grid size.
 #pragma once
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "gemm.cuh"
+#include "gemm_pair.cuh"
 #include "host.h"
 
 namespace tpce {
-// Internal linkage: every translation unit gets its own kernels and launch
-// state (a kernel instantiated in two units is two device functions).
 namespace {
 
 // An operand as it sits in memory (row-major, row pitch `ld` elements).
@@ -22,9 +22,46 @@ struct Operand {
     int64_t rows, cols, ld;
 };
 
+// An output the epilogue writes with TMA stores: [rows, cols], row pitch ld
+// elements of the epilogue's output type.
+struct OutView {
+    void *ptr;
+    int64_t rows, cols, ld;
+};
+
 // Tiles are walked in groups of `group_m` row-blocks, row-block fastest, so
 // the CTAs of one wave share a few A and B panels in L2.
 inline int pick_group_m(int tiles_m) { return std::max(1, std::min(tiles_m, 16)); }
+
+// Tile widths a launch may use.
+enum : unsigned { kBN128 = 1u, kBN192 = 2u, kBN256 = 4u };
+// Build-time tuning knob: the tile widths launch_gemm_auto may choose from.
+#ifndef TPCE_BN_MASK
+#define TPCE_BN_MASK 7u
+#endif
+
+// The tile width that finishes an M x N output soonest: the waves of
+// 128 x BN tiles over the SMs times the tile time, taken as BN plus a fixed
+// per-tile cost worth 96 columns (fitted on GB300: 192-wide tiles win only
+// where they save a whole wave, e.g. N = 3072 on 64 row-blocks, and lose on
+// N = 12288); 128-wide tiles are charged 10% more for their higher operand
+// traffic per FLOP.
+inline int pick_bn(int64_t M, int64_t N, int sms, unsigned allowed) {
+    int best = 0;
+    double best_cost = 0.0;
+    for (int bn : {256, 192, 128}) {
+        const unsigned bit = bn == 256 ? kBN256 : (bn == 192 ? kBN192 : kBN128);
+        if (!(allowed & bit)) continue;
+        const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
+        const int64_t waves = (tiles + sms - 1) / sms;
+        const double cost = static_cast<double>(waves) * (bn + 96) * (bn == 128 ? 1.1 : 1.0);
+        if (best == 0 || cost < best_cost - 1e-9) {
+            best = bn;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
 
 // Raise the kernel's dynamic shared-memory limit, once per device. `done` must
 // be distinct per kernel instantiation (kernels of equal signature share a
@@ -42,19 +79,32 @@ inline tpce_status set_smem_attr(K kern, uint32_t bytes, bool (&done)[64], std::
     return TPCE_OK;
 }
 
-// D = A * B with the epilogue Epi. Offsets shift the operands' coordinates
-// inside their tensor maps (used to address one vocabulary chunk of E).
-template <int BN, bool A_MN, bool B_MN, class Epi>
-tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, int M, int N, int K, int a_off_mn,
-                        int a_off_k, int b_off_mn, int b_off_k, const typename Epi::Params &ep,
+// D = A * B with the epilogue Epi, writing outs[0 .. Epi::kOuts). Offsets
+// shift the operands' coordinates inside their tensor maps (used to address
+// one vocabulary chunk of E).
+template <typename ElemT, int BN, bool A_MN, bool B_MN, class Epi>
+tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, const OutView *outs, int M, int N,
+                        int K, int a_off_mn, int a_off_k, int b_off_mn, int b_off_k, const typename Epi::Params &ep,
                         cudaStream_t stream, bool timed = true) {
-    using Cfg = TileCfg<BN>;
+    using Cfg = KernelCfg<BN, Epi>;
+    using OutT = typename Epi::Out;
+    constexpr bool kF32 = std::is_same<ElemT, float>::value;
+    constexpr uint32_t kBoxK = kRowBytes / sizeof(ElemT);  // contraction elements per 128-byte row
     if (M <= 0 || N <= 0 || K <= 0) return TPCE_ERR_SHAPE;
-    CUtensorMap ta, tb;
-    bool ok = A_MN ? make_tmap_bf16(&ta, a.ptr, a.cols, a.rows, a.ld, 64, 64)
-                   : make_tmap_bf16(&ta, a.ptr, a.cols, a.rows, a.ld, 64, kBM);
-    ok = ok && (B_MN ? make_tmap_bf16(&tb, b.ptr, b.cols, b.rows, b.ld, 64, 64)
-                     : make_tmap_bf16(&tb, b.ptr, b.cols, b.rows, b.ld, 64, BN));
+    const int dt = kF32 ? 1 : 0;
+    CUtensorMap ta, tb, tc[2];
+    bool ok = A_MN ? make_tmap(&ta, dt, a.ptr, a.cols, a.rows, a.ld, 64, 64)
+                   : make_tmap(&ta, dt, a.ptr, a.cols, a.rows, a.ld, kBoxK, kBM);
+    ok = ok && (B_MN ? make_tmap(&tb, dt, b.ptr, b.cols, b.rows, b.ld, 64, 64)
+                     : make_tmap(&tb, dt, b.ptr, b.cols, b.rows, b.ld, kBoxK, BN));
+    const int odt = std::is_same<OutT, float>::value ? 1 : 0;
+    for (int k = 0; k < 2; ++k) {
+        if (k < Epi::kOuts)
+            ok = ok && make_tmap(&tc[k], odt, outs[k].ptr, outs[k].cols, outs[k].rows, outs[k].ld, 32, 32,
+                                 Stage<OutT>::kSwizzle);
+        else
+            tc[k] = ta;  // unused by this epilogue
+    }
     if (!ok) return fail(TPCE_ERR_CUDA, "cuTensorMapEncodeTiled rejected an operand of %s", name);
 
     GemmShape s;
@@ -63,14 +113,14 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, in
     s.K = K;
     s.tiles_m = (M + kBM - 1) / kBM;
     s.tiles_n = (N + BN - 1) / BN;
-    s.k_blocks = (K + kBK - 1) / kBK;
+    s.k_blocks = (K + static_cast<int>(kBoxK) - 1) / static_cast<int>(kBoxK);
     s.group_m = pick_group_m(s.tiles_m);
     s.a_off_mn = a_off_mn;
     s.a_off_k = a_off_k;
     s.b_off_mn = b_off_mn;
     s.b_off_k = b_off_k;
 
-    auto kern = tc_gemm_kernel<BN, A_MN, B_MN, Epi>;
+    auto kern = tc_gemm_kernel<ElemT, BN, A_MN, B_MN, Epi>;
     static std::mutex attr_mu;
     static bool attr_done[64] = {};
     tpce_status st = set_smem_attr(kern, Cfg::kSmemBytes, attr_done, attr_mu);
@@ -81,8 +131,96 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, in
     const int64_t tiles = static_cast<int64_t>(s.tiles_m) * s.tiles_n;
     const int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
     KernelTimer timer(timed ? name : nullptr, stream);
-    kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(ta, tb, s, ep, err);
+    kern<<<grid, 64 + 32 * Epi::kWarps, Cfg::kSmemBytes, stream>>>(ta, tb, tc[0], tc[1], s, ep, err);
     return check_launch(name);
+}
+
+// The CTA-pair kernel (bf16 operands): a 256 x BN tile per cluster of two CTAs.
+// Build-time switch: 256 (default) runs every bf16 GEMM on CTA pairs with
+// 256 x 256 tiles; 0 keeps the one-CTA kernel (measured on GB300: the pair
+// kernel is 10-12% faster, e.g. 1640 -> 1830 TFLOP/s on the 70B MLP step).
+#ifndef TPCE_PAIR_BN
+#define TPCE_PAIR_BN 256
+#endif
+
+template <int BN, bool A_MN, bool B_MN, class Epi>
+tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &b, const OutView *outs, int M, int N,
+                             int K, int a_off_mn, int a_off_k, int b_off_mn, int b_off_k,
+                             const typename Epi::Params &ep, cudaStream_t stream) {
+    using Cfg = PairCfg<BN, Epi>;
+    using OutT = typename Epi::Out;
+    if (M <= 0 || N <= 0 || K <= 0) return TPCE_ERR_SHAPE;
+    CUtensorMap ta, tb, tc[2];
+    bool ok = A_MN ? make_tmap(&ta, 0, a.ptr, a.cols, a.rows, a.ld, 64, 64)
+                   : make_tmap(&ta, 0, a.ptr, a.cols, a.rows, a.ld, 64, kBM);
+    ok = ok && (B_MN ? make_tmap(&tb, 0, b.ptr, b.cols, b.rows, b.ld, 64, 64)
+                     : make_tmap(&tb, 0, b.ptr, b.cols, b.rows, b.ld, 64, BN / 2));
+    const int odt = std::is_same<OutT, float>::value ? 1 : 0;
+    for (int k = 0; k < 2; ++k) {
+        if (k < Epi::kOuts)
+            ok = ok && make_tmap(&tc[k], odt, outs[k].ptr, outs[k].cols, outs[k].rows, outs[k].ld, 32, 32,
+                                 Stage<OutT>::kSwizzle);
+        else
+            tc[k] = ta;
+    }
+    if (!ok) return fail(TPCE_ERR_CUDA, "cuTensorMapEncodeTiled rejected an operand of %s", name);
+    GemmShape s;
+    s.M = M;
+    s.N = N;
+    s.K = K;
+    s.tiles_m = (M + 2 * kBM - 1) / (2 * kBM);
+    s.tiles_n = (N + BN - 1) / BN;
+    s.k_blocks = (K + 63) / 64;
+    s.group_m = pick_group_m(s.tiles_m);
+    s.a_off_mn = a_off_mn;
+    s.a_off_k = a_off_k;
+    s.b_off_mn = b_off_mn;
+    s.b_off_k = b_off_k;
+    auto kern = tc_gemm_pair_kernel<BN, A_MN, B_MN, Epi>;
+    static std::mutex attr_mu;
+    static bool attr_done[64] = {};
+    tpce_status st = set_smem_attr(kern, Cfg::kSmemBytes, attr_done, attr_mu);
+    if (st != TPCE_OK) return st;
+    const int sms = num_sms();
+    uint32_t *err = device_error_word();
+    if (sms < 2 || err == nullptr) return fail(TPCE_ERR_CUDA, "device query failed (%s)", name);
+    const int64_t tiles = static_cast<int64_t>(s.tiles_m) * s.tiles_n;
+    const int grid = 2 * static_cast<int>(std::min<int64_t>(tiles, sms / 2));
+    KernelTimer timer(name, stream);
+    kern<<<grid, 64 + 32 * Epi::kWarps, Cfg::kSmemBytes, stream>>>(ta, tb, tc[0], tc[1], s, ep, err);
+    return check_launch(name);
+}
+
+// launch_gemm with the tile width chosen by pick_bn among `Allowed`.
+template <typename ElemT, bool A_MN, bool B_MN, class Epi, unsigned Allowed>
+tpce_status launch_gemm_auto(const char *name, const Operand &a, const Operand &b, const OutView *outs, int M,
+                             int N, int K, int a_off_mn, int a_off_k, int b_off_mn, int b_off_k,
+                             const typename Epi::Params &ep, cudaStream_t stream) {
+    if constexpr (TPCE_PAIR_BN != 0 && std::is_same<ElemT, __nv_bfloat16>::value && Epi::kWarps == 4) {
+        return launch_gemm_pair<TPCE_PAIR_BN, A_MN, B_MN, Epi>(name, a, b, outs, M, N, K, a_off_mn, a_off_k, b_off_mn,
+                                                              b_off_k, ep, stream);
+    } else {
+        const int sms = num_sms();
+        if (sms <= 0) return fail(TPCE_ERR_CUDA, "device query failed (%s)", name);
+        const unsigned allowed = (Allowed & TPCE_BN_MASK) ? (Allowed & TPCE_BN_MASK) : Allowed;
+        const int bn = pick_bn(M, N, sms, allowed);
+        if constexpr ((Allowed & kBN256) != 0) {
+            if (bn == 256)
+                return launch_gemm<ElemT, 256, A_MN, B_MN, Epi>(name, a, b, outs, M, N, K, a_off_mn, a_off_k,
+                                                               b_off_mn, b_off_k, ep, stream);
+        }
+        if constexpr ((Allowed & kBN192) != 0) {
+            if (bn == 192)
+                return launch_gemm<ElemT, 192, A_MN, B_MN, Epi>(name, a, b, outs, M, N, K, a_off_mn, a_off_k,
+                                                               b_off_mn, b_off_k, ep, stream);
+        }
+        if constexpr ((Allowed & kBN128) != 0) {
+            if (bn == 128)
+                return launch_gemm<ElemT, 128, A_MN, B_MN, Epi>(name, a, b, outs, M, N, K, a_off_mn, a_off_k,
+                                                               b_off_mn, b_off_k, ep, stream);
+        }
+        return fail(TPCE_ERR_SHAPE, "no tile width for %s", name);
+    }
 }
 
 }  // namespace

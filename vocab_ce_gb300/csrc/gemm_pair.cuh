@@ -1,0 +1,279 @@
+// gemm_pair.cuh -- the CTA-pair form of the tensor-core GEMM (bf16 operands).
+//
+// Two CTAs of a cluster share one 256 x BN output tile: the even CTA's MMA
+// thread issues tcgen05.mma.cta_group::2, which multiplies each CTA's own 128
+// rows of A by the full BN columns of B -- half of B held in each CTA's shared
+// memory -- into each CTA's own tensor memory. Per SM a pipeline stage holds
+// 128 rows of A and BN/2 rows of B (32 KB at BN = 256 instead of 48 KB), so
+// six stages fit and each SM reads a third less from L2 for the same FLOPs;
+// the one-CTA kernel is latency-bound on exactly those operand loads.
+//
+// Signalling between the two CTAs:
+//   full[s]    lives in the even CTA; both CTAs' TMA loads count their bytes
+//              on it (cp.async.bulk.tensor .cta_group::2 to the even CTA's
+//              barrier); the even CTA's producer arms it with both CTAs' bytes.
+//   empty[s]   in each CTA, arrived by the even CTA's MMA commit (multicast).
+//   tfull[a]   in each CTA, arrived by the even CTA's MMA commit (multicast).
+//   tempty[a]  lives in the even CTA; the epilogue warps of both CTAs arrive.
+// The epilogue is the one-CTA kernel's, applied to each CTA's 128 rows.
+#pragma once
+
+#include "gemm.cuh"
+
+namespace tpce {
+namespace {
+
+template <int BN, class Epi>
+struct PairCfg {
+    static_assert(BN == 128 || BN == 256, "pair tile width");
+    static constexpr uint32_t kABytes = kBM * kRowBytes;        // this CTA's 128 rows of A
+    static constexpr uint32_t kBBytes = (BN / 2) * kRowBytes;   // this CTA's half of B
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kStagingBytes =
+        static_cast<uint32_t>(Epi::kWarps) * Epi::kOuts * 2 * Stage<typename Epi::Out>::kBytes;
+    static constexpr uint32_t kBarrierBytes = 256;
+    static constexpr uint32_t kFree = kSmemMax - 1024 - kBarrierBytes - kStagingBytes;
+    static constexpr int kStages = (kFree / kStageBytes) > 6 ? 6 : static_cast<int>(kFree / kStageBytes);
+    static_assert(kStages >= 3, "too few pipeline stages");
+    static constexpr uint32_t kTmemCols = 2 * BN <= 256 ? 256 : 512;
+    static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024 + kBarrierBytes;
+};
+
+template <int BN, bool A_MN, bool B_MN, class Epi>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarps, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
+                        const GemmShape shp, const typename Epi::Params ep, uint32_t *err) {
+    using C = PairCfg<BN, Epi>;
+    using ET = ElemTraits<__nv_bfloat16>;
+    using OutT = typename Epi::Out;
+    static_assert(Epi::kWarps == 4, "pair epilogue: one warp per TMEM lane quarter");
+    constexpr int S = C::kStages;
+    constexpr int kBK = ET::kBK;
+    constexpr int kUmmaK = ET::kUmmaK;
+    constexpr int kHalfN = BN / 2;
+    constexpr uint32_t kIdesc = ptx::idesc_f32acc(2 * kBM, BN, ET::kFmt, A_MN, B_MN);
+    constexpr int kChunks = BN / 32;
+    constexpr int kOuts = Epi::kOuts;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *staging = smem + S * C::kStageBytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(staging + C::kStagingBytes);
+    uint64_t *empty = full + S;
+    uint64_t *tfull = empty + S;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();  // 0: the even CTA, which issues the MMAs
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            ptx::mbar_init(&full[i], 1);
+            ptx::mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&tfull[i], 1);
+            ptx::mbar_init(&tempty[i], 2 * Epi::kWarps);
+        }
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(tmem_slot, C::kTmemCols);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    // both CTAs' barriers exist before either signals the other
+    ptx::cluster_sync();
+
+    const int num_tiles = shp.tiles_m * shp.tiles_n;  // tiles of 256 x BN
+    const int cluster_id = blockIdx.x >> 1;
+    const int clusters = gridDim.x >> 1;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0;
+            uint32_t issued_parity = 0;
+            for (int tile = cluster_id; tile < num_tiles && !*abort_flag; tile += clusters) {
+                int mb, nb;
+                tile_coords(tile, shp, mb, nb);
+                const int m0 = mb * (2 * kBM) + static_cast<int>(rank) * kBM;
+                const int nh0 = nb * BN + static_cast<int>(rank) * kHalfN;
+                for (int kb = 0; kb < shp.k_blocks; ++kb) {
+                    if (!ptx::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, 1)) break;
+                    const uint32_t bar = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
+                    issued |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    uint8_t *sa = smem + stage * C::kStageBytes;
+                    uint8_t *sb = sa + C::kABytes;
+                    const int k0 = kb * kBK;
+                    if (!A_MN) {
+                        ptx::tma_load_2d_pair(sa, &tmA, bar, k0 + shp.a_off_k, m0 + shp.a_off_mn);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < kBM / 64; ++j)
+                            ptx::tma_load_2d_pair(sa + j * kMnBlockBytes, &tmA, bar, m0 + shp.a_off_mn + 64 * j,
+                                                  k0 + shp.a_off_k);
+                    }
+                    if (!B_MN) {
+                        ptx::tma_load_2d_pair(sb, &tmB, bar, k0 + shp.b_off_k, nh0 + shp.b_off_mn);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < kHalfN / 64; ++j)
+                            ptx::tma_load_2d_pair(sb + j * kMnBlockBytes, &tmB, bar, nh0 + shp.b_off_mn + 64 * j,
+                                                  k0 + shp.b_off_k);
+                    }
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (*abort_flag && rank == 0) {
+                // the even CTA's full barriers count both CTAs' loads: let them land
+                for (int s = 0; s < S; ++s)
+                    if (issued & (1u << s)) ptx::mbar_wait_drain(&full[s], (issued_parity >> s) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (even CTA)
+        if (lane == 0 && rank == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            for (int tile = cluster_id; tile < num_tiles; tile += clusters) {
+                if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, err, 2)) break;
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                bool ok = true;
+                for (int kb = 0; kb < shp.k_blocks; ++kb) {
+                    if (!ptx::mbar_wait(&full[stage], phase, abort_flag, err, 3)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = ptx::smem_u32(smem + stage * C::kStageBytes);
+                    const uint32_t sb = sa + C::kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                        const uint64_t ad = A_MN ? ptx::sdesc_sw128(sa + kk * (kUmmaK * kRowBytes), kMnBlockBytes, 1024)
+                                                 : ptx::sdesc_sw128(sa + kk * 32, 16, 1024);
+                        const uint64_t bd = B_MN ? ptx::sdesc_sw128(sb + kk * (kUmmaK * kRowBytes), kMnBlockBytes, 1024)
+                                                 : ptx::sdesc_sw128(sb + kk * 32, 16, 1024);
+                        ptx::mma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit_pair(&empty[stage]);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit_pair(&tfull[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+            }
+            ptx::mma_commit_pair(drain);
+            ptx::mbar_wait_drain(drain, 0);
+        }
+    } else {
+        // ------------------------------------------------ epilogue warps (both CTAs)
+        const int ew = warp - 2;
+        const int quarter = warp & 3;
+        uint8_t *my_stage = staging + ew * (kOuts * 2 * Stage<OutT>::kBytes);
+        const CUtensorMap *tmC[2] = {&tmC0, &tmC1};
+        int chunk_ctr = 0;
+        bool prev_stored = false;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = cluster_id; tile < num_tiles; tile += clusters) {
+            int mb, nb;
+            tile_coords(tile, shp, mb, nb);
+            const bool ok = ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, err, 4);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            ptx::tc_fence_after();
+            const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+            const int row0 = mb * (2 * kBM) + static_cast<int>(rank) * kBM + quarter * 32;
+            const int row = row0 + lane;
+            const int n0 = nb * BN;
+            typename Epi::Row rs = Epi::begin(ep, row, row < shp.M);
+#pragma unroll 1
+            for (int c = 0; c < kChunks; ++c) {
+                float v[32];
+                ptx::tmem_ld32(taddr + c * 32, v);
+                const int n = n0 + c * 32;
+                const bool col_live = n < shp.N;
+                float o[kOuts > 0 ? kOuts : 1][32];
+                Epi::chunk(ep, rs, row, n, shp.N, row < shp.M && col_live, v, o);
+                if constexpr (kOuts > 0) {
+                    const int buf = chunk_ctr & 1;
+                    if (lane == 0) {
+                        if (prev_stored)
+                            ptx::bulk_wait_read<1>();
+                        else
+                            ptx::bulk_wait_read<0>();
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < kOuts; ++k)
+                        Stage<OutT>::write(my_stage + (2 * k + buf) * Stage<OutT>::kBytes, lane, o[k]);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    const bool do_store = col_live && row0 < shp.M;
+                    if (lane == 0 && do_store) {
+#pragma unroll
+                        for (int k = 0; k < kOuts; ++k) {
+                            const uint8_t *src = my_stage + (2 * k + buf) * Stage<OutT>::kBytes;
+                            if (Epi::mode(ep) == 1)
+                                ptx::tma_reduce_add_2d(tmC[k], src, n, row0);
+                            else
+                                ptx::tma_store_2d(tmC[k], src, n, row0);
+                        }
+                        ptx::bulk_commit();
+                    }
+                    prev_stored = do_store;
+                    ++chunk_ctr;
+                }
+            }
+            Epi::end(ep, rs, row, n0, row < shp.M);
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&tempty[acc]), 0));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+        if (kOuts > 0 && lane == 0) ptx::bulk_wait_all();
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    // neither CTA leaves while the other may still read its shared memory or signal it
+    ptx::cluster_sync();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    }
+}
+
+}  // namespace
+}  // namespace tpce

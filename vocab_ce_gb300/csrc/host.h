@@ -34,16 +34,25 @@ class KernelTimer {
     cudaEvent_t start_ = nullptr;
 };
 
-// 2-D bf16 tensor map with 128-byte swizzle: `inner` contiguous elements per
-// row (row pitch `ld` elements), `outer` rows, box {box_inner, box_outer}.
-bool make_tmap_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t ld,
-                    uint32_t box_inner, uint32_t box_outer);
+// 2-D tensor map over bf16 (dt 0) or fp32 (dt 1) data: `inner` contiguous
+// elements per row (row pitch `ld` elements), `outer` rows, box
+// {box_inner, box_outer}, shared-memory swizzle of 128 or 64 bytes.
+bool make_tmap(CUtensorMap *m, int dt, const void *base, uint64_t inner, uint64_t outer, uint64_t ld,
+               uint32_t box_inner, uint32_t box_outer, int swizzle = 128);
 
-// fp32 column sums out[n] = sum_r X[r, n] of a bf16 [R, N] matrix (row pitch
-// ld), through a partial buffer of colsum_partial_floats(R, N) floats.
+// fp32 -> bf16, n elements (n % 8 == 0, 16-byte aligned)
+tpce_status f32_to_bf16(const float *in, void *out, int64_t n, cudaStream_t s);
+
+// fp32 column sums out[n] = sum_r X[r, n] of a bf16 (dt 0) or fp32 (dt 1)
+// [R, N] matrix (row pitch ld), through a partial buffer of
+// colsum_partial_floats(R, N) floats.
 size_t colsum_partial_floats(int64_t R, int64_t N);
-tpce_status colsum_bf16(const void *X, int64_t R, int64_t N, int64_t ld, float *out, float *partial,
-                        cudaStream_t s);
+tpce_status colsum(int dt, const void *X, int64_t R, int64_t N, int64_t ld, float *out, float *partial,
+                   cudaStream_t s);
+
+// out[c, r] = in[r, c] for an fp32 [R, C] matrix (row pitches ld_in, ld_out).
+tpce_status transpose_f32(const float *in, int64_t R, int64_t C, int64_t ld_in, float *out, int64_t ld_out,
+                          cudaStream_t s);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -102,17 +102,19 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool make_tmap_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t ld,
-                    uint32_t box_inner, uint32_t box_outer) {
+bool make_tmap(CUtensorMap *m, int dt, const void *base, uint64_t inner, uint64_t outer, uint64_t ld,
+               uint32_t box_inner, uint32_t box_outer, int swizzle) {
     auto fn = encode_fn();
-    if (!fn || inner == 0 || outer == 0 || !aligned16(base) || (ld * 2) % 16 != 0) return false;
+    const uint64_t esz = dt == 1 ? 4 : 2;
+    if (!fn || inner == 0 || outer == 0 || !aligned16(base) || (ld * esz) % 16 != 0) return false;
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {ld * 2};
+    cuuint64_t strides[1] = {ld * esz};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(m, dt == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -183,11 +185,29 @@ KernelTimer::~KernelTimer() {
 }
 
 // ------------------------------------------------------------------ column sums
+__device__ __forceinline__ void add8(const __nv_bfloat16 *p, float *acc) {
+    uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = __bfloat1622float2(h[i]);
+        acc[2 * i] += f.x;
+        acc[2 * i + 1] += f.y;
+    }
+}
+__device__ __forceinline__ void add8(const float *p, float *acc) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+}
+
 // Stage 1: block (x, y) sums rows [y*rows_per, (y+1)*rows_per) of 256 columns
-// starting at 256*x; each lane owns 8 adjacent columns (one 16-byte load per
+// starting at 256*x; each lane owns 8 adjacent columns (one vector load per
 // row), the 8 warps stride over the rows, and shared memory combines the warps.
-__global__ void __launch_bounds__(256) colsum_stage1(const __nv_bfloat16 *__restrict__ X, int64_t R, int64_t N,
-                                                     int64_t ld, int64_t rows_per, float *__restrict__ part) {
+template <typename T>
+__global__ void __launch_bounds__(256) colsum_stage1(const T *__restrict__ X, int64_t R, int64_t N, int64_t ld,
+                                                     int64_t rows_per, float *__restrict__ part) {
     __shared__ float red[8][256];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 256 + lane * 8;
@@ -195,16 +215,7 @@ __global__ void __launch_bounds__(256) colsum_stage1(const __nv_bfloat16 *__rest
     const int64_t r1 = min(R, r0 + rows_per);
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (c0 < N) {
-        for (int64_t r = r0 + warp; r < r1; r += 8) {
-            uint4 u = __ldg(reinterpret_cast<const uint4 *>(X + r * ld + c0));
-            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float2 f = __bfloat1622float2(h[i]);
-                acc[2 * i] += f.x;
-                acc[2 * i + 1] += f.y;
-            }
-        }
+        for (int64_t r = r0 + warp; r < r1; r += 8) add8(X + r * ld + c0, acc);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) red[warp][lane * 8 + i] = acc[i];
@@ -227,9 +238,13 @@ __global__ void colsum_stage2(const float *__restrict__ part, int S, int64_t N, 
     out[c] = s;
 }
 
+// Row splits of the column sum: enough blocks to cover the SMs about twice.
+// Fixed (not queried from the device) so workspace sizes are known on the host.
+constexpr int64_t kColsumTargetBlocks = 2 * 152;
+
 static int colsum_splits(int64_t R, int64_t N) {
     const int64_t col_blocks = (N + 255) / 256;
-    int64_t S = (2 * 152 + col_blocks - 1) / col_blocks;
+    int64_t S = (kColsumTargetBlocks + col_blocks - 1) / col_blocks;
     S = std::max<int64_t>(1, std::min<int64_t>(S, 64));
     S = std::min<int64_t>(S, std::max<int64_t>(1, R));
     return static_cast<int>(S);
@@ -237,8 +252,8 @@ static int colsum_splits(int64_t R, int64_t N) {
 
 size_t colsum_partial_floats(int64_t R, int64_t N) { return static_cast<size_t>(colsum_splits(R, N)) * N; }
 
-tpce_status colsum_bf16(const void *X, int64_t R, int64_t N, int64_t ld, float *out, float *partial,
-                        cudaStream_t s) {
+tpce_status colsum(int dt, const void *X, int64_t R, int64_t N, int64_t ld, float *out, float *partial,
+                   cudaStream_t s) {
     if (N <= 0) return TPCE_OK;
     if (R <= 0) return cuda_status(cudaMemsetAsync(out, 0, sizeof(float) * N, s));
     const int S = colsum_splits(R, N);
@@ -246,7 +261,11 @@ tpce_status colsum_bf16(const void *X, int64_t R, int64_t N, int64_t ld, float *
     {
         KernelTimer t("colsum_stage1", s);
         dim3 grid(static_cast<unsigned>((N + 255) / 256), static_cast<unsigned>(S));
-        colsum_stage1<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(X), R, N, ld, rows_per, partial);
+        if (dt == 1)
+            colsum_stage1<float><<<grid, 256, 0, s>>>(static_cast<const float *>(X), R, N, ld, rows_per, partial);
+        else
+            colsum_stage1<__nv_bfloat16>
+                <<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(X), R, N, ld, rows_per, partial);
         if (check_launch("colsum_stage1") != TPCE_OK) return TPCE_ERR_CUDA;
     }
     {
@@ -255,6 +274,61 @@ tpce_status colsum_bf16(const void *X, int64_t R, int64_t N, int64_t ld, float *
         if (check_launch("colsum_stage2") != TPCE_OK) return TPCE_ERR_CUDA;
     }
     return TPCE_OK;
+}
+
+// ------------------------------------------------------------------ fp32 -> bf16
+__global__ void f32_to_bf16_kernel(const float4 *__restrict__ in, uint4 *__restrict__ out, int64_t n8) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const float4 a = __ldg(in + 2 * i), b = __ldg(in + 2 * i + 1);
+        __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y), h1 = __floats2bfloat162_rn(a.z, a.w);
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(b.x, b.y), h3 = __floats2bfloat162_rn(b.z, b.w);
+        uint4 u;
+        u.x = *reinterpret_cast<uint32_t *>(&h0);
+        u.y = *reinterpret_cast<uint32_t *>(&h1);
+        u.z = *reinterpret_cast<uint32_t *>(&h2);
+        u.w = *reinterpret_cast<uint32_t *>(&h3);
+        out[i] = u;
+    }
+}
+
+tpce_status f32_to_bf16(const float *in, void *out, int64_t n, cudaStream_t s) {
+    if (n <= 0) return TPCE_OK;
+    const int64_t n8 = n / 8;
+    const int sms = num_sms();
+    const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, static_cast<int64_t>(std::max(sms, 1)) * 8);
+    KernelTimer t("f32_to_bf16", s);
+    f32_to_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(reinterpret_cast<const float4 *>(in),
+                                                                     static_cast<uint4 *>(out), n8);
+    return check_launch("f32_to_bf16");
+}
+
+// ------------------------------------------------------------------ transpose
+// 32 x 32 tiles through shared memory (one padding column avoids bank conflicts).
+__global__ void __launch_bounds__(256) transpose_f32_kernel(const float *__restrict__ in, int64_t R, int64_t C,
+                                                            int64_t ld_in, float *__restrict__ out, int64_t ld_out) {
+    __shared__ float tile[32][33];
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * 32 + threadIdx.x;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32;
+    for (int j = threadIdx.y; j < 32; j += 8) {
+        const int64_t r = r0 + j;
+        if (r < R && c < C) tile[j][threadIdx.x] = in[r * ld_in + c];
+    }
+    __syncthreads();
+    const int64_t orow = static_cast<int64_t>(blockIdx.x) * 32;  // output row = input column
+    const int64_t ocol = r0 + threadIdx.x;                       // output column = input row
+    for (int j = threadIdx.y; j < 32; j += 8) {
+        if (orow + j < C && ocol < R) out[(orow + j) * ld_out + ocol] = tile[threadIdx.x][j];
+    }
+}
+
+tpce_status transpose_f32(const float *in, int64_t R, int64_t C, int64_t ld_in, float *out, int64_t ld_out,
+                          cudaStream_t s) {
+    if (R <= 0 || C <= 0) return TPCE_OK;
+    KernelTimer t("transpose_f32", s);
+    dim3 grid(static_cast<unsigned>((C + 31) / 32), static_cast<unsigned>((R + 31) / 32));
+    transpose_f32_kernel<<<grid, dim3(32, 8), 0, s>>>(in, R, C, ld_in, out, ld_out);
+    return check_launch("transpose_f32");
 }
 
 }  // namespace tpce
