@@ -123,16 +123,16 @@ tpce_status ce_forward(const CeArgs &a, const CeWs &L, void *ws, float *lse_buf,
     tpce_status st;
     if constexpr (std::is_same<ElemT, __nv_bfloat16>::value && TPCE_PAIR_BN == 256) {
         if (L.bn == 256)
-            st = launch_gemm_pair<256, false, false, EpiCeStats>("ce_fwd_logits_stats", A, B, nullptr, Ti, vpi, hi,
+            st = launch_gemm_pair<256, false, false, EpiCeStats>("ce_fwd_logits_stats", A, B, nullptr, nullptr, Ti, vpi, hi,
                                                                  0, 0, 0, 0, ep, s);
         else
-            st = launch_gemm<ElemT, 128, false, false, EpiCeStats>("ce_fwd_logits_stats", A, B, nullptr, Ti, vpi,
+            st = launch_gemm<ElemT, 128, false, false, EpiCeStats>("ce_fwd_logits_stats", A, B, nullptr, nullptr, Ti, vpi,
                                                                    hi, 0, 0, 0, 0, ep, s);
     } else if (L.bn == 256)
-        st = launch_gemm<ElemT, 256, false, false, EpiCeStats>("ce_fwd_logits_stats", A, B, nullptr, Ti, vpi, hi, 0,
+        st = launch_gemm<ElemT, 256, false, false, EpiCeStats>("ce_fwd_logits_stats", A, B, nullptr, nullptr, Ti, vpi, hi, 0,
                                                                0, 0, 0, ep, s);
     else
-        st = launch_gemm<ElemT, 128, false, false, EpiCeStats>("ce_fwd_logits_stats", A, B, nullptr, Ti, vpi, hi, 0,
+        st = launch_gemm<ElemT, 128, false, false, EpiCeStats>("ce_fwd_logits_stats", A, B, nullptr, nullptr, Ti, vpi, hi, 0,
                                                                0, 0, 0, ep, s);
     if (st != TPCE_OK) return st;
     // exchange of the per-token statistics across shards
@@ -158,7 +158,7 @@ tpce_status ce_backward_bf16(const CeArgs &a, const CeWs &L, void *ws, const flo
             const OutView o[1] = {{dl, a.T, L.vc, L.vc}};
             typename EpiCeDlogits<bf>::Params ep{lse_buf, a.targets, a.grad_scale, vvi, n_base};
             st = launch_gemm_auto<bf, false, false, EpiCeDlogits<bf>, kBN192 | kBN256>(
-                "ce_bwd_logits_dl", A, B, o, Ti, vci, hi, 0, 0, n_base, 0, ep, s);
+                "ce_bwd_logits_dl", A, B, o, nullptr, Ti, vci, hi, 0, 0, n_base, 0, ep, s);
             if (st != TPCE_OK) return st;
         }
         // dE rows of this chunk = dl^T H (no exchange: the rows belong to one shard)
@@ -166,7 +166,7 @@ tpce_status ce_backward_bf16(const CeArgs &a, const CeWs &L, void *ws, const flo
             Operand A{dl, a.T, L.vc, L.vc};  // MN-major: K = T rows, M = vc columns
             Operand B{a.H, a.T, a.h, a.h};   // MN-major: K = T rows, N = h columns
             const OutView o[1] = {{static_cast<bf *>(a.dE) + static_cast<int64_t>(n_base) * a.h, L.vc, a.h, a.h}};
-            st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>("ce_bwd_dE", A, B, o, vci, hi, Ti,
+            st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>("ce_bwd_dE", A, B, o, nullptr, vci, hi, Ti,
                                                                                   0, 0, 0, 0, {nullptr}, s);
             if (st != TPCE_OK) return st;
         }
@@ -177,7 +177,7 @@ tpce_status ce_backward_bf16(const CeArgs &a, const CeWs &L, void *ws, const flo
             Operand B{a.E, a.v_pad, a.h, a.h};  // MN-major: K = v rows (from n_base), N = h columns
             const OutView o[1] = {{acc, a.T, a.h, a.h}};
             st = launch_gemm_auto<bf, false, true, EpiF32Accumulate, kBN192 | kBN256>(
-                "ce_bwd_dH_shard_sum", A, B, o, Ti, hi, vci, 0, 0, 0, n_base, {c == 0 ? 0 : 1}, s);
+                "ce_bwd_dH_shard_sum", A, B, o, nullptr, Ti, hi, vci, 0, 0, 0, n_base, {c == 0 ? 0 : 1}, s);
             if (st != TPCE_OK) return st;
         }
     }
@@ -203,7 +203,7 @@ tpce_status ce_backward_f32(const CeArgs &a, const CeWs &L, void *ws, const floa
             Operand B{a.E, a.v_pad, a.h, a.h};
             const OutView o[1] = {{dl, a.T, L.vc, L.vc}};
             typename EpiCeDlogits<float>::Params ep{lse_buf, a.targets, a.grad_scale, vvi, n_base};
-            st = launch_gemm<float, 128, false, false, EpiCeDlogits<float>>("ce_bwd_logits_dl", A, B, o, Ti, vci, hi,
+            st = launch_gemm<float, 128, false, false, EpiCeDlogits<float>>("ce_bwd_logits_dl", A, B, o, nullptr, Ti, vci, hi,
                                                                             0, 0, n_base, 0, ep, s);
             if (st != TPCE_OK) return st;
         }
@@ -212,7 +212,7 @@ tpce_status ce_backward_f32(const CeArgs &a, const CeWs &L, void *ws, const floa
             Operand A{dlt, L.vc, a.T, Tp};  // K-major: M = vc rows, K = T columns
             Operand B{Ht, a.h, a.T, Tp};    // K-major: N = h rows, K = T columns
             const OutView o[1] = {{static_cast<float *>(a.dE) + static_cast<int64_t>(n_base) * a.h, L.vc, a.h, a.h}};
-            st = launch_gemm<float, 128, false, false, EpiStore<float>>("ce_bwd_dE", A, B, o, vci, hi, Ti, 0, 0, 0,
+            st = launch_gemm<float, 128, false, false, EpiStore<float>>("ce_bwd_dE", A, B, o, nullptr, vci, hi, Ti, 0, 0, 0,
                                                                         0, {nullptr}, s);
             if (st != TPCE_OK) return st;
         }
@@ -220,7 +220,7 @@ tpce_status ce_backward_f32(const CeArgs &a, const CeWs &L, void *ws, const floa
             Operand A{dl, a.T, L.vc, L.vc};        // K-major [T, vc]
             Operand B{Et, a.h, a.v_pad, a.v_pad};  // K-major: N = h rows, K = v columns (from n_base)
             const OutView o[1] = {{a.dH, a.T, a.h, a.h}};
-            st = launch_gemm<float, 128, false, false, EpiF32Accumulate>("ce_bwd_dH_shard_sum", A, B, o, Ti, hi, vci,
+            st = launch_gemm<float, 128, false, false, EpiF32Accumulate>("ce_bwd_dH_shard_sum", A, B, o, nullptr, Ti, hi, vci,
                                                                          0, 0, 0, n_base, {c == 0 ? 0 : 1}, s);
             if (st != TPCE_OK) return st;
         }

@@ -100,13 +100,13 @@ extern "C" tpce_status vocab_parallel_ce_loss_static(const void *H, const void *
     Operand b{E, v_pad, h, h};  // K-major: N = v_pad rows, K = h columns
     EpiCeStats::Params ep{stats, tau, targets, T, vvi, 0, 0, bn};
     if (f32)
-        st = launch_gemm<float, 128, false, false, EpiCeStats>("ce_static_logits_stats", a, b, nullptr, Ti, vpi, hi, 0, 0, 0,
+        st = launch_gemm<float, 128, false, false, EpiCeStats>("ce_static_logits_stats", a, b, nullptr, nullptr, Ti, vpi, hi, 0, 0, 0,
                                                                0, ep, s, /*timed=*/false);
     else if (bn == 256)
-        st = launch_gemm<__nv_bfloat16, 256, false, false, EpiCeStats>("ce_static_logits_stats", a, b, nullptr, Ti,
+        st = launch_gemm<__nv_bfloat16, 256, false, false, EpiCeStats>("ce_static_logits_stats", a, b, nullptr, nullptr, Ti,
                                                                        vpi, hi, 0, 0, 0, 0, ep, s, /*timed=*/false);
     else
-        st = launch_gemm<__nv_bfloat16, 128, false, false, EpiCeStats>("ce_static_logits_stats", a, b, nullptr, Ti, vpi, hi,
+        st = launch_gemm<__nv_bfloat16, 128, false, false, EpiCeStats>("ce_static_logits_stats", a, b, nullptr, nullptr, Ti, vpi, hi,
                                                                        0, 0, 0, 0, ep, s, /*timed=*/false);
     if (st != TPCE_OK) return st;
     ce_combine_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, s>>>(

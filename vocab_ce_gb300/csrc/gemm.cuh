@@ -181,6 +181,20 @@ struct Stage<__nv_bfloat16> {
             *reinterpret_cast<uint4 *>(row + ((j ^ ((r >> 1) & 3)) << 4)) = u;
         }
     }
+    __device__ static void read(const uint8_t *buf, int r, float *v) {
+        const uint8_t *row = buf + r * 64;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(row + ((j ^ ((r >> 1) & 3)) << 4));
+            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(h[i]);
+                v[8 * j + 2 * i] = f.x;
+                v[8 * j + 2 * i + 1] = f.y;
+            }
+        }
+    }
 };
 template <>
 struct Stage<float> {
@@ -194,14 +208,28 @@ struct Stage<float> {
             *reinterpret_cast<float4 *>(row + ((j ^ (r & 7)) << 4)) =
                 make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     }
+    __device__ static void read(const uint8_t *buf, int r, float *v) {
+        const uint8_t *row = buf + r * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 f = *reinterpret_cast<const float4 *>(row + ((j ^ (r & 7)) << 4));
+            v[4 * j] = f.x;
+            v[4 * j + 1] = f.y;
+            v[4 * j + 2] = f.z;
+            v[4 * j + 3] = f.w;
+        }
+    }
 };
 
 // --------------------------------------------------------------------------
 // Epilogues. Each turns the fp32 accumulator values of one 32-column chunk of
 // the thread's output row into kOuts output chunks (stored by the kernel), or
-// reduces them itself (kOuts = 0). begin/end run once per tile and row.
-// `live` is false for rows >= M or chunks at columns >= N: such values are
-// never stored, and the epilogue must not read memory for them.
+// reduces them itself (kOuts = 0). An epilogue with kIns = 1 also receives
+// the matching 32 values of one input tensor of the output's shape, which the
+// kernel brings into shared memory with TMA loads one chunk ahead. begin/end
+// run once per tile and row. `live` is false for rows >= M or chunks at
+// columns >= N: such values are never stored, and the epilogue must not read
+// memory for them.
 // --------------------------------------------------------------------------
 struct NoRow {};
 
@@ -210,6 +238,7 @@ template <typename OutT>
 struct EpiBiasGelu {
     static constexpr int kWarps = kHeavyEpiWarps;
     static constexpr int kOuts = 2;
+    static constexpr int kIns = 0;
     using Out = OutT;
     using Row = NoRow;
     struct Params {
@@ -218,7 +247,7 @@ struct EpiBiasGelu {
     __device__ static int mode(const Params &) { return 0; }
     __device__ static Row begin(const Params &, int, bool) { return {}; }
     __device__ static void chunk(const Params &p, Row &, int, int n, int N, bool, float (&v)[32],
-                                 float (&o)[kOuts][32]) {
+                                 const float (&in)[32], float (&o)[kOuts][32]) {
         float b[32];
         load_bias32(p.bias, n, N, b);
 #pragma unroll
@@ -235,6 +264,7 @@ template <typename OutT>
 struct EpiStore {
     static constexpr int kWarps = kHeavyEpiWarps;
     static constexpr int kOuts = 1;
+    static constexpr int kIns = 0;
     using Out = OutT;
     using Row = NoRow;
     struct Params {
@@ -243,7 +273,7 @@ struct EpiStore {
     __device__ static int mode(const Params &) { return 0; }
     __device__ static Row begin(const Params &, int, bool) { return {}; }
     __device__ static void chunk(const Params &p, Row &, int, int n, int N, bool, float (&v)[32],
-                                 float (&o)[kOuts][32]) {
+                                 const float (&in)[32], float (&o)[kOuts][32]) {
         float b[32];
         load_bias32(p.bias, n, N, b);
 #pragma unroll
@@ -252,32 +282,20 @@ struct EpiStore {
     __device__ static void end(const Params &, Row &, int, int, bool) {}
 };
 
-// dY epilogue of the backward: dU = acc (.) GeLU'(U), U read from the saved activations.
+// dY epilogue of the backward: dU = acc (.) GeLU'(U); the saved U arrives as
+// the kernel-loaded input chunk.
 template <typename OutT>
 struct EpiGeluGrad {
     static constexpr int kWarps = kHeavyEpiWarps;
     static constexpr int kOuts = 1;
+    static constexpr int kIns = 1;
     using Out = OutT;
     using Row = NoRow;
-    struct Params {
-        const OutT *U;
-        int64_t ld;
-    };
+    struct Params {};
     __device__ static int mode(const Params &) { return 0; }
     __device__ static Row begin(const Params &, int, bool) { return {}; }
-    __device__ static void chunk(const Params &p, Row &, int row, int n, int N, bool live, float (&v)[32],
+    __device__ static void chunk(const Params &, Row &, int, int, int, bool, float (&v)[32], const float (&u)[32],
                                  float (&o)[kOuts][32]) {
-        float u[32];
-        const OutT *src = p.U + static_cast<int64_t>(row) * p.ld + n;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (live && n + 8 * q < N) {
-                load8(src + 8 * q, u + 8 * q);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) u[8 * q + i] = 0.0f;
-            }
-        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[0][i] = v[i] * gelu_grad_f(u[i]);
     }
@@ -291,6 +309,7 @@ struct EpiGeluGrad {
 struct EpiCeStats {
     static constexpr int kWarps = 4;
     static constexpr int kOuts = 0;
+    static constexpr int kIns = 0;
     using Out = float;
     struct Row {
         int tgt;
@@ -312,7 +331,7 @@ struct EpiCeStats {
         return Row{live ? __ldg(p.targets + row) : -1, -INFINITY, 0.0f, 0.0f, false};
     }
     __device__ static void chunk(const Params &p, Row &r, int, int n, int, bool, float (&v)[32],
-                                 float (&)[1][32]) {
+                                 const float (&)[32], float (&)[1][32]) {
         const int g0 = p.n_base + n;                 // vocabulary id of v[0]
         const int nvalid = min(32, p.v_valid - g0);  // ids < v_valid are real
         if (nvalid > 0) {
@@ -350,6 +369,7 @@ template <typename OutT>
 struct EpiCeDlogits {
     static constexpr int kWarps = kHeavyEpiWarps;
     static constexpr int kOuts = 1;
+    static constexpr int kIns = 0;
     using Out = OutT;
     struct Row {
         float lse;
@@ -367,7 +387,7 @@ struct EpiCeDlogits {
         return Row{live ? __ldg(p.lse + row) : 0.0f, live ? __ldg(p.targets + row) : -1};
     }
     __device__ static void chunk(const Params &p, Row &r, int, int n, int, bool, float (&v)[32],
-                                 float (&o)[kOuts][32]) {
+                                 const float (&in)[32], float (&o)[kOuts][32]) {
         const int g0 = p.n_base + n;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -384,6 +404,7 @@ struct EpiCeDlogits {
 struct EpiF32Accumulate {
     static constexpr int kWarps = kHeavyEpiWarps;
     static constexpr int kOuts = 1;
+    static constexpr int kIns = 0;
     using Out = float;
     using Row = NoRow;
     struct Params {
@@ -392,7 +413,7 @@ struct EpiF32Accumulate {
     __device__ static int mode(const Params &p) { return p.add; }
     __device__ static Row begin(const Params &, int, bool) { return {}; }
     __device__ static void chunk(const Params &, Row &, int, int, int, bool, float (&v)[32],
-                                 float (&o)[kOuts][32]) {
+                                 const float (&in)[32], float (&o)[kOuts][32]) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[0][i] = v[i];
     }
@@ -400,10 +421,127 @@ struct EpiF32Accumulate {
 };
 
 // --------------------------------------------------------------------------
-// Shared-memory plan of one instantiation: operand stages, then output
-// staging (per epilogue warp: kOuts outputs x 2 buffers), then barriers.
+// The epilogue driver shared by the one-CTA and the CTA-pair kernels.
+// Per epilogue warp, shared memory holds 2 staging buffers per output and 2
+// input buffers (kIns = 1), each a 32 x 32 chunk; the input buffers have one
+// mbarrier each.
+// --------------------------------------------------------------------------
+template <class Epi>
+struct EpiSmem {
+    using OutT = typename Epi::Out;
+    static constexpr uint32_t kChunkBytes = Stage<OutT>::kBytes;
+    static constexpr uint32_t kOutBytes = Epi::kOuts * 2 * kChunkBytes;
+    static constexpr uint32_t kInBytes = Epi::kIns * 2 * kChunkBytes;
+    static constexpr uint32_t kWarpBytes = kOutBytes + kInBytes;
+    static constexpr uint32_t kBytes = static_cast<uint32_t>(Epi::kWarps) * kWarpBytes;
+};
+
+struct EpiWarp {
+    uint8_t *stage;     // this warp's buffers (outputs, then inputs)
+    uint64_t *in_bar;   // this warp's two input barriers
+    int chunk_ctr;      // output chunks staged so far
+    bool prev_stored;   // whether the previous output chunk was stored
+    uint32_t in_issued; // input chunk loads issued
+    uint32_t in_used;   // input chunk loads consumed
+};
+
+// Start the TMA load of the input chunk at (n, row0) into the next input buffer.
+template <class Epi>
+__device__ __forceinline__ void epi_issue_input(EpiWarp &w, const CUtensorMap *tmIn, int lane, int n, int row0) {
+    if constexpr (Epi::kIns > 0) {
+        constexpr uint32_t kB = EpiSmem<Epi>::kChunkBytes;
+        if (lane == 0) {
+            const uint32_t b = w.in_issued & 1u;
+            ptx::mbar_arrive_expect_tx(&w.in_bar[b], kB);
+            ptx::tma_load_2d(w.stage + EpiSmem<Epi>::kOutBytes + b * kB, tmIn, &w.in_bar[b], n, row0);
+        }
+        ++w.in_issued;
+    }
+}
+
+// Land the input loads still in flight (abort path), within a bounded time.
+template <class Epi>
+__device__ __forceinline__ void epi_drain_inputs(EpiWarp &w) {
+    if constexpr (Epi::kIns > 0) {
+        while (w.in_used < w.in_issued) {
+            ptx::mbar_wait_drain(&w.in_bar[w.in_used & 1u], (w.in_used >> 1) & 1u);
+            ++w.in_used;
+        }
+    }
+}
+
+// One tile's epilogue for this warp: chunks [c0, c1) of its 32 rows starting
+// at row0, columns from n0. The input chunk c0 must already be issued.
+// Returns false if a bounded wait gave up.
+template <class Epi>
+__device__ __forceinline__ bool epi_tile(const typename Epi::Params &ep, const GemmShape &shp, uint32_t taddr,
+                                         int row0, int n0, int c0, int c1, int lane, EpiWarp &w,
+                                         const CUtensorMap *tmC0, const CUtensorMap *tmC1,
+                                         const CUtensorMap *tmIn, volatile int *abort_flag, uint32_t *err) {
+    using OutT = typename Epi::Out;
+    constexpr int kOuts = Epi::kOuts;
+    constexpr uint32_t kB = EpiSmem<Epi>::kChunkBytes;
+    const int row = row0 + lane;
+    typename Epi::Row rs = Epi::begin(ep, row, row < shp.M);
+#pragma unroll 1
+    for (int c = c0; c < c1; ++c) {
+        const int n = n0 + c * 32;
+        if (c + 1 < c1) epi_issue_input<Epi>(w, tmIn, lane, n + 32, row0);
+        float v[32];
+        ptx::tmem_ld32(taddr + c * 32, v);
+        float in[32];
+        if constexpr (Epi::kIns > 0) {
+            const uint32_t b = w.in_used & 1u;
+            const bool ok = ptx::mbar_wait(&w.in_bar[b], (w.in_used >> 1) & 1u, abort_flag, err, 5);
+            if (!__all_sync(0xffffffffu, ok)) return false;
+            Stage<OutT>::read(w.stage + EpiSmem<Epi>::kOutBytes + b * kB, lane, in);
+            __syncwarp();  // every lane has read the buffer before it is loaded again
+            ++w.in_used;
+        }
+        const bool col_live = n < shp.N;
+        float o[kOuts > 0 ? kOuts : 1][32];
+        Epi::chunk(ep, rs, row, n, shp.N, row < shp.M && col_live, v, in, o);
+        if constexpr (kOuts > 0) {
+            const int buf = w.chunk_ctr & 1;
+            // the buffer's previous store (two chunks ago) must have read it
+            if (lane == 0) {
+                if (w.prev_stored)
+                    ptx::bulk_wait_read<1>();
+                else
+                    ptx::bulk_wait_read<0>();
+            }
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < kOuts; ++k) Stage<OutT>::write(w.stage + (2 * k + buf) * kB, lane, o[k]);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            const bool do_store = col_live && row0 < shp.M;
+            if (lane == 0 && do_store) {
+#pragma unroll
+                for (int k = 0; k < kOuts; ++k) {
+                    const uint8_t *src = w.stage + (2 * k + buf) * kB;
+                    const CUtensorMap *tm = k == 0 ? tmC0 : tmC1;
+                    if (Epi::mode(ep) == 1)
+                        ptx::tma_reduce_add_2d(tm, src, n, row0);
+                    else
+                        ptx::tma_store_2d(tm, src, n, row0);
+                }
+                ptx::bulk_commit();
+            }
+            w.prev_stored = do_store;
+            ++w.chunk_ctr;
+        }
+    }
+    Epi::end(ep, rs, row, n0, row < shp.M);
+    return true;
+}
+
+// --------------------------------------------------------------------------
+// Shared-memory plan of one instantiation: operand stages, then epilogue
+// staging, then barriers.
 // --------------------------------------------------------------------------
 constexpr uint32_t kSmemMax = 232448;  // opt-in dynamic shared memory per block
+constexpr uint32_t kBarrierBytes = 512;
 
 template <int BN, class Epi>
 struct KernelCfg {
@@ -411,9 +549,7 @@ struct KernelCfg {
     static constexpr uint32_t kABytes = kBM * kRowBytes;
     static constexpr uint32_t kBBytes = BN * kRowBytes;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-    static constexpr uint32_t kStagingBytes =
-        static_cast<uint32_t>(Epi::kWarps) * Epi::kOuts * 2 * Stage<typename Epi::Out>::kBytes;
-    static constexpr uint32_t kBarrierBytes = 256;
+    static constexpr uint32_t kStagingBytes = EpiSmem<Epi>::kBytes;
     static constexpr uint32_t kFree = kSmemMax - 1024 - kBarrierBytes - kStagingBytes;
     static constexpr int kStages = (kFree / kStageBytes) > 6 ? 6 : static_cast<int>(kFree / kStageBytes);
     static_assert(kStages >= 3, "too few pipeline stages");
@@ -428,7 +564,8 @@ template <typename ElemT, int BN, bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
-                   const GemmShape shp, const typename Epi::Params ep, uint32_t *err) {
+                   const __grid_constant__ CUtensorMap tmIn, const GemmShape shp, const typename Epi::Params ep,
+                   uint32_t *err) {
     using C = KernelCfg<BN, Epi>;
     using ET = ElemTraits<ElemT>;
     using OutT = typename Epi::Out;
@@ -451,7 +588,8 @@ __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
     uint64_t *tfull = empty + S;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *in_bars = drain + 1;  // 2 per epilogue warp
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(in_bars + 2 * Epi::kWarps);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -466,6 +604,7 @@ __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
             ptx::mbar_init(&tfull[i], 1);
             ptx::mbar_init(&tempty[i], Epi::kWarps);
         }
+        for (int i = 0; i < 2 * Epi::kWarps; ++i) ptx::mbar_init(&in_bars[i], 1);
         ptx::mbar_init(drain, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -587,72 +726,31 @@ __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
         const int group = ew / 4;                // which share of the tile's columns
         const int c0 = group * kChunks / kGroups;
         const int c1 = (group + 1) * kChunks / kGroups;
-        uint8_t *my_stage = staging + ew * (kOuts * 2 * Stage<OutT>::kBytes);
-        const CUtensorMap *tmC[2] = {&tmC0, &tmC1};
-        int chunk_ctr = 0;
-        bool prev_stored = false;
+        EpiWarp w{staging + ew * EpiSmem<Epi>::kWarpBytes, in_bars + 2 * ew, 0, false, 0u, 0u};
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             int mb, nb;
             tile_coords(tile, shp, mb, nb);
+            const int row0 = mb * kBM + quarter * 32;  // first output row of this warp
+            const int n0 = nb * BN;
+            epi_issue_input<Epi>(w, &tmIn, lane, n0 + c0 * 32, row0);
             // the decision to go on must be warp-uniform: the TMEM loads are warp-collective
             const bool ok = ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, err, 4);
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
-            const int row0 = mb * kBM + quarter * 32;  // first output row of this warp
-            const int row = row0 + lane;
-            const int n0 = nb * BN;
-            typename Epi::Row rs = Epi::begin(ep, row, row < shp.M);
-#pragma unroll 1
-            for (int c = c0; c < c1; ++c) {
-                float v[32];
-                ptx::tmem_ld32(taddr + c * 32, v);
-                const int n = n0 + c * 32;
-                const bool col_live = n < shp.N;
-                float o[kOuts > 0 ? kOuts : 1][32];
-                Epi::chunk(ep, rs, row, n, shp.N, row < shp.M && col_live, v, o);
-                if constexpr (kOuts > 0) {
-                    const int buf = chunk_ctr & 1;
-                    // the buffer's previous store (two chunks ago) must have read it
-                    if (lane == 0) {
-                        if (prev_stored)
-                            ptx::bulk_wait_read<1>();
-                        else
-                            ptx::bulk_wait_read<0>();
-                    }
-                    __syncwarp();
-#pragma unroll
-                    for (int k = 0; k < kOuts; ++k)
-                        Stage<OutT>::write(my_stage + (2 * k + buf) * Stage<OutT>::kBytes, lane, o[k]);
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    const bool do_store = col_live && row0 < shp.M;
-                    if (lane == 0 && do_store) {
-#pragma unroll
-                        for (int k = 0; k < kOuts; ++k) {
-                            const uint8_t *src = my_stage + (2 * k + buf) * Stage<OutT>::kBytes;
-                            if (Epi::mode(ep) == 1)
-                                ptx::tma_reduce_add_2d(tmC[k], src, n, row0);
-                            else
-                                ptx::tma_store_2d(tmC[k], src, n, row0);
-                        }
-                        ptx::bulk_commit();
-                    }
-                    prev_stored = do_store;
-                    ++chunk_ctr;
-                }
-            }
-            Epi::end(ep, rs, row, n0, row < shp.M);
+            if (!epi_tile<Epi>(ep, shp, taddr, row0, n0, c0, c1, lane, w, &tmC0, &tmC1, &tmIn, abort_flag, err))
+                break;
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
-        // every output this warp staged has been written before the CTA exits
+        // every output this warp staged has been written, and every input load landed, before the CTA exits
         if (kOuts > 0 && lane == 0) ptx::bulk_wait_all();
+        epi_drain_inputs<Epi>(w);
         __syncwarp();
     }
 

@@ -83,9 +83,9 @@ inline tpce_status set_smem_attr(K kern, uint32_t bytes, bool (&done)[64], std::
 // shift the operands' coordinates inside their tensor maps (used to address
 // one vocabulary chunk of E).
 template <typename ElemT, int BN, bool A_MN, bool B_MN, class Epi>
-tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, const OutView *outs, int M, int N,
-                        int K, int a_off_mn, int a_off_k, int b_off_mn, int b_off_k, const typename Epi::Params &ep,
-                        cudaStream_t stream, bool timed = true) {
+tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, const OutView *outs,
+                        const OutView *ins, int M, int N, int K, int a_off_mn, int a_off_k, int b_off_mn,
+                        int b_off_k, const typename Epi::Params &ep, cudaStream_t stream, bool timed = true) {
     using Cfg = KernelCfg<BN, Epi>;
     using OutT = typename Epi::Out;
     constexpr bool kF32 = std::is_same<ElemT, float>::value;
@@ -105,6 +105,10 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
         else
             tc[k] = ta;  // unused by this epilogue
     }
+    CUtensorMap tin = ta;  // unused unless the epilogue takes an input
+    if (Epi::kIns > 0)
+        ok = ok && ins && make_tmap(&tin, odt, ins[0].ptr, ins[0].cols, ins[0].rows, ins[0].ld, 32, 32,
+                                    Stage<OutT>::kSwizzle);
     if (!ok) return fail(TPCE_ERR_CUDA, "cuTensorMapEncodeTiled rejected an operand of %s", name);
 
     GemmShape s;
@@ -131,7 +135,7 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
     const int64_t tiles = static_cast<int64_t>(s.tiles_m) * s.tiles_n;
     const int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
     KernelTimer timer(timed ? name : nullptr, stream);
-    kern<<<grid, 64 + 32 * Epi::kWarps, Cfg::kSmemBytes, stream>>>(ta, tb, tc[0], tc[1], s, ep, err);
+    kern<<<grid, 64 + 32 * Epi::kWarps, Cfg::kSmemBytes, stream>>>(ta, tb, tc[0], tc[1], tin, s, ep, err);
     return check_launch(name);
 }
 
@@ -144,9 +148,9 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
 #endif
 
 template <int BN, bool A_MN, bool B_MN, class Epi>
-tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &b, const OutView *outs, int M, int N,
-                             int K, int a_off_mn, int a_off_k, int b_off_mn, int b_off_k,
-                             const typename Epi::Params &ep, cudaStream_t stream) {
+tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &b, const OutView *outs,
+                             const OutView *ins, int M, int N, int K, int a_off_mn, int a_off_k, int b_off_mn,
+                             int b_off_k, const typename Epi::Params &ep, cudaStream_t stream, bool timed = true) {
     using Cfg = PairCfg<BN, Epi>;
     using OutT = typename Epi::Out;
     if (M <= 0 || N <= 0 || K <= 0) return TPCE_ERR_SHAPE;
@@ -163,6 +167,10 @@ tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &
         else
             tc[k] = ta;
     }
+    CUtensorMap tin = ta;  // unused unless the epilogue takes an input
+    if (Epi::kIns > 0)
+        ok = ok && ins && make_tmap(&tin, odt, ins[0].ptr, ins[0].cols, ins[0].rows, ins[0].ld, 32, 32,
+                                    Stage<OutT>::kSwizzle);
     if (!ok) return fail(TPCE_ERR_CUDA, "cuTensorMapEncodeTiled rejected an operand of %s", name);
     GemmShape s;
     s.M = M;
@@ -186,19 +194,19 @@ tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &
     if (sms < 2 || err == nullptr) return fail(TPCE_ERR_CUDA, "device query failed (%s)", name);
     const int64_t tiles = static_cast<int64_t>(s.tiles_m) * s.tiles_n;
     const int grid = 2 * static_cast<int>(std::min<int64_t>(tiles, sms / 2));
-    KernelTimer timer(name, stream);
-    kern<<<grid, 64 + 32 * Epi::kWarps, Cfg::kSmemBytes, stream>>>(ta, tb, tc[0], tc[1], s, ep, err);
+    KernelTimer timer(timed ? name : nullptr, stream);
+    kern<<<grid, 64 + 32 * Epi::kWarps, Cfg::kSmemBytes, stream>>>(ta, tb, tc[0], tc[1], tin, s, ep, err);
     return check_launch(name);
 }
 
 // launch_gemm with the tile width chosen by pick_bn among `Allowed`.
 template <typename ElemT, bool A_MN, bool B_MN, class Epi, unsigned Allowed>
-tpce_status launch_gemm_auto(const char *name, const Operand &a, const Operand &b, const OutView *outs, int M,
-                             int N, int K, int a_off_mn, int a_off_k, int b_off_mn, int b_off_k,
-                             const typename Epi::Params &ep, cudaStream_t stream) {
+tpce_status launch_gemm_auto(const char *name, const Operand &a, const Operand &b, const OutView *outs,
+                             const OutView *ins, int M, int N, int K, int a_off_mn, int a_off_k, int b_off_mn,
+                             int b_off_k, const typename Epi::Params &ep, cudaStream_t stream) {
     if constexpr (TPCE_PAIR_BN != 0 && std::is_same<ElemT, __nv_bfloat16>::value && Epi::kWarps == 4) {
-        return launch_gemm_pair<TPCE_PAIR_BN, A_MN, B_MN, Epi>(name, a, b, outs, M, N, K, a_off_mn, a_off_k, b_off_mn,
-                                                              b_off_k, ep, stream);
+        return launch_gemm_pair<TPCE_PAIR_BN, A_MN, B_MN, Epi>(name, a, b, outs, ins, M, N, K, a_off_mn, a_off_k,
+                                                              b_off_mn, b_off_k, ep, stream);
     } else {
         const int sms = num_sms();
         if (sms <= 0) return fail(TPCE_ERR_CUDA, "device query failed (%s)", name);
@@ -206,17 +214,17 @@ tpce_status launch_gemm_auto(const char *name, const Operand &a, const Operand &
         const int bn = pick_bn(M, N, sms, allowed);
         if constexpr ((Allowed & kBN256) != 0) {
             if (bn == 256)
-                return launch_gemm<ElemT, 256, A_MN, B_MN, Epi>(name, a, b, outs, M, N, K, a_off_mn, a_off_k,
+                return launch_gemm<ElemT, 256, A_MN, B_MN, Epi>(name, a, b, outs, ins, M, N, K, a_off_mn, a_off_k,
                                                                b_off_mn, b_off_k, ep, stream);
         }
         if constexpr ((Allowed & kBN192) != 0) {
             if (bn == 192)
-                return launch_gemm<ElemT, 192, A_MN, B_MN, Epi>(name, a, b, outs, M, N, K, a_off_mn, a_off_k,
+                return launch_gemm<ElemT, 192, A_MN, B_MN, Epi>(name, a, b, outs, ins, M, N, K, a_off_mn, a_off_k,
                                                                b_off_mn, b_off_k, ep, stream);
         }
         if constexpr ((Allowed & kBN128) != 0) {
             if (bn == 128)
-                return launch_gemm<ElemT, 128, A_MN, B_MN, Epi>(name, a, b, outs, M, N, K, a_off_mn, a_off_k,
+                return launch_gemm<ElemT, 128, A_MN, B_MN, Epi>(name, a, b, outs, ins, M, N, K, a_off_mn, a_off_k,
                                                                b_off_mn, b_off_k, ep, stream);
         }
         return fail(TPCE_ERR_SHAPE, "no tile width for %s", name);

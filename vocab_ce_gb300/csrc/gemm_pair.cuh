@@ -29,9 +29,7 @@ struct PairCfg {
     static constexpr uint32_t kABytes = kBM * kRowBytes;        // this CTA's 128 rows of A
     static constexpr uint32_t kBBytes = (BN / 2) * kRowBytes;   // this CTA's half of B
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-    static constexpr uint32_t kStagingBytes =
-        static_cast<uint32_t>(Epi::kWarps) * Epi::kOuts * 2 * Stage<typename Epi::Out>::kBytes;
-    static constexpr uint32_t kBarrierBytes = 256;
+    static constexpr uint32_t kStagingBytes = EpiSmem<Epi>::kBytes;
     static constexpr uint32_t kFree = kSmemMax - 1024 - kBarrierBytes - kStagingBytes;
     static constexpr int kStages = (kFree / kStageBytes) > 6 ? 6 : static_cast<int>(kFree / kStageBytes);
     static_assert(kStages >= 3, "too few pipeline stages");
@@ -43,10 +41,10 @@ template <int BN, bool A_MN, bool B_MN, class Epi>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarps, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
-                        const GemmShape shp, const typename Epi::Params ep, uint32_t *err) {
+                        const __grid_constant__ CUtensorMap tmIn, const GemmShape shp,
+                        const typename Epi::Params ep, uint32_t *err) {
     using C = PairCfg<BN, Epi>;
     using ET = ElemTraits<__nv_bfloat16>;
-    using OutT = typename Epi::Out;
     static_assert(Epi::kWarps == 4, "pair epilogue: one warp per TMEM lane quarter");
     constexpr int S = C::kStages;
     constexpr int kBK = ET::kBK;
@@ -64,7 +62,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
     uint64_t *tfull = empty + S;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *in_bars = drain + 1;  // 2 per epilogue warp
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(in_bars + 2 * Epi::kWarps);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -80,6 +79,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
             ptx::mbar_init(&tfull[i], 1);
             ptx::mbar_init(&tempty[i], 2 * Epi::kWarps);
         }
+        for (int i = 0; i < 2 * Epi::kWarps; ++i) ptx::mbar_init(&in_bars[i], 1);
         ptx::mbar_init(drain, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -198,62 +198,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
         // ------------------------------------------------ epilogue warps (both CTAs)
         const int ew = warp - 2;
         const int quarter = warp & 3;
-        uint8_t *my_stage = staging + ew * (kOuts * 2 * Stage<OutT>::kBytes);
-        const CUtensorMap *tmC[2] = {&tmC0, &tmC1};
-        int chunk_ctr = 0;
-        bool prev_stored = false;
+        EpiWarp w{staging + ew * EpiSmem<Epi>::kWarpBytes, in_bars + 2 * ew, 0, false, 0u, 0u};
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = cluster_id; tile < num_tiles; tile += clusters) {
             int mb, nb;
             tile_coords(tile, shp, mb, nb);
+            const int row0 = mb * (2 * kBM) + static_cast<int>(rank) * kBM + quarter * 32;
+            const int n0 = nb * BN;
+            epi_issue_input<Epi>(w, &tmIn, lane, n0, row0);
             const bool ok = ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, err, 4);
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
-            const int row0 = mb * (2 * kBM) + static_cast<int>(rank) * kBM + quarter * 32;
-            const int row = row0 + lane;
-            const int n0 = nb * BN;
-            typename Epi::Row rs = Epi::begin(ep, row, row < shp.M);
-#pragma unroll 1
-            for (int c = 0; c < kChunks; ++c) {
-                float v[32];
-                ptx::tmem_ld32(taddr + c * 32, v);
-                const int n = n0 + c * 32;
-                const bool col_live = n < shp.N;
-                float o[kOuts > 0 ? kOuts : 1][32];
-                Epi::chunk(ep, rs, row, n, shp.N, row < shp.M && col_live, v, o);
-                if constexpr (kOuts > 0) {
-                    const int buf = chunk_ctr & 1;
-                    if (lane == 0) {
-                        if (prev_stored)
-                            ptx::bulk_wait_read<1>();
-                        else
-                            ptx::bulk_wait_read<0>();
-                    }
-                    __syncwarp();
-#pragma unroll
-                    for (int k = 0; k < kOuts; ++k)
-                        Stage<OutT>::write(my_stage + (2 * k + buf) * Stage<OutT>::kBytes, lane, o[k]);
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    const bool do_store = col_live && row0 < shp.M;
-                    if (lane == 0 && do_store) {
-#pragma unroll
-                        for (int k = 0; k < kOuts; ++k) {
-                            const uint8_t *src = my_stage + (2 * k + buf) * Stage<OutT>::kBytes;
-                            if (Epi::mode(ep) == 1)
-                                ptx::tma_reduce_add_2d(tmC[k], src, n, row0);
-                            else
-                                ptx::tma_store_2d(tmC[k], src, n, row0);
-                        }
-                        ptx::bulk_commit();
-                    }
-                    prev_stored = do_store;
-                    ++chunk_ctr;
-                }
-            }
-            Epi::end(ep, rs, row, n0, row < shp.M);
+            if (!epi_tile<Epi>(ep, shp, taddr, row0, n0, 0, kChunks, lane, w, &tmC0, &tmC1, &tmIn, abort_flag, err))
+                break;
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&tempty[acc]), 0));
@@ -261,6 +220,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
             if (acc == 0) acc_phase ^= 1;
         }
         if (kOuts > 0 && lane == 0) ptx::bulk_wait_all();
+        epi_drain_inputs<Epi>(w);
         __syncwarp();
     }
 

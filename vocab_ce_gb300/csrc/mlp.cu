@@ -90,13 +90,13 @@ tpce_status forward_bf16(const void *X, const void *A, const float *bA, const vo
     Operand b{A, h, f, f};  // MN-major: K = h rows, N = f columns
     const OutView o1[2] = {{U, T, f, f}, {Y, T, f, f}};
     tpce_status st = launch_gemm_auto<bf, false, true, EpiBiasGelu<bf>, kBN192 | kBN256>(
-        "mlp_fwd_gemm1_bias_gelu", a, b, o1, Ti, fi, hi, 0, 0, 0, 0, {bA}, s);
+        "mlp_fwd_gemm1_bias_gelu", a, b, o1, nullptr, Ti, fi, hi, 0, 0, 0, 0, {bA}, s);
     if (st != TPCE_OK) return st;
     // GEMM2 (row-parallel) + g: Z = sum_i Y_i B_i + bB
     Operand a2{Y, T, f, f};  // K-major [T, f]
     Operand b2{B, f, h, h};  // MN-major: K = f rows, N = h columns
     const OutView o2[1] = {{Z, T, h, h}};
-    return launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256>("mlp_fwd_gemm2_shard_sum", a2, b2, o2,
+    return launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256>("mlp_fwd_gemm2_shard_sum", a2, b2, o2, nullptr,
                                                                              Ti, hi, fi, 0, 0, 0, 0, {bB}, s);
 }
 
@@ -114,9 +114,9 @@ tpce_status backward_bf16(const void *dZ, const void *X, const void *A, const vo
         Operand a{dZ, T, h, h};  // K-major [T, h]
         Operand b{B, f, h, h};   // K-major: N = f rows, K = h columns
         const OutView o[1] = {{dU, T, f, f}};
-        typename EpiGeluGrad<bf>::Params ep{static_cast<const bf *>(U), f};
-        st = launch_gemm_auto<bf, false, false, EpiGeluGrad<bf>, kBN192 | kBN256>("mlp_bwd_dY_gelu_grad", a, b, o,
-                                                                                   Ti, fi, hi, 0, 0, 0, 0, ep, s);
+        const OutView in[1] = {{const_cast<void *>(U), T, f, f}};  // read by TMA, never written
+        st = launch_gemm_auto<bf, false, false, EpiGeluGrad<bf>, kBN192 | kBN256>("mlp_bwd_dY_gelu_grad", a, b, o, in,
+                                                                                   Ti, fi, hi, 0, 0, 0, 0, {}, s);
         if (st != TPCE_OK) return st;
     }
     // dB_i = Y_i^T dZ
@@ -124,7 +124,7 @@ tpce_status backward_bf16(const void *dZ, const void *X, const void *A, const vo
         Operand a{Y, T, f, f};   // MN-major: K = T rows, M = f columns
         Operand b{dZ, T, h, h};  // MN-major: K = T rows, N = h columns
         const OutView o[1] = {{dB, f, h, h}};
-        st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>("mlp_bwd_dB", a, b, o, fi, hi, Ti, 0,
+        st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>("mlp_bwd_dB", a, b, o, nullptr, fi, hi, Ti, 0,
                                                                               0, 0, 0, {nullptr}, s);
         if (st != TPCE_OK) return st;
     }
@@ -133,7 +133,7 @@ tpce_status backward_bf16(const void *dZ, const void *X, const void *A, const vo
         Operand a{X, T, h, h};   // MN-major: K = T rows, M = h columns
         Operand b{dU, T, f, f};  // MN-major: K = T rows, N = f columns
         const OutView o[1] = {{dA, h, f, f}};
-        st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>("mlp_bwd_dA", a, b, o, hi, fi, Ti, 0,
+        st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>("mlp_bwd_dA", a, b, o, nullptr, hi, fi, Ti, 0,
                                                                               0, 0, 0, {nullptr}, s);
         if (st != TPCE_OK) return st;
     }
@@ -142,7 +142,7 @@ tpce_status backward_bf16(const void *dZ, const void *X, const void *A, const vo
         Operand a{dU, T, f, f};  // K-major [T, f]
         Operand b{A, h, f, f};   // K-major: N = h rows, K = f columns
         const OutView o[1] = {{dX, T, h, h}};
-        st = launch_gemm_auto<bf, false, false, EpiStore<bf>, kBN192 | kBN256>("mlp_bwd_dX_shard_sum", a, b, o, Ti,
+        st = launch_gemm_auto<bf, false, false, EpiStore<bf>, kBN192 | kBN256>("mlp_bwd_dX_shard_sum", a, b, o, nullptr, Ti,
                                                                                 hi, fi, 0, 0, 0, 0, {nullptr}, s);
         if (st != TPCE_OK) return st;
     }
@@ -164,14 +164,14 @@ tpce_status forward_f32(const float *X, const float *A, const float *bA, const f
         Operand a{X, T, h, h};    // K-major [T, h]
         Operand b{At, f, h, h};   // K-major: N = f rows, K = h columns
         const OutView o[2] = {{U, T, f, f}, {Y, T, f, f}};
-        st = launch_gemm<float, 128, false, false, EpiBiasGelu<float>>("mlp_fwd_gemm1_bias_gelu", a, b, o, Ti, fi,
+        st = launch_gemm<float, 128, false, false, EpiBiasGelu<float>>("mlp_fwd_gemm1_bias_gelu", a, b, o, nullptr, Ti, fi,
                                                                        hi, 0, 0, 0, 0, {bA}, s);
         if (st != TPCE_OK) return st;
     }
     Operand a2{Y, T, f, f};   // K-major [T, f]
     Operand b2{Bt, h, f, f};  // K-major: N = h rows, K = f columns
     const OutView o2[1] = {{Z, T, h, h}};
-    return launch_gemm<float, 128, false, false, EpiStore<float>>("mlp_fwd_gemm2_shard_sum", a2, b2, o2, Ti, hi, fi,
+    return launch_gemm<float, 128, false, false, EpiStore<float>>("mlp_fwd_gemm2_shard_sum", a2, b2, o2, nullptr, Ti, hi, fi,
                                                                   0, 0, 0, 0, {bB}, s);
 }
 
@@ -189,9 +189,9 @@ tpce_status backward_f32(const float *dZ, const float *X, const float *A, const 
         Operand a{dZ, T, h, h};  // K-major [T, h]
         Operand b{B, f, h, h};   // K-major: N = f rows, K = h columns
         const OutView o[1] = {{dU, T, f, f}};
-        typename EpiGeluGrad<float>::Params ep{U, f};
-        st = launch_gemm<float, 128, false, false, EpiGeluGrad<float>>("mlp_bwd_dY_gelu_grad", a, b, o, Ti, fi, hi,
-                                                                       0, 0, 0, 0, ep, s);
+        const OutView in[1] = {{const_cast<float *>(U), T, f, f}};  // read by TMA, never written
+        st = launch_gemm<float, 128, false, false, EpiGeluGrad<float>>("mlp_bwd_dY_gelu_grad", a, b, o, in, Ti, fi,
+                                                                       hi, 0, 0, 0, 0, {}, s);
         if (st != TPCE_OK) return st;
     }
     if ((st = transpose_f32(Y, T, f, f, Yt, Tp, s)) != TPCE_OK) return st;
@@ -202,7 +202,7 @@ tpce_status backward_f32(const float *dZ, const float *X, const float *A, const 
         Operand a{Yt, f, T, Tp};   // K-major: M = f rows, K = T columns
         Operand b{dZt, h, T, Tp};  // K-major: N = h rows, K = T columns
         const OutView o[1] = {{dB, f, h, h}};
-        st = launch_gemm<float, 128, false, false, EpiStore<float>>("mlp_bwd_dB", a, b, o, fi, hi, Ti, 0, 0, 0, 0,
+        st = launch_gemm<float, 128, false, false, EpiStore<float>>("mlp_bwd_dB", a, b, o, nullptr, fi, hi, Ti, 0, 0, 0, 0,
                                                                     {nullptr}, s);
         if (st != TPCE_OK) return st;
     }
@@ -210,7 +210,7 @@ tpce_status backward_f32(const float *dZ, const float *X, const float *A, const 
         Operand a{Xt, h, T, Tp};   // K-major: M = h rows, K = T columns
         Operand b{dUt, f, T, Tp};  // K-major: N = f rows, K = T columns
         const OutView o[1] = {{dA, h, f, f}};
-        st = launch_gemm<float, 128, false, false, EpiStore<float>>("mlp_bwd_dA", a, b, o, hi, fi, Ti, 0, 0, 0, 0,
+        st = launch_gemm<float, 128, false, false, EpiStore<float>>("mlp_bwd_dA", a, b, o, nullptr, hi, fi, Ti, 0, 0, 0, 0,
                                                                     {nullptr}, s);
         if (st != TPCE_OK) return st;
     }
@@ -218,7 +218,7 @@ tpce_status backward_f32(const float *dZ, const float *X, const float *A, const 
         Operand a{dU, T, f, f};  // K-major [T, f]
         Operand b{A, h, f, f};   // K-major: N = h rows, K = f columns
         const OutView o[1] = {{dX, T, h, h}};
-        st = launch_gemm<float, 128, false, false, EpiStore<float>>("mlp_bwd_dX_shard_sum", a, b, o, Ti, hi, fi, 0,
+        st = launch_gemm<float, 128, false, false, EpiStore<float>>("mlp_bwd_dX_shard_sum", a, b, o, nullptr, Ti, hi, fi, 0,
                                                                     0, 0, 0, {nullptr}, s);
         if (st != TPCE_OK) return st;
     }
