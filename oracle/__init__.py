@@ -75,6 +75,18 @@ def _load():
         lib.oracle_ce.argtypes = [I64, I64, I64, I64, P, P, P, D, P, P, P, P]
         lib.oracle_ce_sharded.restype = None
         lib.oracle_ce_sharded.argtypes = [I64, I64, I64, I64, ctypes.c_int, P, P, P, P, P, P, P]
+        lib.oracle_swish.restype = D
+        lib.oracle_swish.argtypes = [D]
+        lib.oracle_swish_grad.restype = D
+        lib.oracle_swish_grad.argtypes = [D]
+        lib.oracle_swiglu_forward.restype = None
+        lib.oracle_swiglu_forward.argtypes = [I64, I64, I64, P, P, P, P, P, P, P, P]
+        lib.oracle_swiglu_backward.restype = None
+        lib.oracle_swiglu_backward.argtypes = [I64, I64, I64, P, P, P, P, P, P, P, P, P, P]
+        lib.oracle_swiglu_backward_cols.restype = None
+        lib.oracle_swiglu_backward_cols.argtypes = [I64, I64, I64, P, P, P, P, P, I64, P, P, P, P, P, P]
+        lib.oracle_swiglu_sharded.restype = None
+        lib.oracle_swiglu_sharded.argtypes = [I64, I64, I64, ctypes.c_int, P, P, P, P, P, P, P, P, P, P]
         _lib = lib
         return lib
 
@@ -189,3 +201,63 @@ def ce_sharded(H, E, targets, v_valid: int, t: int) -> Dict[str, np.ndarray]:
     _load().oracle_ce_sharded(T, h, v_pad, v_valid, t, _ptr(H), _ptr(E), _ptr(tg),
                               _ptr(m), _ptr(s), _ptr(tau), _ptr(loss))
     return {"m": m, "s": s, "tau": tau, "loss": loss}
+
+
+def swish(x: float) -> float:
+    return float(_load().oracle_swish(float(x)))
+
+
+def swish_grad(x: float) -> float:
+    return float(_load().oracle_swish_grad(float(x)))
+
+
+def swiglu_forward(X, W1, b1, W2, b2) -> Dict[str, np.ndarray]:
+    """GU = X W1 + b1 ([G | Up]), Y = Swish(G) * Up, Z = Y W2 + b2 (unsharded)."""
+    X, W1, b1, W2, b2 = map(_f64, (X, W1, b1, W2, b2))
+    T, h = X.shape
+    f = W1.shape[1] // 2
+    GU = np.empty((T, 2 * f)); Y = np.empty((T, f)); Z = np.empty((T, h))
+    _load().oracle_swiglu_forward(T, h, f, _ptr(X), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2),
+                                  _ptr(GU), _ptr(Y), _ptr(Z))
+    return {"GU": GU, "Y": Y, "Z": Z}
+
+
+def swiglu_backward(X, W1, b1, W2, dZ,
+                    want: Sequence[str] = ("dX", "dW1", "db1", "dW2", "db2")) -> Dict[str, np.ndarray]:
+    """Chain-rule gradients of the unsharded SwiGLU block for upstream dZ."""
+    X, W1, b1, W2, dZ = map(_f64, (X, W1, b1, W2, dZ))
+    T, h = X.shape
+    f = W1.shape[1] // 2
+    shapes = {"dX": (T, h), "dW1": (h, 2 * f), "db1": (2 * f,), "dW2": (f, h), "db2": (h,)}
+    out = {k: np.empty(shapes[k]) for k in want}
+    _load().oracle_swiglu_backward(T, h, f, _ptr(X), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(dZ),
+                                   _ptr(out.get("dX")), _ptr(out.get("dW1")), _ptr(out.get("db1")),
+                                   _ptr(out.get("dW2")), _ptr(out.get("db2")))
+    return out
+
+
+def swiglu_backward_cols(X, W1, b1, W2, dZ, cols) -> Dict[str, np.ndarray]:
+    """dW1[:, cols] (gate), dW1[:, f + cols] (up), db1 at both, dW2[cols, :]."""
+    X, W1, b1, W2, dZ = map(_f64, (X, W1, b1, W2, dZ))
+    cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+    T, h = X.shape
+    f = W1.shape[1] // 2
+    n = len(cols)
+    dWg = np.empty((h, n)); dWu = np.empty((h, n)); dbg = np.empty((n,)); dbu = np.empty((n,))
+    dW2 = np.empty((n, h))
+    _load().oracle_swiglu_backward_cols(T, h, f, _ptr(X), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(dZ),
+                                        n, _ptr(cols), _ptr(dWg), _ptr(dWu), _ptr(dbg), _ptr(dbu), _ptr(dW2))
+    return {"dW1_gate": dWg, "dW1_up": dWu, "db1_gate": dbg, "db1_up": dbu, "dW2": dW2}
+
+
+def swiglu_sharded(X, W1, b1, W2, b2, dZ, t: int) -> Dict[str, np.ndarray]:
+    """The SwiGLU block computed shard by shard (gate/up columns, W2 rows)."""
+    X, W1, b1, W2, b2, dZ = map(_f64, (X, W1, b1, W2, b2, dZ))
+    T, h = X.shape
+    f = W1.shape[1] // 2
+    if f % t:
+        raise ValueError("f must divide by t")
+    Z = np.empty((T, h)); dX = np.empty((T, h)); dW1 = np.empty((h, 2 * f)); dW2 = np.empty((f, h))
+    _load().oracle_swiglu_sharded(T, h, f, t, _ptr(X), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), _ptr(dZ),
+                                  _ptr(Z), _ptr(dX), _ptr(dW1), _ptr(dW2))
+    return {"Z": Z, "dX": dX, "dW1": dW1, "dW2": dW2}

@@ -26,6 +26,9 @@
  *   [LEC] "Cutting a Model Into Pieces" (lecture 3): "Megatron-LM: cutting
  *         inside the layer".
  *   [DEP] "Megatron-LM, in depth" (aicassindra): "Failure modes".
+ *   [70B] "Distributed tensor parallelism: scale fine-tuning of 70B-parameter
+ *         LLMs with Megatron-LM" (mohashari.github.io): "The Mechanics of
+ *         Tensor Parallelism (TP) in Megatron-LM", "The MLP Block".
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *   - GeLU is the exact erf form x * Phi(x); its derivative Phi(x) + x phi(x).
@@ -36,6 +39,8 @@
  *     [0, v_valid); padded ids take no part in the max or the sum of exps
  *     and get a zero gradient.
  *   - The gradient returned is that of grad_scale * sum_t loss_t.
+ *   - Swish in the SwiGLU block is x * sigmoid(x) (beta = 1); the first
+ *     weight W1 = [W_gate | W_up] is one [h, 2f] matrix, gate columns first.
  */
 #include <math.h>
 #include <stdint.h>
@@ -452,4 +457,275 @@ void oracle_ce_sharded(int64_t T, int64_t h, int64_t v_pad, int64_t v_valid, int
         loss[tok] = M + log(S) - tau[tok];
         free(l);
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* The SwiGLU variant of the block. [70B] "The MLP Block":
+ *   MLP(x) = (Swish(x W_gate) (.) (x W_up)) W_down,
+ * W_gate and W_up split by columns (column-parallel), W_down by rows
+ * (row-parallel) with the partial products summed. Biases are optional and,
+ * as in the GeLU block, the row-parallel bias enters once.
+ * Layout: W1 = [W_gate | W_up] is [h, 2f] (gate columns 0..f-1, up columns
+ * f..2f-1), b1 [2f]; W2 = W_down is [f, h], b2 [h]; GU = [G | Up] is [T, 2f]
+ * with G = X W_gate + b_gate and Up = X W_up + b_up; Y = Swish(G) (.) Up is
+ * [T, f]; Z = Y W2 + b2 is [T, h]. */
+
+/* Swish(x) = x sigmoid(x) = x / (1 + e^{-x}). */
+double oracle_swish(double x)
+{
+    return x / (1.0 + exp(-x));
+}
+
+/* d/dx [x sigmoid(x)] = sigmoid(x) + x sigmoid(x) (1 - sigmoid(x)). */
+double oracle_swish_grad(double x)
+{
+    double s = 1.0 / (1.0 + exp(-x));
+    return s + x * s * (1.0 - s);
+}
+
+/* Forward, unsharded. GU, Y, Z may be NULL; b1, b2 may be NULL (zero). */
+void oracle_swiglu_forward(int64_t T, int64_t h, int64_t f,
+                           const double *X, const double *W1, const double *b1,
+                           const double *W2, const double *b2,
+                           double *GU, double *Y, double *Z)
+{
+    int64_t f2 = 2 * f;
+    int64_t t;
+#pragma omp parallel for schedule(static)
+    for (t = 0; t < T; t++) {
+        double *gu = (double *)malloc(sizeof(double) * (size_t)f2);
+        double *y = (double *)malloc(sizeof(double) * (size_t)f);
+        for (int64_t j = 0; j < f2; j++)
+            gu[j] = b1 ? b1[j] : 0.0;
+        for (int64_t k = 0; k < h; k++) {
+            double x = X[t * h + k];
+            for (int64_t j = 0; j < f2; j++)
+                gu[j] += x * W1[k * f2 + j];
+        }
+        for (int64_t j = 0; j < f; j++)
+            y[j] = oracle_swish(gu[j]) * gu[f + j];
+        if (Z) {
+            for (int64_t n = 0; n < h; n++)
+                Z[t * h + n] = b2 ? b2[n] : 0.0;
+            for (int64_t j = 0; j < f; j++) {
+                double yj = y[j];
+                for (int64_t n = 0; n < h; n++)
+                    Z[t * h + n] += yj * W2[j * h + n];
+            }
+        }
+        if (GU) memcpy(GU + t * f2, gu, sizeof(double) * (size_t)f2);
+        if (Y) memcpy(Y + t * f, y, sizeof(double) * (size_t)f);
+        free(gu);
+        free(y);
+    }
+}
+
+/* Backward, unsharded, by the chain rule of oracle_swiglu_forward:
+ *   dW2 = Y^T dZ,  db2 = sum_t dZ,  dY = dZ W2^T,
+ *   dG = dY (.) Up (.) Swish'(G),  dUp = dY (.) Swish(G),  dGU = [dG | dUp],
+ *   dW1 = X^T dGU,  db1 = sum_t dGU,  dX = dGU W1^T.
+ * G, Up and Y are recomputed from X, W1, b1. Any output may be NULL. */
+void oracle_swiglu_backward(int64_t T, int64_t h, int64_t f,
+                            const double *X, const double *W1, const double *b1,
+                            const double *W2, const double *dZ,
+                            double *dX, double *dW1, double *db1,
+                            double *dW2, double *db2)
+{
+    int64_t f2 = 2 * f;
+    double *GU = (double *)malloc(sizeof(double) * (size_t)(T * f2));
+    double *Y = (double *)malloc(sizeof(double) * (size_t)(T * f));
+    double *dGU = (double *)malloc(sizeof(double) * (size_t)(T * f2));
+    oracle_swiglu_forward(T, h, f, X, W1, b1, W2, NULL, GU, Y, NULL);
+
+    int64_t t, j, k, n;
+#pragma omp parallel for schedule(static)
+    for (t = 0; t < T; t++) {
+        for (int64_t jj = 0; jj < f; jj++) {
+            double dy = 0.0;
+            for (int64_t nn = 0; nn < h; nn++)
+                dy += dZ[t * h + nn] * W2[jj * h + nn];
+            double g = GU[t * f2 + jj], u = GU[t * f2 + f + jj];
+            dGU[t * f2 + jj] = dy * u * oracle_swish_grad(g);
+            dGU[t * f2 + f + jj] = dy * oracle_swish(g);
+        }
+    }
+    if (dX) {
+#pragma omp parallel for schedule(static)
+        for (t = 0; t < T; t++) {
+            for (int64_t kk = 0; kk < h; kk++) {
+                double acc = 0.0;
+                for (int64_t jj = 0; jj < f2; jj++)
+                    acc += dGU[t * f2 + jj] * W1[kk * f2 + jj];
+                dX[t * h + kk] = acc;
+            }
+        }
+    }
+    if (dW1) {
+#pragma omp parallel for schedule(static)
+        for (k = 0; k < h; k++) {
+            for (int64_t jj = 0; jj < f2; jj++)
+                dW1[k * f2 + jj] = 0.0;
+            for (int64_t tt = 0; tt < T; tt++) {
+                double x = X[tt * h + k];
+                for (int64_t jj = 0; jj < f2; jj++)
+                    dW1[k * f2 + jj] += x * dGU[tt * f2 + jj];
+            }
+        }
+    }
+    if (dW2) {
+#pragma omp parallel for schedule(static)
+        for (j = 0; j < f; j++) {
+            for (int64_t nn = 0; nn < h; nn++)
+                dW2[j * h + nn] = 0.0;
+            for (int64_t tt = 0; tt < T; tt++) {
+                double y = Y[tt * f + j];
+                for (int64_t nn = 0; nn < h; nn++)
+                    dW2[j * h + nn] += y * dZ[tt * h + nn];
+            }
+        }
+    }
+    if (db1) {
+        for (j = 0; j < f2; j++) {
+            double acc = 0.0;
+            for (t = 0; t < T; t++)
+                acc += dGU[t * f2 + j];
+            db1[j] = acc;
+        }
+    }
+    if (db2) {
+        for (n = 0; n < h; n++) {
+            double acc = 0.0;
+            for (t = 0; t < T; t++)
+                acc += dZ[t * h + n];
+            db2[n] = acc;
+        }
+    }
+    free(GU);
+    free(Y);
+    free(dGU);
+}
+
+/* Selected columns j (0 <= j < f) of the SwiGLU weight gradients, from the
+ * same definitions: the gate column j and the up column f + j of dW1 and db1,
+ * and row j of dW2. O(T h) work per column, for full-size spot checks.
+ * Outputs: dW1g_cols, dW1u_cols [h][ncols], db1g_cols, db1u_cols [ncols],
+ * dW2_rows [ncols][h]. */
+void oracle_swiglu_backward_cols(int64_t T, int64_t h, int64_t f,
+                                 const double *X, const double *W1, const double *b1,
+                                 const double *W2, const double *dZ,
+                                 int64_t ncols, const int64_t *cols,
+                                 double *dW1g_cols, double *dW1u_cols,
+                                 double *db1g_cols, double *db1u_cols, double *dW2_rows)
+{
+    int64_t f2 = 2 * f;
+    int64_t c;
+#pragma omp parallel for schedule(dynamic)
+    for (c = 0; c < ncols; c++) {
+        int64_t j = cols[c];
+        double *dg = (double *)malloc(sizeof(double) * (size_t)T);
+        double *du = (double *)malloc(sizeof(double) * (size_t)T);
+        double *y = (double *)malloc(sizeof(double) * (size_t)T);
+        double *wg = (double *)calloc((size_t)h, sizeof(double));
+        double *wu = (double *)calloc((size_t)h, sizeof(double));
+        double *w2 = (double *)calloc((size_t)h, sizeof(double));
+        for (int64_t t = 0; t < T; t++) {
+            double g = b1 ? b1[j] : 0.0, u = b1 ? b1[f + j] : 0.0;
+            for (int64_t k = 0; k < h; k++) {
+                g += X[t * h + k] * W1[k * f2 + j];
+                u += X[t * h + k] * W1[k * f2 + f + j];
+            }
+            double dy = 0.0;
+            for (int64_t n = 0; n < h; n++)
+                dy += dZ[t * h + n] * W2[j * h + n];
+            dg[t] = dy * u * oracle_swish_grad(g);
+            du[t] = dy * oracle_swish(g);
+            y[t] = oracle_swish(g) * u;
+        }
+        double sg = 0.0, su = 0.0;
+        for (int64_t t = 0; t < T; t++) {
+            sg += dg[t];
+            su += du[t];
+        }
+        db1g_cols[c] = sg;
+        db1u_cols[c] = su;
+        for (int64_t t = 0; t < T; t++) {
+            for (int64_t k = 0; k < h; k++) {
+                wg[k] += X[t * h + k] * dg[t];
+                wu[k] += X[t * h + k] * du[t];
+            }
+            for (int64_t n = 0; n < h; n++)
+                w2[n] += y[t] * dZ[t * h + n];
+        }
+        for (int64_t k = 0; k < h; k++) {
+            dW1g_cols[k * ncols + c] = wg[k];
+            dW1u_cols[k * ncols + c] = wu[k];
+        }
+        memcpy(dW2_rows + c * h, w2, sizeof(double) * (size_t)h);
+        free(dg);
+        free(du);
+        free(y);
+        free(wg);
+        free(wu);
+        free(w2);
+    }
+}
+
+/* The SwiGLU block computed shard by shard, as [70B] "The MLP Block" lays
+ * it out: shard i holds gate columns [i fs, (i+1) fs) and the same up
+ * columns (f + i fs ...) of W1, and rows [i fs, (i+1) fs) of W2; it computes
+ * Y_i = Swish(X W_gate,i) (.) (X W_up,i) and the partial Z_i = Y_i W2_i with
+ * no exchange; Z = sum_i Z_i, then b2 once. Backward: every shard sees the
+ * same dZ; the partial dX_i are summed. Requires f % t == 0. */
+void oracle_swiglu_sharded(int64_t T, int64_t h, int64_t f, int t,
+                           const double *X, const double *W1, const double *b1,
+                           const double *W2, const double *b2, const double *dZ,
+                           double *Z, double *dX, double *dW1, double *dW2)
+{
+    int64_t fs = f / t, f2 = 2 * f, fs2 = 2 * fs;
+    double *Zi = (double *)malloc(sizeof(double) * (size_t)(T * h));
+    double *dXi = (double *)malloc(sizeof(double) * (size_t)(T * h));
+    double *W1i = (double *)malloc(sizeof(double) * (size_t)(h * fs2));
+    double *b1i = (double *)malloc(sizeof(double) * (size_t)fs2);
+    double *W2i = (double *)malloc(sizeof(double) * (size_t)(fs * h));
+    double *dW1i = (double *)malloc(sizeof(double) * (size_t)(h * fs2));
+    double *dW2i = (double *)malloc(sizeof(double) * (size_t)(fs * h));
+    for (int64_t e = 0; e < T * h; e++) {
+        Z[e] = 0.0;
+        dX[e] = 0.0;
+    }
+    for (int i = 0; i < t; i++) {
+        int64_t g0 = (int64_t)i * fs, u0 = f + (int64_t)i * fs;
+        for (int64_t k = 0; k < h; k++)
+            for (int64_t j = 0; j < fs; j++) {
+                W1i[k * fs2 + j] = W1[k * f2 + g0 + j];
+                W1i[k * fs2 + fs + j] = W1[k * f2 + u0 + j];
+            }
+        for (int64_t j = 0; j < fs; j++) {
+            b1i[j] = b1 ? b1[g0 + j] : 0.0;
+            b1i[fs + j] = b1 ? b1[u0 + j] : 0.0;
+        }
+        memcpy(W2i, W2 + g0 * h, sizeof(double) * (size_t)(fs * h));
+        oracle_swiglu_forward(T, h, fs, X, W1i, b1i, W2i, NULL, NULL, NULL, Zi);
+        for (int64_t e = 0; e < T * h; e++)
+            Z[e] += Zi[e];
+        oracle_swiglu_backward(T, h, fs, X, W1i, b1i, W2i, dZ, dXi, dW1i, NULL, dW2i, NULL);
+        for (int64_t e = 0; e < T * h; e++)
+            dX[e] += dXi[e];
+        for (int64_t k = 0; k < h; k++)
+            for (int64_t j = 0; j < fs; j++) {
+                dW1[k * f2 + g0 + j] = dW1i[k * fs2 + j];
+                dW1[k * f2 + u0 + j] = dW1i[k * fs2 + fs + j];
+            }
+        memcpy(dW2 + g0 * h, dW2i, sizeof(double) * (size_t)(fs * h));
+    }
+    for (int64_t tt = 0; tt < T; tt++)
+        for (int64_t n = 0; n < h; n++)
+            Z[tt * h + n] += b2 ? b2[n] : 0.0;
+    free(Zi);
+    free(dXi);
+    free(W1i);
+    free(b1i);
+    free(W2i);
+    free(dW1i);
+    free(dW2i);
 }
