@@ -15,7 +15,8 @@ roofline of the dominant kernel, SM clocks during the timed region, and the
 CPU oracle timed on a bounded sample on this host.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W]
-                       [--impl ours|reference] [--workload gpt8b|mlp70b|ce128k|sweep]
+                       [--impl ours|reference]
+                       [--workload gpt8b|mlp70b|ce128k|swiglu70b|sweep]
 Multi-GPU (one process per GPU under torchrun): every rank runs its own
 independent batch (data parallel, weak scaling); there is no collective on
 the data path, only a barrier and a max over ranks of the elapsed time.
@@ -46,8 +47,8 @@ UNIT = "TFLOP/s"
 # fallbacks only if the generated MEASURED_PEAKS.json is absent
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # tokens the CPU oracle processes per timed sample
-CPU_SAMPLE_TOKENS = {"gpt8b": 512, "mlp70b": 192, "ce128k": 96, "sweep": 512}
-REF_STEP_TOKENS = {"gpt8b": 8, "mlp70b": 4, "ce128k": 2, "sweep": 8}
+CPU_SAMPLE_TOKENS = {"gpt8b": 512, "mlp70b": 192, "ce128k": 96, "swiglu70b": 144, "sweep": 512}
+REF_STEP_TOKENS = {"gpt8b": 8, "mlp70b": 4, "ce128k": 2, "swiglu70b": 3, "sweep": 8}
 
 
 # ---------------------------------------------------------------------- setup
@@ -57,7 +58,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["gpt8b", "mlp70b", "ce128k", "sweep"], default="gpt8b")
+    p.add_argument("--workload", choices=["gpt8b", "mlp70b", "ce128k", "swiglu70b", "sweep"], default="gpt8b")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
@@ -81,7 +82,9 @@ def peaks():
 
 
 def flops(w):
-    mlp = 12.0 * w.T * w.h * w.f if w.f else 0.0
+    # GeLU block: 4 T h f forward + 8 T h f backward; SwiGLU: GEMM1 is twice as
+    # wide (6 T h f forward, 12 T h f backward)
+    mlp = (18.0 if w.act == "swiglu" else 12.0) * w.T * w.h * w.f if w.f else 0.0
     ce = 8.0 * w.T * w.h * w.v_pad if w.v_pad else 0.0
     return mlp, ce
 
@@ -91,6 +94,7 @@ def workload_config(w, name):
         "gpt8b": "8.3B-shaped block: MLP fwd+bwd + fused vocab-parallel CE fwd+bwd",
         "mlp70b": "70B-shaped MLP fwd+bwd",
         "ce128k": "vocab-parallel fused logit GEMM + CE fwd+bwd, 128,256-token vocabulary",
+        "swiglu70b": "70B-shaped SwiGLU MLP fwd+bwd (gate/up column-parallel, down row-parallel)",
         "sweep": "shard-count sweep of the 8.3B MLP fwd+bwd",
     }[name]
     cfg = {"workload": f"{desc}: T={w.T} (b={w.b}, s={w.s}), h={w.h}", "T": w.T, "h": w.h, "t": w.t,
@@ -192,18 +196,31 @@ class Step:
         self.tp = tp
         self.w = w
         self.dev = dev
-        self.mi = wl.mlp_inputs(w, seed=seed, device=dev) if w.f else None
+        self.glu = w.act == "swiglu"
+        if not w.f:
+            self.mi = None
+        else:
+            self.mi = (wl.swiglu_inputs if self.glu else wl.mlp_inputs)(w, seed=seed, device=dev)
         self.ci = wl.ce_inputs(w, seed=seed, device=dev) if w.v_pad else None
         T, h, f = w.T, w.h, w.f
         bf = torch.bfloat16
         self.out = {}
-        if w.f:
+        if w.f and not self.glu:
             self.fo = {k: torch.empty(s, dtype=bf, device=dev) for k, s in (("Z", (T, h)), ("U", (T, f)), ("Y", (T, f)))}
             self.bo = {"dX": torch.empty((T, h), dtype=bf, device=dev), "dA": torch.empty((h, f), dtype=bf, device=dev),
                        "dB": torch.empty((f, h), dtype=bf, device=dev),
                        "dbA": torch.empty(f, dtype=torch.float32, device=dev),
                        "dbB": torch.empty(h, dtype=torch.float32, device=dev)}
             self.mws = torch.empty(max(1, tp.mlp_workspace_bytes(T, h, f, w.t)), dtype=torch.uint8, device=dev)
+        elif w.f:
+            self.fo = {k: torch.empty(s, dtype=bf, device=dev)
+                       for k, s in (("Z", (T, h)), ("GU", (T, 2 * f)), ("Y", (T, f)))}
+            self.bo = {"dX": torch.empty((T, h), dtype=bf, device=dev),
+                       "dW1": torch.empty((h, 2 * f), dtype=bf, device=dev),
+                       "dW2": torch.empty((f, h), dtype=bf, device=dev),
+                       "db1": torch.empty(2 * f, dtype=torch.float32, device=dev),
+                       "db2": torch.empty(h, dtype=torch.float32, device=dev)}
+            self.mws = torch.empty(max(1, tp.swiglu_workspace_bytes(T, h, f, w.t)), dtype=torch.uint8, device=dev)
         if w.v_pad:
             self.co = {"loss": torch.empty(T, dtype=torch.float32, device=dev),
                        "lse": torch.empty(T, dtype=torch.float32, device=dev),
@@ -214,6 +231,11 @@ class Step:
     def mlp(self, mi=None):
         mi = mi or self.mi
         tp, w = self.tp, self.w
+        if self.glu:
+            fo = tp.tp_swiglu_forward(mi["X"], mi["W1"], mi["W2"], w.t, mi["b1"], mi["b2"], out=self.fo)
+            tp.tp_swiglu_backward(mi["dZ"], mi["X"], mi["W1"], mi["W2"], fo["GU"], fo["Y"], w.t, out=self.bo,
+                                  ws=self.mws)
+            return
         fo = tp.tp_mlp_forward(mi["X"], mi["A"], mi["B"], w.t, mi["bA"], mi["bB"], out=self.fo)
         tp.tp_mlp_backward(mi["dZ"], mi["X"], mi["A"], mi["B"], fo["U"], fo["Y"], w.t, out=self.bo, ws=self.mws)
 
@@ -246,7 +268,10 @@ def oracle_sample(w, mi, ci, n_tokens):
         return x.detach().float().cpu().numpy().astype(np.float64)
 
     s = {}
-    if mi is not None:
+    if mi is not None and "W1" in mi:
+        s.update(X=f64(mi["X"][:n_tokens]), dZ=f64(mi["dZ"][:n_tokens]), W1=f64(mi["W1"]), W2=f64(mi["W2"]),
+                 b1=f64(mi["b1"]), b2=f64(mi["b2"]))
+    elif mi is not None:
         s.update(X=f64(mi["X"][:n_tokens]), dZ=f64(mi["dZ"][:n_tokens]), A=f64(mi["A"]), B=f64(mi["B"]),
                  bA=f64(mi["bA"]), bB=f64(mi["bB"]))
     if ci is not None:
@@ -258,7 +283,10 @@ def oracle_sample(w, mi, ci, n_tokens):
 def oracle_step(w, s):
     import oracle
 
-    if "X" in s:
+    if "W1" in s:
+        oracle.swiglu_forward(s["X"], s["W1"], s["b1"], s["W2"], s["b2"])
+        oracle.swiglu_backward(s["X"], s["W1"], s["b1"], s["W2"], s["dZ"])
+    elif "X" in s:
         oracle.mlp_forward(s["X"], s["A"], s["bA"], s["B"], s["bB"])
         oracle.mlp_backward(s["X"], s["A"], s["bA"], s["B"], s["dZ"])
     if "H" in s:
@@ -285,7 +313,7 @@ def run_reference(args, w, name):
         return 0
     oracle.build()
     n = REF_STEP_TOKENS[name]
-    mi = wl.mlp_inputs(w, seed=0) if w.f else None
+    mi = ((wl.swiglu_inputs if w.act == "swiglu" else wl.mlp_inputs)(w, seed=0)) if w.f else None
     ci = wl.ce_inputs(w, seed=0) if w.v_pad else None
     s = oracle_sample(w, mi, ci, n)
     for _ in range(args.warmup):
@@ -410,7 +438,7 @@ def run_ours(args, w, name):
         def e2e_step():
             for k, v in host.items():
                 dev_in[k].copy_(v, non_blocking=True)
-            mi = {k: dev_in[k] for k in ("X", "A", "B", "bA", "bB", "dZ")} if w.f else None
+            mi = {k: dev_in[k] for k in step.mi} if w.f else None
             ci = {k: dev_in[k] for k in ("H", "E", "targets")} if w.v_pad else None
             step.run(mi, ci)
             if w.v_pad:
@@ -485,6 +513,9 @@ def kernel_flops_per_step(name, w):
         "mlp_fwd_gemm1_bias_gelu": 2.0 * T * h * f, "mlp_fwd_gemm2_shard_sum": 2.0 * T * f * h,
         "mlp_bwd_dY_gelu_grad": 2.0 * T * h * f, "mlp_bwd_dB": 2.0 * T * f * h, "mlp_bwd_dA": 2.0 * T * h * f,
         "mlp_bwd_dX_shard_sum": 2.0 * T * f * h,
+        "swiglu_fwd_gemm1_gate_up": 4.0 * T * h * f, "swiglu_fwd_gemm2_shard_sum": 2.0 * T * f * h,
+        "swiglu_bwd_dY_swiglu_grad": 2.0 * T * h * f, "swiglu_bwd_dW2": 2.0 * T * f * h,
+        "swiglu_bwd_dW1": 4.0 * T * h * f, "swiglu_bwd_dX_shard_sum": 4.0 * T * f * h,
         "ce_fwd_logits_stats": 2.0 * T * h * vp, "ce_bwd_logits_dl": 2.0 * T * h * vp,
         "ce_bwd_dE": 2.0 * T * h * vp, "ce_bwd_dH_shard_sum": 2.0 * T * h * vp,
     }

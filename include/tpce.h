@@ -158,6 +158,67 @@ tpce_status tp_mlp_backward(const void *dZ, const void *X, const void *A, const 
                             void *ws, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * The SwiGLU variant of the block ("Distributed tensor parallelism: scale
+ * fine-tuning of 70B-parameter LLMs with Megatron-LM", section "The MLP
+ * Block"): MLP(X) = (Swish(X W_gate) (.) (X W_up)) W_down, with W_gate and
+ * W_up column-parallel and W_down row-parallel. Swish(x) = x sigmoid(x).
+ *
+ * W1 = [W_gate | W_up] is one [h, 2f] matrix: columns 0..f-1 are the gate,
+ * f..2f-1 the up projection. Shard i owns gate columns [i f/t, (i+1) f/t)
+ * and the same range of up columns (f + i f/t ...), and rows [i f/t, ...) of
+ * W2 = W_down [f, h]. b1 [2f] (gate biases, then up biases) and b2 [h] are
+ * fp32 and may be NULL; b2 is added once, after the shard sum.
+ *
+ * tpce_swiglu_workspace_bytes covers both calls of one dtype (bf16: the
+ * backward's [dG | dUp]; TPCE_F32 adds transposed copies of W1, W2, Y, dZ, X
+ * and [dG | dUp]). Returns 0 for invalid shapes.
+ * ------------------------------------------------------------------------- */
+size_t tpce_swiglu_workspace_bytes(int64_t T, int64_t h, int64_t f, int t, int dtype);
+
+/* ---------------------------------------------------------------------------
+ * tp_swiglu_forward -- the SwiGLU block, forward.
+ *   [G | Up] = X W1 + b1        (column-parallel GEMM1: each output tile
+ *                                holds the gate and up columns of the same
+ *                                shard columns; no exchange)
+ *   Y = Swish(G) (.) Up
+ *   Z = sum_i Y_i W2_i + b2     (row-parallel GEMM2; g = sum over shards, in
+ *                                the accumulator)
+ * Inputs:  X [T, h], W1 [h, 2f], W2 [f, h]; b1, b2 as above.
+ * Outputs: Z [T, h]; GU = [G | Up] [T, 2f] and Y [T, f] are written for the
+ *          backward.
+ * Shapes:  as tp_mlp_forward (h >= 8, h % 8 == 0, f % t == 0,
+ *          (f / t) % 64 == 0; T == 0 is a no-op, pointers may then be NULL).
+ * Workspace: none for TPCE_BF16; for TPCE_F32,
+ *          tpce_swiglu_workspace_bytes(T, h, f, t, TPCE_F32) bytes.
+ * ------------------------------------------------------------------------- */
+tpce_status tp_swiglu_forward(const void *X, const void *W1, const float *b1,
+                              const void *W2, const float *b2,
+                              int64_t T, int64_t h, int64_t f, int t, int dtype,
+                              void *Z, void *GU, void *Y,
+                              void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * tp_swiglu_backward -- gradients of the SwiGLU block for upstream dZ.
+ * g* gives dZ to every shard:
+ *   dW2_i = Y_i^T dZ,  dY_i = dZ W2_i^T,
+ *   dG_i = dY_i (.) Up_i (.) Swish'(G_i),  dUp_i = dY_i (.) Swish(G_i),
+ *   dW1 = X^T [dG | dUp],  db1 = sum_tokens [dG | dUp],  db2 = sum_tokens dZ,
+ * and f* sums the shard partials  dX = sum_i [dG_i | dUp_i] W1_i^T  (in the
+ * accumulator), Swish'(g) = s (1 + g (1 - s)), s = sigmoid(g).
+ * Inputs:  dZ [T, h], X [T, h], W1 [h, 2f], W2 [f, h], and the GU [T, 2f]
+ *          and Y [T, f] that tp_swiglu_forward wrote for the same X, W1, b1.
+ * Outputs: dX [T, h], dW1 [h, 2f], dW2 [f, h]; db1 [2f] and db2 [h] fp32,
+ *          may be NULL (not computed).
+ * Shapes:  as tp_swiglu_forward. T == 0 writes zero weight/bias gradients.
+ * Workspace: tpce_swiglu_workspace_bytes(T, h, f, t, dtype) bytes.
+ * ------------------------------------------------------------------------- */
+tpce_status tp_swiglu_backward(const void *dZ, const void *X, const void *W1, const void *W2,
+                               const void *GU, const void *Y,
+                               int64_t T, int64_t h, int64_t f, int t, int dtype,
+                               void *dX, void *dW1, float *db1, void *dW2, float *db2,
+                               void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
  * vocab_parallel_ce -- logit GEMM fused with softmax cross-entropy, the
  * vocabulary split into t shards of v_pad / t rows of E.
  * Forward, per shard i and token r (the logits l = H E_i^T stay in fp32

@@ -117,6 +117,33 @@ def test_mlp_validation(L):
     assert st == 4
 
 
+def test_swiglu_validation_and_workspace(L):
+    import vocab_ce_gb300 as tp
+    import torch
+
+    def fwd(T=64, h=64, f=256, t=2, dtype=0, X=FAKE):
+        return L.tp_swiglu_forward(X, FAKE, None, FAKE, None, T, h, f, t, dtype, FAKE, FAKE, FAKE, None, 0, None)
+    assert fwd(f=256, t=3) == 2                        # f % t
+    assert fwd(f=256, t=8) == 2                        # f / t = 32 is not whole 64-wide blocks
+    assert fwd(h=60) == 2
+    assert fwd(X=MISALIGNED) == 3
+    assert fwd(X=None) == 1
+    assert fwd(dtype=1) == 4                           # the fp32 forward needs its workspace
+    assert fwd(T=0) == 0
+    st = L.tp_swiglu_backward(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 64, 256, 2, 0,
+                              FAKE, FAKE, None, FAKE, None, None, 0, None)
+    assert st == 4
+    # the backward holds [dG | dUp] [T, 2f] in bf16 plus a small column-sum buffer
+    T, h, f = 4096, 8192, 28672
+    b = tp.swiglu_workspace_bytes(T, h, f, 8)
+    assert T * 2 * f * 2 <= b < T * 2 * f * 2 + 64 * 2 * f * 4 + 4096
+    # fp32: transposed W1 [2f, h], W2, Y, dZ, X and [dG | dUp]
+    T, h, f = 32, 64, 256
+    b32 = tp.swiglu_workspace_bytes(T, h, f, 2, dtype=torch.float32)
+    assert b32 >= 4 * (T * 2 * f + 2 * f * h + f * h + f * T + 2 * h * T + 2 * f * T)
+    assert L.tpce_swiglu_workspace_bytes(10, 64, 100, 3, 0) == 0
+
+
 def test_ce_validation(L):
     def ce(T=64, h=64, vp=512, vv=500, t=2, ws=None, wsb=0, H=FAKE, tg=FAKE):
         return L.vocab_parallel_ce(H, FAKE, tg, T, h, vp, vv, t, 1.0, 0, FAKE, None, FAKE, FAKE, ws, wsb, None)

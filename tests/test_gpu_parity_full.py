@@ -5,8 +5,9 @@ The oracle cannot redo a full-size GEMM in plain fp64 loops in seconds, so it
 checks outputs it can compute one by one: every row of Z, U, Y, dX, loss, lse
 and dH belongs to one token, so 64 sampled tokens (first and last included)
 are recomputed from their own rows; a column j of dA / dbA and a row j of dB
-need only O(T h) work, so 32 sampled j are recomputed over all tokens; dbB is
-the token sum of dZ, recomputed in full. dE needs the softmax of every token,
+need only O(T h) work, so 32 sampled j are recomputed over all tokens (for
+SwiGLU: gate column j, up column f + j and row j of W2); dbB is the token sum
+of dZ, recomputed in full. dE needs the softmax of every token,
 so it is checked in full on a run over the first tokens at the full h and v.
 The shard sweep checks that t = 1 and t = 16 give bit-identical outputs at
 full size.
@@ -92,6 +93,35 @@ def test_mlp70b_full_size():
 def test_ce128k_full_size():
     dev = gpu_or_skip()
     check_ce_full(wl.WORKLOADS["ce128k"], dev, de_tokens=32)
+
+
+def check_swiglu_full(w, dev, seed=0):
+    si = wl.swiglu_inputs(w, seed=seed, device=dev)
+    fwd = tp.tp_swiglu_forward(si["X"], si["W1"], si["W2"], w.t, si["b1"], si["b2"])
+    bwd = tp.tp_swiglu_backward(si["dZ"], si["X"], si["W1"], si["W2"], fwd["GU"], fwd["Y"], w.t)
+    assert tp.device_status() == 0
+    rows = wl.sample_indices(w.T, N_ROWS, seed=seed)
+    cols = wl.sample_indices(w.f, N_COLS, seed=seed + 1)
+    X, W1, W2, dZ = (_host(si[k]) for k in ("X", "W1", "W2", "dZ"))
+    b1, b2 = _host(si["b1"]), _host(si["b2"])
+    of = oracle.swiglu_forward(X[rows], W1, b1, W2, b2)
+    ob = oracle.swiglu_backward(X[rows], W1, b1, W2, dZ[rows], want=("dX",))
+    for k in ("GU", "Y", "Z"):
+        assert_rel(k, _host(fwd[k])[rows], of[k])
+    assert_rel("dX", _host(bwd["dX"])[rows], ob["dX"])
+    oc = oracle.swiglu_backward_cols(X, W1, b1, W2, dZ, cols)
+    up = cols + w.f
+    assert_rel("dW1[:, gate cols]", _host(bwd["dW1"])[:, cols], oc["dW1_gate"])
+    assert_rel("dW1[:, up cols]", _host(bwd["dW1"])[:, up], oc["dW1_up"])
+    assert_rel("db1[gate cols]", _host(bwd["db1"])[cols], oc["db1_gate"])
+    assert_rel("db1[up cols]", _host(bwd["db1"])[up], oc["db1_up"])
+    assert_rel("dW2[cols, :]", _host(bwd["dW2"])[cols, :], oc["dW2"])
+    assert_rel("db2", _host(bwd["db2"]), oracle.bias_grad(dZ))
+
+
+def test_swiglu70b_full_size():
+    dev = gpu_or_skip()
+    check_swiglu_full(wl.WORKLOADS["swiglu70b"], dev)
 
 
 def test_shard_sweep_full_size_bit_identical():

@@ -6,9 +6,11 @@ The compute lives in the CUDA library ``lib/libtpce.so`` (C ABI in
 """
 
 from .api import (TpceError, ce_workspace_bytes, device_status, device_status_detail,
-                  mlp_workspace_bytes, pad_vocab, profile_enable, profile_read, tp_mlp_backward,
-                  tp_mlp_forward, vocab_parallel_ce, vocab_parallel_ce_loss_static)
+                  mlp_workspace_bytes, pad_vocab, profile_enable, profile_read, swiglu_workspace_bytes,
+                  tp_mlp_backward, tp_mlp_forward, tp_swiglu_backward, tp_swiglu_forward,
+                  vocab_parallel_ce, vocab_parallel_ce_loss_static)
 
 __all__ = ["TpceError", "ce_workspace_bytes", "device_status", "device_status_detail",
-           "mlp_workspace_bytes", "pad_vocab", "profile_enable", "profile_read", "tp_mlp_backward",
-           "tp_mlp_forward", "vocab_parallel_ce", "vocab_parallel_ce_loss_static"]
+           "mlp_workspace_bytes", "pad_vocab", "profile_enable", "profile_read", "swiglu_workspace_bytes",
+           "tp_mlp_backward", "tp_mlp_forward", "tp_swiglu_backward", "tp_swiglu_forward",
+           "vocab_parallel_ce", "vocab_parallel_ce_loss_static"]

@@ -37,6 +37,10 @@ SIGNATURES = {
     "tp_mlp_forward": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "tp_mlp_backward": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I,
                              _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "tpce_swiglu_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I, _I]),
+    "tp_swiglu_forward": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "tp_swiglu_backward": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I,
+                                _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "vocab_parallel_ce": (_I, [_P, _P, _P, _I64, _I64, _I64, _I64, _I, _F, _I,
                                _P, _P, _P, _P, _P, _SZ, _P]),
     "vocab_parallel_ce_loss_static": (_I, [_P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _P, _P, _P]),

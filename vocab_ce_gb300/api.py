@@ -121,6 +121,70 @@ def tp_mlp_backward(dZ: torch.Tensor, X: torch.Tensor, A: torch.Tensor, B: torch
     return res
 
 
+def swiglu_workspace_bytes(T: int, h: int, f: int, t: int, dtype=torch.bfloat16) -> int:
+    return int(lib().tpce_swiglu_workspace_bytes(T, h, f, t, _DT[dtype]))
+
+
+def tp_swiglu_forward(X: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, t: int,
+                      b1: Optional[torch.Tensor] = None, b2: Optional[torch.Tensor] = None,
+                      out: Optional[Dict[str, torch.Tensor]] = None, ws: Optional[torch.Tensor] = None,
+                      stream=None) -> Dict[str, torch.Tensor]:
+    """Z = sum_i (Swish(X Wg_i + bg_i) * (X Wu_i + bu_i)) W2_i + b2 over t shards,
+    W1 = [W_gate | W_up] of shape [h, 2f]; returns Z, GU = [G | Up], Y."""
+    T, h = X.shape
+    f = W2.shape[0]
+    dt = X.dtype
+    for name, x, shp in (("X", X, (T, h)), ("W1", W1, (h, 2 * f)), ("W2", W2, (f, h))):
+        _need(x, name, dt, shp)
+    for name, b, n in (("b1", b1, 2 * f), ("b2", b2, h)):
+        if b is not None:
+            _need(b, name, torch.float32, (n,))
+    out = dict(out or {})
+    Z = out.get("Z") if out.get("Z") is not None else torch.empty((T, h), dtype=dt, device=X.device)
+    GU = out.get("GU") if out.get("GU") is not None else torch.empty((T, 2 * f), dtype=dt, device=X.device)
+    Y = out.get("Y") if out.get("Y") is not None else torch.empty((T, f), dtype=dt, device=X.device)
+    w = None
+    if dt == torch.float32 and T > 0:  # the tf32 path stages transposed operands
+        w = _workspace(swiglu_workspace_bytes(T, h, f, t, dt), X.device, ws)
+    st = lib().tp_swiglu_forward(_ptr(X), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), T, h, f, t, _DT[dt],
+                                 _ptr(Z), _ptr(GU), _ptr(Y), _ptr(w),
+                                 0 if w is None else w.numel() * w.element_size(), _stream(stream))
+    check(st, "tp_swiglu_forward")
+    return {"Z": Z, "GU": GU, "Y": Y}
+
+
+def tp_swiglu_backward(dZ: torch.Tensor, X: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor,
+                       GU: torch.Tensor, Y: torch.Tensor, t: int, bias_grads: bool = True,
+                       out: Optional[Dict[str, torch.Tensor]] = None, ws: Optional[torch.Tensor] = None,
+                       stream=None) -> Dict[str, torch.Tensor]:
+    """dX (f* sum over shards), dW1, dW2 and optionally db1, db2."""
+    T, h = X.shape
+    f = W2.shape[0]
+    dt = X.dtype
+    for name, x, shp in (("dZ", dZ, (T, h)), ("X", X, (T, h)), ("W1", W1, (h, 2 * f)), ("W2", W2, (f, h)),
+                         ("GU", GU, (T, 2 * f)), ("Y", Y, (T, f))):
+        _need(x, name, dt, shp)
+    out = dict(out or {})
+    dev = X.device
+
+    def get(k, shp, d):
+        return out.get(k) if out.get(k) is not None else torch.empty(shp, dtype=d, device=dev)
+
+    dX, dW1, dW2 = get("dX", (T, h), dt), get("dW1", (h, 2 * f), dt), get("dW2", (f, h), dt)
+    db1 = get("db1", (2 * f,), torch.float32) if bias_grads else None
+    db2 = get("db2", (h,), torch.float32) if bias_grads else None
+    nbytes = swiglu_workspace_bytes(T, h, f, t, dt) if T > 0 else 0
+    w = _workspace(nbytes, dev, ws)
+    st = lib().tp_swiglu_backward(_ptr(dZ), _ptr(X), _ptr(W1), _ptr(W2), _ptr(GU), _ptr(Y), T, h, f, t, _DT[dt],
+                                  _ptr(dX), _ptr(dW1), _ptr(db1), _ptr(dW2), _ptr(db2), _ptr(w),
+                                  0 if w is None else w.numel() * w.element_size(), _stream(stream))
+    check(st, "tp_swiglu_backward")
+    res = {"dX": dX, "dW1": dW1, "dW2": dW2}
+    if bias_grads:
+        res.update(db1=db1, db2=db2)
+    return res
+
+
 def vocab_parallel_ce(H: torch.Tensor, E: torch.Tensor, targets: torch.Tensor, v_valid: int, t: int,
                       grad_scale: float = 1.0, grads: bool = True, want_dH: bool = True, want_dE: bool = True,
                       out: Optional[Dict[str, torch.Tensor]] = None, ws: Optional[torch.Tensor] = None,

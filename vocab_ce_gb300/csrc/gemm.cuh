@@ -74,6 +74,7 @@ struct GemmShape {
     int group_m;               // rasterisation: tiles_m are walked in groups of this many
     int a_off_mn, a_off_k;     // coordinate offsets of the A operand inside its tensor map
     int b_off_mn, b_off_k;     // same for B
+    int b_gate_off;            // gated tiles: B column (or row) offset of the second half, else 0
 };
 
 __device__ __forceinline__ void tile_coords(int tile, const GemmShape &s, int &m_blk, int &n_blk) {
@@ -154,6 +155,10 @@ __device__ __forceinline__ float gelu_grad_f(float u) {
     return fmaf(u * 0.39894228040143267794f, g, Phi);
 }
 
+// Swish(x) = x sigmoid(x), sigmoid(x) = 1 / (1 + e^{-x}); for x << 0 the
+// exponential overflows to +inf and the quotient to 0, the right limit.
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
 // --------------------------------------------------------------------------
 // Output staging. An epilogue warp writes each 32-row x 32-column chunk of an
 // output into a shared-memory buffer, one row per lane, swizzled exactly as
@@ -224,18 +229,45 @@ struct Stage<float> {
 // --------------------------------------------------------------------------
 // Epilogues. Each turns the fp32 accumulator values of one 32-column chunk of
 // the thread's output row into kOuts output chunks (stored by the kernel), or
-// reduces them itself (kOuts = 0). An epilogue with kIns = 1 also receives
-// the matching 32 values of one input tensor of the output's shape, which the
-// kernel brings into shared memory with TMA loads one chunk ahead. begin/end
-// run once per tile and row. `live` is false for rows >= M or chunks at
-// columns >= N: such values are never stored, and the epilogue must not read
-// memory for them.
+// reduces them itself (kOuts = 0). An epilogue with kIns = 1 or 2 also
+// receives, in in[0 .. kIns), the matching 32 values of kIns inputs of the
+// output's shape, which the kernel brings into shared memory with TMA loads
+// one chunk ahead. begin/end run once per tile and row. `live` is false for
+// rows >= M or chunks at columns >= N: such values are never stored, and the
+// epilogue must not read memory for them.
+//
+// Where the outputs and inputs go (defaults in EpiBase):
+//   out_map(k)     which of the kernel's two output tensor maps output k uses;
+//   out_col(p, k)  column offset of output k inside that map;
+//   in_col(p, i)   column offset of input i inside the input map.
+// A gated epilogue (kGated) runs on tiles whose accumulator holds two halves,
+// [gate | up], each of the same output columns: the B tile's first half comes
+// from B's columns n.., the second from n + b_gate_off... The epilogue sees
+// the gate half in v and the up half in in[0]; a tile spans half as many
+// output columns as accumulator columns.
 // --------------------------------------------------------------------------
 struct NoRow {};
 
+struct EpiBase {
+    static constexpr bool kGated = false;
+    __host__ __device__ static constexpr int out_map(int k) { return k; }
+    template <class P>
+    __device__ static int out_col(const P &, int) { return 0; }
+    template <class P>
+    __device__ static int in_col(const P &, int) { return 0; }
+};
+
+// Number of distinct output tensor maps an epilogue stores through.
+template <class Epi>
+constexpr int num_out_maps() {
+    int m = 0;
+    for (int k = 0; k < Epi::kOuts; ++k) m = Epi::out_map(k) + 1 > m ? Epi::out_map(k) + 1 : m;
+    return m;
+}
+
 // GEMM1 epilogue: U = acc + bA, Y = GeLU(U).
 template <typename OutT>
-struct EpiBiasGelu {
+struct EpiBiasGelu : EpiBase {
     static constexpr int kWarps = kHeavyEpiWarps;
     static constexpr int kOuts = 2;
     static constexpr int kIns = 0;
@@ -247,7 +279,7 @@ struct EpiBiasGelu {
     __device__ static int mode(const Params &) { return 0; }
     __device__ static Row begin(const Params &, int, bool) { return {}; }
     __device__ static void chunk(const Params &p, Row &, int, int n, int N, bool, float (&v)[32],
-                                 const float (&in)[32], float (&o)[kOuts][32]) {
+                                 const float (&in)[2][32], float (&o)[kOuts][32]) {
         float b[32];
         load_bias32(p.bias, n, N, b);
 #pragma unroll
@@ -261,7 +293,7 @@ struct EpiBiasGelu {
 
 // Plain epilogue: out = acc (+ bias).
 template <typename OutT>
-struct EpiStore {
+struct EpiStore : EpiBase {
     static constexpr int kWarps = kHeavyEpiWarps;
     static constexpr int kOuts = 1;
     static constexpr int kIns = 0;
@@ -273,7 +305,7 @@ struct EpiStore {
     __device__ static int mode(const Params &) { return 0; }
     __device__ static Row begin(const Params &, int, bool) { return {}; }
     __device__ static void chunk(const Params &p, Row &, int, int n, int N, bool, float (&v)[32],
-                                 const float (&in)[32], float (&o)[kOuts][32]) {
+                                 const float (&in)[2][32], float (&o)[kOuts][32]) {
         float b[32];
         load_bias32(p.bias, n, N, b);
 #pragma unroll
@@ -285,7 +317,7 @@ struct EpiStore {
 // dY epilogue of the backward: dU = acc (.) GeLU'(U); the saved U arrives as
 // the kernel-loaded input chunk.
 template <typename OutT>
-struct EpiGeluGrad {
+struct EpiGeluGrad : EpiBase {
     static constexpr int kWarps = kHeavyEpiWarps;
     static constexpr int kOuts = 1;
     static constexpr int kIns = 1;
@@ -294,10 +326,78 @@ struct EpiGeluGrad {
     struct Params {};
     __device__ static int mode(const Params &) { return 0; }
     __device__ static Row begin(const Params &, int, bool) { return {}; }
-    __device__ static void chunk(const Params &, Row &, int, int, int, bool, float (&v)[32], const float (&u)[32],
+    __device__ static void chunk(const Params &, Row &, int, int, int, bool, float (&v)[32], const float (&u)[2][32],
                                  float (&o)[kOuts][32]) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[0][i] = v[i] * gelu_grad_f(u[i]);
+        for (int i = 0; i < 32; ++i) o[0][i] = v[i] * gelu_grad_f(u[0][i]);
+    }
+    __device__ static void end(const Params &, Row &, int, int, bool) {}
+};
+
+// SwiGLU forward (gated tile): G = acc_gate + b_gate, Up = acc_up + b_up,
+// Y = Swish(G) Up. Outputs: G and Up into the [T, 2f] map at columns n and
+// f_off + n, Y into the [T, f] map.
+template <typename OutT>
+struct EpiSwiGlu : EpiBase {
+    static constexpr int kWarps = kHeavyEpiWarps;
+    static constexpr int kOuts = 3;
+    static constexpr int kIns = 0;
+    static constexpr bool kGated = true;
+    using Out = OutT;
+    using Row = NoRow;
+    struct Params {
+        const float *bias;  // [2 f_off] (gate biases, then up biases) or null
+        int f_off;          // f: column offset of the up half in W1, the bias and GU
+    };
+    __host__ __device__ static constexpr int out_map(int k) { return k == 2 ? 1 : 0; }
+    __device__ static int out_col(const Params &p, int k) { return k == 1 ? p.f_off : 0; }
+    __device__ static int mode(const Params &) { return 0; }
+    __device__ static Row begin(const Params &, int, bool) { return {}; }
+    __device__ static void chunk(const Params &p, Row &, int, int n, int N, bool, float (&v)[32],
+                                 const float (&in)[2][32], float (&o)[kOuts][32]) {
+        float bg[32], bu[32];
+        load_bias32(p.bias, n, N, bg);
+        load_bias32(p.bias ? p.bias + p.f_off : nullptr, n, N, bu);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float g = v[i] + bg[i];
+            const float u = in[0][i] + bu[i];
+            o[0][i] = g;
+            o[1][i] = u;
+            o[2][i] = g * sigmoid_f(g) * u;
+        }
+    }
+    __device__ static void end(const Params &, Row &, int, int, bool) {}
+};
+
+// SwiGLU dY epilogue of the backward: with dY = acc and the saved G, Up as the
+// two inputs, dG = dY Up Swish'(G), dUp = dY Swish(G), where
+// Swish'(g) = s (1 + g (1 - s)), s = sigmoid(g). Outputs into the [T, 2f] map
+// at columns n and f_off + n.
+template <typename OutT>
+struct EpiSwiGluGrad : EpiBase {
+    static constexpr int kWarps = kHeavyEpiWarps;
+    static constexpr int kOuts = 2;
+    static constexpr int kIns = 2;
+    using Out = OutT;
+    using Row = NoRow;
+    struct Params {
+        int f_off;  // f: column offset of the up half in GU and dGU
+    };
+    __host__ __device__ static constexpr int out_map(int) { return 0; }
+    __device__ static int out_col(const Params &p, int k) { return k == 1 ? p.f_off : 0; }
+    __device__ static int in_col(const Params &p, int i) { return i == 1 ? p.f_off : 0; }
+    __device__ static int mode(const Params &) { return 0; }
+    __device__ static Row begin(const Params &, int, bool) { return {}; }
+    __device__ static void chunk(const Params &, Row &, int, int, int, bool, float (&v)[32],
+                                 const float (&in)[2][32], float (&o)[kOuts][32]) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float g = in[0][i], u = in[1][i];
+            const float s = sigmoid_f(g);
+            o[0][i] = v[i] * u * (s * fmaf(g, 1.0f - s, 1.0f));
+            o[1][i] = v[i] * (g * s);
+        }
     }
     __device__ static void end(const Params &, Row &, int, int, bool) {}
 };
@@ -306,7 +406,7 @@ struct EpiGeluGrad {
 // exp(l - max)) over the real ids, plus the target logit where the target
 // falls in this tile. The logits never leave the registers. One warp per TMEM
 // lane quarter, so each thread sees its token's whole tile row.
-struct EpiCeStats {
+struct EpiCeStats : EpiBase {
     static constexpr int kWarps = 4;
     static constexpr int kOuts = 0;
     static constexpr int kIns = 0;
@@ -331,7 +431,7 @@ struct EpiCeStats {
         return Row{live ? __ldg(p.targets + row) : -1, -INFINITY, 0.0f, 0.0f, false};
     }
     __device__ static void chunk(const Params &p, Row &r, int, int n, int, bool, float (&v)[32],
-                                 const float (&)[32], float (&)[1][32]) {
+                                 const float (&)[2][32], float (&)[1][32]) {
         const int g0 = p.n_base + n;                 // vocabulary id of v[0]
         const int nvalid = min(32, p.v_valid - g0);  // ids < v_valid are real
         if (nvalid > 0) {
@@ -366,7 +466,7 @@ struct EpiCeStats {
 // CE pass 2, first GEMM: recomputed logits -> dl = g (exp(l - lse) - onehot),
 // zero on padded ids.
 template <typename OutT>
-struct EpiCeDlogits {
+struct EpiCeDlogits : EpiBase {
     static constexpr int kWarps = kHeavyEpiWarps;
     static constexpr int kOuts = 1;
     static constexpr int kIns = 0;
@@ -387,7 +487,7 @@ struct EpiCeDlogits {
         return Row{live ? __ldg(p.lse + row) : 0.0f, live ? __ldg(p.targets + row) : -1};
     }
     __device__ static void chunk(const Params &p, Row &r, int, int n, int, bool, float (&v)[32],
-                                 const float (&in)[32], float (&o)[kOuts][32]) {
+                                 const float (&in)[2][32], float (&o)[kOuts][32]) {
         const int g0 = p.n_base + n;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -401,7 +501,7 @@ struct EpiCeDlogits {
 
 // fp32 output stored (mode 0) or added element-wise into global memory by the
 // TMA reduction (mode 1): dH summed over vocabulary chunks, in chunk order.
-struct EpiF32Accumulate {
+struct EpiF32Accumulate : EpiBase {
     static constexpr int kWarps = kHeavyEpiWarps;
     static constexpr int kOuts = 1;
     static constexpr int kIns = 0;
@@ -413,7 +513,7 @@ struct EpiF32Accumulate {
     __device__ static int mode(const Params &p) { return p.add; }
     __device__ static Row begin(const Params &, int, bool) { return {}; }
     __device__ static void chunk(const Params &, Row &, int, int, int, bool, float (&v)[32],
-                                 const float (&in)[32], float (&o)[kOuts][32]) {
+                                 const float (&in)[2][32], float (&o)[kOuts][32]) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[0][i] = v[i];
     }
@@ -423,8 +523,8 @@ struct EpiF32Accumulate {
 // --------------------------------------------------------------------------
 // The epilogue driver shared by the one-CTA and the CTA-pair kernels.
 // Per epilogue warp, shared memory holds 2 staging buffers per output and 2
-// input buffers (kIns = 1), each a 32 x 32 chunk; the input buffers have one
-// mbarrier each.
+// sets of kIns input buffers, each a 32 x 32 chunk; each input set has one
+// mbarrier.
 // --------------------------------------------------------------------------
 template <class Epi>
 struct EpiSmem {
@@ -445,15 +545,20 @@ struct EpiWarp {
     uint32_t in_used;   // input chunk loads consumed
 };
 
-// Start the TMA load of the input chunk at (n, row0) into the next input buffer.
+// Start the TMA loads of the input chunks at (n + in_col(i), row0) into the
+// next input set.
 template <class Epi>
-__device__ __forceinline__ void epi_issue_input(EpiWarp &w, const CUtensorMap *tmIn, int lane, int n, int row0) {
+__device__ __forceinline__ void epi_issue_input(EpiWarp &w, const typename Epi::Params &ep, const CUtensorMap *tmIn,
+                                                int lane, int n, int row0) {
     if constexpr (Epi::kIns > 0) {
         constexpr uint32_t kB = EpiSmem<Epi>::kChunkBytes;
         if (lane == 0) {
             const uint32_t b = w.in_issued & 1u;
-            ptx::mbar_arrive_expect_tx(&w.in_bar[b], kB);
-            ptx::tma_load_2d(w.stage + EpiSmem<Epi>::kOutBytes + b * kB, tmIn, &w.in_bar[b], n, row0);
+            ptx::mbar_arrive_expect_tx(&w.in_bar[b], Epi::kIns * kB);
+#pragma unroll
+            for (int i = 0; i < Epi::kIns; ++i)
+                ptx::tma_load_2d(w.stage + EpiSmem<Epi>::kOutBytes + (b * Epi::kIns + i) * kB, tmIn, &w.in_bar[b],
+                                 n + Epi::in_col(ep, i), row0);
         }
         ++w.in_issued;
     }
@@ -471,31 +576,36 @@ __device__ __forceinline__ void epi_drain_inputs(EpiWarp &w) {
 }
 
 // One tile's epilogue for this warp: chunks [c0, c1) of its 32 rows starting
-// at row0, columns from n0. The input chunk c0 must already be issued.
+// at row0, columns from n0. The input chunk c0 must already be issued. Gated
+// epilogues read the up half of chunk c at TMEM column up_col + 32 c.
 // Returns false if a bounded wait gave up.
 template <class Epi>
 __device__ __forceinline__ bool epi_tile(const typename Epi::Params &ep, const GemmShape &shp, uint32_t taddr,
-                                         int row0, int n0, int c0, int c1, int lane, EpiWarp &w,
+                                         uint32_t up_col, int row0, int n0, int c0, int c1, int lane, EpiWarp &w,
                                          const CUtensorMap *tmC0, const CUtensorMap *tmC1,
                                          const CUtensorMap *tmIn, volatile int *abort_flag, uint32_t *err) {
     using OutT = typename Epi::Out;
     constexpr int kOuts = Epi::kOuts;
     constexpr uint32_t kB = EpiSmem<Epi>::kChunkBytes;
+    static_assert(Epi::kIns <= 2 && !(Epi::kGated && Epi::kIns > 0), "epilogue inputs");
     const int row = row0 + lane;
     typename Epi::Row rs = Epi::begin(ep, row, row < shp.M);
 #pragma unroll 1
     for (int c = c0; c < c1; ++c) {
         const int n = n0 + c * 32;
-        if (c + 1 < c1) epi_issue_input<Epi>(w, tmIn, lane, n + 32, row0);
+        if (c + 1 < c1) epi_issue_input<Epi>(w, ep, tmIn, lane, n + 32, row0);
         float v[32];
         ptx::tmem_ld32(taddr + c * 32, v);
-        float in[32];
+        float in[2][32];
+        if constexpr (Epi::kGated) ptx::tmem_ld32(taddr + up_col + c * 32, in[0]);
         if constexpr (Epi::kIns > 0) {
             const uint32_t b = w.in_used & 1u;
             const bool ok = ptx::mbar_wait(&w.in_bar[b], (w.in_used >> 1) & 1u, abort_flag, err, 5);
             if (!__all_sync(0xffffffffu, ok)) return false;
-            Stage<OutT>::read(w.stage + EpiSmem<Epi>::kOutBytes + b * kB, lane, in);
-            __syncwarp();  // every lane has read the buffer before it is loaded again
+#pragma unroll
+            for (int i = 0; i < Epi::kIns; ++i)
+                Stage<OutT>::read(w.stage + EpiSmem<Epi>::kOutBytes + (b * Epi::kIns + i) * kB, lane, in[i]);
+            __syncwarp();  // every lane has read the buffers before they are loaded again
             ++w.in_used;
         }
         const bool col_live = n < shp.N;
@@ -520,11 +630,12 @@ __device__ __forceinline__ bool epi_tile(const typename Epi::Params &ep, const G
 #pragma unroll
                 for (int k = 0; k < kOuts; ++k) {
                     const uint8_t *src = w.stage + (2 * k + buf) * kB;
-                    const CUtensorMap *tm = k == 0 ? tmC0 : tmC1;
+                    const CUtensorMap *tm = Epi::out_map(k) == 0 ? tmC0 : tmC1;
+                    const int col = n + Epi::out_col(ep, k);
                     if (Epi::mode(ep) == 1)
-                        ptx::tma_reduce_add_2d(tm, src, n, row0);
+                        ptx::tma_reduce_add_2d(tm, src, col, row0);
                     else
-                        ptx::tma_store_2d(tm, src, n, row0);
+                        ptx::tma_store_2d(tm, src, col, row0);
                 }
                 ptx::bulk_commit();
             }
@@ -577,8 +688,10 @@ __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
     constexpr int kUmmaK = ET::kUmmaK;
     constexpr uint32_t kIdesc = ptx::idesc_f32acc(kBM, BN, ET::kFmt, A_MN, B_MN);
     constexpr int kGroups = Epi::kWarps / 4;  // epilogue warps per TMEM lane quarter
-    constexpr int kChunks = BN / 32;
+    constexpr int kTileN = Epi::kGated ? BN / 2 : BN;  // output columns per tile
+    constexpr int kChunks = kTileN / 32;
     constexpr int kOuts = Epi::kOuts;
+    static_assert(!Epi::kGated || BN % 128 == 0, "gated tiles: halves of whole 64-wide blocks");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -634,7 +747,7 @@ __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
             for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
                 int mb, nb;
                 tile_coords(tile, shp, mb, nb);
-                const int m0 = mb * kBM, n0 = nb * BN;
+                const int m0 = mb * kBM, n0 = nb * kTileN;
                 for (int kb = 0; kb < shp.k_blocks; ++kb) {
                     if (!ptx::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, 1)) break;
                     ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
@@ -652,12 +765,24 @@ __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
                                              m0 + shp.a_off_mn + 64 * j, k0 + shp.a_off_k);
                     }
                     if (!B_MN) {
-                        ptx::tma_load_2d(sb, &tmB, &full[stage], k0 + shp.b_off_k, n0 + shp.b_off_mn);
+                        if constexpr (Epi::kGated) {
+                            // two boxes of BN/2 rows: the gate rows, then the up rows
+                            ptx::tma_load_2d(sb, &tmB, &full[stage], k0 + shp.b_off_k, n0 + shp.b_off_mn);
+                            ptx::tma_load_2d(sb + (BN / 2) * kRowBytes, &tmB, &full[stage], k0 + shp.b_off_k,
+                                             n0 + shp.b_gate_off + shp.b_off_mn);
+                        } else {
+                            ptx::tma_load_2d(sb, &tmB, &full[stage], k0 + shp.b_off_k, n0 + shp.b_off_mn);
+                        }
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BN / 64; ++j)
-                            ptx::tma_load_2d(sb + j * kMnBlockBytes, &tmB, &full[stage],
-                                             n0 + shp.b_off_mn + 64 * j, k0 + shp.b_off_k);
+                        for (int j = 0; j < BN / 64; ++j) {
+                            // gated: blocks j >= BN/128 are the up columns
+                            const int col = Epi::kGated && j >= BN / 128
+                                                ? n0 + shp.b_gate_off + 64 * (j - BN / 128)
+                                                : n0 + 64 * j;
+                            ptx::tma_load_2d(sb + j * kMnBlockBytes, &tmB, &full[stage], col + shp.b_off_mn,
+                                             k0 + shp.b_off_k);
+                        }
                     }
                     if (++stage == S) {
                         stage = 0;
@@ -733,14 +858,15 @@ __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
             int mb, nb;
             tile_coords(tile, shp, mb, nb);
             const int row0 = mb * kBM + quarter * 32;  // first output row of this warp
-            const int n0 = nb * BN;
-            epi_issue_input<Epi>(w, &tmIn, lane, n0 + c0 * 32, row0);
+            const int n0 = nb * kTileN;
+            epi_issue_input<Epi>(w, ep, &tmIn, lane, n0 + c0 * 32, row0);
             // the decision to go on must be warp-uniform: the TMEM loads are warp-collective
             const bool ok = ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, err, 4);
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
-            if (!epi_tile<Epi>(ep, shp, taddr, row0, n0, c0, c1, lane, w, &tmC0, &tmC1, &tmIn, abort_flag, err))
+            if (!epi_tile<Epi>(ep, shp, taddr, BN / 2, row0, n0, c0, c1, lane, w, &tmC0, &tmC1, &tmIn, abort_flag,
+                               err))
                 break;
             ptx::tc_fence_before();
             __syncwarp();

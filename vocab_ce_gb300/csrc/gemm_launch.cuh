@@ -79,14 +79,19 @@ inline tpce_status set_smem_attr(K kern, uint32_t bytes, bool (&done)[64], std::
     return TPCE_OK;
 }
 
-// D = A * B with the epilogue Epi, writing outs[0 .. Epi::kOuts). Offsets
-// shift the operands' coordinates inside their tensor maps (used to address
-// one vocabulary chunk of E).
+// D = A * B with the epilogue Epi, storing through the output tensors
+// outs[0 .. num_out_maps<Epi>()) and reading the input tensor ins[0] (epilogues
+// with inputs). Offsets shift the operands' coordinates inside their tensor
+// maps (used to address one vocabulary chunk of E). Gated epilogues: N counts
+// output columns, and the second half of each B tile starts b_gate_off
+// columns (rows, K-major) after the first.
 template <typename ElemT, int BN, bool A_MN, bool B_MN, class Epi>
 tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, const OutView *outs,
                         const OutView *ins, int M, int N, int K, int a_off_mn, int a_off_k, int b_off_mn,
-                        int b_off_k, const typename Epi::Params &ep, cudaStream_t stream, bool timed = true) {
+                        int b_off_k, const typename Epi::Params &ep, cudaStream_t stream, bool timed = true,
+                        int b_gate_off = 0) {
     using Cfg = KernelCfg<BN, Epi>;
+    constexpr int kTileN = Epi::kGated ? BN / 2 : BN;
     using OutT = typename Epi::Out;
     constexpr bool kF32 = std::is_same<ElemT, float>::value;
     constexpr uint32_t kBoxK = kRowBytes / sizeof(ElemT);  // contraction elements per 128-byte row
@@ -96,10 +101,10 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
     bool ok = A_MN ? make_tmap(&ta, dt, a.ptr, a.cols, a.rows, a.ld, 64, 64)
                    : make_tmap(&ta, dt, a.ptr, a.cols, a.rows, a.ld, kBoxK, kBM);
     ok = ok && (B_MN ? make_tmap(&tb, dt, b.ptr, b.cols, b.rows, b.ld, 64, 64)
-                     : make_tmap(&tb, dt, b.ptr, b.cols, b.rows, b.ld, kBoxK, BN));
+                     : make_tmap(&tb, dt, b.ptr, b.cols, b.rows, b.ld, kBoxK, kTileN));
     const int odt = std::is_same<OutT, float>::value ? 1 : 0;
     for (int k = 0; k < 2; ++k) {
-        if (k < Epi::kOuts)
+        if (k < num_out_maps<Epi>())
             ok = ok && make_tmap(&tc[k], odt, outs[k].ptr, outs[k].cols, outs[k].rows, outs[k].ld, 32, 32,
                                  Stage<OutT>::kSwizzle);
         else
@@ -116,13 +121,14 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
     s.N = N;
     s.K = K;
     s.tiles_m = (M + kBM - 1) / kBM;
-    s.tiles_n = (N + BN - 1) / BN;
+    s.tiles_n = (N + kTileN - 1) / kTileN;
     s.k_blocks = (K + static_cast<int>(kBoxK) - 1) / static_cast<int>(kBoxK);
     s.group_m = pick_group_m(s.tiles_m);
     s.a_off_mn = a_off_mn;
     s.a_off_k = a_off_k;
     s.b_off_mn = b_off_mn;
     s.b_off_k = b_off_k;
+    s.b_gate_off = b_gate_off;
 
     auto kern = tc_gemm_kernel<ElemT, BN, A_MN, B_MN, Epi>;
     static std::mutex attr_mu;
@@ -150,8 +156,10 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
 template <int BN, bool A_MN, bool B_MN, class Epi>
 tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &b, const OutView *outs,
                              const OutView *ins, int M, int N, int K, int a_off_mn, int a_off_k, int b_off_mn,
-                             int b_off_k, const typename Epi::Params &ep, cudaStream_t stream, bool timed = true) {
+                             int b_off_k, const typename Epi::Params &ep, cudaStream_t stream, bool timed = true,
+                             int b_gate_off = 0) {
     using Cfg = PairCfg<BN, Epi>;
+    constexpr int kTileN = Epi::kGated ? BN / 2 : BN;
     using OutT = typename Epi::Out;
     if (M <= 0 || N <= 0 || K <= 0) return TPCE_ERR_SHAPE;
     CUtensorMap ta, tb, tc[2];
@@ -161,7 +169,7 @@ tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &
                      : make_tmap(&tb, 0, b.ptr, b.cols, b.rows, b.ld, 64, BN / 2));
     const int odt = std::is_same<OutT, float>::value ? 1 : 0;
     for (int k = 0; k < 2; ++k) {
-        if (k < Epi::kOuts)
+        if (k < num_out_maps<Epi>())
             ok = ok && make_tmap(&tc[k], odt, outs[k].ptr, outs[k].cols, outs[k].rows, outs[k].ld, 32, 32,
                                  Stage<OutT>::kSwizzle);
         else
@@ -177,13 +185,14 @@ tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &
     s.N = N;
     s.K = K;
     s.tiles_m = (M + 2 * kBM - 1) / (2 * kBM);
-    s.tiles_n = (N + BN - 1) / BN;
+    s.tiles_n = (N + kTileN - 1) / kTileN;
     s.k_blocks = (K + 63) / 64;
     s.group_m = pick_group_m(s.tiles_m);
     s.a_off_mn = a_off_mn;
     s.a_off_k = a_off_k;
     s.b_off_mn = b_off_mn;
     s.b_off_k = b_off_k;
+    s.b_gate_off = b_gate_off;
     auto kern = tc_gemm_pair_kernel<BN, A_MN, B_MN, Epi>;
     static std::mutex attr_mu;
     static bool attr_done[64] = {};
@@ -203,29 +212,31 @@ tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &
 template <typename ElemT, bool A_MN, bool B_MN, class Epi, unsigned Allowed>
 tpce_status launch_gemm_auto(const char *name, const Operand &a, const Operand &b, const OutView *outs,
                              const OutView *ins, int M, int N, int K, int a_off_mn, int a_off_k, int b_off_mn,
-                             int b_off_k, const typename Epi::Params &ep, cudaStream_t stream) {
+                             int b_off_k, const typename Epi::Params &ep, cudaStream_t stream, int b_gate_off = 0) {
+    static_assert(!Epi::kGated || (Allowed & kBN192) == 0, "gated tiles are 128 or 256 wide");
     if constexpr (TPCE_PAIR_BN != 0 && std::is_same<ElemT, __nv_bfloat16>::value && Epi::kWarps == 4) {
         return launch_gemm_pair<TPCE_PAIR_BN, A_MN, B_MN, Epi>(name, a, b, outs, ins, M, N, K, a_off_mn, a_off_k,
-                                                              b_off_mn, b_off_k, ep, stream);
+                                                              b_off_mn, b_off_k, ep, stream, true, b_gate_off);
     } else {
         const int sms = num_sms();
         if (sms <= 0) return fail(TPCE_ERR_CUDA, "device query failed (%s)", name);
         const unsigned allowed = (Allowed & TPCE_BN_MASK) ? (Allowed & TPCE_BN_MASK) : Allowed;
-        const int bn = pick_bn(M, N, sms, allowed);
+        // a gated tile's accumulator spans twice its output columns
+        const int bn = pick_bn(M, Epi::kGated ? 2 * static_cast<int64_t>(N) : N, sms, allowed);
         if constexpr ((Allowed & kBN256) != 0) {
             if (bn == 256)
                 return launch_gemm<ElemT, 256, A_MN, B_MN, Epi>(name, a, b, outs, ins, M, N, K, a_off_mn, a_off_k,
-                                                               b_off_mn, b_off_k, ep, stream);
+                                                               b_off_mn, b_off_k, ep, stream, true, b_gate_off);
         }
         if constexpr ((Allowed & kBN192) != 0) {
             if (bn == 192)
                 return launch_gemm<ElemT, 192, A_MN, B_MN, Epi>(name, a, b, outs, ins, M, N, K, a_off_mn, a_off_k,
-                                                               b_off_mn, b_off_k, ep, stream);
+                                                               b_off_mn, b_off_k, ep, stream, true, b_gate_off);
         }
         if constexpr ((Allowed & kBN128) != 0) {
             if (bn == 128)
                 return launch_gemm<ElemT, 128, A_MN, B_MN, Epi>(name, a, b, outs, ins, M, N, K, a_off_mn, a_off_k,
-                                                               b_off_mn, b_off_k, ep, stream);
+                                                               b_off_mn, b_off_k, ep, stream, true, b_gate_off);
         }
         return fail(TPCE_ERR_SHAPE, "no tile width for %s", name);
     }

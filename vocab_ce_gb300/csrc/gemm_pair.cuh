@@ -51,8 +51,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
     constexpr int kUmmaK = ET::kUmmaK;
     constexpr int kHalfN = BN / 2;
     constexpr uint32_t kIdesc = ptx::idesc_f32acc(2 * kBM, BN, ET::kFmt, A_MN, B_MN);
-    constexpr int kChunks = BN / 32;
+    constexpr int kTileN = Epi::kGated ? BN / 2 : BN;  // output columns per tile
+    constexpr int kChunks = kTileN / 32;
     constexpr int kOuts = Epi::kOuts;
+    static_assert(!Epi::kGated || BN % 128 == 0, "gated tiles: halves of whole 64-wide blocks");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -114,7 +116,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
                 int mb, nb;
                 tile_coords(tile, shp, mb, nb);
                 const int m0 = mb * (2 * kBM) + static_cast<int>(rank) * kBM;
-                const int nh0 = nb * BN + static_cast<int>(rank) * kHalfN;
+                // this CTA's half of the B tile; gated tiles: the even CTA loads
+                // the gate columns, the odd CTA the same columns of the up half
+                const int nh0 = Epi::kGated ? nb * kTileN + static_cast<int>(rank) * shp.b_gate_off
+                                            : nb * BN + static_cast<int>(rank) * kHalfN;
                 for (int kb = 0; kb < shp.k_blocks; ++kb) {
                     if (!ptx::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, 1)) break;
                     const uint32_t bar = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
@@ -205,13 +210,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
             int mb, nb;
             tile_coords(tile, shp, mb, nb);
             const int row0 = mb * (2 * kBM) + static_cast<int>(rank) * kBM + quarter * 32;
-            const int n0 = nb * BN;
-            epi_issue_input<Epi>(w, &tmIn, lane, n0, row0);
+            const int n0 = nb * kTileN;
+            epi_issue_input<Epi>(w, ep, &tmIn, lane, n0, row0);
             const bool ok = ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, err, 4);
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
-            if (!epi_tile<Epi>(ep, shp, taddr, row0, n0, 0, kChunks, lane, w, &tmC0, &tmC1, &tmIn, abort_flag, err))
+            if (!epi_tile<Epi>(ep, shp, taddr, BN / 2, row0, n0, 0, kChunks, lane, w, &tmC0, &tmC1, &tmIn, abort_flag,
+                               err))
                 break;
             ptx::tc_fence_before();
             __syncwarp();

@@ -1,7 +1,8 @@
-// mlp.cu -- tp_mlp_forward / tp_mlp_backward: the Megatron 1D tensor-parallel
-// MLP block with its t shards laid out on one GPU.
+// mlp.cu -- the Megatron 1D tensor-parallel MLP block with its t shards laid
+// out on one GPU: tp_mlp_forward / tp_mlp_backward (GeLU) and
+// tp_swiglu_forward / tp_swiglu_backward (the SwiGLU variant).
 //
-// Forward ("Mathematical Foundations of Megatron-LM 1D Slicing", sections
+// GeLU block ("Mathematical Foundations of Megatron-LM 1D Slicing", sections
 // "Column-Parallel Linear Layer" and "Row-Parallel Linear Layer"):
 //   GEMM1  U = X A + bA, Y = GeLU(U)  -- N runs over the concatenated column
 //          blocks A_1..A_t; GeLU is applied in the epilogue, per shard, with
@@ -13,10 +14,21 @@
 // every shard; f* sums the shard partials of dX, again in the accumulator of
 // the dX GEMM (K over the concatenated shard ranges).
 //
+// SwiGLU block ("Distributed tensor parallelism: scale fine-tuning of
+// 70B-parameter LLMs with Megatron-LM", section "The MLP Block"):
+// Y = Swish(X W_gate) (.) (X W_up), Z = Y W_down. W1 = [W_gate | W_up] is one
+// [h, 2f] matrix; shard i owns gate columns i f/t.. and the same up columns.
+// GEMM1 runs on gated tiles: each accumulator holds the gate and the up
+// columns of the same output columns, so Swish(G) Up is formed in the
+// epilogue. GEMM2 and the g / f* shard sums are the GeLU block's; the
+// backward's dY epilogue forms [dG | dUp] and the weight-gradient and dX
+// GEMMs run over the 2f columns of W1.
+//
 // bf16 tensors use the bf16 tensor-core path with operands read in place in
 // either major order. fp32 tensors use the tf32 path, whose operands are
-// K-major: the operands stored the other way (A and B in the forward, Y, dZ,
-// X, dU in the weight gradients) are first transposed into the workspace.
+// K-major: the operands stored the other way (the weights in the forward; Y,
+// dZ, X and the pre-activation gradient in the weight gradients) are first
+// transposed into the workspace.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -30,10 +42,16 @@ namespace {
 
 constexpr int64_t kMaxDim = INT_MAX - 1024;  // kernel coordinates are 32-bit
 
-tpce_status check_mlp_shape(int64_t T, int64_t h, int64_t f, int t, int dtype) {
+// The nonlinearity between the two GEMMs.
+enum class Act { GeLU, SwiGLU };
+
+// Columns of the first GEMM's output (and of W1, b1, dU): f, or 2f for SwiGLU.
+inline int64_t pre_width(Act act, int64_t f) { return act == Act::SwiGLU ? 2 * f : f; }
+
+tpce_status check_mlp_shape(Act act, int64_t T, int64_t h, int64_t f, int t, int dtype) {
     if (dtype != TPCE_BF16 && dtype != TPCE_F32) return TPCE_ERR_INVALID;
     if (T < 0 || h < 8 || f < 1 || t < 1) return TPCE_ERR_SHAPE;
-    if (T > kMaxDim || h > kMaxDim || f > kMaxDim) return TPCE_ERR_SHAPE;
+    if (T > kMaxDim || h > kMaxDim || pre_width(act, f) > kMaxDim) return TPCE_ERR_SHAPE;
     if (h % 8 != 0) return TPCE_ERR_SHAPE;           // 16-byte row pitch
     if (f % t != 0) return TPCE_ERR_SHAPE;           // equal shards
     if ((f / t) % 64 != 0) return TPCE_ERR_SHAPE;    // a shard is whole 64-wide blocks
@@ -43,33 +61,35 @@ tpce_status check_mlp_shape(int64_t T, int64_t h, int64_t f, int t, int dtype) {
 
 inline int64_t pad4(int64_t x) { return (x + 3) / 4 * 4; }  // fp32 rows padded to 16 bytes
 
-// Workspace layout. bf16: dU [T, f] and the column-sum partials. fp32 adds the
-// transposed operands of the tf32 path: A^T, B^T (forward), Y^T, dZ^T, X^T,
-// dU^T (backward), the token-major ones with rows padded to a multiple of 4.
+// Workspace layout. bf16: dU [T, fw] (fw = f, or 2f for SwiGLU: [dG | dUp])
+// and the column-sum partials. fp32 adds the transposed operands of the tf32
+// path: W1^T, W2^T (forward), Y^T, dZ^T, X^T, dU^T (backward), the
+// token-major ones with rows padded to a multiple of 4.
 struct MlpWs {
     size_t dU, partial, At, Bt, Yt, dZt, Xt, dUt, total;
 };
 
-MlpWs mlp_ws_layout(int64_t T, int64_t h, int64_t f, int dtype) {
+MlpWs mlp_ws_layout(Act act, int64_t T, int64_t h, int64_t f, int dtype) {
     MlpWs L{};
     const size_t esz = dtype == TPCE_F32 ? 4 : 2;
+    const int64_t fw = pre_width(act, f);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t at = off;
         off = round_up(off + bytes, 256);
         return at;
     };
-    L.dU = take(static_cast<size_t>(T) * f * esz);
-    const size_t pf = std::max(colsum_partial_floats(T, f), colsum_partial_floats(T, h));
+    L.dU = take(static_cast<size_t>(T) * fw * esz);
+    const size_t pf = std::max(colsum_partial_floats(T, fw), colsum_partial_floats(T, h));
     L.partial = take(pf * sizeof(float));
     if (dtype == TPCE_F32) {
         const size_t Tp = static_cast<size_t>(pad4(T));
-        L.At = take(static_cast<size_t>(f) * h * 4);
+        L.At = take(static_cast<size_t>(fw) * h * 4);
         L.Bt = take(static_cast<size_t>(h) * f * 4);
         L.Yt = take(static_cast<size_t>(f) * Tp * 4);
         L.dZt = take(static_cast<size_t>(h) * Tp * 4);
         L.Xt = take(static_cast<size_t>(h) * Tp * 4);
-        L.dUt = take(static_cast<size_t>(f) * Tp * 4);
+        L.dUt = take(static_cast<size_t>(fw) * Tp * 4);
     }
     L.total = off;
     return L;
@@ -81,42 +101,61 @@ T *at(void *ws, size_t off) {
 }
 
 // ---------------------------------------------------------------- bf16 path
-tpce_status forward_bf16(const void *X, const void *A, const float *bA, const void *B, const float *bB, int64_t T,
-                         int64_t h, int64_t f, void *Z, void *U, void *Y, cudaStream_t s) {
+// Forward. GeLU: A [h, f], U_save = U [T, f]. SwiGLU: A = W1 [h, 2f],
+// U_save = [G | Up] [T, 2f].
+tpce_status forward_bf16(Act act, const void *X, const void *A, const float *bA, const void *B, const float *bB,
+                         int64_t T, int64_t h, int64_t f, void *Z, void *U, void *Y, cudaStream_t s) {
     using bf = __nv_bfloat16;
     const int Ti = static_cast<int>(T), hi = static_cast<int>(h), fi = static_cast<int>(f);
-    // GEMM1 (column-parallel): U = X A + bA, Y = GeLU(U)
-    Operand a{X, T, h, h};  // K-major [T, h]
-    Operand b{A, h, f, f};  // MN-major: K = h rows, N = f columns
-    const OutView o1[2] = {{U, T, f, f}, {Y, T, f, f}};
-    tpce_status st = launch_gemm_auto<bf, false, true, EpiBiasGelu<bf>, kBN192 | kBN256>(
-        "mlp_fwd_gemm1_bias_gelu", a, b, o1, nullptr, Ti, fi, hi, 0, 0, 0, 0, {bA}, s);
+    const int64_t fw = pre_width(act, f);
+    tpce_status st;
+    Operand a{X, T, h, h};    // K-major [T, h]
+    Operand b{A, h, fw, fw};  // MN-major: K = h rows, N = fw columns
+    const OutView o1[2] = {{U, T, fw, fw}, {Y, T, f, f}};
+    if (act == Act::GeLU) {
+        // GEMM1 (column-parallel): U = X A + bA, Y = GeLU(U)
+        st = launch_gemm_auto<bf, false, true, EpiBiasGelu<bf>, kBN192 | kBN256>(
+            "mlp_fwd_gemm1_bias_gelu", a, b, o1, nullptr, Ti, fi, hi, 0, 0, 0, 0, {bA}, s);
+    } else {
+        // GEMM1 (column-parallel, gated): [G | Up] = X W1 + b1, Y = Swish(G) Up
+        st = launch_gemm_auto<bf, false, true, EpiSwiGlu<bf>, kBN128 | kBN256>(
+            "swiglu_fwd_gemm1_gate_up", a, b, o1, nullptr, Ti, fi, hi, 0, 0, 0, 0, {bA, fi}, s, fi);
+    }
     if (st != TPCE_OK) return st;
     // GEMM2 (row-parallel) + g: Z = sum_i Y_i B_i + bB
     Operand a2{Y, T, f, f};  // K-major [T, f]
     Operand b2{B, f, h, h};  // MN-major: K = f rows, N = h columns
     const OutView o2[1] = {{Z, T, h, h}};
-    return launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256>("mlp_fwd_gemm2_shard_sum", a2, b2, o2, nullptr,
-                                                                             Ti, hi, fi, 0, 0, 0, 0, {bB}, s);
+    return launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256>(
+        act == Act::GeLU ? "mlp_fwd_gemm2_shard_sum" : "swiglu_fwd_gemm2_shard_sum", a2, b2, o2, nullptr, Ti, hi, fi, 0,
+        0, 0, 0, {bB}, s);
 }
 
-tpce_status backward_bf16(const void *dZ, const void *X, const void *A, const void *B, const void *U,
+tpce_status backward_bf16(Act act, const void *dZ, const void *X, const void *A, const void *B, const void *U,
                           const void *Y, int64_t T, int64_t h, int64_t f, void *dX, void *dA, float *dbA, void *dB,
                           float *dbB, void *ws, const MlpWs &L, cudaStream_t s) {
     using bf = __nv_bfloat16;
     bf *dU = at<bf>(ws, L.dU);
     float *partial = at<float>(ws, L.partial);
-    const int Ti = static_cast<int>(T), hi = static_cast<int>(h), fi = static_cast<int>(f);
+    const int64_t fw = pre_width(act, f);
+    const int Ti = static_cast<int>(T), hi = static_cast<int>(h), fi = static_cast<int>(f),
+              fwi = static_cast<int>(fw);
+    const bool glu = act == Act::SwiGLU;
     tpce_status st;
     // g* is the identity: every shard reads the same dZ.
-    // dY_i = dZ B_i^T, fused with dU_i = dY_i (.) GeLU'(U_i)
+    // dY_i = dZ B_i^T, fused with dU_i = dY_i (.) GeLU'(U_i), or for SwiGLU
+    // with [dG_i | dUp_i] from the saved [G_i | Up_i]
     {
         Operand a{dZ, T, h, h};  // K-major [T, h]
         Operand b{B, f, h, h};   // K-major: N = f rows, K = h columns
-        const OutView o[1] = {{dU, T, f, f}};
-        const OutView in[1] = {{const_cast<void *>(U), T, f, f}};  // read by TMA, never written
-        st = launch_gemm_auto<bf, false, false, EpiGeluGrad<bf>, kBN192 | kBN256>("mlp_bwd_dY_gelu_grad", a, b, o, in,
-                                                                                   Ti, fi, hi, 0, 0, 0, 0, {}, s);
+        const OutView o[1] = {{dU, T, fw, fw}};
+        const OutView in[1] = {{const_cast<void *>(U), T, fw, fw}};  // read by TMA, never written
+        if (!glu)
+            st = launch_gemm_auto<bf, false, false, EpiGeluGrad<bf>, kBN192 | kBN256>(
+                "mlp_bwd_dY_gelu_grad", a, b, o, in, Ti, fi, hi, 0, 0, 0, 0, {}, s);
+        else
+            st = launch_gemm_auto<bf, false, false, EpiSwiGluGrad<bf>, kBN192 | kBN256>(
+                "swiglu_bwd_dY_swiglu_grad", a, b, o, in, Ti, fi, hi, 0, 0, 0, 0, {fi}, s);
         if (st != TPCE_OK) return st;
     }
     // dB_i = Y_i^T dZ
@@ -124,58 +163,67 @@ tpce_status backward_bf16(const void *dZ, const void *X, const void *A, const vo
         Operand a{Y, T, f, f};   // MN-major: K = T rows, M = f columns
         Operand b{dZ, T, h, h};  // MN-major: K = T rows, N = h columns
         const OutView o[1] = {{dB, f, h, h}};
-        st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>("mlp_bwd_dB", a, b, o, nullptr, fi, hi, Ti, 0,
-                                                                              0, 0, 0, {nullptr}, s);
+        st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>(glu ? "swiglu_bwd_dW2" : "mlp_bwd_dB", a,
+                                                                              b, o, nullptr, fi, hi, Ti, 0, 0, 0, 0,
+                                                                              {nullptr}, s);
         if (st != TPCE_OK) return st;
     }
     // dA_i = X^T dU_i
     {
-        Operand a{X, T, h, h};   // MN-major: K = T rows, M = h columns
-        Operand b{dU, T, f, f};  // MN-major: K = T rows, N = f columns
-        const OutView o[1] = {{dA, h, f, f}};
-        st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>("mlp_bwd_dA", a, b, o, nullptr, hi, fi, Ti, 0,
-                                                                              0, 0, 0, {nullptr}, s);
+        Operand a{X, T, h, h};     // MN-major: K = T rows, M = h columns
+        Operand b{dU, T, fw, fw};  // MN-major: K = T rows, N = fw columns
+        const OutView o[1] = {{dA, h, fw, fw}};
+        st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>(glu ? "swiglu_bwd_dW1" : "mlp_bwd_dA", a,
+                                                                              b, o, nullptr, hi, fwi, Ti, 0, 0, 0, 0,
+                                                                              {nullptr}, s);
         if (st != TPCE_OK) return st;
     }
     // f*: dX = sum_i dU_i A_i^T, the shard sum taken in the accumulator
     {
-        Operand a{dU, T, f, f};  // K-major [T, f]
-        Operand b{A, h, f, f};   // K-major: N = h rows, K = f columns
+        Operand a{dU, T, fw, fw};  // K-major [T, fw]
+        Operand b{A, h, fw, fw};   // K-major: N = h rows, K = fw columns
         const OutView o[1] = {{dX, T, h, h}};
-        st = launch_gemm_auto<bf, false, false, EpiStore<bf>, kBN192 | kBN256>("mlp_bwd_dX_shard_sum", a, b, o, nullptr, Ti,
-                                                                                hi, fi, 0, 0, 0, 0, {nullptr}, s);
+        st = launch_gemm_auto<bf, false, false, EpiStore<bf>, kBN192 | kBN256>(
+            glu ? "swiglu_bwd_dX_shard_sum" : "mlp_bwd_dX_shard_sum", a, b, o, nullptr, Ti, hi, fwi, 0, 0, 0, 0,
+            {nullptr}, s);
         if (st != TPCE_OK) return st;
     }
-    if (dbA && (st = colsum(0, dU, T, f, f, dbA, partial, s)) != TPCE_OK) return st;
+    if (dbA && (st = colsum(0, dU, T, fw, fw, dbA, partial, s)) != TPCE_OK) return st;
     if (dbB && (st = colsum(0, dZ, T, h, h, dbB, partial, s)) != TPCE_OK) return st;
     return TPCE_OK;
 }
 
 // ---------------------------------------------------------------- fp32 (tf32) path
-tpce_status forward_f32(const float *X, const float *A, const float *bA, const float *B, const float *bB, int64_t T,
-                        int64_t h, int64_t f, float *Z, float *U, float *Y, void *ws, const MlpWs &L,
+tpce_status forward_f32(Act act, const float *X, const float *A, const float *bA, const float *B, const float *bB,
+                        int64_t T, int64_t h, int64_t f, float *Z, float *U, float *Y, void *ws, const MlpWs &L,
                         cudaStream_t s) {
     float *At = at<float>(ws, L.At), *Bt = at<float>(ws, L.Bt);
+    const int64_t fw = pre_width(act, f);
     const int Ti = static_cast<int>(T), hi = static_cast<int>(h), fi = static_cast<int>(f);
-    tpce_status st = transpose_f32(A, h, f, f, At, h, s);  // A^T [f, h]
+    tpce_status st = transpose_f32(A, h, fw, fw, At, h, s);  // A^T [fw, h]
     if (st != TPCE_OK) return st;
     if ((st = transpose_f32(B, f, h, h, Bt, f, s)) != TPCE_OK) return st;  // B^T [h, f]
     {
         Operand a{X, T, h, h};    // K-major [T, h]
-        Operand b{At, f, h, h};   // K-major: N = f rows, K = h columns
-        const OutView o[2] = {{U, T, f, f}, {Y, T, f, f}};
-        st = launch_gemm<float, 128, false, false, EpiBiasGelu<float>>("mlp_fwd_gemm1_bias_gelu", a, b, o, nullptr, Ti, fi,
-                                                                       hi, 0, 0, 0, 0, {bA}, s);
+        Operand b{At, fw, h, h};  // K-major: N = fw rows, K = h columns
+        const OutView o[2] = {{U, T, fw, fw}, {Y, T, f, f}};
+        if (act == Act::GeLU)
+            st = launch_gemm<float, 128, false, false, EpiBiasGelu<float>>("mlp_fwd_gemm1_bias_gelu", a, b, o, nullptr,
+                                                                           Ti, fi, hi, 0, 0, 0, 0, {bA}, s);
+        else  // gated tiles: rows n.. of W1^T are gate columns, rows f + n.. the up columns
+            st = launch_gemm<float, 128, false, false, EpiSwiGlu<float>>("swiglu_fwd_gemm1_gate_up", a, b, o, nullptr,
+                                                                         Ti, fi, hi, 0, 0, 0, 0, {bA, fi}, s, true, fi);
         if (st != TPCE_OK) return st;
     }
     Operand a2{Y, T, f, f};   // K-major [T, f]
     Operand b2{Bt, h, f, f};  // K-major: N = h rows, K = f columns
     const OutView o2[1] = {{Z, T, h, h}};
-    return launch_gemm<float, 128, false, false, EpiStore<float>>("mlp_fwd_gemm2_shard_sum", a2, b2, o2, nullptr, Ti, hi, fi,
-                                                                  0, 0, 0, 0, {bB}, s);
+    return launch_gemm<float, 128, false, false, EpiStore<float>>(
+        act == Act::GeLU ? "mlp_fwd_gemm2_shard_sum" : "swiglu_fwd_gemm2_shard_sum", a2, b2, o2, nullptr, Ti, hi, fi, 0,
+        0, 0, 0, {bB}, s);
 }
 
-tpce_status backward_f32(const float *dZ, const float *X, const float *A, const float *B, const float *U,
+tpce_status backward_f32(Act act, const float *dZ, const float *X, const float *A, const float *B, const float *U,
                          const float *Y, int64_t T, int64_t h, int64_t f, float *dX, float *dA, float *dbA,
                          float *dB, float *dbB, void *ws, const MlpWs &L, cudaStream_t s) {
     float *dU = at<float>(ws, L.dU);
@@ -183,64 +231,68 @@ tpce_status backward_f32(const float *dZ, const float *X, const float *A, const 
     float *Yt = at<float>(ws, L.Yt), *dZt = at<float>(ws, L.dZt), *Xt = at<float>(ws, L.Xt),
           *dUt = at<float>(ws, L.dUt);
     const int64_t Tp = pad4(T);
-    const int Ti = static_cast<int>(T), hi = static_cast<int>(h), fi = static_cast<int>(f);
+    const int64_t fw = pre_width(act, f);
+    const int Ti = static_cast<int>(T), hi = static_cast<int>(h), fi = static_cast<int>(f),
+              fwi = static_cast<int>(fw);
+    const bool glu = act == Act::SwiGLU;
     tpce_status st;
     {
         Operand a{dZ, T, h, h};  // K-major [T, h]
         Operand b{B, f, h, h};   // K-major: N = f rows, K = h columns
-        const OutView o[1] = {{dU, T, f, f}};
-        const OutView in[1] = {{const_cast<float *>(U), T, f, f}};  // read by TMA, never written
-        st = launch_gemm<float, 128, false, false, EpiGeluGrad<float>>("mlp_bwd_dY_gelu_grad", a, b, o, in, Ti, fi,
-                                                                       hi, 0, 0, 0, 0, {}, s);
+        const OutView o[1] = {{dU, T, fw, fw}};
+        const OutView in[1] = {{const_cast<float *>(U), T, fw, fw}};  // read by TMA, never written
+        if (!glu)
+            st = launch_gemm<float, 128, false, false, EpiGeluGrad<float>>("mlp_bwd_dY_gelu_grad", a, b, o, in, Ti, fi,
+                                                                           hi, 0, 0, 0, 0, {}, s);
+        else
+            st = launch_gemm<float, 128, false, false, EpiSwiGluGrad<float>>("swiglu_bwd_dY_swiglu_grad", a, b, o, in,
+                                                                             Ti, fi, hi, 0, 0, 0, 0, {fi}, s);
         if (st != TPCE_OK) return st;
     }
     if ((st = transpose_f32(Y, T, f, f, Yt, Tp, s)) != TPCE_OK) return st;
     if ((st = transpose_f32(dZ, T, h, h, dZt, Tp, s)) != TPCE_OK) return st;
     if ((st = transpose_f32(X, T, h, h, Xt, Tp, s)) != TPCE_OK) return st;
-    if ((st = transpose_f32(dU, T, f, f, dUt, Tp, s)) != TPCE_OK) return st;
+    if ((st = transpose_f32(dU, T, fw, fw, dUt, Tp, s)) != TPCE_OK) return st;
     {
         Operand a{Yt, f, T, Tp};   // K-major: M = f rows, K = T columns
         Operand b{dZt, h, T, Tp};  // K-major: N = h rows, K = T columns
         const OutView o[1] = {{dB, f, h, h}};
-        st = launch_gemm<float, 128, false, false, EpiStore<float>>("mlp_bwd_dB", a, b, o, nullptr, fi, hi, Ti, 0, 0, 0, 0,
-                                                                    {nullptr}, s);
+        st = launch_gemm<float, 128, false, false, EpiStore<float>>(glu ? "swiglu_bwd_dW2" : "mlp_bwd_dB", a, b, o,
+                                                                    nullptr, fi, hi, Ti, 0, 0, 0, 0, {nullptr}, s);
         if (st != TPCE_OK) return st;
     }
     {
-        Operand a{Xt, h, T, Tp};   // K-major: M = h rows, K = T columns
-        Operand b{dUt, f, T, Tp};  // K-major: N = f rows, K = T columns
-        const OutView o[1] = {{dA, h, f, f}};
-        st = launch_gemm<float, 128, false, false, EpiStore<float>>("mlp_bwd_dA", a, b, o, nullptr, hi, fi, Ti, 0, 0, 0, 0,
-                                                                    {nullptr}, s);
+        Operand a{Xt, h, T, Tp};    // K-major: M = h rows, K = T columns
+        Operand b{dUt, fw, T, Tp};  // K-major: N = fw rows, K = T columns
+        const OutView o[1] = {{dA, h, fw, fw}};
+        st = launch_gemm<float, 128, false, false, EpiStore<float>>(glu ? "swiglu_bwd_dW1" : "mlp_bwd_dA", a, b, o,
+                                                                    nullptr, hi, fwi, Ti, 0, 0, 0, 0, {nullptr}, s);
         if (st != TPCE_OK) return st;
     }
     {
-        Operand a{dU, T, f, f};  // K-major [T, f]
-        Operand b{A, h, f, f};   // K-major: N = h rows, K = f columns
+        Operand a{dU, T, fw, fw};  // K-major [T, fw]
+        Operand b{A, h, fw, fw};   // K-major: N = h rows, K = fw columns
         const OutView o[1] = {{dX, T, h, h}};
-        st = launch_gemm<float, 128, false, false, EpiStore<float>>("mlp_bwd_dX_shard_sum", a, b, o, nullptr, Ti, hi, fi, 0,
-                                                                    0, 0, 0, {nullptr}, s);
+        st = launch_gemm<float, 128, false, false, EpiStore<float>>(
+            glu ? "swiglu_bwd_dX_shard_sum" : "mlp_bwd_dX_shard_sum", a, b, o, nullptr, Ti, hi, fwi, 0, 0, 0, 0,
+            {nullptr}, s);
         if (st != TPCE_OK) return st;
     }
-    if (dbA && (st = colsum(1, dU, T, f, f, dbA, partial, s)) != TPCE_OK) return st;
+    if (dbA && (st = colsum(1, dU, T, fw, fw, dbA, partial, s)) != TPCE_OK) return st;
     if (dbB && (st = colsum(1, dZ, T, h, h, dbB, partial, s)) != TPCE_OK) return st;
     return TPCE_OK;
 }
 
-}  // namespace
-}  // namespace tpce
-
-using namespace tpce;
-
-extern "C" size_t tpce_mlp_workspace_bytes(int64_t T, int64_t h, int64_t f, int t, int dtype) {
-    if (check_mlp_shape(T, h, f, t, dtype) != TPCE_OK) return 0;
-    return mlp_ws_layout(T, h, f, dtype).total;
+// ---------------------------------------------------------------- entry points
+size_t workspace_bytes(Act act, int64_t T, int64_t h, int64_t f, int t, int dtype) {
+    if (check_mlp_shape(act, T, h, f, t, dtype) != TPCE_OK) return 0;
+    return mlp_ws_layout(act, T, h, f, dtype).total;
 }
 
-extern "C" tpce_status tp_mlp_forward(const void *X, const void *A, const float *bA, const void *B, const float *bB,
-                                      int64_t T, int64_t h, int64_t f, int t, int dtype, void *Z, void *U, void *Y,
-                                      void *ws, size_t ws_bytes, void *stream) {
-    tpce_status st = check_mlp_shape(T, h, f, t, dtype);
+tpce_status forward(Act act, const void *X, const void *A, const float *bA, const void *B, const float *bB, int64_t T,
+                    int64_t h, int64_t f, int t, int dtype, void *Z, void *U, void *Y, void *ws, size_t ws_bytes,
+                    void *stream) {
+    tpce_status st = check_mlp_shape(act, T, h, f, t, dtype);
     if (st != TPCE_OK) return st;
     if (T == 0) return TPCE_OK;  // no tokens: nothing to compute (token tensors may be NULL)
     if (!X || !A || !B || !Z || !U || !Y) return TPCE_ERR_INVALID;
@@ -249,19 +301,18 @@ extern "C" tpce_status tp_mlp_forward(const void *X, const void *A, const float 
                           static_cast<const void *>(ws)})
         if (!aligned16(p)) return TPCE_ERR_ALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (dtype == TPCE_BF16) return forward_bf16(X, A, bA, B, bB, T, h, f, Z, U, Y, s);
-    const MlpWs L = mlp_ws_layout(T, h, f, dtype);
+    if (dtype == TPCE_BF16) return forward_bf16(act, X, A, bA, B, bB, T, h, f, Z, U, Y, s);
+    const MlpWs L = mlp_ws_layout(act, T, h, f, dtype);
     if (!ws || ws_bytes < L.total) return TPCE_ERR_WORKSPACE;
-    return forward_f32(static_cast<const float *>(X), static_cast<const float *>(A), bA,
+    return forward_f32(act, static_cast<const float *>(X), static_cast<const float *>(A), bA,
                        static_cast<const float *>(B), bB, T, h, f, static_cast<float *>(Z), static_cast<float *>(U),
                        static_cast<float *>(Y), ws, L, s);
 }
 
-extern "C" tpce_status tp_mlp_backward(const void *dZ, const void *X, const void *A, const void *B, const void *U,
-                                       const void *Y, int64_t T, int64_t h, int64_t f, int t, int dtype, void *dX,
-                                       void *dA, float *dbA, void *dB, float *dbB, void *ws, size_t ws_bytes,
-                                       void *stream) {
-    tpce_status st = check_mlp_shape(T, h, f, t, dtype);
+tpce_status backward(Act act, const void *dZ, const void *X, const void *A, const void *B, const void *U,
+                     const void *Y, int64_t T, int64_t h, int64_t f, int t, int dtype, void *dX, void *dA, float *dbA,
+                     void *dB, float *dbB, void *ws, size_t ws_bytes, void *stream) {
+    tpce_status st = check_mlp_shape(act, T, h, f, t, dtype);
     if (st != TPCE_OK) return st;
     if (!A || !B || !dA || !dB) return TPCE_ERR_INVALID;
     if (T > 0 && (!dZ || !X || !U || !Y || !dX)) return TPCE_ERR_INVALID;
@@ -271,19 +322,60 @@ extern "C" tpce_status tp_mlp_backward(const void *dZ, const void *X, const void
         if (!aligned16(p)) return TPCE_ERR_ALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t esz = dtype == TPCE_F32 ? 4 : 2;
+    const int64_t fw = pre_width(act, f);
     if (T == 0) {
         // no tokens: every weight and bias gradient is an empty sum
-        if (cudaMemsetAsync(dA, 0, static_cast<size_t>(h) * f * esz, s) != cudaSuccess) return TPCE_ERR_CUDA;
+        if (cudaMemsetAsync(dA, 0, static_cast<size_t>(h) * fw * esz, s) != cudaSuccess) return TPCE_ERR_CUDA;
         if (cudaMemsetAsync(dB, 0, static_cast<size_t>(f) * h * esz, s) != cudaSuccess) return TPCE_ERR_CUDA;
-        if (dbA && cudaMemsetAsync(dbA, 0, sizeof(float) * f, s) != cudaSuccess) return TPCE_ERR_CUDA;
+        if (dbA && cudaMemsetAsync(dbA, 0, sizeof(float) * fw, s) != cudaSuccess) return TPCE_ERR_CUDA;
         if (dbB && cudaMemsetAsync(dbB, 0, sizeof(float) * h, s) != cudaSuccess) return TPCE_ERR_CUDA;
         return TPCE_OK;
     }
-    const MlpWs L = mlp_ws_layout(T, h, f, dtype);
+    const MlpWs L = mlp_ws_layout(act, T, h, f, dtype);
     if (!ws || ws_bytes < L.total) return TPCE_ERR_WORKSPACE;
-    if (dtype == TPCE_BF16) return backward_bf16(dZ, X, A, B, U, Y, T, h, f, dX, dA, dbA, dB, dbB, ws, L, s);
-    return backward_f32(static_cast<const float *>(dZ), static_cast<const float *>(X), static_cast<const float *>(A),
-                        static_cast<const float *>(B), static_cast<const float *>(U), static_cast<const float *>(Y),
-                        T, h, f, static_cast<float *>(dX), static_cast<float *>(dA), dbA, static_cast<float *>(dB),
-                        dbB, ws, L, s);
+    if (dtype == TPCE_BF16) return backward_bf16(act, dZ, X, A, B, U, Y, T, h, f, dX, dA, dbA, dB, dbB, ws, L, s);
+    return backward_f32(act, static_cast<const float *>(dZ), static_cast<const float *>(X),
+                        static_cast<const float *>(A), static_cast<const float *>(B), static_cast<const float *>(U),
+                        static_cast<const float *>(Y), T, h, f, static_cast<float *>(dX), static_cast<float *>(dA), dbA,
+                        static_cast<float *>(dB), dbB, ws, L, s);
+}
+
+}  // namespace
+}  // namespace tpce
+
+using namespace tpce;
+
+extern "C" size_t tpce_mlp_workspace_bytes(int64_t T, int64_t h, int64_t f, int t, int dtype) {
+    return workspace_bytes(Act::GeLU, T, h, f, t, dtype);
+}
+
+extern "C" tpce_status tp_mlp_forward(const void *X, const void *A, const float *bA, const void *B, const float *bB,
+                                      int64_t T, int64_t h, int64_t f, int t, int dtype, void *Z, void *U, void *Y,
+                                      void *ws, size_t ws_bytes, void *stream) {
+    return forward(Act::GeLU, X, A, bA, B, bB, T, h, f, t, dtype, Z, U, Y, ws, ws_bytes, stream);
+}
+
+extern "C" tpce_status tp_mlp_backward(const void *dZ, const void *X, const void *A, const void *B, const void *U,
+                                       const void *Y, int64_t T, int64_t h, int64_t f, int t, int dtype, void *dX,
+                                       void *dA, float *dbA, void *dB, float *dbB, void *ws, size_t ws_bytes,
+                                       void *stream) {
+    return backward(Act::GeLU, dZ, X, A, B, U, Y, T, h, f, t, dtype, dX, dA, dbA, dB, dbB, ws, ws_bytes, stream);
+}
+
+extern "C" size_t tpce_swiglu_workspace_bytes(int64_t T, int64_t h, int64_t f, int t, int dtype) {
+    return workspace_bytes(Act::SwiGLU, T, h, f, t, dtype);
+}
+
+extern "C" tpce_status tp_swiglu_forward(const void *X, const void *W1, const float *b1, const void *W2,
+                                         const float *b2, int64_t T, int64_t h, int64_t f, int t, int dtype, void *Z,
+                                         void *GU, void *Y, void *ws, size_t ws_bytes, void *stream) {
+    return forward(Act::SwiGLU, X, W1, b1, W2, b2, T, h, f, t, dtype, Z, GU, Y, ws, ws_bytes, stream);
+}
+
+extern "C" tpce_status tp_swiglu_backward(const void *dZ, const void *X, const void *W1, const void *W2,
+                                          const void *GU, const void *Y, int64_t T, int64_t h, int64_t f, int t,
+                                          int dtype, void *dX, void *dW1, float *db1, void *dW2, float *db2, void *ws,
+                                          size_t ws_bytes, void *stream) {
+    return backward(Act::SwiGLU, dZ, X, W1, W2, GU, Y, T, h, f, t, dtype, dX, dW1, db1, dW2, db2, ws, ws_bytes,
+                    stream);
 }

@@ -50,6 +50,7 @@ class Workload:
     b: int = 0
     s: int = 0
     weight_std: float = 0.02
+    act: str = "gelu"      # the MLP's nonlinearity: "gelu" or "swiglu"
 
     @property
     def b_scale(self) -> float:
@@ -74,6 +75,10 @@ WORKLOADS: Dict[str, Workload] = {
                        dtype="bf16", n_blocks=160, b=1, s=4096),
     "ce128k": Workload("ce128k", T=16384, h=8192, f=0, v_valid=128256, v_pad=129024,
                        t=8, dtype="bf16", n_blocks=160, b=4, s=4096),
+    # the SwiGLU block of the Llama-3-70B page (hidden 8192, TP 8, sequence
+    # 4096); the page gives no FFN width, the model's published 28,672 is used
+    "swiglu70b": Workload("swiglu70b", T=4096, h=8192, f=28672, v_valid=0, v_pad=0, t=8,
+                          dtype="bf16", n_blocks=160, b=1, s=4096, act="swiglu"),
 }
 
 # shard-count sweep over the 8.3B MLP shapes
@@ -86,10 +91,10 @@ def sweep_workload(t: int) -> Workload:
 
 
 def custom(name: str, T: int, h: int, f: int, v_valid: int, v_pad: int, t: int,
-           dtype: str = "bf16", n_blocks: int = 2) -> Workload:
+           dtype: str = "bf16", n_blocks: int = 2, act: str = "gelu") -> Workload:
     """A workload of arbitrary shape with the same input statistics."""
     return Workload(name, T=T, h=h, f=f, v_valid=v_valid, v_pad=v_pad, t=t,
-                    dtype=dtype, n_blocks=n_blocks)
+                    dtype=dtype, n_blocks=n_blocks, act=act)
 
 
 def _gen(device, seed: int, slot: str) -> torch.Generator:
@@ -115,6 +120,20 @@ def mlp_inputs(w: Workload, seed: int = 0, device="cpu") -> Dict[str, torch.Tens
         "B": _normal((w.f, w.h), w.weight_std * w.b_scale, dt, device, seed, "B"),
         "bA": torch.zeros(w.f, dtype=torch.float32, device=device),
         "bB": torch.zeros(w.h, dtype=torch.float32, device=device),
+        "dZ": _normal((w.T, w.h), 1.0, dt, device, seed, "dZ"),
+    }
+
+
+def swiglu_inputs(w: Workload, seed: int = 0, device="cpu") -> Dict[str, torch.Tensor]:
+    """X [T,h], W1 = [W_gate | W_up] [h,2f], W2 [f,h] (dtype), b1 [2f], b2 [h]
+    (fp32 zeros), dZ [T,h]. W1 and W2 take the generator slots of A and B."""
+    dt = w.torch_dtype
+    return {
+        "X": _normal((w.T, w.h), 1.0, dt, device, seed, "X"),
+        "W1": _normal((w.h, 2 * w.f), w.weight_std, dt, device, seed, "A"),
+        "W2": _normal((w.f, w.h), w.weight_std * w.b_scale, dt, device, seed, "B"),
+        "b1": torch.zeros(2 * w.f, dtype=torch.float32, device=device),
+        "b2": torch.zeros(w.h, dtype=torch.float32, device=device),
         "dZ": _normal((w.T, w.h), 1.0, dt, device, seed, "dZ"),
     }
 
