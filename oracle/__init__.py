@@ -87,6 +87,14 @@ def _load():
         lib.oracle_swiglu_backward_cols.argtypes = [I64, I64, I64, P, P, P, P, P, I64, P, P, P, P, P, P]
         lib.oracle_swiglu_sharded.restype = None
         lib.oracle_swiglu_sharded.argtypes = [I64, I64, I64, ctypes.c_int, P, P, P, P, P, P, P, P, P, P]
+        lib.oracle_linear_forward.restype = None
+        lib.oracle_linear_forward.argtypes = [I64, I64, I64, P, P, P, P]
+        lib.oracle_linear_backward.restype = None
+        lib.oracle_linear_backward.argtypes = [I64, I64, I64, P, P, P, P, P, P]
+        lib.oracle_linear_sharded.restype = None
+        lib.oracle_linear_sharded.argtypes = [I64, I64, I64, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P]
+        lib.oracle_qkv_column.restype = I64
+        lib.oracle_qkv_column.argtypes = [ctypes.c_int, I64, I64, I64, I64, I64]
         _lib = lib
         return lib
 
@@ -261,3 +269,53 @@ def swiglu_sharded(X, W1, b1, W2, b2, dZ, t: int) -> Dict[str, np.ndarray]:
     _load().oracle_swiglu_sharded(T, h, f, t, _ptr(X), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), _ptr(dZ),
                                   _ptr(Z), _ptr(dX), _ptr(dW1), _ptr(dW2))
     return {"Z": Z, "dX": dX, "dW1": dW1, "dW2": dW2}
+
+
+def linear_forward(X, W, b=None) -> np.ndarray:
+    """Y = X W + b."""
+    X, W, b = map(_f64, (X, W, b))
+    T, n_in = X.shape
+    n_out = W.shape[1]
+    Y = np.empty((T, n_out))
+    _load().oracle_linear_forward(T, n_in, n_out, _ptr(X), _ptr(W), _ptr(b), _ptr(Y))
+    return Y
+
+
+def linear_backward(X, W, dY, want: Sequence[str] = ("dX", "dW", "db")) -> Dict[str, np.ndarray]:
+    """dX = dY W^T, dW = X^T dY, db = sum over tokens of dY."""
+    X, W, dY = map(_f64, (X, W, dY))
+    T, n_in = X.shape
+    n_out = W.shape[1]
+    shapes = {"dX": (T, n_in), "dW": (n_in, n_out), "db": (n_out,)}
+    out = {k: np.empty(shapes[k]) for k in want}
+    _load().oracle_linear_backward(T, n_in, n_out, _ptr(X), _ptr(W), _ptr(dY), _ptr(out.get("dX")),
+                                   _ptr(out.get("dW")), _ptr(out.get("db")))
+    return out
+
+
+def linear_sharded(X, W, b, dY, t: int, mode: str) -> Dict[str, np.ndarray]:
+    """The linear layer computed shard by shard; mode "column" or "row"."""
+    X, W, b, dY = map(_f64, (X, W, b, dY))
+    T, n_in = X.shape
+    n_out = W.shape[1]
+    m = {"column": 0, "row": 1}[mode]
+    if (n_out if m == 0 else n_in) % t:
+        raise ValueError("the split dimension must divide by t")
+    Y = np.empty((T, n_out)); dX = np.empty((T, n_in)); dW = np.empty((n_in, n_out))
+    _load().oracle_linear_sharded(T, n_in, n_out, t, m, _ptr(X), _ptr(W), _ptr(b), _ptr(dY),
+                                  _ptr(Y), _ptr(dX), _ptr(dW))
+    return {"Y": Y, "dX": dX, "dW": dW}
+
+
+def qkv_column(kind: str, head: int, j: int, n_q: int, n_kv: int, d: int) -> int:
+    """Column of the fused QKV projection holding element j of a query,
+    key or value head (layout grouped by key/value head)."""
+    k = {"q": 0, "k": 1, "v": 2}[kind]
+    return int(_load().oracle_qkv_column(k, head, j, n_q, n_kv, d))
+
+
+def qkv_columns(kind: str, n_q: int, n_kv: int, d: int) -> np.ndarray:
+    """[heads, d] array of the columns of every head of one kind."""
+    n = n_q if kind == "q" else n_kv
+    return np.array([[qkv_column(kind, hh, j, n_q, n_kv, d) for j in range(d)] for hh in range(n)],
+                    dtype=np.int64)

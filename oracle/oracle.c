@@ -28,7 +28,8 @@
  *   [DEP] "Megatron-LM, in depth" (aicassindra): "Failure modes".
  *   [70B] "Distributed tensor parallelism: scale fine-tuning of 70B-parameter
  *         LLMs with Megatron-LM" (mohashari.github.io): "The Mechanics of
- *         Tensor Parallelism (TP) in Megatron-LM", "The MLP Block".
+ *         Tensor Parallelism (TP) in Megatron-LM", "The MLP Block", "The
+ *         Multi-Head Attention Block".
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *   - GeLU is the exact erf form x * Phi(x); its derivative Phi(x) + x phi(x).
@@ -41,6 +42,9 @@
  *   - The gradient returned is that of grad_scale * sum_t loss_t.
  *   - Swish in the SwiGLU block is x * sigmoid(x) (beta = 1); the first
  *     weight W1 = [W_gate | W_up] is one [h, 2f] matrix, gate columns first.
+ *   - The fused QKV weight is laid out by key/value head groups: for each KV
+ *     head g, the query heads that share it, then K_g, then V_g, so that a
+ *     contiguous column split into t blocks hands each shard whole heads.
  */
 #include <math.h>
 #include <stdint.h>
@@ -728,4 +732,145 @@ void oracle_swiglu_sharded(int64_t T, int64_t h, int64_t f, int t,
     free(W2i);
     free(dW1i);
     free(dW2i);
+}
+
+/* ------------------------------------------------------------------------ */
+/* The two primitives of the 70B page ("The Mechanics of Tensor Parallelism
+ * (TP) in Megatron-LM"): ColumnParallelLinear and RowParallelLinear. Both
+ * compute the plain linear layer Y = X W + b, X [T, n_in], W [n_in, n_out],
+ * b [n_out] (NULL: zero); they differ in which dimension of W the shards
+ * split and so in where the shard sum falls. */
+void oracle_linear_forward(int64_t T, int64_t n_in, int64_t n_out,
+                           const double *X, const double *W, const double *b, double *Y)
+{
+    int64_t t;
+#pragma omp parallel for schedule(static)
+    for (t = 0; t < T; t++) {
+        for (int64_t j = 0; j < n_out; j++)
+            Y[t * n_out + j] = b ? b[j] : 0.0;
+        for (int64_t k = 0; k < n_in; k++) {
+            double x = X[t * n_in + k];
+            for (int64_t j = 0; j < n_out; j++)
+                Y[t * n_out + j] += x * W[k * n_out + j];
+        }
+    }
+}
+
+/* Backward of Y = X W + b for upstream dY: dX = dY W^T, dW = X^T dY,
+ * db = sum_t dY. Any output may be NULL. */
+void oracle_linear_backward(int64_t T, int64_t n_in, int64_t n_out,
+                            const double *X, const double *W, const double *dY,
+                            double *dX, double *dW, double *db)
+{
+    int64_t t, k, j;
+    if (dX) {
+#pragma omp parallel for schedule(static)
+        for (t = 0; t < T; t++) {
+            for (int64_t kk = 0; kk < n_in; kk++) {
+                double acc = 0.0;
+                for (int64_t jj = 0; jj < n_out; jj++)
+                    acc += dY[t * n_out + jj] * W[kk * n_out + jj];
+                dX[t * n_in + kk] = acc;
+            }
+        }
+    }
+    if (dW) {
+#pragma omp parallel for schedule(static)
+        for (k = 0; k < n_in; k++) {
+            for (int64_t jj = 0; jj < n_out; jj++)
+                dW[k * n_out + jj] = 0.0;
+            for (int64_t tt = 0; tt < T; tt++) {
+                double x = X[tt * n_in + k];
+                for (int64_t jj = 0; jj < n_out; jj++)
+                    dW[k * n_out + jj] += x * dY[tt * n_out + jj];
+            }
+        }
+    }
+    if (db) {
+        for (j = 0; j < n_out; j++) {
+            double acc = 0.0;
+            for (t = 0; t < T; t++)
+                acc += dY[t * n_out + j];
+            db[j] = acc;
+        }
+    }
+}
+
+/* The same layer computed shard by shard. mode 0 (column-parallel, [MF]
+ * "Column-Parallel Linear Layer"): W = [W_1 .. W_t] by columns, each shard
+ * forms its own columns Y_i = X W_i + b_i with no exchange; in the backward
+ * each shard's partial dX_i = dY_i W_i^T is summed (f*). mode 1
+ * (row-parallel, "Row-Parallel Linear Layer"): W = [W_1; ..; W_t] by rows and
+ * X by the matching columns, Z_i = X_i W_i, Y = sum_i Z_i (g), then b once;
+ * in the backward every shard sees dY (g*) and forms its own columns of dX,
+ * dX_i = dY W_i^T. dW_i = X_i^T dY_i in both. Requires the split dimension to
+ * divide by t. */
+void oracle_linear_sharded(int64_t T, int64_t n_in, int64_t n_out, int t, int mode,
+                           const double *X, const double *W, const double *b, const double *dY,
+                           double *Y, double *dX, double *dW)
+{
+    int64_t in_s = mode == 0 ? n_in : n_in / t;
+    int64_t out_s = mode == 0 ? n_out / t : n_out;
+    double *Xi = (double *)malloc(sizeof(double) * (size_t)(T * in_s));
+    double *Wi = (double *)malloc(sizeof(double) * (size_t)(in_s * out_s));
+    double *bi = (double *)malloc(sizeof(double) * (size_t)out_s);
+    double *dYi = (double *)malloc(sizeof(double) * (size_t)(T * out_s));
+    double *Yi = (double *)malloc(sizeof(double) * (size_t)(T * out_s));
+    double *dXi = (double *)malloc(sizeof(double) * (size_t)(T * in_s));
+    double *dWi = (double *)malloc(sizeof(double) * (size_t)(in_s * out_s));
+    for (int64_t e = 0; e < T * n_out; e++)
+        Y[e] = 0.0;
+    for (int64_t e = 0; e < T * n_in; e++)
+        dX[e] = 0.0;
+    for (int i = 0; i < t; i++) {
+        int64_t r0 = mode == 0 ? 0 : (int64_t)i * in_s;   /* first row of W_i, first column of X_i */
+        int64_t c0 = mode == 0 ? (int64_t)i * out_s : 0;  /* first column of W_i */
+        for (int64_t tt = 0; tt < T; tt++)
+            for (int64_t k = 0; k < in_s; k++)
+                Xi[tt * in_s + k] = X[tt * n_in + r0 + k];
+        for (int64_t k = 0; k < in_s; k++)
+            for (int64_t j = 0; j < out_s; j++)
+                Wi[k * out_s + j] = W[(r0 + k) * n_out + c0 + j];
+        for (int64_t j = 0; j < out_s; j++)
+            bi[j] = (mode == 0 && b) ? b[c0 + j] : 0.0;  /* the row-parallel bias enters after the sum */
+        for (int64_t tt = 0; tt < T; tt++)
+            for (int64_t j = 0; j < out_s; j++)
+                dYi[tt * out_s + j] = dY[tt * n_out + c0 + j];
+        oracle_linear_forward(T, in_s, out_s, Xi, Wi, bi, Yi);
+        oracle_linear_backward(T, in_s, out_s, Xi, Wi, dYi, dXi, dWi, NULL);
+        for (int64_t tt = 0; tt < T; tt++) {
+            for (int64_t j = 0; j < out_s; j++)
+                Y[tt * n_out + c0 + j] += Yi[tt * out_s + j];     /* column: placement; row: g */
+            for (int64_t k = 0; k < in_s; k++)
+                dX[tt * n_in + r0 + k] += dXi[tt * in_s + k];     /* column: f*; row: placement */
+        }
+        for (int64_t k = 0; k < in_s; k++)
+            for (int64_t j = 0; j < out_s; j++)
+                dW[(r0 + k) * n_out + c0 + j] = dWi[k * out_s + j];
+    }
+    if (mode == 1 && b)
+        for (int64_t tt = 0; tt < T; tt++)
+            for (int64_t j = 0; j < n_out; j++)
+                Y[tt * n_out + j] += b[j];
+    free(Xi);
+    free(Wi);
+    free(bi);
+    free(dYi);
+    free(Yi);
+    free(dXi);
+    free(dWi);
+}
+
+/* Column of the fused QKV projection [70B] "The Multi-Head Attention Block"
+ * holding element j (0 <= j < d) of head `head` of kind 0 (query), 1 (key) or
+ * 2 (value), for n_q query heads sharing n_kv key/value heads of width d.
+ * Columns are grouped by key/value head g: the n_q / n_kv query heads of
+ * group g, then K_g, then V_g, each group (n_q / n_kv + 2) d wide. */
+int64_t oracle_qkv_column(int kind, int64_t head, int64_t j, int64_t n_q, int64_t n_kv, int64_t d)
+{
+    int64_t qpg = n_q / n_kv;              /* query heads per group */
+    int64_t gw = (qpg + 2) * d;            /* group width */
+    if (kind == 0)
+        return (head / qpg) * gw + (head % qpg) * d + j;
+    return head * gw + (qpg + kind - 1) * d + j;
 }
