@@ -16,7 +16,7 @@ CPU oracle timed on a bounded sample on this host.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W]
                        [--impl ours|reference]
-                       [--workload gpt8b|mlp70b|ce128k|swiglu70b|sweep]
+                       [--workload gpt8b|mlp70b|ce128k|swiglu70b|attn70b|sweep]
 Multi-GPU (one process per GPU under torchrun): every rank runs its own
 independent batch (data parallel, weak scaling); there is no collective on
 the data path, only a barrier and a max over ranks of the elapsed time.
@@ -47,8 +47,8 @@ UNIT = "TFLOP/s"
 # fallbacks only if the generated MEASURED_PEAKS.json is absent
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # tokens the CPU oracle processes per timed sample
-CPU_SAMPLE_TOKENS = {"gpt8b": 512, "mlp70b": 192, "ce128k": 96, "swiglu70b": 144, "sweep": 512}
-REF_STEP_TOKENS = {"gpt8b": 8, "mlp70b": 4, "ce128k": 2, "swiglu70b": 3, "sweep": 8}
+CPU_SAMPLE_TOKENS = {"gpt8b": 512, "mlp70b": 192, "ce128k": 96, "swiglu70b": 144, "attn70b": 512, "sweep": 512}
+REF_STEP_TOKENS = {"gpt8b": 8, "mlp70b": 4, "ce128k": 2, "swiglu70b": 3, "attn70b": 8, "sweep": 8}
 
 
 # ---------------------------------------------------------------------- setup
@@ -58,7 +58,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["gpt8b", "mlp70b", "ce128k", "swiglu70b", "sweep"], default="gpt8b")
+    p.add_argument("--workload", choices=["gpt8b", "mlp70b", "ce128k", "swiglu70b", "attn70b", "sweep"],
+                   default="gpt8b")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
@@ -86,6 +87,10 @@ def flops(w):
     # wide (6 T h f forward, 12 T h f backward)
     mlp = (18.0 if w.act == "swiglu" else 12.0) * w.T * w.h * w.f if w.f else 0.0
     ce = 8.0 * w.T * w.h * w.v_pad if w.v_pad else 0.0
+    # attention projections: QKV and W_O, each forward + dX + dW
+    if w.n_heads:
+        nqkv = (w.n_heads + 2 * w.n_kv_heads) * w.head_dim
+        mlp += 6.0 * w.T * w.h * nqkv + 6.0 * w.T * (w.n_heads * w.head_dim) * w.h
     return mlp, ce
 
 
@@ -95,6 +100,8 @@ def workload_config(w, name):
         "mlp70b": "70B-shaped MLP fwd+bwd",
         "ce128k": "vocab-parallel fused logit GEMM + CE fwd+bwd, 128,256-token vocabulary",
         "swiglu70b": "70B-shaped SwiGLU MLP fwd+bwd (gate/up column-parallel, down row-parallel)",
+        "attn70b": "70B-shaped attention projections fwd+bwd (QKV column-parallel by GQA heads, W_O row-parallel; "
+                   "attention core excluded)",
         "sweep": "shard-count sweep of the 8.3B MLP fwd+bwd",
     }[name]
     cfg = {"workload": f"{desc}: T={w.T} (b={w.b}, s={w.s}), h={w.h}", "T": w.T, "h": w.h, "t": w.t,
@@ -103,6 +110,8 @@ def workload_config(w, name):
         cfg["f"] = w.f
     if w.v_pad:
         cfg.update(v_valid=w.v_valid, v_pad=w.v_pad)
+    if w.n_heads:
+        cfg.update(n_heads=w.n_heads, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim)
     return cfg
 
 
@@ -202,6 +211,7 @@ class Step:
         else:
             self.mi = (wl.swiglu_inputs if self.glu else wl.mlp_inputs)(w, seed=seed, device=dev)
         self.ci = wl.ce_inputs(w, seed=seed, device=dev) if w.v_pad else None
+        self.ai = wl.attn_inputs(w, seed=seed, device=dev) if w.n_heads else None
         T, h, f = w.T, w.h, w.f
         bf = torch.bfloat16
         self.out = {}
@@ -221,6 +231,16 @@ class Step:
                        "db1": torch.empty(2 * f, dtype=torch.float32, device=dev),
                        "db2": torch.empty(h, dtype=torch.float32, device=dev)}
             self.mws = torch.empty(max(1, tp.swiglu_workspace_bytes(T, h, f, w.t)), dtype=torch.uint8, device=dev)
+        if w.n_heads:
+            nqkv = (w.n_heads + 2 * w.n_kv_heads) * w.head_dim
+            hq = w.n_heads * w.head_dim
+            self.ao = {"QKV": torch.empty((T, nqkv), dtype=bf, device=dev), "Z": torch.empty((T, h), dtype=bf, device=dev)}
+            self.aq = {"dX": torch.empty((T, h), dtype=bf, device=dev), "dWqkv": torch.empty((h, nqkv), dtype=bf, device=dev),
+                       "dbqkv": torch.empty(nqkv, dtype=torch.float32, device=dev)}
+            self.ag = {"dO": torch.empty((T, hq), dtype=bf, device=dev), "dWo": torch.empty((hq, h), dtype=bf, device=dev),
+                       "dbo": torch.empty(h, dtype=torch.float32, device=dev)}
+            self.aws = torch.empty(max(1, tp.attn_workspace_bytes(T, h, w.n_heads, w.n_kv_heads, w.head_dim, w.t)),
+                                   dtype=torch.uint8, device=dev)
         if w.v_pad:
             self.co = {"loss": torch.empty(T, dtype=torch.float32, device=dev),
                        "lse": torch.empty(T, dtype=torch.float32, device=dev),
@@ -239,28 +259,39 @@ class Step:
         fo = tp.tp_mlp_forward(mi["X"], mi["A"], mi["B"], w.t, mi["bA"], mi["bB"], out=self.fo)
         tp.tp_mlp_backward(mi["dZ"], mi["X"], mi["A"], mi["B"], fo["U"], fo["Y"], w.t, out=self.bo, ws=self.mws)
 
+    def attn(self, ai=None):
+        ai = ai or self.ai
+        tp, w = self.tp, self.w
+        nq, nkv, d = w.n_heads, w.n_kv_heads, w.head_dim
+        tp.tp_attn_qkv_forward(ai["X"], ai["Wqkv"], nq, nkv, d, w.t, ai["bqkv"], out=self.ao["QKV"])
+        tp.tp_attn_qkv_backward(ai["dQKV"], ai["X"], ai["Wqkv"], nq, nkv, d, w.t, out=self.aq, ws=self.aws)
+        tp.tp_attn_out_forward(ai["O"], ai["Wo"], nq, d, w.t, ai["bo"], out=self.ao["Z"])
+        tp.tp_attn_out_backward(ai["dZ"], ai["O"], ai["Wo"], nq, d, w.t, out=self.ag, ws=self.aws)
+
     def ce(self, ci=None):
         ci = ci or self.ci
         return self.tp.vocab_parallel_ce(ci["H"], ci["E"], ci["targets"], self.w.v_valid, self.w.t, grad_scale=1.0,
                                          out=self.co, ws=self.cws)
 
-    def run(self, mi=None, ci=None):
+    def run(self, mi=None, ci=None, ai=None):
         if self.w.f:
             self.mlp(mi)
+        if self.w.n_heads:
+            self.attn(ai)
         if self.w.v_pad:
             self.ce(ci)
 
 
 def input_bytes(step):
     b = 0
-    for d in (step.mi, step.ci):
+    for d in (step.mi, step.ci, step.ai):
         if d:
             b += sum(v.numel() * v.element_size() for v in d.values())
     return b
 
 
 # ---------------------------------------------------------------------- CPU oracle
-def oracle_sample(w, mi, ci, n_tokens):
+def oracle_sample(w, mi, ci, n_tokens, ai=None):
     """Host copies of the first n_tokens tokens plus the full weights, as float64."""
     import numpy as np
 
@@ -277,6 +308,8 @@ def oracle_sample(w, mi, ci, n_tokens):
     if ci is not None:
         s.update(H=f64(ci["H"][:n_tokens]), E=f64(ci["E"]),
                  y=ci["targets"][:n_tokens].cpu().numpy().astype(np.int32))
+    if ai is not None:
+        s["attn"] = {k: f64(v[:n_tokens]) if k in ("X", "O", "dQKV", "dZ") else f64(v) for k, v in ai.items()}
     return s
 
 
@@ -289,6 +322,12 @@ def oracle_step(w, s):
     elif "X" in s:
         oracle.mlp_forward(s["X"], s["A"], s["bA"], s["B"], s["bB"])
         oracle.mlp_backward(s["X"], s["A"], s["bA"], s["B"], s["dZ"])
+    if "attn" in s:
+        a = s["attn"]
+        oracle.linear_forward(a["X"], a["Wqkv"], a["bqkv"])
+        oracle.linear_backward(a["X"], a["Wqkv"], a["dQKV"])
+        oracle.linear_forward(a["O"], a["Wo"], a["bo"])
+        oracle.linear_backward(a["O"], a["Wo"], a["dZ"])
     if "H" in s:
         oracle.ce(s["H"], s["E"], s["y"], w.v_valid, grad_scale=1.0)
 
@@ -315,7 +354,8 @@ def run_reference(args, w, name):
     n = REF_STEP_TOKENS[name]
     mi = ((wl.swiglu_inputs if w.act == "swiglu" else wl.mlp_inputs)(w, seed=0)) if w.f else None
     ci = wl.ce_inputs(w, seed=0) if w.v_pad else None
-    s = oracle_sample(w, mi, ci, n)
+    ai = wl.attn_inputs(w, seed=0) if w.n_heads else None
+    s = oracle_sample(w, mi, ci, n, ai)
     for _ in range(args.warmup):
         oracle_step(w, s)
     times = []
@@ -376,6 +416,8 @@ def run_ours(args, w, name):
         ev[i][0].record(stream)
         if w.f:
             step.mlp()
+        if w.n_heads:
+            step.attn()
         ev[i][1].record(stream)
         if w.v_pad:
             step.ce()
@@ -427,10 +469,10 @@ def run_ours(args, w, name):
     e2e = None
     if not args.no_e2e:
         host = {}
-        for src in (step.mi, step.ci):
+        for tag, src in (("m", step.mi), ("c", step.ci), ("a", step.ai)):
             if src:
                 for k, v in src.items():
-                    host[k] = v.cpu().pin_memory()
+                    host[tag + k] = v.cpu().pin_memory()
         dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
         loss_host = torch.empty(w.T, dtype=torch.float32).pin_memory() if w.v_pad else None
         z_host = torch.empty((w.T, w.h), dtype=torch.bfloat16).pin_memory() if not w.v_pad else None
@@ -438,13 +480,14 @@ def run_ours(args, w, name):
         def e2e_step():
             for k, v in host.items():
                 dev_in[k].copy_(v, non_blocking=True)
-            mi = {k: dev_in[k] for k in step.mi} if w.f else None
-            ci = {k: dev_in[k] for k in ("H", "E", "targets")} if w.v_pad else None
-            step.run(mi, ci)
+            mi = {k: dev_in["m" + k] for k in step.mi} if w.f else None
+            ci = {k: dev_in["c" + k] for k in step.ci} if w.v_pad else None
+            ai = {k: dev_in["a" + k] for k in step.ai} if w.n_heads else None
+            step.run(mi, ci, ai)
             if w.v_pad:
                 loss_host.copy_(step.co["loss"], non_blocking=True)
             else:
-                z_host.copy_(step.fo["Z"], non_blocking=True)
+                z_host.copy_(step.fo["Z"] if w.f else step.ao["Z"], non_blocking=True)
 
         for _ in range(2):
             e2e_step()
@@ -478,7 +521,7 @@ def run_ours(args, w, name):
 
         oracle.build()
         n = CPU_SAMPLE_TOKENS[name]
-        s = oracle_sample(w, step.mi, step.ci, n)
+        s = oracle_sample(w, step.mi, step.ci, n, step.ai)
         rate, sec = oracle_rate(w, s, n)
         cpu = {"value": rate, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
                "sample": f"first {n} of {w.T} tokens through the full step (MLP fwd+bwd, CE fwd+bwd with dH and dE) "
@@ -493,6 +536,10 @@ def run_ours(args, w, name):
             "config": {**workload_config(w, name), "parallelism": f"t={w.t} shards on each GPU; dp{ws} (independent batches)",
                        "l2": f"no flush: inputs alone are {ws_bytes / 1e9:.2f} GB per step, > 129 MB L2"},
             "parts": {"mlp_tflops": (mlp_fl / (mlp_ms * 1e-3) / 1e12) if w.f else None, "mlp_ms": mlp_ms if w.f else None,
+                      "attn_proj_tflops": (mlp_fl / (mlp_ms * 1e-3) / 1e12) if w.n_heads else None,
+                      "attn_proj_ms": mlp_ms if w.n_heads else None,
+                      "attn_proj_frac_of_peak": ((mlp_fl / (mlp_ms * 1e-3) / 1e12) / pk["bf16_tflops_sustained"])
+                      if w.n_heads else None,
                       "ce_tokens_per_s": (w.T / (ce_ms * 1e-3)) if w.v_pad else None,
                       "ce_tflops": (ce_fl / (ce_ms * 1e-3) / 1e12) if w.v_pad else None, "ce_ms": ce_ms if w.v_pad else None,
                       "mlp_frac_of_peak": ((mlp_fl / (mlp_ms * 1e-3) / 1e12) / pk["bf16_tflops_sustained"]) if w.f else None,
@@ -519,6 +566,13 @@ def kernel_flops_per_step(name, w):
         "ce_fwd_logits_stats": 2.0 * T * h * vp, "ce_bwd_logits_dl": 2.0 * T * h * vp,
         "ce_bwd_dE": 2.0 * T * h * vp, "ce_bwd_dH_shard_sum": 2.0 * T * h * vp,
     }
+    if w.n_heads:
+        nqkv = (w.n_heads + 2 * w.n_kv_heads) * w.head_dim
+        hq = w.n_heads * w.head_dim
+        for k in ("attn_qkv_fwd", "attn_qkv_bwd_dX_shard_sum", "attn_qkv_bwd_dW"):
+            table[k] = 2.0 * T * h * nqkv
+        for k in ("attn_out_fwd_shard_sum", "attn_out_bwd_dO", "attn_out_bwd_dW"):
+            table[k] = 2.0 * T * hq * h
     return table.get(name)
 
 

@@ -63,6 +63,15 @@ typedef enum {
     TPCE_F32 = 1     /* fp32 tensors, multiplied as tf32 on the tensor cores, fp32 accumulate */
 } tpce_dtype;
 
+/* Which dimension of a linear layer's weight W [n_in, n_out] the t shards
+ * split ("Distributed tensor parallelism: scale fine-tuning of 70B-parameter
+ * LLMs with Megatron-LM", section "The Mechanics of Tensor Parallelism (TP)
+ * in Megatron-LM": ColumnParallelLinear and RowParallelLinear). */
+typedef enum {
+    TPCE_COLUMN_PARALLEL = 0,  /* W split by columns: n_out / t per shard */
+    TPCE_ROW_PARALLEL = 1      /* W split by rows (X by columns): n_in / t per shard */
+} tpce_parallel;
+
 typedef enum {
     TPCE_OK = 0,
     TPCE_ERR_INVALID = 1,      /* null pointer, bad dtype, target id out of range */
@@ -217,6 +226,77 @@ tpce_status tp_swiglu_backward(const void *dZ, const void *X, const void *W1, co
                                int64_t T, int64_t h, int64_t f, int t, int dtype,
                                void *dX, void *dW1, float *db1, void *dW2, float *db2,
                                void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Linear layers: ColumnParallelLinear and RowParallelLinear ("Mathematical
+ * Foundations of Megatron-LM 1D Slicing", sections "Column-Parallel Linear
+ * Layer" and "Row-Parallel Linear Layer"). Both compute
+ *   Y = X W + b,  X [T, n_in], W [n_in, n_out], b [n_out] fp32 or NULL,
+ * and differ in where a shard sum falls (done in a GEMM accumulator here):
+ *   TPCE_COLUMN_PARALLEL  forward: each shard's columns, no exchange;
+ *                         backward: dX = sum_i dY_i W_i^T (f*).
+ *   TPCE_ROW_PARALLEL     forward: Y = sum_i X_i W_i (g), b added once;
+ *                         backward: each shard's columns of dX, no sum.
+ * Backward: dX = dY W^T, dW = X^T dY, db = sum_tokens dY (db may be NULL).
+ * Shapes: n_in, n_out >= 8 and multiples of 8; the split dimension (n_out for
+ * column, n_in for row) divides by t into whole 64-wide blocks. T == 0: the
+ * forward is a no-op, the backward zeroes dW and db.
+ * Workspace: tpce_linear_workspace_bytes (bf16 forward: none; the backward
+ * holds the bias-gradient partials; TPCE_F32 adds transposed copies of W, X
+ * and dY). Returns 0 for invalid shapes.
+ * ------------------------------------------------------------------------- */
+size_t tpce_linear_workspace_bytes(int64_t T, int64_t n_in, int64_t n_out, int t, int parallel,
+                                   int dtype);
+tpce_status tp_linear_forward(const void *X, const void *W, const float *b,
+                              int64_t T, int64_t n_in, int64_t n_out, int t, int parallel,
+                              int dtype, void *Y, void *ws, size_t ws_bytes, void *stream);
+tpce_status tp_linear_backward(const void *dY, const void *X, const void *W,
+                               int64_t T, int64_t n_in, int64_t n_out, int t, int parallel,
+                               int dtype, void *dX, void *dW, float *db,
+                               void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Attention projections ("Distributed tensor parallelism ...", section "The
+ * Multi-Head Attention Block"; "Mathematical Foundations ...", section
+ * "Self-Attention Layer Decomposition"). The attention core between them is
+ * not part of this library.
+ *
+ * tp_attn_qkv_*: the fused Q, K, V projection, column-parallel by heads:
+ *   QKV = X Wqkv + bqkv,  X [T, h], Wqkv [h, (n_heads + 2 n_kv_heads) d],
+ * columns grouped by key/value head g: the n_heads / n_kv_heads query heads
+ * that share K_g and V_g, then K_g, then V_g (each head d wide), so that
+ * shard i's contiguous column block holds whole groups: n_heads / t query
+ * and n_kv_heads / t key/value heads (grouped-query attention; with 64 query
+ * and 8 key/value heads at t = 8, 8 and 1 per shard). The backward's dX is
+ * the f* sum over shards.
+ * Shapes: n_heads % n_kv_heads == 0, n_kv_heads % t == 0, d >= 8, d % 8 == 0,
+ * and a shard's (n_heads + 2 n_kv_heads) d / t columns are whole 64-wide
+ * blocks; the rest as tp_linear_* with n_in = h.
+ *
+ * tp_attn_out_*: the output projection W_O, row-parallel over the
+ * concatenated head outputs O [T, n_heads d]:  Z = sum_i O_i W_O,i + bo,
+ * Wo [n_heads d, h]; n_heads % t == 0 and n_heads d / t whole 64-wide blocks.
+ *
+ * tpce_attn_workspace_bytes covers all four calls of one dtype.
+ * ------------------------------------------------------------------------- */
+size_t tpce_attn_workspace_bytes(int64_t T, int64_t h, int64_t n_heads, int64_t n_kv_heads,
+                                 int64_t head_dim, int t, int dtype);
+tpce_status tp_attn_qkv_forward(const void *X, const void *Wqkv, const float *bqkv,
+                                int64_t T, int64_t h, int64_t n_heads, int64_t n_kv_heads,
+                                int64_t head_dim, int t, int dtype, void *QKV,
+                                void *ws, size_t ws_bytes, void *stream);
+tpce_status tp_attn_qkv_backward(const void *dQKV, const void *X, const void *Wqkv,
+                                 int64_t T, int64_t h, int64_t n_heads, int64_t n_kv_heads,
+                                 int64_t head_dim, int t, int dtype,
+                                 void *dX, void *dWqkv, float *dbqkv,
+                                 void *ws, size_t ws_bytes, void *stream);
+tpce_status tp_attn_out_forward(const void *O, const void *Wo, const float *bo,
+                                int64_t T, int64_t h, int64_t n_heads, int64_t head_dim, int t,
+                                int dtype, void *Z, void *ws, size_t ws_bytes, void *stream);
+tpce_status tp_attn_out_backward(const void *dZ, const void *O, const void *Wo,
+                                 int64_t T, int64_t h, int64_t n_heads, int64_t head_dim, int t,
+                                 int dtype, void *dO, void *dWo, float *dbo,
+                                 void *ws, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
  * vocab_parallel_ce -- logit GEMM fused with softmax cross-entropy, the

@@ -144,6 +144,33 @@ def test_swiglu_validation_and_workspace(L):
     assert L.tpce_swiglu_workspace_bytes(10, 64, 100, 3, 0) == 0
 
 
+def test_linear_and_attention_validation(L):
+    def lin(T=64, n_in=128, n_out=256, t=2, par=0, dtype=0, X=FAKE):
+        return L.tp_linear_forward(X, FAKE, None, T, n_in, n_out, t, par, dtype, FAKE, None, 0, None)
+    # only invalid requests are tried: each is rejected before any launch
+    assert lin(n_out=256, t=3) == 2        # column: n_out % t
+    assert lin(n_out=256, t=8) == 2        # column: a shard of 32 columns is not whole 64-wide blocks
+    assert lin(n_in=128, t=4, par=1) == 2  # row: a shard of 32 rows
+    assert lin(n_in=60) == 2
+    assert lin(par=2) == 1
+    assert lin(X=MISALIGNED) == 3
+    assert lin(X=None) == 1
+    assert lin(dtype=1) == 4               # the fp32 forward needs its workspace
+    assert lin(T=0) == 0
+    st = L.tp_linear_backward(FAKE, FAKE, FAKE, 64, 128, 256, 2, 0, 0, FAKE, FAKE, None, None, 0, None)
+    assert st == 4                         # the backward needs the bias-gradient workspace
+
+    def qkv(nq=8, nkv=2, d=64, t=2):
+        return L.tp_attn_qkv_forward(None, FAKE, None, 64, 256, nq, nkv, d, t, 0, FAKE, None, 0, None)
+    assert qkv(nkv=2, t=4) == 2            # key/value heads must split evenly over the shards
+    assert qkv(nq=8, nkv=3, t=1) == 2      # query heads share key/value heads evenly
+    assert qkv(d=60) == 2
+    assert L.tp_attn_out_forward(FAKE, FAKE, None, 64, 256, 6, 64, 4, 0, FAKE, None, 0, None) == 2
+    assert L.tpce_attn_workspace_bytes(64, 256, 8, 2, 64, 4, 0) == 0
+    assert L.tpce_attn_workspace_bytes(64, 256, 8, 2, 64, 2, 0) > 0
+    assert L.tpce_linear_workspace_bytes(64, 128, 256, 3, 0, 0) == 0
+
+
 def test_ce_validation(L):
     def ce(T=64, h=64, vp=512, vv=500, t=2, ws=None, wsb=0, H=FAKE, tg=FAKE):
         return L.vocab_parallel_ce(H, FAKE, tg, T, h, vp, vv, t, 1.0, 0, FAKE, None, FAKE, FAKE, ws, wsb, None)

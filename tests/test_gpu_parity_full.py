@@ -124,6 +124,33 @@ def test_swiglu70b_full_size():
     check_swiglu_full(wl.WORKLOADS["swiglu70b"], dev)
 
 
+def test_attn70b_full_size():
+    # QKV and W_O projections of the 70B attention block: sampled rows of the
+    # forward outputs and dX / dO, sampled columns of the weight gradients
+    # (column j of dW needs only column j of the upstream gradient)
+    dev = gpu_or_skip()
+    w = wl.WORKLOADS["attn70b"]
+    nq, nkv, d = w.n_heads, w.n_kv_heads, w.head_dim
+    ai = wl.attn_inputs(w, seed=0, device=dev)
+    qkv = tp.tp_attn_qkv_forward(ai["X"], ai["Wqkv"], nq, nkv, d, w.t, ai["bqkv"])
+    gq = tp.tp_attn_qkv_backward(ai["dQKV"], ai["X"], ai["Wqkv"], nq, nkv, d, w.t)
+    z = tp.tp_attn_out_forward(ai["O"], ai["Wo"], nq, d, w.t, ai["bo"])
+    go = tp.tp_attn_out_backward(ai["dZ"], ai["O"], ai["Wo"], nq, d, w.t)
+    assert tp.device_status() == 0
+    h = {k: _host(v) for k, v in ai.items()}
+    rows = wl.sample_indices(w.T, N_ROWS, seed=0)
+    for name, x, W, b, dY, y, g in (("qkv", "X", "Wqkv", "bqkv", "dQKV", qkv, gq), ("out", "O", "Wo", "bo", "dZ", z, go)):
+        assert_rel(f"{name} Y", _host(y)[rows], oracle.linear_forward(h[x][rows], h[W], h[b]))
+        dx_key = "dX" if name == "qkv" else "dO"
+        ob = oracle.linear_backward(h[x][rows], h[W], h[dY][rows], want=("dX",))
+        assert_rel(f"{name} {dx_key}", _host(g[dx_key])[rows], ob["dX"])
+        cols = wl.sample_indices(h[W].shape[1], N_COLS, seed=1)
+        oc = oracle.linear_backward(h[x], h[W][:, cols], h[dY][:, cols], want=("dW", "db"))
+        dw_key, db_key = ("dWqkv", "dbqkv") if name == "qkv" else ("dWo", "dbo")
+        assert_rel(f"{name} {dw_key}[:, cols]", _host(g[dw_key])[:, cols], oc["dW"])
+        assert_rel(f"{name} {db_key}[cols]", _host(g[db_key])[cols], oc["db"])
+
+
 def test_shard_sweep_full_size_bit_identical():
     dev = gpu_or_skip()
     outs = {}

@@ -20,6 +20,8 @@ STATUS = {
 }
 TPCE_BF16 = 0
 TPCE_F32 = 1
+TPCE_COLUMN_PARALLEL = 0
+TPCE_ROW_PARALLEL = 1
 
 # every symbol include/tpce.h declares, with (restype, argtypes)
 _P = ctypes.c_void_p
@@ -41,6 +43,14 @@ SIGNATURES = {
     "tp_swiglu_forward": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "tp_swiglu_backward": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I,
                                 _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "tpce_linear_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I, _I, _I]),
+    "tp_linear_forward": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _P, _SZ, _P]),
+    "tp_linear_backward": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "tpce_attn_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64, _I64, _I, _I]),
+    "tp_attn_qkv_forward": (_I, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I, _I, _P, _P, _SZ, _P]),
+    "tp_attn_qkv_backward": (_I, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "tp_attn_out_forward": (_I, [_P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _P, _P, _SZ, _P]),
+    "tp_attn_out_backward": (_I, [_P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "vocab_parallel_ce": (_I, [_P, _P, _P, _I64, _I64, _I64, _I64, _I, _F, _I,
                                _P, _P, _P, _P, _P, _SZ, _P]),
     "vocab_parallel_ce_loss_static": (_I, [_P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _P, _P, _P]),

@@ -12,7 +12,7 @@ from typing import Dict, Optional
 
 import torch
 
-from ._lib import TPCE_BF16, TPCE_F32, TpceError, check, lib
+from ._lib import TPCE_BF16, TPCE_COLUMN_PARALLEL, TPCE_F32, TPCE_ROW_PARALLEL, TpceError, check, lib
 
 _DT = {torch.bfloat16: TPCE_BF16, torch.float32: TPCE_F32}
 
@@ -182,6 +182,164 @@ def tp_swiglu_backward(dZ: torch.Tensor, X: torch.Tensor, W1: torch.Tensor, W2: 
     res = {"dX": dX, "dW1": dW1, "dW2": dW2}
     if bias_grads:
         res.update(db1=db1, db2=db2)
+    return res
+
+
+_PAR = {"column": TPCE_COLUMN_PARALLEL, "row": TPCE_ROW_PARALLEL}
+
+
+def _wsize(w: Optional[torch.Tensor]) -> int:
+    return 0 if w is None else w.numel() * w.element_size()
+
+
+def linear_workspace_bytes(T: int, n_in: int, n_out: int, t: int, parallel: str = "column",
+                           dtype=torch.bfloat16) -> int:
+    return int(lib().tpce_linear_workspace_bytes(T, n_in, n_out, t, _PAR[parallel], _DT[dtype]))
+
+
+def tp_linear_forward(X: torch.Tensor, W: torch.Tensor, t: int, parallel: str = "column",
+                      b: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                      ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Y = X W + b over t shards of W's columns ("column") or rows ("row")."""
+    T, n_in = X.shape
+    n_out = W.shape[1]
+    dt = X.dtype
+    _need(X, "X", dt, (T, n_in))
+    _need(W, "W", dt, (n_in, n_out))
+    if b is not None:
+        _need(b, "b", torch.float32, (n_out,))
+    Y = out if out is not None else torch.empty((T, n_out), dtype=dt, device=X.device)
+    w = None
+    if dt == torch.float32 and T > 0:
+        w = _workspace(linear_workspace_bytes(T, n_in, n_out, t, parallel, dt), X.device, ws)
+    st = lib().tp_linear_forward(_ptr(X), _ptr(W), _ptr(b), T, n_in, n_out, t, _PAR[parallel], _DT[dt], _ptr(Y),
+                                 _ptr(w), _wsize(w), _stream(stream))
+    check(st, "tp_linear_forward")
+    return Y
+
+
+def tp_linear_backward(dY: torch.Tensor, X: torch.Tensor, W: torch.Tensor, t: int, parallel: str = "column",
+                       bias_grad: bool = True, out: Optional[Dict[str, torch.Tensor]] = None,
+                       ws: Optional[torch.Tensor] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """dX = dY W^T, dW = X^T dY and optionally db = sum over tokens of dY."""
+    T, n_in = X.shape
+    n_out = W.shape[1]
+    dt = X.dtype
+    for name, x, shp in (("dY", dY, (T, n_out)), ("X", X, (T, n_in)), ("W", W, (n_in, n_out))):
+        _need(x, name, dt, shp)
+    out = dict(out or {})
+    dev = X.device
+    dX = out.get("dX") if out.get("dX") is not None else torch.empty((T, n_in), dtype=dt, device=dev)
+    dW = out.get("dW") if out.get("dW") is not None else torch.empty((n_in, n_out), dtype=dt, device=dev)
+    db = None
+    if bias_grad:
+        db = out.get("db") if out.get("db") is not None else torch.empty(n_out, dtype=torch.float32, device=dev)
+    w = _workspace(linear_workspace_bytes(T, n_in, n_out, t, parallel, dt) if T > 0 else 0, dev, ws)
+    st = lib().tp_linear_backward(_ptr(dY), _ptr(X), _ptr(W), T, n_in, n_out, t, _PAR[parallel], _DT[dt],
+                                  _ptr(dX), _ptr(dW), _ptr(db), _ptr(w), _wsize(w), _stream(stream))
+    check(st, "tp_linear_backward")
+    res = {"dX": dX, "dW": dW}
+    if bias_grad:
+        res["db"] = db
+    return res
+
+
+def attn_workspace_bytes(T: int, h: int, n_heads: int, n_kv_heads: int, head_dim: int, t: int,
+                         dtype=torch.bfloat16) -> int:
+    return int(lib().tpce_attn_workspace_bytes(T, h, n_heads, n_kv_heads, head_dim, t, _DT[dtype]))
+
+
+def tp_attn_qkv_forward(X: torch.Tensor, Wqkv: torch.Tensor, n_heads: int, n_kv_heads: int, head_dim: int, t: int,
+                        bqkv: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                        ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """QKV = X Wqkv + bqkv, column-parallel by (grouped-query) heads."""
+    T, h = X.shape
+    n = (n_heads + 2 * n_kv_heads) * head_dim
+    dt = X.dtype
+    _need(X, "X", dt, (T, h))
+    _need(Wqkv, "Wqkv", dt, (h, n))
+    if bqkv is not None:
+        _need(bqkv, "bqkv", torch.float32, (n,))
+    QKV = out if out is not None else torch.empty((T, n), dtype=dt, device=X.device)
+    w = None
+    if dt == torch.float32 and T > 0:
+        w = _workspace(attn_workspace_bytes(T, h, n_heads, n_kv_heads, head_dim, t, dt), X.device, ws)
+    st = lib().tp_attn_qkv_forward(_ptr(X), _ptr(Wqkv), _ptr(bqkv), T, h, n_heads, n_kv_heads, head_dim, t, _DT[dt],
+                                   _ptr(QKV), _ptr(w), _wsize(w), _stream(stream))
+    check(st, "tp_attn_qkv_forward")
+    return QKV
+
+
+def tp_attn_qkv_backward(dQKV: torch.Tensor, X: torch.Tensor, Wqkv: torch.Tensor, n_heads: int, n_kv_heads: int,
+                         head_dim: int, t: int, bias_grad: bool = True, out: Optional[Dict[str, torch.Tensor]] = None,
+                         ws: Optional[torch.Tensor] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """dX (f* sum over shards), dWqkv and optionally dbqkv."""
+    T, h = X.shape
+    n = (n_heads + 2 * n_kv_heads) * head_dim
+    dt = X.dtype
+    for name, x, shp in (("dQKV", dQKV, (T, n)), ("X", X, (T, h)), ("Wqkv", Wqkv, (h, n))):
+        _need(x, name, dt, shp)
+    out = dict(out or {})
+    dev = X.device
+    dX = out.get("dX") if out.get("dX") is not None else torch.empty((T, h), dtype=dt, device=dev)
+    dW = out.get("dWqkv") if out.get("dWqkv") is not None else torch.empty((h, n), dtype=dt, device=dev)
+    db = None
+    if bias_grad:
+        db = out.get("dbqkv") if out.get("dbqkv") is not None else torch.empty(n, dtype=torch.float32, device=dev)
+    w = _workspace(attn_workspace_bytes(T, h, n_heads, n_kv_heads, head_dim, t, dt) if T > 0 else 0, dev, ws)
+    st = lib().tp_attn_qkv_backward(_ptr(dQKV), _ptr(X), _ptr(Wqkv), T, h, n_heads, n_kv_heads, head_dim, t,
+                                    _DT[dt], _ptr(dX), _ptr(dW), _ptr(db), _ptr(w), _wsize(w), _stream(stream))
+    check(st, "tp_attn_qkv_backward")
+    res = {"dX": dX, "dWqkv": dW}
+    if bias_grad:
+        res["dbqkv"] = db
+    return res
+
+
+def tp_attn_out_forward(O: torch.Tensor, Wo: torch.Tensor, n_heads: int, head_dim: int, t: int,
+                        bo: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                        ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Z = sum_i O_i Wo_i + bo: the row-parallel output projection."""
+    T, hq = O.shape
+    h = Wo.shape[1]
+    dt = O.dtype
+    _need(O, "O", dt, (T, n_heads * head_dim))
+    _need(Wo, "Wo", dt, (n_heads * head_dim, h))
+    if bo is not None:
+        _need(bo, "bo", torch.float32, (h,))
+    Z = out if out is not None else torch.empty((T, h), dtype=dt, device=O.device)
+    w = None
+    if dt == torch.float32 and T > 0:
+        w = _workspace(linear_workspace_bytes(T, hq, h, t, "row", dt), O.device, ws)
+    st = lib().tp_attn_out_forward(_ptr(O), _ptr(Wo), _ptr(bo), T, h, n_heads, head_dim, t, _DT[dt], _ptr(Z),
+                                   _ptr(w), _wsize(w), _stream(stream))
+    check(st, "tp_attn_out_forward")
+    return Z
+
+
+def tp_attn_out_backward(dZ: torch.Tensor, O: torch.Tensor, Wo: torch.Tensor, n_heads: int, head_dim: int, t: int,
+                         bias_grad: bool = True, out: Optional[Dict[str, torch.Tensor]] = None,
+                         ws: Optional[torch.Tensor] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """dO (each shard's own head columns), dWo and optionally dbo."""
+    T, hq = O.shape
+    h = Wo.shape[1]
+    dt = O.dtype
+    for name, x, shp in (("dZ", dZ, (T, h)), ("O", O, (T, n_heads * head_dim)), ("Wo", Wo, (n_heads * head_dim, h))):
+        _need(x, name, dt, shp)
+    out = dict(out or {})
+    dev = O.device
+    dO = out.get("dO") if out.get("dO") is not None else torch.empty((T, hq), dtype=dt, device=dev)
+    dW = out.get("dWo") if out.get("dWo") is not None else torch.empty((hq, h), dtype=dt, device=dev)
+    db = None
+    if bias_grad:
+        db = out.get("dbo") if out.get("dbo") is not None else torch.empty(h, dtype=torch.float32, device=dev)
+    w = _workspace(linear_workspace_bytes(T, hq, h, t, "row", dt) if T > 0 else 0, dev, ws)
+    st = lib().tp_attn_out_backward(_ptr(dZ), _ptr(O), _ptr(Wo), T, h, n_heads, head_dim, t, _DT[dt], _ptr(dO),
+                                    _ptr(dW), _ptr(db), _ptr(w), _wsize(w), _stream(stream))
+    check(st, "tp_attn_out_backward")
+    res = {"dO": dO, "dWo": dW}
+    if bias_grad:
+        res["dbo"] = db
     return res
 
 

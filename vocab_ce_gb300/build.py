@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(ROOT, "_build", "tpce")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libtpce.so")
 
-SOURCES = ["runtime.cu", "mlp.cu", "ce.cu", "ce_static.cu"]
+SOURCES = ["runtime.cu", "mlp.cu", "linear.cu", "ce.cu", "ce_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

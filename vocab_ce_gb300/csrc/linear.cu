@@ -1,0 +1,293 @@
+// linear.cu -- the two linear primitives of Megatron's 1D tensor parallelism,
+// ColumnParallelLinear and RowParallelLinear, with their t shards laid out on
+// one GPU, and the attention projections built on them.
+//
+// "Distributed tensor parallelism: scale fine-tuning of 70B-parameter LLMs
+// with Megatron-LM", sections "The Mechanics of Tensor Parallelism (TP) in
+// Megatron-LM" and "The Multi-Head Attention Block"; "Mathematical
+// Foundations of Megatron-LM 1D Slicing", sections "Column-Parallel Linear
+// Layer", "Row-Parallel Linear Layer" and "Self-Attention Layer
+// Decomposition".
+//
+// Both primitives compute Y = X W + b. They differ in the dimension of W the
+// shards split, and so in where a shard sum falls:
+//   column-parallel  W = [W_1 .. W_t] by columns. Forward: each shard's
+//                    columns, no exchange. Backward: dX = sum_i dY_i W_i^T
+//                    (f*), taken in the accumulator of the dX GEMM, whose K
+//                    runs over the concatenated shard column ranges.
+//   row-parallel     W = [W_1; ..; W_t] by rows, X by the matching columns.
+//                    Forward: Y = sum_i X_i W_i (g) in the accumulator, then
+//                    b once. Backward: each shard's columns of dX, no sum.
+// On one GPU both are the same three GEMMs; the mode sets the validation and
+// the kernel names.
+//
+// Attention: the fused QKV projection is column-parallel by heads (its
+// columns grouped by key/value head, so that a contiguous split gives each
+// shard whole heads: for each KV head g, the query heads sharing it, then K_g,
+// then V_g); the output projection W_O is row-parallel over the concatenated
+// head outputs. The attention core between them is not part of this library.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+
+#include "gemm_launch.cuh"
+#include "host.h"
+
+namespace tpce {
+namespace {
+
+constexpr int64_t kMaxDim = INT_MAX - 1024;  // kernel coordinates are 32-bit
+
+struct LinearNames {
+    const char *fwd, *dX, *dW;
+};
+
+tpce_status check_linear_shape(int64_t T, int64_t n_in, int64_t n_out, int t, int parallel, int dtype) {
+    if (dtype != TPCE_BF16 && dtype != TPCE_F32) return TPCE_ERR_INVALID;
+    if (parallel != TPCE_COLUMN_PARALLEL && parallel != TPCE_ROW_PARALLEL) return TPCE_ERR_INVALID;
+    if (T < 0 || n_in < 8 || n_out < 8 || t < 1) return TPCE_ERR_SHAPE;
+    if (T > kMaxDim || n_in > kMaxDim || n_out > kMaxDim) return TPCE_ERR_SHAPE;
+    if (n_in % 8 != 0 || n_out % 8 != 0) return TPCE_ERR_SHAPE;  // 16-byte row pitch
+    const int64_t split = parallel == TPCE_COLUMN_PARALLEL ? n_out : n_in;
+    if (split % t != 0) return TPCE_ERR_SHAPE;         // equal shards
+    if ((split / t) % 64 != 0) return TPCE_ERR_SHAPE;  // a shard is whole 64-wide blocks
+    if (dtype == TPCE_F32 && (T + 31) / 32 > 65535) return TPCE_ERR_SHAPE;  // transpose grid
+    return TPCE_OK;
+}
+
+inline int64_t pad4(int64_t x) { return (x + 3) / 4 * 4; }
+
+// Workspace: the column-sum partials (bias gradient); fp32 adds the
+// transposed operands of the tf32 path: W^T (forward), X^T and dY^T
+// (weight gradient), token-major ones with rows padded to a multiple of 4.
+struct LinWs {
+    size_t partial, Wt, Xt, dYt, total;
+};
+
+LinWs lin_ws_layout(int64_t T, int64_t n_in, int64_t n_out, int dtype) {
+    LinWs L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = round_up(off + bytes, 256);
+        return at;
+    };
+    L.partial = take(colsum_partial_floats(T, n_out) * sizeof(float));
+    if (dtype == TPCE_F32) {
+        const size_t Tp = static_cast<size_t>(pad4(T));
+        L.Wt = take(static_cast<size_t>(n_out) * n_in * 4);
+        L.Xt = take(static_cast<size_t>(n_in) * Tp * 4);
+        L.dYt = take(static_cast<size_t>(n_out) * Tp * 4);
+    }
+    L.total = off;
+    return L;
+}
+
+template <typename T>
+T *at(void *ws, size_t off) {
+    return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off);
+}
+
+tpce_status forward_impl(const LinearNames &nm, const void *X, const void *W, const float *b, int64_t T, int64_t n_in,
+                         int64_t n_out, int dtype, void *Y, void *ws, const LinWs &L, cudaStream_t s) {
+    const int Ti = static_cast<int>(T), ii = static_cast<int>(n_in), oi = static_cast<int>(n_out);
+    if (dtype == TPCE_BF16) {
+        using bf = __nv_bfloat16;
+        Operand a{X, T, n_in, n_in};      // K-major [T, n_in]
+        Operand bw{W, n_in, n_out, n_out};  // MN-major: K = n_in rows, N = n_out columns
+        const OutView o[1] = {{Y, T, n_out, n_out}};
+        return launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256>(nm.fwd, a, bw, o, nullptr, Ti, oi, ii,
+                                                                                 0, 0, 0, 0, {b}, s);
+    }
+    float *Wt = at<float>(ws, L.Wt);
+    tpce_status st = transpose_f32(static_cast<const float *>(W), n_in, n_out, n_out, Wt, n_in, s);  // W^T
+    if (st != TPCE_OK) return st;
+    Operand a{X, T, n_in, n_in};       // K-major [T, n_in]
+    Operand bw{Wt, n_out, n_in, n_in};  // K-major: N = n_out rows, K = n_in columns
+    const OutView o[1] = {{Y, T, n_out, n_out}};
+    return launch_gemm<float, 128, false, false, EpiStore<float>>(nm.fwd, a, bw, o, nullptr, Ti, oi, ii, 0, 0, 0, 0,
+                                                                  {b}, s);
+}
+
+tpce_status backward_impl(const LinearNames &nm, const void *dY, const void *X, const void *W, int64_t T, int64_t n_in,
+                          int64_t n_out, int dtype, void *dX, void *dW, float *db, void *ws, const LinWs &L,
+                          cudaStream_t s) {
+    const int Ti = static_cast<int>(T), ii = static_cast<int>(n_in), oi = static_cast<int>(n_out);
+    float *partial = at<float>(ws, L.partial);
+    tpce_status st;
+    if (dtype == TPCE_BF16) {
+        using bf = __nv_bfloat16;
+        // dX = dY W^T (column-parallel: the f* sum over shards in the accumulator)
+        {
+            Operand a{dY, T, n_out, n_out};   // K-major [T, n_out]
+            Operand bw{W, n_in, n_out, n_out};  // K-major: N = n_in rows, K = n_out columns
+            const OutView o[1] = {{dX, T, n_in, n_in}};
+            st = launch_gemm_auto<bf, false, false, EpiStore<bf>, kBN192 | kBN256>(nm.dX, a, bw, o, nullptr, Ti, ii, oi,
+                                                                                    0, 0, 0, 0, {nullptr}, s);
+            if (st != TPCE_OK) return st;
+        }
+        // dW = X^T dY (each shard's own block of W)
+        {
+            Operand a{X, T, n_in, n_in};     // MN-major: K = T rows, M = n_in columns
+            Operand bw{dY, T, n_out, n_out};  // MN-major: K = T rows, N = n_out columns
+            const OutView o[1] = {{dW, n_in, n_out, n_out}};
+            st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>(nm.dW, a, bw, o, nullptr, ii, oi, Ti, 0,
+                                                                                  0, 0, 0, {nullptr}, s);
+            if (st != TPCE_OK) return st;
+        }
+        if (db && (st = colsum(0, dY, T, n_out, n_out, db, partial, s)) != TPCE_OK) return st;
+        return TPCE_OK;
+    }
+    const int64_t Tp = pad4(T);
+    float *Xt = at<float>(ws, L.Xt), *dYt = at<float>(ws, L.dYt);
+    {
+        Operand a{dY, T, n_out, n_out};   // K-major [T, n_out]
+        Operand bw{W, n_in, n_out, n_out};  // K-major: N = n_in rows, K = n_out columns
+        const OutView o[1] = {{dX, T, n_in, n_in}};
+        st = launch_gemm<float, 128, false, false, EpiStore<float>>(nm.dX, a, bw, o, nullptr, Ti, ii, oi, 0, 0, 0, 0,
+                                                                    {nullptr}, s);
+        if (st != TPCE_OK) return st;
+    }
+    if ((st = transpose_f32(static_cast<const float *>(X), T, n_in, n_in, Xt, Tp, s)) != TPCE_OK) return st;
+    if ((st = transpose_f32(static_cast<const float *>(dY), T, n_out, n_out, dYt, Tp, s)) != TPCE_OK) return st;
+    {
+        Operand a{Xt, n_in, T, Tp};    // K-major: M = n_in rows, K = T columns
+        Operand bw{dYt, n_out, T, Tp};  // K-major: N = n_out rows, K = T columns
+        const OutView o[1] = {{dW, n_in, n_out, n_out}};
+        st = launch_gemm<float, 128, false, false, EpiStore<float>>(nm.dW, a, bw, o, nullptr, ii, oi, Ti, 0, 0, 0, 0,
+                                                                    {nullptr}, s);
+        if (st != TPCE_OK) return st;
+    }
+    if (db && (st = colsum(1, dY, T, n_out, n_out, db, partial, s)) != TPCE_OK) return st;
+    return TPCE_OK;
+}
+
+tpce_status linear_forward(const LinearNames &nm, const void *X, const void *W, const float *b, int64_t T,
+                           int64_t n_in, int64_t n_out, int t, int parallel, int dtype, void *Y, void *ws,
+                           size_t ws_bytes, void *stream) {
+    tpce_status st = check_linear_shape(T, n_in, n_out, t, parallel, dtype);
+    if (st != TPCE_OK) return st;
+    if (T == 0) return TPCE_OK;  // no tokens: nothing to compute (token tensors may be NULL)
+    if (!X || !W || !Y) return TPCE_ERR_INVALID;
+    for (const void *p : {X, W, static_cast<const void *>(b), static_cast<const void *>(Y),
+                          static_cast<const void *>(ws)})
+        if (!aligned16(p)) return TPCE_ERR_ALIGN;
+    const LinWs L = lin_ws_layout(T, n_in, n_out, dtype);
+    if (dtype == TPCE_F32 && (!ws || ws_bytes < L.total)) return TPCE_ERR_WORKSPACE;
+    return forward_impl(nm, X, W, b, T, n_in, n_out, dtype, Y, ws, L, static_cast<cudaStream_t>(stream));
+}
+
+tpce_status linear_backward(const LinearNames &nm, const void *dY, const void *X, const void *W, int64_t T,
+                            int64_t n_in, int64_t n_out, int t, int parallel, int dtype, void *dX, void *dW, float *db,
+                            void *ws, size_t ws_bytes, void *stream) {
+    tpce_status st = check_linear_shape(T, n_in, n_out, t, parallel, dtype);
+    if (st != TPCE_OK) return st;
+    if (!W || !dW) return TPCE_ERR_INVALID;
+    if (T > 0 && (!dY || !X || !dX)) return TPCE_ERR_INVALID;
+    for (const void *p : {dY, X, W, static_cast<const void *>(dX), static_cast<const void *>(dW),
+                          static_cast<const void *>(db), static_cast<const void *>(ws)})
+        if (!aligned16(p)) return TPCE_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        // no tokens: the weight and bias gradients are empty sums
+        const size_t esz = dtype == TPCE_F32 ? 4 : 2;
+        if (cudaMemsetAsync(dW, 0, static_cast<size_t>(n_in) * n_out * esz, s) != cudaSuccess) return TPCE_ERR_CUDA;
+        if (db && cudaMemsetAsync(db, 0, sizeof(float) * n_out, s) != cudaSuccess) return TPCE_ERR_CUDA;
+        return TPCE_OK;
+    }
+    const LinWs L = lin_ws_layout(T, n_in, n_out, dtype);
+    if (!ws || ws_bytes < L.total) return TPCE_ERR_WORKSPACE;
+    return backward_impl(nm, dY, X, W, T, n_in, n_out, dtype, dX, dW, db, ws, L, s);
+}
+
+const LinearNames kColumnNames{"linear_column_fwd", "linear_column_bwd_dX_shard_sum", "linear_column_bwd_dW"};
+const LinearNames kRowNames{"linear_row_fwd_shard_sum", "linear_row_bwd_dX", "linear_row_bwd_dW"};
+const LinearNames kQkvNames{"attn_qkv_fwd", "attn_qkv_bwd_dX_shard_sum", "attn_qkv_bwd_dW"};
+const LinearNames kOutNames{"attn_out_fwd_shard_sum", "attn_out_bwd_dO", "attn_out_bwd_dW"};
+
+inline const LinearNames &linear_names(int parallel) {
+    return parallel == TPCE_ROW_PARALLEL ? kRowNames : kColumnNames;
+}
+
+// Head counts of the attention projections: whole key/value groups per shard.
+tpce_status check_heads(int64_t n_heads, int64_t n_kv_heads, int64_t head_dim, int t) {
+    if (n_heads < 1 || n_kv_heads < 1 || head_dim < 8 || t < 1) return TPCE_ERR_SHAPE;
+    if (n_heads % n_kv_heads != 0) return TPCE_ERR_SHAPE;  // query heads share key/value heads evenly
+    if (n_kv_heads % t != 0) return TPCE_ERR_SHAPE;        // each shard holds whole key/value heads
+    if (head_dim % 8 != 0) return TPCE_ERR_SHAPE;
+    if (n_heads + 2 * n_kv_heads > kMaxDim / head_dim) return TPCE_ERR_SHAPE;
+    return TPCE_OK;
+}
+
+}  // namespace
+}  // namespace tpce
+
+using namespace tpce;
+
+extern "C" size_t tpce_linear_workspace_bytes(int64_t T, int64_t n_in, int64_t n_out, int t, int parallel,
+                                              int dtype) {
+    if (check_linear_shape(T, n_in, n_out, t, parallel, dtype) != TPCE_OK) return 0;
+    return lin_ws_layout(T, n_in, n_out, dtype).total;
+}
+
+extern "C" tpce_status tp_linear_forward(const void *X, const void *W, const float *b, int64_t T, int64_t n_in,
+                                         int64_t n_out, int t, int parallel, int dtype, void *Y, void *ws,
+                                         size_t ws_bytes, void *stream) {
+    return linear_forward(linear_names(parallel), X, W, b, T, n_in, n_out, t, parallel, dtype, Y, ws, ws_bytes,
+                          stream);
+}
+
+extern "C" tpce_status tp_linear_backward(const void *dY, const void *X, const void *W, int64_t T, int64_t n_in,
+                                          int64_t n_out, int t, int parallel, int dtype, void *dX, void *dW, float *db,
+                                          void *ws, size_t ws_bytes, void *stream) {
+    return linear_backward(linear_names(parallel), dY, X, W, T, n_in, n_out, t, parallel, dtype, dX, dW, db, ws,
+                           ws_bytes, stream);
+}
+
+extern "C" size_t tpce_attn_workspace_bytes(int64_t T, int64_t h, int64_t n_heads, int64_t n_kv_heads,
+                                            int64_t head_dim, int t, int dtype) {
+    if (check_heads(n_heads, n_kv_heads, head_dim, t) != TPCE_OK) return 0;
+    const int64_t qkv = (n_heads + 2 * n_kv_heads) * head_dim, hq = n_heads * head_dim;
+    const size_t a = tpce_linear_workspace_bytes(T, h, qkv, t, TPCE_COLUMN_PARALLEL, dtype);
+    const size_t b = tpce_linear_workspace_bytes(T, hq, h, t, TPCE_ROW_PARALLEL, dtype);
+    if (a == 0 || b == 0) return 0;
+    return a > b ? a : b;
+}
+
+extern "C" tpce_status tp_attn_qkv_forward(const void *X, const void *Wqkv, const float *bqkv, int64_t T, int64_t h,
+                                           int64_t n_heads, int64_t n_kv_heads, int64_t head_dim, int t, int dtype,
+                                           void *QKV, void *ws, size_t ws_bytes, void *stream) {
+    tpce_status st = check_heads(n_heads, n_kv_heads, head_dim, t);
+    if (st != TPCE_OK) return st;
+    return linear_forward(kQkvNames, X, Wqkv, bqkv, T, h, (n_heads + 2 * n_kv_heads) * head_dim, t,
+                          TPCE_COLUMN_PARALLEL, dtype, QKV, ws, ws_bytes, stream);
+}
+
+extern "C" tpce_status tp_attn_qkv_backward(const void *dQKV, const void *X, const void *Wqkv, int64_t T, int64_t h,
+                                            int64_t n_heads, int64_t n_kv_heads, int64_t head_dim, int t, int dtype,
+                                            void *dX, void *dWqkv, float *dbqkv, void *ws, size_t ws_bytes,
+                                            void *stream) {
+    tpce_status st = check_heads(n_heads, n_kv_heads, head_dim, t);
+    if (st != TPCE_OK) return st;
+    return linear_backward(kQkvNames, dQKV, X, Wqkv, T, h, (n_heads + 2 * n_kv_heads) * head_dim, t,
+                           TPCE_COLUMN_PARALLEL, dtype, dX, dWqkv, dbqkv, ws, ws_bytes, stream);
+}
+
+extern "C" tpce_status tp_attn_out_forward(const void *O, const void *Wo, const float *bo, int64_t T, int64_t h,
+                                           int64_t n_heads, int64_t head_dim, int t, int dtype, void *Z, void *ws,
+                                           size_t ws_bytes, void *stream) {
+    if (n_heads < 1 || head_dim < 8 || head_dim % 8 != 0 || n_heads % t != 0 || n_heads > kMaxDim / head_dim)
+        return TPCE_ERR_SHAPE;
+    return linear_forward(kOutNames, O, Wo, bo, T, n_heads * head_dim, h, t, TPCE_ROW_PARALLEL, dtype, Z, ws, ws_bytes,
+                          stream);
+}
+
+extern "C" tpce_status tp_attn_out_backward(const void *dZ, const void *O, const void *Wo, int64_t T, int64_t h,
+                                            int64_t n_heads, int64_t head_dim, int t, int dtype, void *dO, void *dWo,
+                                            float *dbo, void *ws, size_t ws_bytes, void *stream) {
+    if (n_heads < 1 || head_dim < 8 || head_dim % 8 != 0 || n_heads % t != 0 || n_heads > kMaxDim / head_dim)
+        return TPCE_ERR_SHAPE;
+    return linear_backward(kOutNames, dZ, O, Wo, T, n_heads * head_dim, h, t, TPCE_ROW_PARALLEL, dtype, dO, dWo, dbo,
+                           ws, ws_bytes, stream);
+}

@@ -31,7 +31,8 @@ from typing import Dict, Optional
 import torch
 
 # fixed generator slot per tensor
-_SLOTS = {"X": 1, "A": 2, "B": 3, "dZ": 4, "H": 5, "E": 6, "targets": 7}
+_SLOTS = {"X": 1, "A": 2, "B": 3, "dZ": 4, "H": 5, "E": 6, "targets": 7, "Wqkv": 8, "Wo": 9, "O": 10,
+          "dQKV": 11}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -51,6 +52,9 @@ class Workload:
     s: int = 0
     weight_std: float = 0.02
     act: str = "gelu"      # the MLP's nonlinearity: "gelu" or "swiglu"
+    n_heads: int = 0       # attention projections: query heads (0: none in this workload)
+    n_kv_heads: int = 0    # key/value heads (grouped-query attention)
+    head_dim: int = 0
 
     @property
     def b_scale(self) -> float:
@@ -79,6 +83,10 @@ WORKLOADS: Dict[str, Workload] = {
     # 4096); the page gives no FFN width, the model's published 28,672 is used
     "swiglu70b": Workload("swiglu70b", T=4096, h=8192, f=28672, v_valid=0, v_pad=0, t=8,
                           dtype="bf16", n_blocks=160, b=1, s=4096, act="swiglu"),
+    # the attention projections of the same model: 64 query heads sharing 8
+    # key/value heads of width 128 (the page's figures), t = 8
+    "attn70b": Workload("attn70b", T=4096, h=8192, f=0, v_valid=0, v_pad=0, t=8, dtype="bf16",
+                        n_blocks=160, b=1, s=4096, n_heads=64, n_kv_heads=8, head_dim=128),
 }
 
 # shard-count sweep over the 8.3B MLP shapes
@@ -91,10 +99,12 @@ def sweep_workload(t: int) -> Workload:
 
 
 def custom(name: str, T: int, h: int, f: int, v_valid: int, v_pad: int, t: int,
-           dtype: str = "bf16", n_blocks: int = 2, act: str = "gelu") -> Workload:
+           dtype: str = "bf16", n_blocks: int = 2, act: str = "gelu", n_heads: int = 0,
+           n_kv_heads: int = 0, head_dim: int = 0) -> Workload:
     """A workload of arbitrary shape with the same input statistics."""
     return Workload(name, T=T, h=h, f=f, v_valid=v_valid, v_pad=v_pad, t=t,
-                    dtype=dtype, n_blocks=n_blocks, act=act)
+                    dtype=dtype, n_blocks=n_blocks, act=act, n_heads=n_heads,
+                    n_kv_heads=n_kv_heads, head_dim=head_dim)
 
 
 def _gen(device, seed: int, slot: str) -> torch.Generator:
@@ -134,6 +144,27 @@ def swiglu_inputs(w: Workload, seed: int = 0, device="cpu") -> Dict[str, torch.T
         "W2": _normal((w.f, w.h), w.weight_std * w.b_scale, dt, device, seed, "B"),
         "b1": torch.zeros(2 * w.f, dtype=torch.float32, device=device),
         "b2": torch.zeros(w.h, dtype=torch.float32, device=device),
+        "dZ": _normal((w.T, w.h), 1.0, dt, device, seed, "dZ"),
+    }
+
+
+def attn_inputs(w: Workload, seed: int = 0, device="cpu") -> Dict[str, torch.Tensor]:
+    """Inputs of the attention projections: X [T,h], Wqkv [h,(n_q+2 n_kv) d],
+    O [T, n_q d] (the attention core's output, which this library does not
+    compute, drawn N(0,1)), Wo [n_q d, h] (scaled like B: it feeds the
+    residual), upstream gradients dQKV [T,(n_q+2 n_kv) d] and dZ [T,h], and
+    zero fp32 biases bqkv, bo."""
+    dt = w.torch_dtype
+    nqkv = (w.n_heads + 2 * w.n_kv_heads) * w.head_dim
+    hq = w.n_heads * w.head_dim
+    return {
+        "X": _normal((w.T, w.h), 1.0, dt, device, seed, "X"),
+        "Wqkv": _normal((w.h, nqkv), w.weight_std, dt, device, seed, "Wqkv"),
+        "bqkv": torch.zeros(nqkv, dtype=torch.float32, device=device),
+        "O": _normal((w.T, hq), 1.0, dt, device, seed, "O"),
+        "Wo": _normal((hq, w.h), w.weight_std * w.b_scale, dt, device, seed, "Wo"),
+        "bo": torch.zeros(w.h, dtype=torch.float32, device=device),
+        "dQKV": _normal((w.T, nqkv), 1.0, dt, device, seed, "dQKV"),
         "dZ": _normal((w.T, w.h), 1.0, dt, device, seed, "dZ"),
     }
 
