@@ -16,7 +16,8 @@ CPU oracle timed on a bounded sample on this host.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W]
                        [--impl ours|reference]
-                       [--workload gpt8b|mlp70b|ce128k|swiglu70b|attn70b|sweep]
+                       [--workload gpt8b|gpt8b_chain|mlp70b|ce128k|ce128k_eval|swiglu70b|
+                                   attn70b|sweep]
 Multi-GPU (one process per GPU under torchrun): every rank runs its own
 independent batch (data parallel, weak scaling); there is no collective on
 the data path, only a barrier and a max over ranks of the elapsed time.
@@ -47,8 +48,10 @@ UNIT = "TFLOP/s"
 # fallbacks only if the generated MEASURED_PEAKS.json is absent
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # tokens the CPU oracle processes per timed sample
-CPU_SAMPLE_TOKENS = {"gpt8b": 512, "mlp70b": 192, "ce128k": 96, "swiglu70b": 144, "attn70b": 512, "sweep": 512}
-REF_STEP_TOKENS = {"gpt8b": 8, "mlp70b": 4, "ce128k": 2, "swiglu70b": 3, "attn70b": 8, "sweep": 8}
+CPU_SAMPLE_TOKENS = {"gpt8b": 512, "gpt8b_chain": 512, "mlp70b": 192, "ce128k": 96, "ce128k_eval": 256,
+                     "swiglu70b": 144, "attn70b": 512, "sweep": 512}
+REF_STEP_TOKENS = {"gpt8b": 8, "gpt8b_chain": 8, "mlp70b": 4, "ce128k": 2, "ce128k_eval": 4, "swiglu70b": 3,
+                   "attn70b": 8, "sweep": 8}
 
 
 # ---------------------------------------------------------------------- setup
@@ -58,8 +61,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["gpt8b", "mlp70b", "ce128k", "swiglu70b", "attn70b", "sweep"],
-                   default="gpt8b")
+    p.add_argument("--workload", choices=["gpt8b", "gpt8b_chain", "mlp70b", "ce128k", "ce128k_eval", "swiglu70b",
+                                          "attn70b", "sweep"], default="gpt8b")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
@@ -86,7 +89,8 @@ def flops(w):
     # GeLU block: 4 T h f forward + 8 T h f backward; SwiGLU: GEMM1 is twice as
     # wide (6 T h f forward, 12 T h f backward)
     mlp = (18.0 if w.act == "swiglu" else 12.0) * w.T * w.h * w.f if w.f else 0.0
-    ce = 8.0 * w.T * w.h * w.v_pad if w.v_pad else 0.0
+    # CE: 2 T h v_pad for the logits, 6 more with gradients (recompute, dE, dH)
+    ce = (8.0 if w.ce_grads else 2.0) * w.T * w.h * w.v_pad if w.v_pad else 0.0
     # attention projections: QKV and W_O, each forward + dX + dW
     if w.n_heads:
         nqkv = (w.n_heads + 2 * w.n_kv_heads) * w.head_dim
@@ -97,6 +101,8 @@ def flops(w):
 def workload_config(w, name):
     desc = {
         "gpt8b": "8.3B-shaped block: MLP fwd+bwd + fused vocab-parallel CE fwd+bwd",
+        "gpt8b_chain": "8.3B-shaped block chained into its loss: MLP fwd, CE fwd+bwd on H = Z, MLP bwd with dZ = dH",
+        "ce128k_eval": "vocab-parallel fused logit GEMM + CE forward only (per-token loss), 128,256-token vocabulary",
         "mlp70b": "70B-shaped MLP fwd+bwd",
         "ce128k": "vocab-parallel fused logit GEMM + CE fwd+bwd, 128,256-token vocabulary",
         "swiglu70b": "70B-shaped SwiGLU MLP fwd+bwd (gate/up column-parallel, down row-parallel)",
@@ -243,21 +249,34 @@ class Step:
                                    dtype=torch.uint8, device=dev)
         if w.v_pad:
             self.co = {"loss": torch.empty(T, dtype=torch.float32, device=dev),
-                       "lse": torch.empty(T, dtype=torch.float32, device=dev),
-                       "dH": torch.empty((T, h), dtype=bf, device=dev),
-                       "dE": torch.empty((w.v_pad, h), dtype=bf, device=dev)}
-            self.cws = torch.empty(tp.ce_workspace_bytes(T, h, w.v_pad, w.t), dtype=torch.uint8, device=dev)
+                       "lse": torch.empty(T, dtype=torch.float32, device=dev)}
+            if w.ce_grads:
+                self.co.update(dH=torch.empty((T, h), dtype=bf, device=dev),
+                               dE=torch.empty((w.v_pad, h), dtype=bf, device=dev))
+            self.cws = torch.empty(tp.ce_workspace_bytes(T, h, w.v_pad, w.t, grads=w.ce_grads), dtype=torch.uint8,
+                                   device=dev)
+        # inputs a chained step does not read: dZ comes from the CE, H from the MLP
+        self.unused = {("m", "dZ"), ("c", "H")} if w.chain else set()
 
-    def mlp(self, mi=None):
+    def mlp_fwd(self, mi=None):
         mi = mi or self.mi
         tp, w = self.tp, self.w
         if self.glu:
-            fo = tp.tp_swiglu_forward(mi["X"], mi["W1"], mi["W2"], w.t, mi["b1"], mi["b2"], out=self.fo)
-            tp.tp_swiglu_backward(mi["dZ"], mi["X"], mi["W1"], mi["W2"], fo["GU"], fo["Y"], w.t, out=self.bo,
-                                  ws=self.mws)
-            return
-        fo = tp.tp_mlp_forward(mi["X"], mi["A"], mi["B"], w.t, mi["bA"], mi["bB"], out=self.fo)
-        tp.tp_mlp_backward(mi["dZ"], mi["X"], mi["A"], mi["B"], fo["U"], fo["Y"], w.t, out=self.bo, ws=self.mws)
+            return tp.tp_swiglu_forward(mi["X"], mi["W1"], mi["W2"], w.t, mi["b1"], mi["b2"], out=self.fo)
+        return tp.tp_mlp_forward(mi["X"], mi["A"], mi["B"], w.t, mi["bA"], mi["bB"], out=self.fo)
+
+    def mlp_bwd(self, mi=None, dZ=None):
+        mi = mi or self.mi
+        dZ = mi["dZ"] if dZ is None else dZ
+        tp, w, fo = self.tp, self.w, self.fo
+        if self.glu:
+            tp.tp_swiglu_backward(dZ, mi["X"], mi["W1"], mi["W2"], fo["GU"], fo["Y"], w.t, out=self.bo, ws=self.mws)
+        else:
+            tp.tp_mlp_backward(dZ, mi["X"], mi["A"], mi["B"], fo["U"], fo["Y"], w.t, out=self.bo, ws=self.mws)
+
+    def mlp(self, mi=None):
+        self.mlp_fwd(mi)
+        self.mlp_bwd(mi)
 
     def attn(self, ai=None):
         ai = ai or self.ai
@@ -268,25 +287,38 @@ class Step:
         tp.tp_attn_out_forward(ai["O"], ai["Wo"], nq, d, w.t, ai["bo"], out=self.ao["Z"])
         tp.tp_attn_out_backward(ai["dZ"], ai["O"], ai["Wo"], nq, d, w.t, out=self.ag, ws=self.aws)
 
-    def ce(self, ci=None):
+    def ce(self, ci=None, H=None):
         ci = ci or self.ci
-        return self.tp.vocab_parallel_ce(ci["H"], ci["E"], ci["targets"], self.w.v_valid, self.w.t, grad_scale=1.0,
-                                         out=self.co, ws=self.cws)
+        H = ci["H"] if H is None else H
+        return self.tp.vocab_parallel_ce(H, ci["E"], ci["targets"], self.w.v_valid, self.w.t, grad_scale=1.0,
+                                         grads=self.w.ce_grads, out=self.co, ws=self.cws)
+
+    def segments(self, mi=None, ci=None, ai=None):
+        """The step as (part, call) pairs in launch order."""
+        w = self.w
+        if w.chain:
+            return [("mlp", lambda: self.mlp_fwd(mi)),
+                    ("ce", lambda: self.ce(ci, H=self.fo["Z"])),
+                    ("mlp", lambda: self.mlp_bwd(mi, dZ=self.co["dH"]))]
+        seg = []
+        if w.f:
+            seg.append(("mlp", lambda: self.mlp(mi)))
+        if w.n_heads:
+            seg.append(("mlp", lambda: self.attn(ai)))
+        if w.v_pad:
+            seg.append(("ce", lambda: self.ce(ci)))
+        return seg
 
     def run(self, mi=None, ci=None, ai=None):
-        if self.w.f:
-            self.mlp(mi)
-        if self.w.n_heads:
-            self.attn(ai)
-        if self.w.v_pad:
-            self.ce(ci)
+        for _, fn in self.segments(mi, ci, ai):
+            fn()
 
 
 def input_bytes(step):
     b = 0
-    for d in (step.mi, step.ci, step.ai):
+    for tag, d in (("m", step.mi), ("c", step.ci), ("a", step.ai)):
         if d:
-            b += sum(v.numel() * v.element_size() for v in d.values())
+            b += sum(v.numel() * v.element_size() for k, v in d.items() if (tag, k) not in step.unused)
     return b
 
 
@@ -316,6 +348,12 @@ def oracle_sample(w, mi, ci, n_tokens, ai=None):
 def oracle_step(w, s):
     import oracle
 
+    if w.chain:
+        # the same chain: H = Z of the block, dZ = dH of the loss
+        z = oracle.mlp_forward(s["X"], s["A"], s["bA"], s["B"], s["bB"])["Z"]
+        c = oracle.ce(z, s["E"], s["y"], w.v_valid, grad_scale=1.0)
+        oracle.mlp_backward(s["X"], s["A"], s["bA"], s["B"], c["dH"])
+        return
     if "W1" in s:
         oracle.swiglu_forward(s["X"], s["W1"], s["b1"], s["W2"], s["b2"])
         oracle.swiglu_backward(s["X"], s["W1"], s["b1"], s["W2"], s["dZ"])
@@ -329,7 +367,7 @@ def oracle_step(w, s):
         oracle.linear_forward(a["O"], a["Wo"], a["bo"])
         oracle.linear_backward(a["O"], a["Wo"], a["dZ"])
     if "H" in s:
-        oracle.ce(s["H"], s["E"], s["y"], w.v_valid, grad_scale=1.0)
+        oracle.ce(s["H"], s["E"], s["y"], w.v_valid, grad_scale=1.0, grads=w.ce_grads)
 
 
 def oracle_rate(w, s, n_tokens, reps=1):
@@ -403,8 +441,9 @@ def run_ours(args, w, name):
 
     # ---------------- timed region (device-resident inputs)
     mlp_fl, ce_fl = flops(w)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    segs = step.segments()
+    ev = [[(part, torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for part, _ in segs]
+          for _ in range(args.steps)]
     clocks = ClockSampler(dev, enabled=not args.no_clocks)
     barrier()
     torch.cuda.synchronize()
@@ -413,15 +452,10 @@ def run_ours(args, w, name):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        ev[i][0].record(stream)
-        if w.f:
-            step.mlp()
-        if w.n_heads:
-            step.attn()
-        ev[i][1].record(stream)
-        if w.v_pad:
-            step.ce()
-        ev[i][2].record(stream)
+        for (_, a, b), (_, fn) in zip(ev[i], segs):
+            a.record(stream)
+            fn()
+            b.record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -437,8 +471,8 @@ def run_ours(args, w, name):
         dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
         elapsed_ms = float(tmax.item())
     ms_step = elapsed_ms / args.steps
-    mlp_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / args.steps
-    ce_ms = sum(b.elapsed_time(c) for _, b, c in ev) / args.steps
+    mlp_ms = sum(a.elapsed_time(b) for e in ev for part, a, b in e if part == "mlp") / args.steps
+    ce_ms = sum(a.elapsed_time(b) for e in ev for part, a, b in e if part == "ce") / args.steps
     value = ws * (mlp_fl + ce_fl) / (ms_step * 1e-3) / 1e12
 
     pk, pk_src = peaks()
@@ -472,7 +506,8 @@ def run_ours(args, w, name):
         for tag, src in (("m", step.mi), ("c", step.ci), ("a", step.ai)):
             if src:
                 for k, v in src.items():
-                    host[tag + k] = v.cpu().pin_memory()
+                    if (tag, k) not in step.unused:
+                        host[tag + k] = v.cpu().pin_memory()
         dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
         loss_host = torch.empty(w.T, dtype=torch.float32).pin_memory() if w.v_pad else None
         z_host = torch.empty((w.T, w.h), dtype=torch.bfloat16).pin_memory() if not w.v_pad else None
@@ -480,8 +515,8 @@ def run_ours(args, w, name):
         def e2e_step():
             for k, v in host.items():
                 dev_in[k].copy_(v, non_blocking=True)
-            mi = {k: dev_in["m" + k] for k in step.mi} if w.f else None
-            ci = {k: dev_in["c" + k] for k in step.ci} if w.v_pad else None
+            mi = {k: dev_in["m" + k] for k in step.mi if ("m", k) not in step.unused} if w.f else None
+            ci = {k: dev_in["c" + k] for k in step.ci if ("c", k) not in step.unused} if w.v_pad else None
             ai = {k: dev_in["a" + k] for k in step.ai} if w.n_heads else None
             step.run(mi, ci, ai)
             if w.v_pad:
@@ -524,8 +559,8 @@ def run_ours(args, w, name):
         s = oracle_sample(w, step.mi, step.ci, n, step.ai)
         rate, sec = oracle_rate(w, s, n)
         cpu = {"value": rate, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-               "sample": f"first {n} of {w.T} tokens through the full step (MLP fwd+bwd, CE fwd+bwd with dH and dE) "
-                         f"at full h, f, v; {sec:.1f} s; same FLOP-per-token convention as value"}
+               "sample": f"first {n} of {w.T} tokens through the full step ({workload_config(w, name)['workload'].split(':')[0]}) "
+                         f"at full widths; {sec:.1f} s; same FLOP-per-token convention as value"}
 
     if rank != 0:
         return 0

@@ -52,6 +52,8 @@ class Workload:
     s: int = 0
     weight_std: float = 0.02
     act: str = "gelu"      # the MLP's nonlinearity: "gelu" or "swiglu"
+    chain: bool = False    # the MLP's Z is the CE's H and the CE's dH the MLP's dZ
+    ce_grads: bool = True  # False: the CE is the forward-only (evaluation) loss
     n_heads: int = 0       # attention projections: query heads (0: none in this workload)
     n_kv_heads: int = 0    # key/value heads (grouped-query attention)
     head_dim: int = 0
@@ -88,6 +90,11 @@ WORKLOADS: Dict[str, Workload] = {
     "attn70b": Workload("attn70b", T=4096, h=8192, f=0, v_valid=0, v_pad=0, t=8, dtype="bf16",
                         n_blocks=160, b=1, s=4096, n_heads=64, n_kv_heads=8, head_dim=128),
 }
+
+# the 8.3B block chained into its head (last layer + loss, a training step),
+# and the 128,256-token loss forward only (evaluation)
+WORKLOADS["gpt8b_chain"] = dataclasses.replace(WORKLOADS["gpt8b"], name="gpt8b_chain", chain=True)
+WORKLOADS["ce128k_eval"] = dataclasses.replace(WORKLOADS["ce128k"], name="ce128k_eval", ce_grads=False)
 
 # shard-count sweep over the 8.3B MLP shapes
 SWEEP_T = (1, 2, 4, 8, 16)
