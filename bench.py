@@ -179,7 +179,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------- traffic from committed ncu summaries
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("gemm.cuh", "gemm_pair.cuh", "ptx.cuh"):
+    for f in ("gemm.cuh", "gemm_pair.cuh", "gemm_launch.cuh", "ptx.cuh"):
         with open(os.path.join(ROOT, "vocab_ce_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

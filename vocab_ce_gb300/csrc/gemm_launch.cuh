@@ -30,8 +30,26 @@ struct OutView {
 };
 
 // Tiles are walked in groups of `group_m` row-blocks, row-block fastest, so
-// the CTAs of one wave share a few A and B panels in L2.
-inline int pick_group_m(int tiles_m) { return std::max(1, std::min(tiles_m, 16)); }
+// the CTAs of one wave share a few A and B panels in L2. A group's A panels
+// (group_m row-blocks x K) are reused by every column block the group walks;
+// a panel budget can cap the group so that they stay in L2. Build-time tuning
+// knobs: the budget and the smallest group. Default: 16 row-blocks whatever
+// K is. Measured on GB300: at K = 8192 the 16-block group re-reads A from
+// DRAM (92 GB per 129K-vocabulary logit GEMM against 8.7 GB ideal), yet
+// budgets of 16-32 MB with groups of 2-8 were no faster on any workload
+// (within +-1.5%, slower on that logit GEMM): the kernels are bound by the
+// tensor pipe and the power cap, not by DRAM.
+#ifndef TPCE_GROUP_PANEL_BYTES
+#define TPCE_GROUP_PANEL_BYTES (64ll << 20)
+#endif
+#ifndef TPCE_GROUP_MIN
+#define TPCE_GROUP_MIN 16
+#endif
+inline int pick_group_m(int tiles_m, int64_t rows_per_block, int64_t K, int64_t elem_bytes) {
+    const int64_t panel = std::max<int64_t>(1, rows_per_block * K * elem_bytes);  // one row-block's A panel
+    const int64_t g = std::max<int64_t>(TPCE_GROUP_MIN, std::min<int64_t>(16, TPCE_GROUP_PANEL_BYTES / panel));
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles_m, g)));
+}
 
 // Tile widths a launch may use.
 enum : unsigned { kBN128 = 1u, kBN192 = 2u, kBN256 = 4u };
@@ -123,7 +141,7 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
     s.tiles_m = (M + kBM - 1) / kBM;
     s.tiles_n = (N + kTileN - 1) / kTileN;
     s.k_blocks = (K + static_cast<int>(kBoxK) - 1) / static_cast<int>(kBoxK);
-    s.group_m = pick_group_m(s.tiles_m);
+    s.group_m = pick_group_m(s.tiles_m, kBM, K, sizeof(ElemT));
     s.a_off_mn = a_off_mn;
     s.a_off_k = a_off_k;
     s.b_off_mn = b_off_mn;
@@ -187,7 +205,7 @@ tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &
     s.tiles_m = (M + 2 * kBM - 1) / (2 * kBM);
     s.tiles_n = (N + kTileN - 1) / kTileN;
     s.k_blocks = (K + 63) / 64;
-    s.group_m = pick_group_m(s.tiles_m);
+    s.group_m = pick_group_m(s.tiles_m, 2 * kBM, K, 2);
     s.a_off_mn = a_off_mn;
     s.a_off_k = a_off_k;
     s.b_off_mn = b_off_mn;
