@@ -95,6 +95,8 @@ def _load():
         lib.oracle_linear_sharded.argtypes = [I64, I64, I64, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P]
         lib.oracle_qkv_column.restype = I64
         lib.oracle_qkv_column.argtypes = [ctypes.c_int, I64, I64, I64, I64, I64]
+        lib.oracle_mlp_seq_parallel.restype = None
+        lib.oracle_mlp_seq_parallel.argtypes = [I64, I64, I64, ctypes.c_int, P, P, P, P, P, P, P, P, P, P]
         _lib = lib
         return lib
 
@@ -319,3 +321,26 @@ def qkv_columns(kind: str, n_q: int, n_kv: int, d: int) -> np.ndarray:
     n = n_q if kind == "q" else n_kv
     return np.array([[qkv_column(kind, hh, j, n_q, n_kv, d) for j in range(d)] for hh in range(n)],
                     dtype=np.int64)
+
+
+def _ptr_array(arrs):
+    return (ctypes.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
+
+
+def mlp_seq_parallel(X_chunks, A, bA, B, bB, dZ_chunks) -> Dict[str, object]:
+    """The block with sequence-parallel entry (all-gather of the X chunks) and
+    exit (reduce-scatter into Z chunks), and the mirrored backward."""
+    Xc = [_f64(x) for x in X_chunks]
+    dZc = [_f64(x) for x in dZ_chunks]
+    A, bA, B, bB = map(_f64, (A, bA, B, bB))
+    t = len(Xc)
+    rows, h = Xc[0].shape
+    f = A.shape[1]
+    if any(x.shape != (rows, h) for x in Xc + dZc) or len(dZc) != t or f % t:
+        raise ValueError("t chunks of equal shape and f % t == 0 required")
+    Zc = [np.empty((rows, h)) for _ in range(t)]
+    dXc = [np.empty((rows, h)) for _ in range(t)]
+    dA = np.empty((h, f)); dB = np.empty((f, h))
+    _load().oracle_mlp_seq_parallel(rows * t, h, f, t, _ptr_array(Xc), _ptr(A), _ptr(bA), _ptr(B), _ptr(bB),
+                                    _ptr_array(dZc), _ptr_array(Zc), _ptr_array(dXc), _ptr(dA), _ptr(dB))
+    return {"Z": Zc, "dX": dXc, "dA": dA, "dB": dB}

@@ -874,3 +874,74 @@ int64_t oracle_qkv_column(int kind, int64_t head, int64_t j, int64_t n_q, int64_
         return (head / qpg) * gw + (head % qpg) * d + j;
     return head * gw + (qpg + kind - 1) * d + j;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Sequence parallelism, [MF] "Sequence Parallelism": outside the tensor-
+ * parallel region each of the t ranks holds one sequence chunk, rows
+ * [r T/t, (r+1) T/t), of the activations. The block is entered by an
+ * all-gather of the X chunks into the full sequence and left by a
+ * reduce-scatter: rank r receives, for its own rows only, the sum over the
+ * shards of the row-parallel partials Z_i (then bB). The backward mirrors
+ * it: an all-gather of the dZ chunks, each shard's own backward over the
+ * full sequence, and a reduce-scatter of the partial dX_i into dX chunks.
+ * X_chunks, dZ_chunks, Z_chunks and dX_chunks are t arrays of [T/t, h];
+ * dA [h, f], dB [f, h]. Requires T % t == 0 and f % t == 0. */
+void oracle_mlp_seq_parallel(int64_t T, int64_t h, int64_t f, int t,
+                             const double *const *X_chunks, const double *A, const double *bA,
+                             const double *B, const double *bB, const double *const *dZ_chunks,
+                             double *const *Z_chunks, double *const *dX_chunks, double *dA, double *dB)
+{
+    int64_t rows = T / t, fs = f / t;
+    double *X = (double *)malloc(sizeof(double) * (size_t)(T * h));
+    double *dZ = (double *)malloc(sizeof(double) * (size_t)(T * h));
+    double *Zi = (double *)malloc(sizeof(double) * (size_t)(T * h));
+    double *dXi = (double *)malloc(sizeof(double) * (size_t)(T * h));
+    double *Ai = (double *)malloc(sizeof(double) * (size_t)(h * fs));
+    double *bAi = (double *)malloc(sizeof(double) * (size_t)fs);
+    double *Bi = (double *)malloc(sizeof(double) * (size_t)(fs * h));
+    double *dAi = (double *)malloc(sizeof(double) * (size_t)(h * fs));
+    double *dBi = (double *)malloc(sizeof(double) * (size_t)(fs * h));
+    /* all-gather: chunk r fills rows [r rows, (r+1) rows) */
+    for (int r = 0; r < t; r++) {
+        memcpy(X + (int64_t)r * rows * h, X_chunks[r], sizeof(double) * (size_t)(rows * h));
+        memcpy(dZ + (int64_t)r * rows * h, dZ_chunks[r], sizeof(double) * (size_t)(rows * h));
+    }
+    for (int r = 0; r < t; r++)
+        for (int64_t e = 0; e < rows * h; e++) {
+            Z_chunks[r][e] = 0.0;
+            dX_chunks[r][e] = 0.0;
+        }
+    for (int i = 0; i < t; i++) {
+        for (int64_t k = 0; k < h; k++)
+            for (int64_t j = 0; j < fs; j++)
+                Ai[k * fs + j] = A[k * f + (int64_t)i * fs + j];
+        for (int64_t j = 0; j < fs; j++)
+            bAi[j] = bA ? bA[(int64_t)i * fs + j] : 0.0;
+        memcpy(Bi, B + (int64_t)i * fs * h, sizeof(double) * (size_t)(fs * h));
+        oracle_mlp_forward(T, h, fs, X, Ai, bAi, Bi, NULL, NULL, NULL, Zi);
+        oracle_mlp_backward(T, h, fs, X, Ai, bAi, Bi, dZ, dXi, dAi, NULL, dBi, NULL);
+        /* reduce-scatter: rank r adds shard i's partial for its own rows */
+        for (int r = 0; r < t; r++)
+            for (int64_t e = 0; e < rows * h; e++) {
+                Z_chunks[r][e] += Zi[(int64_t)r * rows * h + e];
+                dX_chunks[r][e] += dXi[(int64_t)r * rows * h + e];
+            }
+        for (int64_t k = 0; k < h; k++)
+            for (int64_t j = 0; j < fs; j++)
+                dA[k * f + (int64_t)i * fs + j] = dAi[k * fs + j];
+        memcpy(dB + (int64_t)i * fs * h, dBi, sizeof(double) * (size_t)(fs * h));
+    }
+    for (int r = 0; r < t; r++)
+        for (int64_t rr = 0; rr < rows; rr++)
+            for (int64_t n = 0; n < h; n++)
+                Z_chunks[r][rr * h + n] += bB ? bB[n] : 0.0;
+    free(X);
+    free(dZ);
+    free(Zi);
+    free(dXi);
+    free(Ai);
+    free(bAi);
+    free(Bi);
+    free(dAi);
+    free(dBi);
+}

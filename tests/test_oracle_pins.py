@@ -320,3 +320,44 @@ def test_ce_out_of_range_target_is_nan():
 
 def test_oracle_reports_threads():
     assert oracle.num_threads() >= 1
+
+
+# --------------------------------------------------------------------------
+# Sequence parallelism: all-gather entry, reduce-scatter exit
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("t", [1, 2, 3, 6])
+def test_seq_parallel_equals_unsharded_rows(t):
+    # the reduce-scatter exit hands rank r exactly rows r of the all-reduced Z
+    # ("All-Reduce = Reduce-Scatter + All-Gather"), and the backward's dX chunks
+    # are the rows of the unsharded dX; the weight gradients are unchanged
+    T, h, f = 12, 5, 12
+    r = rng(41)
+    X, A, B = r.standard_normal((T, h)), r.standard_normal((h, f)), r.standard_normal((f, h))
+    bA, bB, dZ = r.standard_normal(f), r.standard_normal(h), r.standard_normal((T, h))
+    rows = T // t
+    sp = oracle.mlp_seq_parallel([X[i * rows:(i + 1) * rows] for i in range(t)], A, bA, B, bB,
+                                 [dZ[i * rows:(i + 1) * rows] for i in range(t)])
+    ref_f = oracle.mlp_forward(X, A, bA, B, bB)
+    ref_b = oracle.mlp_backward(X, A, bA, B, dZ)
+    np.testing.assert_allclose(np.concatenate(sp["Z"]), ref_f["Z"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(np.concatenate(sp["dX"]), ref_b["dX"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(sp["dA"], ref_b["dA"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(sp["dB"], ref_b["dB"], rtol=1e-12, atol=1e-12)
+
+
+def test_seq_parallel_chunk_order_matters():
+    # permuting the X chunks permutes the Z chunks the same way (the exit is a
+    # scatter by sequence position, not a sum over chunks)
+    T, h, f, t = 8, 4, 8, 4
+    r = rng(42)
+    X, A, B = r.standard_normal((T, h)), r.standard_normal((h, f)), r.standard_normal((f, h))
+    dZ = r.standard_normal((T, h))
+    chunks = [X[i * 2:(i + 1) * 2] for i in range(t)]
+    dzc = [dZ[i * 2:(i + 1) * 2] for i in range(t)]
+    perm = [2, 0, 3, 1]
+    a = oracle.mlp_seq_parallel(chunks, A, None, B, None, dzc)
+    b = oracle.mlp_seq_parallel([chunks[p] for p in perm], A, None, B, None, [dzc[p] for p in perm])
+    for k, p in enumerate(perm):
+        np.testing.assert_allclose(b["Z"][k], a["Z"][p], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(b["dX"][k], a["dX"][p], rtol=1e-12, atol=1e-12)
