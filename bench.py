@@ -16,8 +16,8 @@ CPU oracle timed on a bounded sample on this host.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W]
                        [--impl ours|reference]
-                       [--workload gpt8b|gpt8b_chain|mlp70b|ce128k|ce128k_eval|swiglu70b|
-                                   attn70b|sweep]
+                       [--workload gpt8b|gpt8b_chain|mlp70b|mlp70b_sp|ce128k|ce128k_eval|
+                                   swiglu70b|attn70b|sweep]
 Multi-GPU (one process per GPU under torchrun): every rank runs its own
 independent batch (data parallel, weak scaling); there is no collective on
 the data path, only a barrier and a max over ranks of the elapsed time.
@@ -48,9 +48,9 @@ UNIT = "TFLOP/s"
 # fallbacks only if the generated MEASURED_PEAKS.json is absent
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # tokens the CPU oracle processes per timed sample
-CPU_SAMPLE_TOKENS = {"gpt8b": 512, "gpt8b_chain": 512, "mlp70b": 192, "ce128k": 96, "ce128k_eval": 256,
+CPU_SAMPLE_TOKENS = {"gpt8b": 512, "gpt8b_chain": 512, "mlp70b": 192, "mlp70b_sp": 192, "ce128k": 96, "ce128k_eval": 256,
                      "swiglu70b": 144, "attn70b": 512, "sweep": 512}
-REF_STEP_TOKENS = {"gpt8b": 8, "gpt8b_chain": 8, "mlp70b": 4, "ce128k": 2, "ce128k_eval": 4, "swiglu70b": 3,
+REF_STEP_TOKENS = {"gpt8b": 8, "gpt8b_chain": 8, "mlp70b": 4, "mlp70b_sp": 4, "ce128k": 2, "ce128k_eval": 4, "swiglu70b": 3,
                    "attn70b": 8, "sweep": 8}
 
 
@@ -61,8 +61,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["gpt8b", "gpt8b_chain", "mlp70b", "ce128k", "ce128k_eval", "swiglu70b",
-                                          "attn70b", "sweep"], default="gpt8b")
+    p.add_argument("--workload", choices=["gpt8b", "gpt8b_chain", "mlp70b", "mlp70b_sp", "ce128k", "ce128k_eval",
+                                          "swiglu70b", "attn70b", "sweep"], default="gpt8b")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
@@ -104,6 +104,7 @@ def workload_config(w, name):
         "gpt8b_chain": "8.3B-shaped block chained into its loss: MLP fwd, CE fwd+bwd on H = Z, MLP bwd with dZ = dH",
         "ce128k_eval": "vocab-parallel fused logit GEMM + CE forward only (per-token loss), 128,256-token vocabulary",
         "mlp70b": "70B-shaped MLP fwd+bwd",
+        "mlp70b_sp": "70B-shaped MLP fwd+bwd with sequence-parallel entry/exit (X, Z, dZ, dX as t sequence chunks)",
         "ce128k": "vocab-parallel fused logit GEMM + CE fwd+bwd, 128,256-token vocabulary",
         "swiglu70b": "70B-shaped SwiGLU MLP fwd+bwd (gate/up column-parallel, down row-parallel)",
         "attn70b": "70B-shaped attention projections fwd+bwd (QKV column-parallel by GQA heads, W_O row-parallel; "
@@ -216,6 +217,13 @@ class Step:
             self.mi = None
         else:
             self.mi = (wl.swiglu_inputs if self.glu else wl.mlp_inputs)(w, seed=seed, device=dev)
+        if w.f and w.sp:
+            # one buffer per rank's sequence chunk of X and dZ
+            rows = w.T // w.t
+            for k in ("X", "dZ"):
+                full = self.mi.pop(k)
+                for r in range(w.t):
+                    self.mi[f"{k}{r}"] = full[r * rows:(r + 1) * rows].clone()
         self.ci = wl.ce_inputs(w, seed=seed, device=dev) if w.v_pad else None
         self.ai = wl.attn_inputs(w, seed=seed, device=dev) if w.n_heads else None
         T, h, f = w.T, w.h, w.f
@@ -223,6 +231,10 @@ class Step:
         self.out = {}
         if w.f and not self.glu:
             self.fo = {k: torch.empty(s, dtype=bf, device=dev) for k, s in (("Z", (T, h)), ("U", (T, f)), ("Y", (T, f)))}
+            if w.sp:
+                rows = T // w.t
+                self.zc = [torch.empty((rows, h), dtype=bf, device=dev) for _ in range(w.t)]
+                self.dxc = [torch.empty((rows, h), dtype=bf, device=dev) for _ in range(w.t)]
             self.bo = {"dX": torch.empty((T, h), dtype=bf, device=dev), "dA": torch.empty((h, f), dtype=bf, device=dev),
                        "dB": torch.empty((f, h), dtype=bf, device=dev),
                        "dbA": torch.empty(f, dtype=torch.float32, device=dev),
@@ -261,14 +273,24 @@ class Step:
     def mlp_fwd(self, mi=None):
         mi = mi or self.mi
         tp, w = self.tp, self.w
+        if w.sp:
+            xc = [mi[f"X{r}"] for r in range(w.t)]
+            return tp.tp_mlp_forward_sp(xc, mi["A"], mi["B"], w.t, mi["bA"], mi["bB"],
+                                        out={"Z": self.zc, "U": self.fo["U"], "Y": self.fo["Y"]})
         if self.glu:
             return tp.tp_swiglu_forward(mi["X"], mi["W1"], mi["W2"], w.t, mi["b1"], mi["b2"], out=self.fo)
         return tp.tp_mlp_forward(mi["X"], mi["A"], mi["B"], w.t, mi["bA"], mi["bB"], out=self.fo)
 
     def mlp_bwd(self, mi=None, dZ=None):
         mi = mi or self.mi
-        dZ = mi["dZ"] if dZ is None else dZ
         tp, w, fo = self.tp, self.w, self.fo
+        if w.sp:
+            xc = [mi[f"X{r}"] for r in range(w.t)]
+            dzc = [mi[f"dZ{r}"] for r in range(w.t)]
+            tp.tp_mlp_backward_sp(dzc, xc, mi["A"], mi["B"], fo["U"], fo["Y"], w.t, out={**self.bo, "dX": self.dxc},
+                                  ws=self.mws)
+            return
+        dZ = mi["dZ"] if dZ is None else dZ
         if self.glu:
             tp.tp_swiglu_backward(dZ, mi["X"], mi["W1"], mi["W2"], fo["GU"], fo["Y"], w.t, out=self.bo, ws=self.mws)
         else:
@@ -335,7 +357,9 @@ def oracle_sample(w, mi, ci, n_tokens, ai=None):
         s.update(X=f64(mi["X"][:n_tokens]), dZ=f64(mi["dZ"][:n_tokens]), W1=f64(mi["W1"]), W2=f64(mi["W2"]),
                  b1=f64(mi["b1"]), b2=f64(mi["b2"]))
     elif mi is not None:
-        s.update(X=f64(mi["X"][:n_tokens]), dZ=f64(mi["dZ"][:n_tokens]), A=f64(mi["A"]), B=f64(mi["B"]),
+        # sequence-parallel steps hold X and dZ as chunks: the sample is the first chunk's first tokens
+        X, dZ = (mi[k] if k in mi else mi[k + "0"] for k in ("X", "dZ"))
+        s.update(X=f64(X[:n_tokens]), dZ=f64(dZ[:n_tokens]), A=f64(mi["A"]), B=f64(mi["B"]),
                  bA=f64(mi["bA"]), bB=f64(mi["bB"]))
     if ci is not None:
         s.update(H=f64(ci["H"][:n_tokens]), E=f64(ci["E"]),
@@ -508,31 +532,55 @@ def run_ours(args, w, name):
                 for k, v in src.items():
                     if (tag, k) not in step.unused:
                         host[tag + k] = v.cpu().pin_memory()
-        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        # two device copies of the inputs: step i+1's inputs are copied on a
+        # second stream while step i computes from the other set
+        dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
         loss_host = torch.empty(w.T, dtype=torch.float32).pin_memory() if w.v_pad else None
         z_host = torch.empty((w.T, w.h), dtype=torch.bfloat16).pin_memory() if not w.v_pad else None
+        copy_stream = torch.cuda.Stream(device=dev)
+        copied = [torch.cuda.Event() for _ in range(2)]    # set s holds its step's inputs
+        consumed = [torch.cuda.Event() for _ in range(2)]  # the step that read set s has finished
 
-        def e2e_step():
-            for k, v in host.items():
-                dev_in[k].copy_(v, non_blocking=True)
-            mi = {k: dev_in["m" + k] for k in step.mi if ("m", k) not in step.unused} if w.f else None
-            ci = {k: dev_in["c" + k] for k in step.ci if ("c", k) not in step.unused} if w.v_pad else None
-            ai = {k: dev_in["a" + k] for k in step.ai} if w.n_heads else None
+        def issue_copy(i):
+            s_ = i % 2
+            with torch.cuda.stream(copy_stream):
+                if i >= 2:
+                    copy_stream.wait_event(consumed[s_])
+                for k, v in host.items():
+                    dev_in[s_][k].copy_(v, non_blocking=True)
+                copied[s_].record(copy_stream)
+
+        def compute(i):
+            s_ = i % 2
+            d = dev_in[s_]
+            stream.wait_event(copied[s_])
+            mi = {k: d["m" + k] for k in step.mi if ("m", k) not in step.unused} if w.f else None
+            ci = {k: d["c" + k] for k in step.ci if ("c", k) not in step.unused} if w.v_pad else None
+            ai = {k: d["a" + k] for k in step.ai} if w.n_heads else None
             step.run(mi, ci, ai)
+            consumed[s_].record(stream)
             if w.v_pad:
                 loss_host.copy_(step.co["loss"], non_blocking=True)
             else:
-                z_host.copy_(step.fo["Z"] if w.f else step.ao["Z"], non_blocking=True)
+                z_src = (torch.cat(step.zc) if w.sp else step.fo["Z"]) if w.f else step.ao["Z"]
+                z_host.copy_(z_src, non_blocking=True)
 
-        for _ in range(2):
-            e2e_step()
+        def e2e_run(n, start_event=None):
+            if start_event is not None:
+                copy_stream.wait_event(start_event)  # the first copy starts inside the timed region
+            issue_copy(0)
+            for i in range(n):
+                if i + 1 < n:
+                    issue_copy(i + 1)
+                compute(i)
+
+        e2e_run(2)
         torch.cuda.synchronize()
         barrier()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        e2e_run(args.steps, a)
         b.record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -547,7 +595,9 @@ def run_ours(args, w, name):
         d2h = (loss_host.numel() * 4) if w.v_pad else z_host.numel() * 2
         e2e = {"value": ws * (mlp_fl + ce_fl) / (e_ms / args.steps * 1e-3) / 1e12, "unit": UNIT,
                "ms_per_step": e_ms / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "path": "vocab_ce_gb300 Python API -> C ABI; inputs copied from pinned host memory every step"}
+               "path": "vocab_ce_gb300 Python API -> C ABI; every step's inputs copied from pinned host memory "
+                       "(on a second stream, double-buffered: step i+1's copy overlaps step i's compute; the first "
+                       "copy and the last result read are inside the timed region)"}
 
     # ---------------- CPU oracle baseline (rank 0 at N = 1 only)
     cpu = None

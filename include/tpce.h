@@ -167,6 +167,38 @@ tpce_status tp_mlp_backward(const void *dZ, const void *X, const void *A, const 
                             void *ws, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * Sequence-parallel entry and exit ("Mathematical Foundations of Megatron-LM
+ * 1D Slicing ...", section "Sequence Parallelism"). Outside the
+ * tensor-parallel region each of the t ranks holds one sequence chunk of the
+ * activations, rows [r T/t, (r+1) T/t). These calls take X, Z, dZ and dX as
+ * t chunk buffers, one per rank:
+ *   entry: the column-parallel GEMM reads the all-gathered X directly from
+ *          the X chunks (and the backward reads the all-gathered dZ);
+ *   exit:  the row-parallel GEMM's epilogue writes each shard-summed row of
+ *          Z into the chunk that owns it -- the reduce-scatter -- and the
+ *          backward writes dX the same way.
+ * Every other tensor (A, B, biases, U, Y, the weight gradients) is as in
+ * tp_mlp_forward / tp_mlp_backward, and so is the arithmetic: the results
+ * are the rows of the dense calls' results, bit for bit.
+ * Chunk arguments: host arrays of t device pointers, read during the call
+ * only; chunk r is [T/t, h] row-major, 16-byte aligned.
+ * Shapes: as the dense calls, and t <= 16, T % t == 0, (T / t) % 128 == 0
+ * (whole 128-row tile blocks per chunk). T == 0: the forward is a no-op, the
+ * backward zeroes the weight and bias gradients.
+ * Workspace: as the dense calls.
+ * ------------------------------------------------------------------------- */
+tpce_status tp_mlp_forward_sp(const void *const *X_chunks, const void *A, const float *bA,
+                              const void *B, const float *bB,
+                              int64_t T, int64_t h, int64_t f, int t, int dtype,
+                              void *const *Z_chunks, void *U, void *Y,
+                              void *ws, size_t ws_bytes, void *stream);
+tpce_status tp_mlp_backward_sp(const void *const *dZ_chunks, const void *const *X_chunks,
+                               const void *A, const void *B, const void *U, const void *Y,
+                               int64_t T, int64_t h, int64_t f, int t, int dtype,
+                               void *const *dX_chunks, void *dA, float *dbA, void *dB, float *dbB,
+                               void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
  * The SwiGLU variant of the block ("Distributed tensor parallelism: scale
  * fine-tuning of 70B-parameter LLMs with Megatron-LM", section "The MLP
  * Block"): MLP(X) = (Swish(X W_gate) (.) (X W_up)) W_down, with W_gate and
@@ -226,6 +258,19 @@ tpce_status tp_swiglu_backward(const void *dZ, const void *X, const void *W1, co
                                int64_t T, int64_t h, int64_t f, int t, int dtype,
                                void *dX, void *dW1, float *db1, void *dW2, float *db2,
                                void *ws, size_t ws_bytes, void *stream);
+
+/* The sequence-parallel forms of the SwiGLU block: as tp_mlp_forward_sp /
+ * tp_mlp_backward_sp, with the tensors of tp_swiglu_forward / backward. */
+tpce_status tp_swiglu_forward_sp(const void *const *X_chunks, const void *W1, const float *b1,
+                                 const void *W2, const float *b2,
+                                 int64_t T, int64_t h, int64_t f, int t, int dtype,
+                                 void *const *Z_chunks, void *GU, void *Y,
+                                 void *ws, size_t ws_bytes, void *stream);
+tpce_status tp_swiglu_backward_sp(const void *const *dZ_chunks, const void *const *X_chunks,
+                                  const void *W1, const void *W2, const void *GU, const void *Y,
+                                  int64_t T, int64_t h, int64_t f, int t, int dtype,
+                                  void *const *dX_chunks, void *dW1, float *db1, void *dW2, float *db2,
+                                  void *ws, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Linear layers: ColumnParallelLinear and RowParallelLinear ("Mathematical

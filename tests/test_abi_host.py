@@ -171,6 +171,37 @@ def test_linear_and_attention_validation(L):
     assert L.tpce_linear_workspace_bytes(64, 128, 256, 3, 0, 0) == 0
 
 
+def test_seq_parallel_validation(L):
+    import ctypes as C
+
+    def arr(ptrs):
+        return (C.c_void_p * len(ptrs))(*ptrs)
+    good = [1 << 20] * 4
+
+    def fwd(T=512, h=64, f=256, t=4, X=None, Z=None):
+        X = arr(good[:t] if X is None else X)
+        Z = arr(good[:t] if Z is None else Z)
+        return L.tp_mlp_forward_sp(X, FAKE, None, FAKE, None, T, h, f, t, 0, Z, FAKE, FAKE, None, 0, None)
+    assert fwd(T=500) == 2                                  # T % t
+    assert fwd(T=256) == 2                                  # chunks of 64 rows: not whole 128-row blocks
+    assert fwd(X=[1 << 20, 0, 1 << 20, 1 << 20]) == 1       # a null chunk
+    assert fwd(Z=[1 << 20, (1 << 20) + 8, 1 << 20, 1 << 20]) == 3   # a misaligned chunk
+    assert L.tp_mlp_forward_sp(None, FAKE, None, FAKE, None, 512, 64, 256, 4, 0, arr(good), FAKE, FAKE, None, 0,
+                               None) == 1
+    assert fwd(T=0) == 0
+    # more chunks than the library maps
+    big = arr([1 << 20] * 32)
+    assert L.tp_mlp_forward_sp(big, FAKE, None, FAKE, None, 32 * 128, 64, 32 * 64, 32, 0, big, FAKE, FAKE, None, 0,
+                               None) == 2
+    # backward: the workspace check comes after the chunk checks
+    st = L.tp_mlp_backward_sp(arr(good), arr(good), FAKE, FAKE, FAKE, FAKE, 512, 64, 256, 4, 0, arr(good), FAKE,
+                              None, FAKE, None, None, 0, None)
+    assert st == 4
+    st = L.tp_swiglu_backward_sp(arr(good), arr(good[:3] + [0]), FAKE, FAKE, FAKE, FAKE, 512, 64, 256, 4, 0,
+                                 arr(good), FAKE, None, FAKE, None, None, 0, None)
+    assert st == 1
+
+
 def test_ce_validation(L):
     def ce(T=64, h=64, vp=512, vv=500, t=2, ws=None, wsb=0, H=FAKE, tg=FAKE):
         return L.vocab_parallel_ce(H, FAKE, tg, T, h, vp, vv, t, 1.0, 0, FAKE, None, FAKE, FAKE, ws, wsb, None)

@@ -185,6 +185,118 @@ def tp_swiglu_backward(dZ: torch.Tensor, X: torch.Tensor, W1: torch.Tensor, W2: 
     return res
 
 
+def _ptr_list(xs):
+    return (ctypes.c_void_p * len(xs))(*[x.data_ptr() for x in xs])
+
+
+def _chunks(xs, name, t, rows, h, dt, dev):
+    if len(xs) != t:
+        raise ValueError(f"{name}: {t} sequence chunks expected, got {len(xs)}")
+    for i, x in enumerate(xs):
+        _need(x, f"{name}[{i}]", dt, (rows, h))
+        if x.device != dev:
+            raise ValueError(f"{name}[{i}] is on {x.device}, expected {dev}")
+
+
+def _mlp_sp(glu, X_chunks, W1, W2, t, b1, b2, out, ws, stream):
+    rows, h = X_chunks[0].shape
+    T = rows * t
+    f = W2.shape[0]
+    fw = 2 * f if glu else f
+    dt, dev = X_chunks[0].dtype, X_chunks[0].device
+    _chunks(X_chunks, "X_chunks", t, rows, h, dt, dev)
+    _need(W1, "W1" if glu else "A", dt, (h, fw))
+    _need(W2, "W2" if glu else "B", dt, (f, h))
+    for name, b, n in (("b1", b1, fw), ("b2", b2, h)):
+        if b is not None:
+            _need(b, name, torch.float32, (n,))
+    out = dict(out or {})
+    Zc = out.get("Z")
+    if Zc is None:
+        Zc = [torch.empty((rows, h), dtype=dt, device=dev) for _ in range(t)]
+    if isinstance(Zc, torch.Tensor):
+        raise ValueError("out['Z'] must be a list of t sequence-chunk tensors")
+    _chunks(Zc, "Z", t, rows, h, dt, dev)
+    ukey = "GU" if glu else "U"
+    U = out.get(ukey) if out.get(ukey) is not None else torch.empty((T, fw), dtype=dt, device=dev)
+    Y = out.get("Y") if out.get("Y") is not None else torch.empty((T, f), dtype=dt, device=dev)
+    w = None
+    if dt == torch.float32 and T > 0:
+        q = swiglu_workspace_bytes if glu else mlp_workspace_bytes
+        w = _workspace(q(T, h, f, t, dt), dev, ws)
+    xp, zp = _ptr_list(X_chunks), _ptr_list(Zc)
+    fn = lib().tp_swiglu_forward_sp if glu else lib().tp_mlp_forward_sp
+    st = fn(xp, _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), T, h, f, t, _DT[dt], zp, _ptr(U), _ptr(Y), _ptr(w),
+            0 if w is None else w.numel() * w.element_size(), _stream(stream))
+    check(st, "tp_swiglu_forward_sp" if glu else "tp_mlp_forward_sp")
+    return {"Z": Zc, ukey: U, "Y": Y}
+
+
+def _mlp_sp_bwd(glu, dZ_chunks, X_chunks, W1, W2, U, Y, t, bias_grads, out, ws, stream):
+    rows, h = X_chunks[0].shape
+    T = rows * t
+    f = W2.shape[0]
+    fw = 2 * f if glu else f
+    dt, dev = X_chunks[0].dtype, X_chunks[0].device
+    _chunks(X_chunks, "X_chunks", t, rows, h, dt, dev)
+    _chunks(dZ_chunks, "dZ_chunks", t, rows, h, dt, dev)
+    for name, x, shp in (("W1" if glu else "A", W1, (h, fw)), ("W2" if glu else "B", W2, (f, h)),
+                         ("GU" if glu else "U", U, (T, fw)), ("Y", Y, (T, f))):
+        _need(x, name, dt, shp)
+    out = dict(out or {})
+    k1, k2, kb1, kb2 = ("dW1", "dW2", "db1", "db2") if glu else ("dA", "dB", "dbA", "dbB")
+    dXc = out.get("dX")
+    if dXc is None:
+        dXc = [torch.empty((rows, h), dtype=dt, device=dev) for _ in range(t)]
+    if isinstance(dXc, torch.Tensor):
+        raise ValueError("out['dX'] must be a list of t sequence-chunk tensors")
+    _chunks(dXc, "dX", t, rows, h, dt, dev)
+
+    def get(k, shp, d):
+        return out.get(k) if out.get(k) is not None else torch.empty(shp, dtype=d, device=dev)
+
+    d1, d2 = get(k1, (h, fw), dt), get(k2, (f, h), dt)
+    db1 = get(kb1, (fw,), torch.float32) if bias_grads else None
+    db2 = get(kb2, (h,), torch.float32) if bias_grads else None
+    q = swiglu_workspace_bytes if glu else mlp_workspace_bytes
+    w = _workspace(q(T, h, f, t, dt) if T > 0 else 0, dev, ws)
+    dzp, xp, dxp = _ptr_list(dZ_chunks), _ptr_list(X_chunks), _ptr_list(dXc)
+    fn = lib().tp_swiglu_backward_sp if glu else lib().tp_mlp_backward_sp
+    st = fn(dzp, xp, _ptr(W1), _ptr(W2), _ptr(U), _ptr(Y), T, h, f, t, _DT[dt], dxp, _ptr(d1), _ptr(db1), _ptr(d2),
+            _ptr(db2), _ptr(w), 0 if w is None else w.numel() * w.element_size(), _stream(stream))
+    check(st, "tp_swiglu_backward_sp" if glu else "tp_mlp_backward_sp")
+    res = {"dX": dXc, k1: d1, k2: d2}
+    if bias_grads:
+        res.update({kb1: db1, kb2: db2})
+    return res
+
+
+def tp_mlp_forward_sp(X_chunks, A: torch.Tensor, B: torch.Tensor, t: int, bA: Optional[torch.Tensor] = None,
+                      bB: Optional[torch.Tensor] = None, out=None, ws: Optional[torch.Tensor] = None, stream=None):
+    """The GeLU block with sequence-parallel entry and exit: X and Z as t
+    sequence chunks [T/t, h] (lists of tensors); returns Z (list), U, Y."""
+    return _mlp_sp(False, X_chunks, A, B, t, bA, bB, out, ws, stream)
+
+
+def tp_mlp_backward_sp(dZ_chunks, X_chunks, A: torch.Tensor, B: torch.Tensor, U: torch.Tensor, Y: torch.Tensor,
+                       t: int, bias_grads: bool = True, out=None, ws: Optional[torch.Tensor] = None, stream=None):
+    """Backward of tp_mlp_forward_sp: dX (list of chunks), dA, dB, dbA, dbB."""
+    return _mlp_sp_bwd(False, dZ_chunks, X_chunks, A, B, U, Y, t, bias_grads, out, ws, stream)
+
+
+def tp_swiglu_forward_sp(X_chunks, W1: torch.Tensor, W2: torch.Tensor, t: int, b1: Optional[torch.Tensor] = None,
+                         b2: Optional[torch.Tensor] = None, out=None, ws: Optional[torch.Tensor] = None, stream=None):
+    """The SwiGLU block with sequence-parallel entry and exit; returns Z (list), GU, Y."""
+    return _mlp_sp(True, X_chunks, W1, W2, t, b1, b2, out, ws, stream)
+
+
+def tp_swiglu_backward_sp(dZ_chunks, X_chunks, W1: torch.Tensor, W2: torch.Tensor, GU: torch.Tensor,
+                          Y: torch.Tensor, t: int, bias_grads: bool = True, out=None,
+                          ws: Optional[torch.Tensor] = None, stream=None):
+    """Backward of tp_swiglu_forward_sp: dX (list of chunks), dW1, dW2, db1, db2."""
+    return _mlp_sp_bwd(True, dZ_chunks, X_chunks, W1, W2, GU, Y, t, bias_grads, out, ws, stream)
+
+
 _PAR = {"column": TPCE_COLUMN_PARALLEL, "row": TPCE_ROW_PARALLEL}
 
 

@@ -88,6 +88,101 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmShape &s, int &m
 }
 
 // --------------------------------------------------------------------------
+// Sequence-chunked operands. With sequence parallelism the activations enter
+// and leave the tensor-parallel region as t sequence chunks in t separate
+// buffers (one per rank): the column-parallel GEMM reads the all-gathered
+// input from them, the row-parallel GEMM's epilogue writes the shard-summed
+// output into them. One role of a launch may be chunked: the A operand, the
+// B operand or output map 0. Its rows (the outer coordinate of its tensor
+// map: M or K for an operand, M for the output) are split into chunks of
+// `rows` rows, each with its own tensor map; a 128-row box never straddles
+// two chunks because `rows` is a multiple of 128.
+// --------------------------------------------------------------------------
+constexpr int kMaxChunks = 16;
+enum : int { kChunkNone = 0, kChunkA = 1, kChunkB = 2, kChunkC = 3 };
+
+template <int kChunk>
+struct ChunkSet {
+    CUtensorMap m[kChunk != kChunkNone ? kMaxChunks : 1];
+    int rows;   // rows per chunk
+    int count;  // chunks in use
+};
+
+// Chunk c's map, picked by a switch so that every address handed to TMA is a
+// fixed offset into the kernel parameter.
+template <int kChunk>
+__device__ __forceinline__ const CUtensorMap *chunk_map_at(const ChunkSet<kChunk> &cs, int c) {
+    static_assert(kChunk == kChunkNone || kMaxChunks == 16, "the switch below lists 16 chunks");
+    if constexpr (kChunk == kChunkNone) {
+        return &cs.m[0];
+    } else {
+        switch (c) {
+            case 1: return &cs.m[1];
+            case 2: return &cs.m[2];
+            case 3: return &cs.m[3];
+            case 4: return &cs.m[4];
+            case 5: return &cs.m[5];
+            case 6: return &cs.m[6];
+            case 7: return &cs.m[7];
+            case 8: return &cs.m[8];
+            case 9: return &cs.m[9];
+            case 10: return &cs.m[10];
+            case 11: return &cs.m[11];
+            case 12: return &cs.m[12];
+            case 13: return &cs.m[13];
+            case 14: return &cs.m[14];
+            case 15: return &cs.m[15];
+            default: return &cs.m[0];
+        }
+    }
+}
+
+// The map holding outer coordinate y, and y rebased into that chunk. Rows
+// past the last chunk stay in it (past its end: TMA fills them with zeros).
+template <int kChunk>
+__device__ __forceinline__ const CUtensorMap *chunk_map(const ChunkSet<kChunk> &cs, int &y) {
+    int c = y / cs.rows;
+    c = c < cs.count - 1 ? c : cs.count - 1;
+    y -= c * cs.rows;
+    return chunk_map_at(cs, c);
+}
+
+// The chunk an operand's loads are in, kept across the K loop so that the
+// producer never divides or switches per k-block: K-major operands (outer
+// coordinate M or N) pick their chunk once per tile; MN-major ones (outer
+// coordinate K) step `dy` rows per k-block and change map only at a chunk
+// boundary (dy divides the chunk rows).
+template <int kChunk>
+struct ChunkCursor {
+    const CUtensorMap *map;
+    int y;  // outer coordinate inside the current chunk
+    int c;  // current chunk
+    __device__ __forceinline__ void init(const ChunkSet<kChunk> &cs, int y0) {
+        c = y0 / cs.rows;
+        c = c < cs.count - 1 ? c : cs.count - 1;
+        y = y0 - c * cs.rows;
+        map = chunk_map_at(cs, c);
+    }
+    __device__ __forceinline__ void advance(const ChunkSet<kChunk> &cs, int dy) {
+        y += dy;
+        if (y >= cs.rows && c < cs.count - 1) {
+            y -= cs.rows;
+            ++c;
+            map = chunk_map_at(cs, c);
+        }
+    }
+};
+
+// Bring every chunk's descriptor into the TMA descriptor cache up front
+// (switching maps mid-tile otherwise stalls on descriptor fetches).
+template <int kChunk>
+__device__ __forceinline__ void prefetch_chunk_maps(const ChunkSet<kChunk> &cs) {
+    if constexpr (kChunk != kChunkNone) {
+        for (int c = 0; c < cs.count; ++c) ptx::prefetch_tmap(chunk_map_at(cs, c));
+    }
+}
+
+// --------------------------------------------------------------------------
 // 8-element loads for the epilogues (16- or 32-byte aligned)
 // --------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -579,16 +674,21 @@ __device__ __forceinline__ void epi_drain_inputs(EpiWarp &w) {
 // at row0, columns from n0. The input chunk c0 must already be issued. Gated
 // epilogues read the up half of chunk c at TMEM column up_col + 32 c.
 // Returns false if a bounded wait gave up.
-template <class Epi>
+template <class Epi, int kChunk>
 __device__ __forceinline__ bool epi_tile(const typename Epi::Params &ep, const GemmShape &shp, uint32_t taddr,
                                          uint32_t up_col, int row0, int n0, int c0, int c1, int lane, EpiWarp &w,
                                          const CUtensorMap *tmC0, const CUtensorMap *tmC1,
-                                         const CUtensorMap *tmIn, volatile int *abort_flag, uint32_t *err) {
+                                         const CUtensorMap *tmIn, const ChunkSet<kChunk> *cs,
+                                         volatile int *abort_flag, uint32_t *err) {
     using OutT = typename Epi::Out;
     constexpr int kOuts = Epi::kOuts;
     constexpr uint32_t kB = EpiSmem<Epi>::kChunkBytes;
     static_assert(Epi::kIns <= 2 && !(Epi::kGated && Epi::kIns > 0), "epilogue inputs");
     const int row = row0 + lane;
+    // output map 0 and the row coordinate in it (a sequence chunk, if chunked)
+    const CUtensorMap *tm0 = tmC0;
+    int y0 = row0;
+    if constexpr (kChunk == kChunkC) tm0 = chunk_map(*cs, y0);
     typename Epi::Row rs = Epi::begin(ep, row, row < shp.M);
 #pragma unroll 1
     for (int c = c0; c < c1; ++c) {
@@ -630,12 +730,13 @@ __device__ __forceinline__ bool epi_tile(const typename Epi::Params &ep, const G
 #pragma unroll
                 for (int k = 0; k < kOuts; ++k) {
                     const uint8_t *src = w.stage + (2 * k + buf) * kB;
-                    const CUtensorMap *tm = Epi::out_map(k) == 0 ? tmC0 : tmC1;
+                    const CUtensorMap *tm = Epi::out_map(k) == 0 ? tm0 : tmC1;
                     const int col = n + Epi::out_col(ep, k);
+                    const int y = Epi::out_map(k) == 0 ? y0 : row0;
                     if (Epi::mode(ep) == 1)
-                        ptx::tma_reduce_add_2d(tm, src, col, row0);
+                        ptx::tma_reduce_add_2d(tm, src, col, y);
                     else
-                        ptx::tma_store_2d(tm, src, col, row0);
+                        ptx::tma_store_2d(tm, src, col, y);
                 }
                 ptx::bulk_commit();
             }
@@ -671,12 +772,12 @@ struct KernelCfg {
 // --------------------------------------------------------------------------
 // The kernel
 // --------------------------------------------------------------------------
-template <typename ElemT, int BN, bool A_MN, bool B_MN, class Epi>
+template <typename ElemT, int BN, bool A_MN, bool B_MN, class Epi, int kChunk>
 __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
-                   const __grid_constant__ CUtensorMap tmIn, const GemmShape shp, const typename Epi::Params ep,
-                   uint32_t *err) {
+                   const __grid_constant__ CUtensorMap tmIn, const __grid_constant__ ChunkSet<kChunk> cs,
+                   const GemmShape shp, const typename Epi::Params ep, uint32_t *err) {
     using C = KernelCfg<BN, Epi>;
     using ET = ElemTraits<ElemT>;
     using OutT = typename Epi::Out;
@@ -692,6 +793,7 @@ __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
     constexpr int kChunks = kTileN / 32;
     constexpr int kOuts = Epi::kOuts;
     static_assert(!Epi::kGated || BN % 128 == 0, "gated tiles: halves of whole 64-wide blocks");
+    static_assert(!(Epi::kGated && kChunk == kChunkB), "gated tiles read an unchunked B");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -725,6 +827,10 @@ __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmB);
+        if constexpr (kChunk == kChunkA || kChunk == kChunkB) prefetch_chunk_maps(cs);
+    }
+    if constexpr (kChunk == kChunkC) {
+        if (warp == 2 && lane == 0) prefetch_chunk_maps(cs);
     }
     if (warp == 1) {
         ptx::tmem_alloc(tmem_slot, C::kTmemCols);
@@ -748,6 +854,9 @@ __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
                 int mb, nb;
                 tile_coords(tile, shp, mb, nb);
                 const int m0 = mb * kBM, n0 = nb * kTileN;
+                ChunkCursor<kChunk> cur;
+                if constexpr (kChunk == kChunkA) cur.init(cs, A_MN ? shp.a_off_k : m0 + shp.a_off_mn);
+                if constexpr (kChunk == kChunkB) cur.init(cs, B_MN ? shp.b_off_k : n0 + shp.b_off_mn);
                 for (int kb = 0; kb < shp.k_blocks; ++kb) {
                     if (!ptx::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, 1)) break;
                     ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
@@ -756,22 +865,36 @@ __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
                     uint8_t *sa = smem + stage * C::kStageBytes;
                     uint8_t *sb = sa + C::kABytes;
                     const int k0 = kb * kBK;
+                    // A's outer coordinate: M (K-major) or K (MN-major)
+                    int ya = A_MN ? k0 + shp.a_off_k : m0 + shp.a_off_mn;
+                    const CUtensorMap *ma = &tmA;
+                    if constexpr (kChunk == kChunkA) {
+                        ma = cur.map;
+                        ya = cur.y;
+                    }
                     if (!A_MN) {
-                        ptx::tma_load_2d(sa, &tmA, &full[stage], k0 + shp.a_off_k, m0 + shp.a_off_mn);
+                        ptx::tma_load_2d(sa, ma, &full[stage], k0 + shp.a_off_k, ya);
                     } else {
 #pragma unroll
                         for (int j = 0; j < kBM / 64; ++j)
-                            ptx::tma_load_2d(sa + j * kMnBlockBytes, &tmA, &full[stage],
-                                             m0 + shp.a_off_mn + 64 * j, k0 + shp.a_off_k);
+                            ptx::tma_load_2d(sa + j * kMnBlockBytes, ma, &full[stage], m0 + shp.a_off_mn + 64 * j, ya);
                     }
+                    // B's outer coordinate: N (K-major) or K (MN-major)
+                    int yb = B_MN ? k0 + shp.b_off_k : n0 + shp.b_off_mn;
+                    const CUtensorMap *mb = &tmB;
+                    if constexpr (kChunk == kChunkB) {
+                        mb = cur.map;
+                        yb = cur.y;
+                    }
+                    if constexpr ((kChunk == kChunkA && A_MN) || (kChunk == kChunkB && B_MN)) cur.advance(cs, kBK);
                     if (!B_MN) {
                         if constexpr (Epi::kGated) {
                             // two boxes of BN/2 rows: the gate rows, then the up rows
-                            ptx::tma_load_2d(sb, &tmB, &full[stage], k0 + shp.b_off_k, n0 + shp.b_off_mn);
-                            ptx::tma_load_2d(sb + (BN / 2) * kRowBytes, &tmB, &full[stage], k0 + shp.b_off_k,
+                            ptx::tma_load_2d(sb, mb, &full[stage], k0 + shp.b_off_k, yb);
+                            ptx::tma_load_2d(sb + (BN / 2) * kRowBytes, mb, &full[stage], k0 + shp.b_off_k,
                                              n0 + shp.b_gate_off + shp.b_off_mn);
                         } else {
-                            ptx::tma_load_2d(sb, &tmB, &full[stage], k0 + shp.b_off_k, n0 + shp.b_off_mn);
+                            ptx::tma_load_2d(sb, mb, &full[stage], k0 + shp.b_off_k, yb);
                         }
                     } else {
 #pragma unroll
@@ -780,8 +903,7 @@ __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
                             const int col = Epi::kGated && j >= BN / 128
                                                 ? n0 + shp.b_gate_off + 64 * (j - BN / 128)
                                                 : n0 + 64 * j;
-                            ptx::tma_load_2d(sb + j * kMnBlockBytes, &tmB, &full[stage], col + shp.b_off_mn,
-                                             k0 + shp.b_off_k);
+                            ptx::tma_load_2d(sb + j * kMnBlockBytes, mb, &full[stage], col + shp.b_off_mn, yb);
                         }
                     }
                     if (++stage == S) {
@@ -865,8 +987,8 @@ __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
-            if (!epi_tile<Epi>(ep, shp, taddr, BN / 2, row0, n0, c0, c1, lane, w, &tmC0, &tmC1, &tmIn, abort_flag,
-                               err))
+            if (!epi_tile<Epi, kChunk>(ep, shp, taddr, BN / 2, row0, n0, c0, c1, lane, w, &tmC0, &tmC1, &tmIn, &cs,
+                                       abort_flag, err))
                 break;
             ptx::tc_fence_before();
             __syncwarp();

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 #include <type_traits>
 
@@ -28,6 +29,33 @@ struct OutView {
     void *ptr;
     int64_t rows, cols, ld;
 };
+
+// The rows of the chunked role of a launch (see ChunkSet) in separate
+// buffers: `count` device pointers (a host array, read during the launch
+// only), each holding `rows` rows with the role's row pitch and columns.
+struct Chunks {
+    const void *const *ptrs;
+    int64_t rows;
+    int count;
+};
+
+// Tensor maps of the chunks of one role, built like the role's own map.
+template <int kChunk, typename Build>
+inline bool build_chunk_maps(ChunkSet<kChunk> &cs, const Chunks *ch, Build build) {
+    std::memset(static_cast<void *>(&cs), 0, sizeof(cs));
+    if constexpr (kChunk == kChunkNone) {
+        return ch == nullptr;
+    } else {
+        if (!ch || ch->count < 1 || ch->count > kMaxChunks || ch->rows <= 0 || ch->rows % 128 != 0 ||
+            ch->rows > (1 << 30))
+            return false;
+        cs.rows = static_cast<int>(ch->rows);
+        cs.count = ch->count;
+        for (int c = 0; c < ch->count; ++c)
+            if (!ch->ptrs[c] || !build(&cs.m[c], ch->ptrs[c], ch->rows)) return false;
+        return true;
+    }
+}
 
 // Tiles are walked in groups of `group_m` row-blocks, row-block fastest, so
 // the CTAs of one wave share a few A and B panels in L2. A group's A panels
@@ -103,11 +131,13 @@ inline tpce_status set_smem_attr(K kern, uint32_t bytes, bool (&done)[64], std::
 // maps (used to address one vocabulary chunk of E). Gated epilogues: N counts
 // output columns, and the second half of each B tile starts b_gate_off
 // columns (rows, K-major) after the first.
-template <typename ElemT, int BN, bool A_MN, bool B_MN, class Epi>
+// With kChunk != kChunkNone, `chunks` holds that role's buffers (the role's
+// own Operand/OutView gives its columns and row pitch; its pointer is unused).
+template <typename ElemT, int BN, bool A_MN, bool B_MN, class Epi, int kChunk = kChunkNone>
 tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, const OutView *outs,
                         const OutView *ins, int M, int N, int K, int a_off_mn, int a_off_k, int b_off_mn,
                         int b_off_k, const typename Epi::Params &ep, cudaStream_t stream, bool timed = true,
-                        int b_gate_off = 0) {
+                        int b_gate_off = 0, const Chunks *chunks = nullptr) {
     using Cfg = KernelCfg<BN, Epi>;
     constexpr int kTileN = Epi::kGated ? BN / 2 : BN;
     using OutT = typename Epi::Out;
@@ -115,14 +145,35 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
     constexpr uint32_t kBoxK = kRowBytes / sizeof(ElemT);  // contraction elements per 128-byte row
     if (M <= 0 || N <= 0 || K <= 0) return TPCE_ERR_SHAPE;
     const int dt = kF32 ? 1 : 0;
-    CUtensorMap ta, tb, tc[2];
-    bool ok = A_MN ? make_tmap(&ta, dt, a.ptr, a.cols, a.rows, a.ld, 64, 64)
-                   : make_tmap(&ta, dt, a.ptr, a.cols, a.rows, a.ld, kBoxK, kBM);
-    ok = ok && (B_MN ? make_tmap(&tb, dt, b.ptr, b.cols, b.rows, b.ld, 64, 64)
-                     : make_tmap(&tb, dt, b.ptr, b.cols, b.rows, b.ld, kBoxK, kTileN));
     const int odt = std::is_same<OutT, float>::value ? 1 : 0;
+    auto map_a = [&](CUtensorMap *m, const void *p, int64_t rows) {
+        return A_MN ? make_tmap(m, dt, p, a.cols, rows, a.ld, 64, 64) : make_tmap(m, dt, p, a.cols, rows, a.ld, kBoxK, kBM);
+    };
+    auto map_b = [&](CUtensorMap *m, const void *p, int64_t rows) {
+        return B_MN ? make_tmap(m, dt, p, b.cols, rows, b.ld, 64, 64)
+                    : make_tmap(m, dt, p, b.cols, rows, b.ld, kBoxK, kTileN);
+    };
+    auto map_c = [&](CUtensorMap *m, const void *p, int64_t rows) {
+        return make_tmap(m, odt, p, outs[0].cols, rows, outs[0].ld, 32, 32, Stage<OutT>::kSwizzle);
+    };
+    ChunkSet<kChunk> cs;
+    bool ok = kChunk == kChunkA   ? build_chunk_maps(cs, chunks, map_a)
+              : kChunk == kChunkB ? build_chunk_maps(cs, chunks, map_b)
+                                  : build_chunk_maps(cs, chunks, map_c);
+    if (!ok) return fail(TPCE_ERR_INVALID, "bad sequence chunks for %s", name);
+    CUtensorMap ta, tb, tc[2];
+    if (kChunk == kChunkA)
+        ta = cs.m[0];
+    else
+        ok = map_a(&ta, a.ptr, a.rows);
+    if (kChunk == kChunkB)
+        tb = cs.m[0];
+    else
+        ok = ok && map_b(&tb, b.ptr, b.rows);
     for (int k = 0; k < 2; ++k) {
-        if (k < num_out_maps<Epi>())
+        if (k == 0 && kChunk == kChunkC)
+            tc[0] = cs.m[0];
+        else if (k < num_out_maps<Epi>())
             ok = ok && make_tmap(&tc[k], odt, outs[k].ptr, outs[k].cols, outs[k].rows, outs[k].ld, 32, 32,
                                  Stage<OutT>::kSwizzle);
         else
@@ -148,7 +199,7 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
     s.b_off_k = b_off_k;
     s.b_gate_off = b_gate_off;
 
-    auto kern = tc_gemm_kernel<ElemT, BN, A_MN, B_MN, Epi>;
+    auto kern = tc_gemm_kernel<ElemT, BN, A_MN, B_MN, Epi, kChunk>;
     static std::mutex attr_mu;
     static bool attr_done[64] = {};
     tpce_status st = set_smem_attr(kern, Cfg::kSmemBytes, attr_done, attr_mu);
@@ -159,7 +210,7 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
     const int64_t tiles = static_cast<int64_t>(s.tiles_m) * s.tiles_n;
     const int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
     KernelTimer timer(timed ? name : nullptr, stream);
-    kern<<<grid, 64 + 32 * Epi::kWarps, Cfg::kSmemBytes, stream>>>(ta, tb, tc[0], tc[1], tin, s, ep, err);
+    kern<<<grid, 64 + 32 * Epi::kWarps, Cfg::kSmemBytes, stream>>>(ta, tb, tc[0], tc[1], tin, cs, s, ep, err);
     return check_launch(name);
 }
 
@@ -171,23 +222,43 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
 #define TPCE_PAIR_BN 256
 #endif
 
-template <int BN, bool A_MN, bool B_MN, class Epi>
+template <int BN, bool A_MN, bool B_MN, class Epi, int kChunk = kChunkNone>
 tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &b, const OutView *outs,
                              const OutView *ins, int M, int N, int K, int a_off_mn, int a_off_k, int b_off_mn,
                              int b_off_k, const typename Epi::Params &ep, cudaStream_t stream, bool timed = true,
-                             int b_gate_off = 0) {
+                             int b_gate_off = 0, const Chunks *chunks = nullptr) {
     using Cfg = PairCfg<BN, Epi>;
     constexpr int kTileN = Epi::kGated ? BN / 2 : BN;
     using OutT = typename Epi::Out;
     if (M <= 0 || N <= 0 || K <= 0) return TPCE_ERR_SHAPE;
-    CUtensorMap ta, tb, tc[2];
-    bool ok = A_MN ? make_tmap(&ta, 0, a.ptr, a.cols, a.rows, a.ld, 64, 64)
-                   : make_tmap(&ta, 0, a.ptr, a.cols, a.rows, a.ld, 64, kBM);
-    ok = ok && (B_MN ? make_tmap(&tb, 0, b.ptr, b.cols, b.rows, b.ld, 64, 64)
-                     : make_tmap(&tb, 0, b.ptr, b.cols, b.rows, b.ld, 64, BN / 2));
     const int odt = std::is_same<OutT, float>::value ? 1 : 0;
+    auto map_a = [&](CUtensorMap *m, const void *p, int64_t rows) {
+        return A_MN ? make_tmap(m, 0, p, a.cols, rows, a.ld, 64, 64) : make_tmap(m, 0, p, a.cols, rows, a.ld, 64, kBM);
+    };
+    auto map_b = [&](CUtensorMap *m, const void *p, int64_t rows) {
+        return B_MN ? make_tmap(m, 0, p, b.cols, rows, b.ld, 64, 64) : make_tmap(m, 0, p, b.cols, rows, b.ld, 64, BN / 2);
+    };
+    auto map_c = [&](CUtensorMap *m, const void *p, int64_t rows) {
+        return make_tmap(m, odt, p, outs[0].cols, rows, outs[0].ld, 32, 32, Stage<OutT>::kSwizzle);
+    };
+    ChunkSet<kChunk> cs;
+    bool ok = kChunk == kChunkA   ? build_chunk_maps(cs, chunks, map_a)
+              : kChunk == kChunkB ? build_chunk_maps(cs, chunks, map_b)
+                                  : build_chunk_maps(cs, chunks, map_c);
+    if (!ok) return fail(TPCE_ERR_INVALID, "bad sequence chunks for %s", name);
+    CUtensorMap ta, tb, tc[2];
+    if (kChunk == kChunkA)
+        ta = cs.m[0];
+    else
+        ok = map_a(&ta, a.ptr, a.rows);
+    if (kChunk == kChunkB)
+        tb = cs.m[0];
+    else
+        ok = ok && map_b(&tb, b.ptr, b.rows);
     for (int k = 0; k < 2; ++k) {
-        if (k < num_out_maps<Epi>())
+        if (k == 0 && kChunk == kChunkC)
+            tc[0] = cs.m[0];
+        else if (k < num_out_maps<Epi>())
             ok = ok && make_tmap(&tc[k], odt, outs[k].ptr, outs[k].cols, outs[k].rows, outs[k].ld, 32, 32,
                                  Stage<OutT>::kSwizzle);
         else
@@ -211,7 +282,7 @@ tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &
     s.b_off_mn = b_off_mn;
     s.b_off_k = b_off_k;
     s.b_gate_off = b_gate_off;
-    auto kern = tc_gemm_pair_kernel<BN, A_MN, B_MN, Epi>;
+    auto kern = tc_gemm_pair_kernel<BN, A_MN, B_MN, Epi, kChunk>;
     static std::mutex attr_mu;
     static bool attr_done[64] = {};
     tpce_status st = set_smem_attr(kern, Cfg::kSmemBytes, attr_done, attr_mu);
@@ -222,19 +293,21 @@ tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &
     const int64_t tiles = static_cast<int64_t>(s.tiles_m) * s.tiles_n;
     const int grid = 2 * static_cast<int>(std::min<int64_t>(tiles, sms / 2));
     KernelTimer timer(timed ? name : nullptr, stream);
-    kern<<<grid, 64 + 32 * Epi::kWarps, Cfg::kSmemBytes, stream>>>(ta, tb, tc[0], tc[1], tin, s, ep, err);
+    kern<<<grid, 64 + 32 * Epi::kWarps, Cfg::kSmemBytes, stream>>>(ta, tb, tc[0], tc[1], tin, cs, s, ep, err);
     return check_launch(name);
 }
 
 // launch_gemm with the tile width chosen by pick_bn among `Allowed`.
-template <typename ElemT, bool A_MN, bool B_MN, class Epi, unsigned Allowed>
+template <typename ElemT, bool A_MN, bool B_MN, class Epi, unsigned Allowed, int kChunk = kChunkNone>
 tpce_status launch_gemm_auto(const char *name, const Operand &a, const Operand &b, const OutView *outs,
                              const OutView *ins, int M, int N, int K, int a_off_mn, int a_off_k, int b_off_mn,
-                             int b_off_k, const typename Epi::Params &ep, cudaStream_t stream, int b_gate_off = 0) {
+                             int b_off_k, const typename Epi::Params &ep, cudaStream_t stream, int b_gate_off = 0,
+                             const Chunks *chunks = nullptr) {
     static_assert(!Epi::kGated || (Allowed & kBN192) == 0, "gated tiles are 128 or 256 wide");
     if constexpr (TPCE_PAIR_BN != 0 && std::is_same<ElemT, __nv_bfloat16>::value && Epi::kWarps == 4) {
-        return launch_gemm_pair<TPCE_PAIR_BN, A_MN, B_MN, Epi>(name, a, b, outs, ins, M, N, K, a_off_mn, a_off_k,
-                                                              b_off_mn, b_off_k, ep, stream, true, b_gate_off);
+        return launch_gemm_pair<TPCE_PAIR_BN, A_MN, B_MN, Epi, kChunk>(name, a, b, outs, ins, M, N, K, a_off_mn,
+                                                                      a_off_k, b_off_mn, b_off_k, ep, stream, true,
+                                                                      b_gate_off, chunks);
     } else {
         const int sms = num_sms();
         if (sms <= 0) return fail(TPCE_ERR_CUDA, "device query failed (%s)", name);
@@ -243,18 +316,21 @@ tpce_status launch_gemm_auto(const char *name, const Operand &a, const Operand &
         const int bn = pick_bn(M, Epi::kGated ? 2 * static_cast<int64_t>(N) : N, sms, allowed);
         if constexpr ((Allowed & kBN256) != 0) {
             if (bn == 256)
-                return launch_gemm<ElemT, 256, A_MN, B_MN, Epi>(name, a, b, outs, ins, M, N, K, a_off_mn, a_off_k,
-                                                               b_off_mn, b_off_k, ep, stream, true, b_gate_off);
+                return launch_gemm<ElemT, 256, A_MN, B_MN, Epi, kChunk>(name, a, b, outs, ins, M, N, K, a_off_mn,
+                                                                       a_off_k, b_off_mn, b_off_k, ep, stream, true,
+                                                                       b_gate_off, chunks);
         }
         if constexpr ((Allowed & kBN192) != 0) {
             if (bn == 192)
-                return launch_gemm<ElemT, 192, A_MN, B_MN, Epi>(name, a, b, outs, ins, M, N, K, a_off_mn, a_off_k,
-                                                               b_off_mn, b_off_k, ep, stream, true, b_gate_off);
+                return launch_gemm<ElemT, 192, A_MN, B_MN, Epi, kChunk>(name, a, b, outs, ins, M, N, K, a_off_mn,
+                                                                       a_off_k, b_off_mn, b_off_k, ep, stream, true,
+                                                                       b_gate_off, chunks);
         }
         if constexpr ((Allowed & kBN128) != 0) {
             if (bn == 128)
-                return launch_gemm<ElemT, 128, A_MN, B_MN, Epi>(name, a, b, outs, ins, M, N, K, a_off_mn, a_off_k,
-                                                               b_off_mn, b_off_k, ep, stream, true, b_gate_off);
+                return launch_gemm<ElemT, 128, A_MN, B_MN, Epi, kChunk>(name, a, b, outs, ins, M, N, K, a_off_mn,
+                                                                       a_off_k, b_off_mn, b_off_k, ep, stream, true,
+                                                                       b_gate_off, chunks);
         }
         return fail(TPCE_ERR_SHAPE, "no tile width for %s", name);
     }

@@ -37,12 +37,12 @@ struct PairCfg {
     static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024 + kBarrierBytes;
 };
 
-template <int BN, bool A_MN, bool B_MN, class Epi>
+template <int BN, bool A_MN, bool B_MN, class Epi, int kChunk>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarps, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
-                        const __grid_constant__ CUtensorMap tmIn, const GemmShape shp,
-                        const typename Epi::Params ep, uint32_t *err) {
+                        const __grid_constant__ CUtensorMap tmIn, const __grid_constant__ ChunkSet<kChunk> cs,
+                        const GemmShape shp, const typename Epi::Params ep, uint32_t *err) {
     using C = PairCfg<BN, Epi>;
     using ET = ElemTraits<__nv_bfloat16>;
     static_assert(Epi::kWarps == 4, "pair epilogue: one warp per TMEM lane quarter");
@@ -55,6 +55,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
     constexpr int kChunks = kTileN / 32;
     constexpr int kOuts = Epi::kOuts;
     static_assert(!Epi::kGated || BN % 128 == 0, "gated tiles: halves of whole 64-wide blocks");
+    static_assert(!(Epi::kGated && kChunk == kChunkB), "gated tiles read an unchunked B");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -89,6 +90,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmB);
+        if constexpr (kChunk == kChunkA || kChunk == kChunkB) prefetch_chunk_maps(cs);
+    }
+    if constexpr (kChunk == kChunkC) {
+        if (warp == 2 && lane == 0) prefetch_chunk_maps(cs);
     }
     if (warp == 1) {
         ptx::tmem_alloc_pair(tmem_slot, C::kTmemCols);
@@ -120,6 +125,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
                 // the gate columns, the odd CTA the same columns of the up half
                 const int nh0 = Epi::kGated ? nb * kTileN + static_cast<int>(rank) * shp.b_gate_off
                                             : nb * BN + static_cast<int>(rank) * kHalfN;
+                ChunkCursor<kChunk> cur;
+                if constexpr (kChunk == kChunkA) cur.init(cs, A_MN ? shp.a_off_k : m0 + shp.a_off_mn);
+                if constexpr (kChunk == kChunkB) cur.init(cs, B_MN ? shp.b_off_k : nh0 + shp.b_off_mn);
                 for (int kb = 0; kb < shp.k_blocks; ++kb) {
                     if (!ptx::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, 1)) break;
                     const uint32_t bar = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
@@ -129,21 +137,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
                     uint8_t *sa = smem + stage * C::kStageBytes;
                     uint8_t *sb = sa + C::kABytes;
                     const int k0 = kb * kBK;
+                    // outer coordinates: A's M (K-major) or K (MN-major), likewise B's N or K
+                    int ya = A_MN ? k0 + shp.a_off_k : m0 + shp.a_off_mn;
+                    int yb = B_MN ? k0 + shp.b_off_k : nh0 + shp.b_off_mn;
+                    const CUtensorMap *ma = &tmA;
+                    const CUtensorMap *mb = &tmB;
+                    if constexpr (kChunk == kChunkA) {
+                        ma = cur.map;
+                        ya = cur.y;
+                    }
+                    if constexpr (kChunk == kChunkB) {
+                        mb = cur.map;
+                        yb = cur.y;
+                    }
+                    if constexpr ((kChunk == kChunkA && A_MN) || (kChunk == kChunkB && B_MN)) cur.advance(cs, kBK);
                     if (!A_MN) {
-                        ptx::tma_load_2d_pair(sa, &tmA, bar, k0 + shp.a_off_k, m0 + shp.a_off_mn);
+                        ptx::tma_load_2d_pair(sa, ma, bar, k0 + shp.a_off_k, ya);
                     } else {
 #pragma unroll
                         for (int j = 0; j < kBM / 64; ++j)
-                            ptx::tma_load_2d_pair(sa + j * kMnBlockBytes, &tmA, bar, m0 + shp.a_off_mn + 64 * j,
-                                                  k0 + shp.a_off_k);
+                            ptx::tma_load_2d_pair(sa + j * kMnBlockBytes, ma, bar, m0 + shp.a_off_mn + 64 * j, ya);
                     }
                     if (!B_MN) {
-                        ptx::tma_load_2d_pair(sb, &tmB, bar, k0 + shp.b_off_k, nh0 + shp.b_off_mn);
+                        ptx::tma_load_2d_pair(sb, mb, bar, k0 + shp.b_off_k, yb);
                     } else {
 #pragma unroll
                         for (int j = 0; j < kHalfN / 64; ++j)
-                            ptx::tma_load_2d_pair(sb + j * kMnBlockBytes, &tmB, bar, nh0 + shp.b_off_mn + 64 * j,
-                                                  k0 + shp.b_off_k);
+                            ptx::tma_load_2d_pair(sb + j * kMnBlockBytes, mb, bar, nh0 + shp.b_off_mn + 64 * j, yb);
                     }
                     if (++stage == S) {
                         stage = 0;
@@ -216,8 +236,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
-            if (!epi_tile<Epi>(ep, shp, taddr, BN / 2, row0, n0, 0, kChunks, lane, w, &tmC0, &tmC1, &tmIn, abort_flag,
-                               err))
+            if (!epi_tile<Epi, kChunk>(ep, shp, taddr, BN / 2, row0, n0, 0, kChunks, lane, w, &tmC0, &tmC1, &tmIn,
+                                       &cs, abort_flag, err))
                 break;
             ptx::tc_fence_before();
             __syncwarp();

@@ -49,6 +49,11 @@ tpce_status f32_to_bf16(const float *in, void *out, int64_t n, cudaStream_t s);
 size_t colsum_partial_floats(int64_t R, int64_t N);
 tpce_status colsum(int dt, const void *X, int64_t R, int64_t N, int64_t ld, float *out, float *partial,
                    cudaStream_t s);
+// The same over rows split into `count` buffers of `rows` rows each (row
+// pitch ld): the column sums of their concatenation. count <= kMaxRowChunks.
+constexpr int kMaxRowChunks = 16;
+tpce_status colsum_chunks(int dt, const void *const *chunks, int count, int64_t rows, int64_t N, int64_t ld,
+                          float *out, float *partial, cudaStream_t s);
 
 // out[c, r] = in[r, c] for an fp32 [R, C] matrix (row pitches ld_in, ld_out).
 tpce_status transpose_f32(const float *in, int64_t R, int64_t C, int64_t ld_in, float *out, int64_t ld_out,

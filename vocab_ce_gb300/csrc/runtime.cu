@@ -202,12 +202,30 @@ __device__ __forceinline__ void add8(const float *p, float *acc) {
     acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
 }
 
+// Row addressing of the column sum's input: one [R, N] matrix with row pitch
+// ld, or its rows split over sequence-chunk buffers of `rows` rows each.
+template <typename T>
+struct DenseRows {
+    const T *X;
+    int64_t ld;
+    __device__ const T *row(int64_t r) const { return X + r * ld; }
+};
+template <typename T>
+struct ChunkedRows {
+    const T *p[kMaxRowChunks];
+    int64_t rows, ld;
+    __device__ const T *row(int64_t r) const {
+        const int64_t c = r / rows;
+        return p[c] + (r - c * rows) * ld;
+    }
+};
+
 // Stage 1: block (x, y) sums rows [y*rows_per, (y+1)*rows_per) of 256 columns
 // starting at 256*x; each lane owns 8 adjacent columns (one vector load per
 // row), the 8 warps stride over the rows, and shared memory combines the warps.
-template <typename T>
-__global__ void __launch_bounds__(256) colsum_stage1(const T *__restrict__ X, int64_t R, int64_t N, int64_t ld,
-                                                     int64_t rows_per, float *__restrict__ part) {
+template <typename T, class Rows>
+__global__ void __launch_bounds__(256) colsum_stage1(const Rows rows_of, int64_t R, int64_t N, int64_t rows_per,
+                                                     float *__restrict__ part) {
     __shared__ float red[8][256];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 256 + lane * 8;
@@ -215,7 +233,7 @@ __global__ void __launch_bounds__(256) colsum_stage1(const T *__restrict__ X, in
     const int64_t r1 = min(R, r0 + rows_per);
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (c0 < N) {
-        for (int64_t r = r0 + warp; r < r1; r += 8) add8(X + r * ld + c0, acc);
+        for (int64_t r = r0 + warp; r < r1; r += 8) add8(rows_of.row(r) + c0, acc);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) red[warp][lane * 8 + i] = acc[i];
@@ -252,8 +270,8 @@ static int colsum_splits(int64_t R, int64_t N) {
 
 size_t colsum_partial_floats(int64_t R, int64_t N) { return static_cast<size_t>(colsum_splits(R, N)) * N; }
 
-tpce_status colsum(int dt, const void *X, int64_t R, int64_t N, int64_t ld, float *out, float *partial,
-                   cudaStream_t s) {
+template <class Rows>
+static tpce_status colsum_impl(const Rows &rows_of, int64_t R, int64_t N, float *out, float *partial, cudaStream_t s) {
     if (N <= 0) return TPCE_OK;
     if (R <= 0) return cuda_status(cudaMemsetAsync(out, 0, sizeof(float) * N, s));
     const int S = colsum_splits(R, N);
@@ -261,11 +279,8 @@ tpce_status colsum(int dt, const void *X, int64_t R, int64_t N, int64_t ld, floa
     {
         KernelTimer t("colsum_stage1", s);
         dim3 grid(static_cast<unsigned>((N + 255) / 256), static_cast<unsigned>(S));
-        if (dt == 1)
-            colsum_stage1<float><<<grid, 256, 0, s>>>(static_cast<const float *>(X), R, N, ld, rows_per, partial);
-        else
-            colsum_stage1<__nv_bfloat16>
-                <<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(X), R, N, ld, rows_per, partial);
+        using T = typename std::remove_const<typename std::remove_pointer<decltype(rows_of.row(0))>::type>::type;
+        colsum_stage1<T, Rows><<<grid, 256, 0, s>>>(rows_of, R, N, rows_per, partial);
         if (check_launch("colsum_stage1") != TPCE_OK) return TPCE_ERR_CUDA;
     }
     {
@@ -274,6 +289,29 @@ tpce_status colsum(int dt, const void *X, int64_t R, int64_t N, int64_t ld, floa
         if (check_launch("colsum_stage2") != TPCE_OK) return TPCE_ERR_CUDA;
     }
     return TPCE_OK;
+}
+
+tpce_status colsum(int dt, const void *X, int64_t R, int64_t N, int64_t ld, float *out, float *partial,
+                   cudaStream_t s) {
+    if (dt == 1) return colsum_impl(DenseRows<float>{static_cast<const float *>(X), ld}, R, N, out, partial, s);
+    return colsum_impl(DenseRows<__nv_bfloat16>{static_cast<const __nv_bfloat16 *>(X), ld}, R, N, out, partial, s);
+}
+
+tpce_status colsum_chunks(int dt, const void *const *chunks, int count, int64_t rows, int64_t N, int64_t ld,
+                          float *out, float *partial, cudaStream_t s) {
+    if (count < 1 || count > kMaxRowChunks || rows < 1) return TPCE_ERR_INVALID;
+    if (dt == 1) {
+        ChunkedRows<float> c{};
+        for (int i = 0; i < count; ++i) c.p[i] = static_cast<const float *>(chunks[i]);
+        c.rows = rows;
+        c.ld = ld;
+        return colsum_impl(c, rows * count, N, out, partial, s);
+    }
+    ChunkedRows<__nv_bfloat16> c{};
+    for (int i = 0; i < count; ++i) c.p[i] = static_cast<const __nv_bfloat16 *>(chunks[i]);
+    c.rows = rows;
+    c.ld = ld;
+    return colsum_impl(c, rows * count, N, out, partial, s);
 }
 
 // ------------------------------------------------------------------ fp32 -> bf16

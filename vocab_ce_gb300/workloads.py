@@ -54,6 +54,7 @@ class Workload:
     act: str = "gelu"      # the MLP's nonlinearity: "gelu" or "swiglu"
     chain: bool = False    # the MLP's Z is the CE's H and the CE's dH the MLP's dZ
     ce_grads: bool = True  # False: the CE is the forward-only (evaluation) loss
+    sp: bool = False       # sequence-parallel entry/exit: X, Z, dZ, dX as t sequence chunks
     n_heads: int = 0       # attention projections: query heads (0: none in this workload)
     n_kv_heads: int = 0    # key/value heads (grouped-query attention)
     head_dim: int = 0
@@ -95,6 +96,8 @@ WORKLOADS: Dict[str, Workload] = {
 # and the 128,256-token loss forward only (evaluation)
 WORKLOADS["gpt8b_chain"] = dataclasses.replace(WORKLOADS["gpt8b"], name="gpt8b_chain", chain=True)
 WORKLOADS["ce128k_eval"] = dataclasses.replace(WORKLOADS["ce128k"], name="ce128k_eval", ce_grads=False)
+# the 70B MLP with sequence-parallel entry and exit (t = 8 chunks of 512 tokens)
+WORKLOADS["mlp70b_sp"] = dataclasses.replace(WORKLOADS["mlp70b"], name="mlp70b_sp", sp=True)
 
 # shard-count sweep over the 8.3B MLP shapes
 SWEEP_T = (1, 2, 4, 8, 16)
