@@ -300,6 +300,30 @@ tpce_status tp_linear_backward(const void *dY, const void *X, const void *W,
                                int dtype, void *dX, void *dW, float *db,
                                void *ws, size_t ws_bytes, void *stream);
 
+/* Sequence-parallel forms of the linear layers ("Mathematical Foundations ...",
+ * section "Sequence Parallelism"), with the chunk conventions of
+ * tp_mlp_forward_sp (host arrays of t device pointers, chunk r = rows
+ * [r T/t, (r+1) T/t), (T / t) % 128 == 0, t <= 16):
+ *   column-parallel entry: X as chunks (the GEMM reads the all-gathered X);
+ *     the backward writes dX as chunks (the f* sum reduce-scattered);
+ *   row-parallel exit: Y as chunks (the g sum reduce-scattered); the
+ *     backward reads the gathered dY from its chunks.
+ * Results are the rows of the dense calls' results. */
+tpce_status tp_column_linear_forward_sp(const void *const *X_chunks, const void *W, const float *b,
+                                        int64_t T, int64_t n_in, int64_t n_out, int t, int dtype,
+                                        void *Y, void *ws, size_t ws_bytes, void *stream);
+tpce_status tp_column_linear_backward_sp(const void *dY, const void *const *X_chunks, const void *W,
+                                         int64_t T, int64_t n_in, int64_t n_out, int t, int dtype,
+                                         void *const *dX_chunks, void *dW, float *db,
+                                         void *ws, size_t ws_bytes, void *stream);
+tpce_status tp_row_linear_forward_sp(const void *X, const void *W, const float *b,
+                                     int64_t T, int64_t n_in, int64_t n_out, int t, int dtype,
+                                     void *const *Y_chunks, void *ws, size_t ws_bytes, void *stream);
+tpce_status tp_row_linear_backward_sp(const void *const *dY_chunks, const void *X, const void *W,
+                                      int64_t T, int64_t n_in, int64_t n_out, int t, int dtype,
+                                      void *dX, void *dW, float *db,
+                                      void *ws, size_t ws_bytes, void *stream);
+
 /* ---------------------------------------------------------------------------
  * Attention projections ("Distributed tensor parallelism ...", section "The
  * Multi-Head Attention Block"; "Mathematical Foundations ...", section
@@ -342,6 +366,27 @@ tpce_status tp_attn_out_backward(const void *dZ, const void *O, const void *Wo,
                                  int64_t T, int64_t h, int64_t n_heads, int64_t head_dim, int t,
                                  int dtype, void *dO, void *dWo, float *dbo,
                                  void *ws, size_t ws_bytes, void *stream);
+
+/* Sequence-parallel forms of the attention projections: the QKV projection
+ * is the column-parallel entry (X and dX as chunks), the output projection
+ * the row-parallel exit (Z and dZ as chunks); chunk rules as above. */
+tpce_status tp_attn_qkv_forward_sp(const void *const *X_chunks, const void *Wqkv, const float *bqkv,
+                                   int64_t T, int64_t h, int64_t n_heads, int64_t n_kv_heads,
+                                   int64_t head_dim, int t, int dtype, void *QKV,
+                                   void *ws, size_t ws_bytes, void *stream);
+tpce_status tp_attn_qkv_backward_sp(const void *dQKV, const void *const *X_chunks, const void *Wqkv,
+                                    int64_t T, int64_t h, int64_t n_heads, int64_t n_kv_heads,
+                                    int64_t head_dim, int t, int dtype,
+                                    void *const *dX_chunks, void *dWqkv, float *dbqkv,
+                                    void *ws, size_t ws_bytes, void *stream);
+tpce_status tp_attn_out_forward_sp(const void *O, const void *Wo, const float *bo,
+                                   int64_t T, int64_t h, int64_t n_heads, int64_t head_dim, int t,
+                                   int dtype, void *const *Z_chunks, void *ws, size_t ws_bytes,
+                                   void *stream);
+tpce_status tp_attn_out_backward_sp(const void *const *dZ_chunks, const void *O, const void *Wo,
+                                    int64_t T, int64_t h, int64_t n_heads, int64_t head_dim, int t,
+                                    int dtype, void *dO, void *dWo, float *dbo,
+                                    void *ws, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
  * vocab_parallel_ce -- logit GEMM fused with softmax cross-entropy, the

@@ -202,6 +202,30 @@ def test_seq_parallel_validation(L):
     assert st == 1
 
 
+def test_linear_seq_parallel_validation(L):
+    import ctypes as C
+
+    def arr(ptrs):
+        return (C.c_void_p * len(ptrs))(*ptrs)
+    good = [1 << 20] * 4
+    # column entry: X chunks of 64 rows are not whole 128-row blocks
+    assert L.tp_column_linear_forward_sp(arr(good), FAKE, None, 256, 128, 256, 4, 0, FAKE, None, 0, None) == 2
+    assert L.tp_column_linear_forward_sp(arr(good[:3] + [0]), FAKE, None, 512, 128, 256, 4, 0, FAKE, None, 0,
+                                         None) == 1
+    assert L.tp_column_linear_forward_sp(arr(good), FAKE, None, 0, 128, 256, 4, 0, FAKE, None, 0, None) == 0
+    # row exit: a misaligned Y chunk
+    assert L.tp_row_linear_forward_sp(FAKE, FAKE, None, 512, 256, 128, 4, 0, arr(good[:3] + [(1 << 20) + 4]), None,
+                                      0, None) == 3
+    # backward without its workspace, after the chunk checks pass
+    assert L.tp_row_linear_backward_sp(arr(good), FAKE, FAKE, 512, 256, 128, 4, 0, FAKE, FAKE, None, None, 0,
+                                       None) == 4
+    assert L.tp_column_linear_backward_sp(FAKE, arr(good), FAKE, 512, 128, 256, 4, 0, arr(good), FAKE, None, None,
+                                          0, None) == 4
+    # attention: the head rules still apply
+    assert L.tp_attn_qkv_forward_sp(arr(good), FAKE, None, 512, 256, 8, 2, 64, 4, 0, FAKE, None, 0, None) == 2
+    assert L.tp_attn_out_forward_sp(FAKE, FAKE, None, 512, 256, 6, 64, 4, 0, arr(good), None, 0, None) == 2
+
+
 def test_ce_validation(L):
     def ce(T=64, h=64, vp=512, vv=500, t=2, ws=None, wsb=0, H=FAKE, tg=FAKE):
         return L.vocab_parallel_ce(H, FAKE, tg, T, h, vp, vv, t, 1.0, 0, FAKE, None, FAKE, FAKE, ws, wsb, None)

@@ -118,3 +118,80 @@ def test_seq_parallel_chunks_are_separate_buffers():
     for i in range(t):
         gap = out_pool[(2 * order[i] + 1) * rows:(2 * order[i] + 2) * rows]
         assert torch.all(gap == 7.0)
+
+
+LIN_SP_CASES = {
+    # name: (T, n_in, n_out, t, dtype)
+    # both partitions valid: n_out / t (column) and n_in / t (row) are whole 64-wide blocks
+    "bf16": (512, 512, 256, 4, "bf16"),
+    "bf16_wide": (1024, 512, 1024, 8, "bf16"),
+    "f32": (256, 128, 256, 2, "f32"),
+}
+
+
+@pytest.mark.parametrize("case", list(LIN_SP_CASES))
+def test_linear_seq_parallel_matches_oracle_and_dense(case):
+    dev = gpu_or_skip()
+    T, n_in, n_out, t, dtype = LIN_SP_CASES[case]
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    g = torch.Generator().manual_seed(77)
+    X = torch.randn(T, n_in, generator=g).to(dt)
+    Wc = (0.05 * torch.randn(n_in, n_out, generator=g)).to(dt)     # column-parallel: split n_out
+    Wr = (0.05 * torch.randn(n_in, n_out, generator=g)).to(dt)     # row-parallel: split n_in
+    b = (0.1 * torch.randn(n_out, generator=g)).float()
+    dY = torch.randn(T, n_out, generator=g).to(dt)
+    Xd, Wcd, Wrd, bd, dYd = (x.to(dev) for x in (X, Wc, Wr, b, dY))
+    rows = T // t
+    # column-parallel entry: X (and dX) as chunks
+    Yc = tp.tp_column_linear_forward_sp(_split(Xd, t), Wcd, t, bd)
+    gc = tp.tp_column_linear_backward_sp(dYd, _split(Xd, t), Wcd, t)
+    # row-parallel exit: Y (and dY) as chunks
+    Yr = tp.tp_row_linear_forward_sp(Xd, Wrd, t, bd)
+    gr = tp.tp_row_linear_backward_sp(_split(dYd, t), Xd, Wrd, t)
+    assert tp.device_status() == 0
+    assert_rel("column Y", Yc, oracle.linear_forward(X, Wc, b))
+    oc = oracle.linear_backward(X, Wc, dY)
+    assert_rel("column dX", torch.cat(gc["dX"]), oc["dX"])
+    assert_rel("column dW", gc["dW"], oc["dW"])
+    assert_rel("column db", gc["db"], oc["db"])
+    yr = oracle.linear_forward(X, Wr, b)
+    for r in range(t):
+        assert_rel(f"row Y[{r}]", Yr[r], yr[r * rows:(r + 1) * rows])
+    orr = oracle.linear_backward(X, Wr, dY)
+    for k in ("dX", "dW", "db"):
+        assert_rel(f"row {k}", gr[k], orr[k])
+    # bit for bit the dense calls
+    Yc_d = tp.tp_linear_forward(Xd, Wcd, t, "column", bd)
+    gc_d = tp.tp_linear_backward(dYd, Xd, Wcd, t, "column")
+    Yr_d = tp.tp_linear_forward(Xd, Wrd, t, "row", bd)
+    gr_d = tp.tp_linear_backward(dYd, Xd, Wrd, t, "row")
+    assert torch.equal(Yc, Yc_d) and torch.equal(torch.cat(Yr), Yr_d)
+    assert torch.equal(torch.cat(gc["dX"]), gc_d["dX"])
+    for k in ("dW", "db"):
+        assert torch.equal(gc[k], gc_d[k]) and torch.equal(gr[k], gr_d[k]), k
+    assert torch.equal(gr["dX"], gr_d["dX"])
+
+
+def test_attention_projections_seq_parallel():
+    dev = gpu_or_skip()
+    T, h, nq, nkv, d, t = 512, 256, 8, 4, 64, 4
+    w = wl.custom("sp_attn", T=T, h=h, f=0, v_valid=0, v_pad=0, t=t, n_heads=nq, n_kv_heads=nkv, head_dim=d)
+    ai = wl.attn_inputs(w, seed=0)
+    g = {k: v.to(dev) for k, v in ai.items()}
+    qkv = tp.tp_attn_qkv_forward_sp(_split(g["X"], t), g["Wqkv"], nq, nkv, d, t, g["bqkv"])
+    gq = tp.tp_attn_qkv_backward_sp(g["dQKV"], _split(g["X"], t), g["Wqkv"], nq, nkv, d, t)
+    zc = tp.tp_attn_out_forward_sp(g["O"], g["Wo"], nq, d, t, g["bo"])
+    go = tp.tp_attn_out_backward_sp(_split(g["dZ"], t), g["O"], g["Wo"], nq, d, t)
+    assert tp.device_status() == 0
+    assert_rel("QKV", qkv, oracle.linear_forward(ai["X"], ai["Wqkv"], ai["bqkv"]))
+    ob = oracle.linear_backward(ai["X"], ai["Wqkv"], ai["dQKV"])
+    assert_rel("dX", torch.cat(gq["dX"]), ob["dX"])
+    assert_rel("dWqkv", gq["dWqkv"], ob["dW"])
+    assert_rel("Z", torch.cat(zc), oracle.linear_forward(ai["O"], ai["Wo"], ai["bo"]))
+    oo = oracle.linear_backward(ai["O"], ai["Wo"], ai["dZ"])
+    assert_rel("dO", go["dO"], oo["dX"])
+    assert_rel("dWo", go["dWo"], oo["dW"])
+    assert_rel("dbo", go["dbo"], oo["db"])
+    # the dense calls give the same bits
+    assert torch.equal(qkv, tp.tp_attn_qkv_forward(g["X"], g["Wqkv"], nq, nkv, d, t, g["bqkv"]))
+    assert torch.equal(torch.cat(zc), tp.tp_attn_out_forward(g["O"], g["Wo"], nq, d, t, g["bo"]))

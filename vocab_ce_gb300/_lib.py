@@ -57,6 +57,14 @@ SIGNATURES = {
     "tp_swiglu_forward_sp": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "tp_swiglu_backward_sp": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I,
                                    _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "tp_column_linear_forward_sp": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _I, _P, _P, _SZ, _P]),
+    "tp_column_linear_backward_sp": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "tp_row_linear_forward_sp": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _I, _P, _P, _SZ, _P]),
+    "tp_row_linear_backward_sp": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "tp_attn_qkv_forward_sp": (_I, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I, _I, _P, _P, _SZ, _P]),
+    "tp_attn_qkv_backward_sp": (_I, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "tp_attn_out_forward_sp": (_I, [_P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _P, _P, _SZ, _P]),
+    "tp_attn_out_backward_sp": (_I, [_P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "vocab_parallel_ce": (_I, [_P, _P, _P, _I64, _I64, _I64, _I64, _I, _F, _I,
                                _P, _P, _P, _P, _P, _SZ, _P]),
     "vocab_parallel_ce_loss_static": (_I, [_P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _P, _P, _P]),

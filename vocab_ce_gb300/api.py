@@ -455,6 +455,199 @@ def tp_attn_out_backward(dZ: torch.Tensor, O: torch.Tensor, Wo: torch.Tensor, n_
     return res
 
 
+def _chunk_list(out, key, t, rows, cols, dt, dev):
+    xs = out.get(key) if out else None
+    if xs is None:
+        xs = [torch.empty((rows, cols), dtype=dt, device=dev) for _ in range(t)]
+    if isinstance(xs, torch.Tensor):
+        raise ValueError(f"out['{key}'] must be a list of t sequence-chunk tensors")
+    _chunks(xs, key, t, rows, cols, dt, dev)
+    return xs
+
+
+def _wsz(T, n_in, n_out, t, parallel, dt, dev, ws, need):
+    w = _workspace(linear_workspace_bytes(T, n_in, n_out, t, parallel, dt) if need else 0, dev, ws)
+    return w, (0 if w is None else w.numel() * w.element_size())
+
+
+def tp_column_linear_forward_sp(X_chunks, W: torch.Tensor, t: int, b: Optional[torch.Tensor] = None,
+                                out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                                stream=None) -> torch.Tensor:
+    """Y = X W + b, column-parallel, X given as t sequence chunks (the all-gather entry)."""
+    rows, n_in = X_chunks[0].shape
+    T, n_out = rows * t, W.shape[1]
+    dt, dev = X_chunks[0].dtype, X_chunks[0].device
+    _chunks(X_chunks, "X_chunks", t, rows, n_in, dt, dev)
+    _need(W, "W", dt, (n_in, n_out))
+    if b is not None:
+        _need(b, "b", torch.float32, (n_out,))
+    Y = out if out is not None else torch.empty((T, n_out), dtype=dt, device=dev)
+    w, wb = _wsz(T, n_in, n_out, t, "column", dt, dev, ws, dt == torch.float32 and T > 0)
+    xp = _ptr_list(X_chunks)
+    check(lib().tp_column_linear_forward_sp(xp, _ptr(W), _ptr(b), T, n_in, n_out, t, _DT[dt], _ptr(Y), _ptr(w), wb,
+                                            _stream(stream)), "tp_column_linear_forward_sp")
+    return Y
+
+
+def tp_column_linear_backward_sp(dY: torch.Tensor, X_chunks, W: torch.Tensor, t: int, bias_grad: bool = True,
+                                 out=None, ws: Optional[torch.Tensor] = None, stream=None) -> Dict[str, object]:
+    """dX as t sequence chunks (the f* sum reduce-scattered), dW, db."""
+    rows, n_in = X_chunks[0].shape
+    T, n_out = rows * t, W.shape[1]
+    dt, dev = X_chunks[0].dtype, X_chunks[0].device
+    _chunks(X_chunks, "X_chunks", t, rows, n_in, dt, dev)
+    _need(dY, "dY", dt, (T, n_out))
+    _need(W, "W", dt, (n_in, n_out))
+    out = dict(out or {})
+    dXc = _chunk_list(out, "dX", t, rows, n_in, dt, dev)
+    dW = out.get("dW") if out.get("dW") is not None else torch.empty((n_in, n_out), dtype=dt, device=dev)
+    db = (out.get("db") if out.get("db") is not None else torch.empty(n_out, dtype=torch.float32, device=dev)) \
+        if bias_grad else None
+    w, wb = _wsz(T, n_in, n_out, t, "column", dt, dev, ws, T > 0)
+    xp, dxp = _ptr_list(X_chunks), _ptr_list(dXc)
+    check(lib().tp_column_linear_backward_sp(_ptr(dY), xp, _ptr(W), T, n_in, n_out, t, _DT[dt], dxp, _ptr(dW),
+                                             _ptr(db), _ptr(w), wb, _stream(stream)), "tp_column_linear_backward_sp")
+    res = {"dX": dXc, "dW": dW}
+    if bias_grad:
+        res["db"] = db
+    return res
+
+
+def tp_row_linear_forward_sp(X: torch.Tensor, W: torch.Tensor, t: int, b: Optional[torch.Tensor] = None,
+                             out=None, ws: Optional[torch.Tensor] = None, stream=None):
+    """Y = sum_i X_i W_i + b, row-parallel, Y returned as t sequence chunks (the reduce-scatter exit)."""
+    T, n_in = X.shape
+    n_out = W.shape[1]
+    dt, dev = X.dtype, X.device
+    _need(X, "X", dt, (T, n_in))
+    _need(W, "W", dt, (n_in, n_out))
+    if b is not None:
+        _need(b, "b", torch.float32, (n_out,))
+    if T % t:
+        raise ValueError("T must divide by t")
+    Yc = _chunk_list({"Y": out} if out is not None else None, "Y", t, T // t, n_out, dt, dev)
+    w, wb = _wsz(T, n_in, n_out, t, "row", dt, dev, ws, dt == torch.float32 and T > 0)
+    yp = _ptr_list(Yc)
+    check(lib().tp_row_linear_forward_sp(_ptr(X), _ptr(W), _ptr(b), T, n_in, n_out, t, _DT[dt], yp, _ptr(w), wb,
+                                         _stream(stream)), "tp_row_linear_forward_sp")
+    return Yc
+
+
+def tp_row_linear_backward_sp(dY_chunks, X: torch.Tensor, W: torch.Tensor, t: int, bias_grad: bool = True, out=None,
+                              ws: Optional[torch.Tensor] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """dX (each shard's columns), dW, db from the gathered dY chunks."""
+    T, n_in = X.shape
+    n_out = W.shape[1]
+    dt, dev = X.dtype, X.device
+    _need(X, "X", dt, (T, n_in))
+    _need(W, "W", dt, (n_in, n_out))
+    _chunks(dY_chunks, "dY_chunks", t, T // t, n_out, dt, dev)
+    out = dict(out or {})
+    dX = out.get("dX") if out.get("dX") is not None else torch.empty((T, n_in), dtype=dt, device=dev)
+    dW = out.get("dW") if out.get("dW") is not None else torch.empty((n_in, n_out), dtype=dt, device=dev)
+    db = (out.get("db") if out.get("db") is not None else torch.empty(n_out, dtype=torch.float32, device=dev)) \
+        if bias_grad else None
+    w, wb = _wsz(T, n_in, n_out, t, "row", dt, dev, ws, T > 0)
+    dyp = _ptr_list(dY_chunks)
+    check(lib().tp_row_linear_backward_sp(dyp, _ptr(X), _ptr(W), T, n_in, n_out, t, _DT[dt], _ptr(dX), _ptr(dW),
+                                          _ptr(db), _ptr(w), wb, _stream(stream)), "tp_row_linear_backward_sp")
+    res = {"dX": dX, "dW": dW}
+    if bias_grad:
+        res["db"] = db
+    return res
+
+
+def tp_attn_qkv_forward_sp(X_chunks, Wqkv: torch.Tensor, n_heads: int, n_kv_heads: int, head_dim: int, t: int,
+                           bqkv: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                           ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """QKV projection with the sequence-parallel entry: X as t sequence chunks."""
+    rows, h = X_chunks[0].shape
+    T, n = rows * t, (n_heads + 2 * n_kv_heads) * head_dim
+    dt, dev = X_chunks[0].dtype, X_chunks[0].device
+    _chunks(X_chunks, "X_chunks", t, rows, h, dt, dev)
+    _need(Wqkv, "Wqkv", dt, (h, n))
+    if bqkv is not None:
+        _need(bqkv, "bqkv", torch.float32, (n,))
+    QKV = out if out is not None else torch.empty((T, n), dtype=dt, device=dev)
+    w, wb = _wsz(T, h, n, t, "column", dt, dev, ws, dt == torch.float32 and T > 0)
+    xp = _ptr_list(X_chunks)
+    check(lib().tp_attn_qkv_forward_sp(xp, _ptr(Wqkv), _ptr(bqkv), T, h, n_heads, n_kv_heads, head_dim, t, _DT[dt],
+                                       _ptr(QKV), _ptr(w), wb, _stream(stream)), "tp_attn_qkv_forward_sp")
+    return QKV
+
+
+def tp_attn_qkv_backward_sp(dQKV: torch.Tensor, X_chunks, Wqkv: torch.Tensor, n_heads: int, n_kv_heads: int,
+                            head_dim: int, t: int, bias_grad: bool = True, out=None,
+                            ws: Optional[torch.Tensor] = None, stream=None) -> Dict[str, object]:
+    """dX as t sequence chunks, dWqkv, dbqkv."""
+    rows, h = X_chunks[0].shape
+    T, n = rows * t, (n_heads + 2 * n_kv_heads) * head_dim
+    dt, dev = X_chunks[0].dtype, X_chunks[0].device
+    _chunks(X_chunks, "X_chunks", t, rows, h, dt, dev)
+    _need(dQKV, "dQKV", dt, (T, n))
+    _need(Wqkv, "Wqkv", dt, (h, n))
+    out = dict(out or {})
+    dXc = _chunk_list(out, "dX", t, rows, h, dt, dev)
+    dW = out.get("dWqkv") if out.get("dWqkv") is not None else torch.empty((h, n), dtype=dt, device=dev)
+    db = (out.get("dbqkv") if out.get("dbqkv") is not None else torch.empty(n, dtype=torch.float32, device=dev)) \
+        if bias_grad else None
+    w, wb = _wsz(T, h, n, t, "column", dt, dev, ws, T > 0)
+    xp, dxp = _ptr_list(X_chunks), _ptr_list(dXc)
+    check(lib().tp_attn_qkv_backward_sp(_ptr(dQKV), xp, _ptr(Wqkv), T, h, n_heads, n_kv_heads, head_dim, t, _DT[dt],
+                                        dxp, _ptr(dW), _ptr(db), _ptr(w), wb, _stream(stream)),
+          "tp_attn_qkv_backward_sp")
+    res = {"dX": dXc, "dWqkv": dW}
+    if bias_grad:
+        res["dbqkv"] = db
+    return res
+
+
+def tp_attn_out_forward_sp(O: torch.Tensor, Wo: torch.Tensor, n_heads: int, head_dim: int, t: int,
+                           bo: Optional[torch.Tensor] = None, out=None, ws: Optional[torch.Tensor] = None,
+                           stream=None):
+    """Output projection with the sequence-parallel exit: Z as t sequence chunks."""
+    T, hq = O.shape
+    h = Wo.shape[1]
+    dt, dev = O.dtype, O.device
+    _need(O, "O", dt, (T, n_heads * head_dim))
+    _need(Wo, "Wo", dt, (hq, h))
+    if bo is not None:
+        _need(bo, "bo", torch.float32, (h,))
+    if T % t:
+        raise ValueError("T must divide by t")
+    Zc = _chunk_list({"Z": out} if out is not None else None, "Z", t, T // t, h, dt, dev)
+    w, wb = _wsz(T, hq, h, t, "row", dt, dev, ws, dt == torch.float32 and T > 0)
+    zp = _ptr_list(Zc)
+    check(lib().tp_attn_out_forward_sp(_ptr(O), _ptr(Wo), _ptr(bo), T, h, n_heads, head_dim, t, _DT[dt], zp, _ptr(w),
+                                       wb, _stream(stream)), "tp_attn_out_forward_sp")
+    return Zc
+
+
+def tp_attn_out_backward_sp(dZ_chunks, O: torch.Tensor, Wo: torch.Tensor, n_heads: int, head_dim: int, t: int,
+                            bias_grad: bool = True, out=None, ws: Optional[torch.Tensor] = None,
+                            stream=None) -> Dict[str, torch.Tensor]:
+    """dO, dWo, dbo from the gathered dZ chunks."""
+    T, hq = O.shape
+    h = Wo.shape[1]
+    dt, dev = O.dtype, O.device
+    _need(O, "O", dt, (T, n_heads * head_dim))
+    _need(Wo, "Wo", dt, (hq, h))
+    _chunks(dZ_chunks, "dZ_chunks", t, T // t, h, dt, dev)
+    out = dict(out or {})
+    dO = out.get("dO") if out.get("dO") is not None else torch.empty((T, hq), dtype=dt, device=dev)
+    dW = out.get("dWo") if out.get("dWo") is not None else torch.empty((hq, h), dtype=dt, device=dev)
+    db = (out.get("dbo") if out.get("dbo") is not None else torch.empty(h, dtype=torch.float32, device=dev)) \
+        if bias_grad else None
+    w, wb = _wsz(T, hq, h, t, "row", dt, dev, ws, T > 0)
+    dzp = _ptr_list(dZ_chunks)
+    check(lib().tp_attn_out_backward_sp(dzp, _ptr(O), _ptr(Wo), T, h, n_heads, head_dim, t, _DT[dt], _ptr(dO),
+                                        _ptr(dW), _ptr(db), _ptr(w), wb, _stream(stream)), "tp_attn_out_backward_sp")
+    res = {"dO": dO, "dWo": dW}
+    if bias_grad:
+        res["dbo"] = db
+    return res
+
+
 def vocab_parallel_ce(H: torch.Tensor, E: torch.Tensor, targets: torch.Tensor, v_valid: int, t: int,
                       grad_scale: float = 1.0, grads: bool = True, want_dH: bool = True, want_dE: bool = True,
                       out: Optional[Dict[str, torch.Tensor]] = None, ws: Optional[torch.Tensor] = None,

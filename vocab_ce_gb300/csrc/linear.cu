@@ -21,6 +21,12 @@
 // On one GPU both are the same three GEMMs; the mode sets the validation and
 // the kernel names.
 //
+// Sequence parallelism ("Mathematical Foundations ...", section "Sequence
+// Parallelism"): the column-parallel entry reads the all-gathered X from t
+// per-rank sequence chunks (and writes dX back into chunks); the
+// row-parallel exit writes each shard-summed row of Y into the chunk that
+// owns it (and reads the gathered dY from chunks in the backward).
+//
 // Attention: the fused QKV projection is column-parallel by heads (its
 // columns grouped by key/value head, so that a contiguous split gives each
 // shard whole heads: for each KV head g, the query heads sharing it, then K_g,
@@ -89,30 +95,100 @@ T *at(void *ws, size_t off) {
     return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off);
 }
 
+// Sequence-chunked activations of one call (null members: dense tensors).
+// Column-parallel entry: x (the X chunks) and out (dX chunks, backward).
+// Row-parallel exit: out (the Y chunks, forward) and dy (dY chunks, backward).
+struct LinSP {
+    const Chunks *x;
+    const Chunks *dy;
+    const Chunks *out;
+};
+
+// Y = X W (+ b) on the bf16 path, with X or Y chunked as sp says.
+template <typename ElemT>
+tpce_status gemm_fwd(const char *name, const Operand &a, const Operand &bw, const OutView *o, int Ti, int oi, int ii,
+                     const float *b, cudaStream_t s, const LinSP *sp) {
+    constexpr bool kBf = std::is_same<ElemT, __nv_bfloat16>::value;
+    if constexpr (kBf) {
+        if (sp && sp->x)
+            return launch_gemm_auto<ElemT, false, true, EpiStore<ElemT>, kBN192 | kBN256, kChunkA>(
+                name, a, bw, o, nullptr, Ti, oi, ii, 0, 0, 0, 0, {b}, s, 0, sp->x);
+        if (sp && sp->out)
+            return launch_gemm_auto<ElemT, false, true, EpiStore<ElemT>, kBN192 | kBN256, kChunkC>(
+                name, a, bw, o, nullptr, Ti, oi, ii, 0, 0, 0, 0, {b}, s, 0, sp->out);
+        return launch_gemm_auto<ElemT, false, true, EpiStore<ElemT>, kBN192 | kBN256>(name, a, bw, o, nullptr, Ti, oi, ii,
+                                                                                   0, 0, 0, 0, {b}, s);
+    } else {
+        if (sp && sp->x)
+            return launch_gemm<float, 128, false, false, EpiStore<float>, kChunkA>(name, a, bw, o, nullptr, Ti, oi, ii, 0,
+                                                                                   0, 0, 0, {b}, s, true, 0, sp->x);
+        if (sp && sp->out)
+            return launch_gemm<float, 128, false, false, EpiStore<float>, kChunkC>(name, a, bw, o, nullptr, Ti, oi, ii, 0,
+                                                                                   0, 0, 0, {b}, s, true, 0, sp->out);
+        return launch_gemm<float, 128, false, false, EpiStore<float>>(name, a, bw, o, nullptr, Ti, oi, ii, 0, 0, 0, 0,
+                                                                      {b}, s);
+    }
+}
+
+// dX = dY W^T, with dY (row exit) or dX (column entry) chunked as sp says.
+template <typename ElemT>
+tpce_status gemm_dx(const char *name, const Operand &a, const Operand &bw, const OutView *o, int Ti, int ii, int oi,
+                    cudaStream_t s, const LinSP *sp) {
+    constexpr bool kBf = std::is_same<ElemT, __nv_bfloat16>::value;
+    if constexpr (kBf) {
+        if (sp && sp->dy)
+            return launch_gemm_auto<ElemT, false, false, EpiStore<ElemT>, kBN192 | kBN256, kChunkA>(
+                name, a, bw, o, nullptr, Ti, ii, oi, 0, 0, 0, 0, {nullptr}, s, 0, sp->dy);
+        if (sp && sp->out)
+            return launch_gemm_auto<ElemT, false, false, EpiStore<ElemT>, kBN192 | kBN256, kChunkC>(
+                name, a, bw, o, nullptr, Ti, ii, oi, 0, 0, 0, 0, {nullptr}, s, 0, sp->out);
+        return launch_gemm_auto<ElemT, false, false, EpiStore<ElemT>, kBN192 | kBN256>(name, a, bw, o, nullptr, Ti, ii,
+                                                                                    oi, 0, 0, 0, 0, {nullptr}, s);
+    } else {
+        if (sp && sp->dy)
+            return launch_gemm<float, 128, false, false, EpiStore<float>, kChunkA>(name, a, bw, o, nullptr, Ti, ii, oi, 0,
+                                                                                   0, 0, 0, {nullptr}, s, true, 0, sp->dy);
+        if (sp && sp->out)
+            return launch_gemm<float, 128, false, false, EpiStore<float>, kChunkC>(
+                name, a, bw, o, nullptr, Ti, ii, oi, 0, 0, 0, 0, {nullptr}, s, true, 0, sp->out);
+        return launch_gemm<float, 128, false, false, EpiStore<float>>(name, a, bw, o, nullptr, Ti, ii, oi, 0, 0, 0, 0,
+                                                                      {nullptr}, s);
+    }
+}
+
+// The transpose of a [T, C] fp32 activation into out [C, Tp], from one buffer
+// or from its sequence chunks (one column block of out per chunk).
+tpce_status transpose_rows(const float *in, const Chunks *ch, int64_t T, int64_t C, float *out, int64_t Tp,
+                           cudaStream_t s) {
+    if (!ch) return transpose_f32(in, T, C, C, out, Tp, s);
+    for (int c = 0; c < ch->count; ++c) {
+        tpce_status st = transpose_f32(static_cast<const float *>(ch->ptrs[c]), ch->rows, C, C, out + c * ch->rows, Tp, s);
+        if (st != TPCE_OK) return st;
+    }
+    return TPCE_OK;
+}
+
 tpce_status forward_impl(const LinearNames &nm, const void *X, const void *W, const float *b, int64_t T, int64_t n_in,
-                         int64_t n_out, int dtype, void *Y, void *ws, const LinWs &L, cudaStream_t s) {
+                         int64_t n_out, int dtype, void *Y, void *ws, const LinWs &L, cudaStream_t s,
+                         const LinSP *sp) {
     const int Ti = static_cast<int>(T), ii = static_cast<int>(n_in), oi = static_cast<int>(n_out);
+    const OutView o[1] = {{Y, T, n_out, n_out}};
     if (dtype == TPCE_BF16) {
-        using bf = __nv_bfloat16;
         Operand a{X, T, n_in, n_in};      // K-major [T, n_in]
         Operand bw{W, n_in, n_out, n_out};  // MN-major: K = n_in rows, N = n_out columns
-        const OutView o[1] = {{Y, T, n_out, n_out}};
-        return launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256>(nm.fwd, a, bw, o, nullptr, Ti, oi, ii,
-                                                                                 0, 0, 0, 0, {b}, s);
+        return gemm_fwd<__nv_bfloat16>(nm.fwd, a, bw, o, Ti, oi, ii, b, s, sp);
     }
     float *Wt = at<float>(ws, L.Wt);
     tpce_status st = transpose_f32(static_cast<const float *>(W), n_in, n_out, n_out, Wt, n_in, s);  // W^T
     if (st != TPCE_OK) return st;
     Operand a{X, T, n_in, n_in};       // K-major [T, n_in]
     Operand bw{Wt, n_out, n_in, n_in};  // K-major: N = n_out rows, K = n_in columns
-    const OutView o[1] = {{Y, T, n_out, n_out}};
-    return launch_gemm<float, 128, false, false, EpiStore<float>>(nm.fwd, a, bw, o, nullptr, Ti, oi, ii, 0, 0, 0, 0,
-                                                                  {b}, s);
+    return gemm_fwd<float>(nm.fwd, a, bw, o, Ti, oi, ii, b, s, sp);
 }
 
 tpce_status backward_impl(const LinearNames &nm, const void *dY, const void *X, const void *W, int64_t T, int64_t n_in,
                           int64_t n_out, int dtype, void *dX, void *dW, float *db, void *ws, const LinWs &L,
-                          cudaStream_t s) {
+                          cudaStream_t s, const LinSP *sp) {
     const int Ti = static_cast<int>(T), ii = static_cast<int>(n_in), oi = static_cast<int>(n_out);
     float *partial = at<float>(ws, L.partial);
     tpce_status st;
@@ -123,20 +199,30 @@ tpce_status backward_impl(const LinearNames &nm, const void *dY, const void *X, 
             Operand a{dY, T, n_out, n_out};   // K-major [T, n_out]
             Operand bw{W, n_in, n_out, n_out};  // K-major: N = n_in rows, K = n_out columns
             const OutView o[1] = {{dX, T, n_in, n_in}};
-            st = launch_gemm_auto<bf, false, false, EpiStore<bf>, kBN192 | kBN256>(nm.dX, a, bw, o, nullptr, Ti, ii, oi,
-                                                                                    0, 0, 0, 0, {nullptr}, s);
-            if (st != TPCE_OK) return st;
+            if ((st = gemm_dx<bf>(nm.dX, a, bw, o, Ti, ii, oi, s, sp)) != TPCE_OK) return st;
         }
         // dW = X^T dY (each shard's own block of W)
         {
             Operand a{X, T, n_in, n_in};     // MN-major: K = T rows, M = n_in columns
             Operand bw{dY, T, n_out, n_out};  // MN-major: K = T rows, N = n_out columns
             const OutView o[1] = {{dW, n_in, n_out, n_out}};
-            st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>(nm.dW, a, bw, o, nullptr, ii, oi, Ti, 0,
-                                                                                  0, 0, 0, {nullptr}, s);
+            if (sp && sp->x)
+                st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256, kChunkA>(
+                    nm.dW, a, bw, o, nullptr, ii, oi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, sp->x);
+            else if (sp && sp->dy)
+                st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256, kChunkB>(
+                    nm.dW, a, bw, o, nullptr, ii, oi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, sp->dy);
+            else
+                st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>(nm.dW, a, bw, o, nullptr, ii, oi,
+                                                                                      Ti, 0, 0, 0, 0, {nullptr}, s);
             if (st != TPCE_OK) return st;
         }
-        if (db && (st = colsum(0, dY, T, n_out, n_out, db, partial, s)) != TPCE_OK) return st;
+        if (db) {
+            st = (sp && sp->dy) ? colsum_chunks(0, sp->dy->ptrs, sp->dy->count, sp->dy->rows, n_out, n_out, db,
+                                                partial, s)
+                                : colsum(0, dY, T, n_out, n_out, db, partial, s);
+            if (st != TPCE_OK) return st;
+        }
         return TPCE_OK;
     }
     const int64_t Tp = pad4(T);
@@ -145,12 +231,12 @@ tpce_status backward_impl(const LinearNames &nm, const void *dY, const void *X, 
         Operand a{dY, T, n_out, n_out};   // K-major [T, n_out]
         Operand bw{W, n_in, n_out, n_out};  // K-major: N = n_in rows, K = n_out columns
         const OutView o[1] = {{dX, T, n_in, n_in}};
-        st = launch_gemm<float, 128, false, false, EpiStore<float>>(nm.dX, a, bw, o, nullptr, Ti, ii, oi, 0, 0, 0, 0,
-                                                                    {nullptr}, s);
-        if (st != TPCE_OK) return st;
+        if ((st = gemm_dx<float>(nm.dX, a, bw, o, Ti, ii, oi, s, sp)) != TPCE_OK) return st;
     }
-    if ((st = transpose_f32(static_cast<const float *>(X), T, n_in, n_in, Xt, Tp, s)) != TPCE_OK) return st;
-    if ((st = transpose_f32(static_cast<const float *>(dY), T, n_out, n_out, dYt, Tp, s)) != TPCE_OK) return st;
+    st = transpose_rows(static_cast<const float *>(X), sp ? sp->x : nullptr, T, n_in, Xt, Tp, s);
+    if (st != TPCE_OK) return st;
+    st = transpose_rows(static_cast<const float *>(dY), sp ? sp->dy : nullptr, T, n_out, dYt, Tp, s);
+    if (st != TPCE_OK) return st;
     {
         Operand a{Xt, n_in, T, Tp};    // K-major: M = n_in rows, K = T columns
         Operand bw{dYt, n_out, T, Tp};  // K-major: N = n_out rows, K = T columns
@@ -159,32 +245,39 @@ tpce_status backward_impl(const LinearNames &nm, const void *dY, const void *X, 
                                                                     {nullptr}, s);
         if (st != TPCE_OK) return st;
     }
-    if (db && (st = colsum(1, dY, T, n_out, n_out, db, partial, s)) != TPCE_OK) return st;
+    if (db) {
+        st = (sp && sp->dy) ? colsum_chunks(1, sp->dy->ptrs, sp->dy->count, sp->dy->rows, n_out, n_out, db, partial, s)
+                            : colsum(1, dY, T, n_out, n_out, db, partial, s);
+        if (st != TPCE_OK) return st;
+    }
     return TPCE_OK;
 }
 
+// With sp, the chunked activations are given there (already validated) and
+// the matching dense pointers are unused.
 tpce_status linear_forward(const LinearNames &nm, const void *X, const void *W, const float *b, int64_t T,
                            int64_t n_in, int64_t n_out, int t, int parallel, int dtype, void *Y, void *ws,
-                           size_t ws_bytes, void *stream) {
+                           size_t ws_bytes, void *stream, const LinSP *sp = nullptr) {
     tpce_status st = check_linear_shape(T, n_in, n_out, t, parallel, dtype);
     if (st != TPCE_OK) return st;
     if (T == 0) return TPCE_OK;  // no tokens: nothing to compute (token tensors may be NULL)
-    if (!X || !W || !Y) return TPCE_ERR_INVALID;
+    if (!W || (!X && !(sp && sp->x)) || (!Y && !(sp && sp->out))) return TPCE_ERR_INVALID;
     for (const void *p : {X, W, static_cast<const void *>(b), static_cast<const void *>(Y),
                           static_cast<const void *>(ws)})
         if (!aligned16(p)) return TPCE_ERR_ALIGN;
     const LinWs L = lin_ws_layout(T, n_in, n_out, dtype);
     if (dtype == TPCE_F32 && (!ws || ws_bytes < L.total)) return TPCE_ERR_WORKSPACE;
-    return forward_impl(nm, X, W, b, T, n_in, n_out, dtype, Y, ws, L, static_cast<cudaStream_t>(stream));
+    return forward_impl(nm, X, W, b, T, n_in, n_out, dtype, Y, ws, L, static_cast<cudaStream_t>(stream), sp);
 }
 
 tpce_status linear_backward(const LinearNames &nm, const void *dY, const void *X, const void *W, int64_t T,
                             int64_t n_in, int64_t n_out, int t, int parallel, int dtype, void *dX, void *dW, float *db,
-                            void *ws, size_t ws_bytes, void *stream) {
+                            void *ws, size_t ws_bytes, void *stream, const LinSP *sp = nullptr) {
     tpce_status st = check_linear_shape(T, n_in, n_out, t, parallel, dtype);
     if (st != TPCE_OK) return st;
     if (!W || !dW) return TPCE_ERR_INVALID;
-    if (T > 0 && (!dY || !X || !dX)) return TPCE_ERR_INVALID;
+    if (T > 0 && ((!dY && !(sp && sp->dy)) || (!X && !(sp && sp->x)) || (!dX && !(sp && sp->out))))
+        return TPCE_ERR_INVALID;
     for (const void *p : {dY, X, W, static_cast<const void *>(dX), static_cast<const void *>(dW),
                           static_cast<const void *>(db), static_cast<const void *>(ws)})
         if (!aligned16(p)) return TPCE_ERR_ALIGN;
@@ -198,7 +291,77 @@ tpce_status linear_backward(const LinearNames &nm, const void *dY, const void *X
     }
     const LinWs L = lin_ws_layout(T, n_in, n_out, dtype);
     if (!ws || ws_bytes < L.total) return TPCE_ERR_WORKSPACE;
-    return backward_impl(nm, dY, X, W, T, n_in, n_out, dtype, dX, dW, db, ws, L, s);
+    return backward_impl(nm, dY, X, W, T, n_in, n_out, dtype, dX, dW, db, ws, L, s, sp);
+}
+
+// Sequence chunks of a [T, C] activation: t buffers of T/t rows (whole
+// 128-row tile blocks), 16-byte aligned.
+tpce_status check_chunks(const void *const *p, int64_t T, int t, Chunks &c) {
+    if (!p) return TPCE_ERR_INVALID;
+    if (t < 1 || t > kMaxChunks || T % t != 0 || (T / t) % 128 != 0) return TPCE_ERR_SHAPE;
+    for (int i = 0; i < t; ++i) {
+        if (!p[i]) return TPCE_ERR_INVALID;
+        if (!aligned16(p[i])) return TPCE_ERR_ALIGN;
+    }
+    c = Chunks{p, T / t, t};
+    return TPCE_OK;
+}
+
+// The sequence-parallel forms: the column-parallel entry (X chunks in; dX
+// chunks out of the backward) and the row-parallel exit (Y chunks out; dY
+// chunks into the backward).
+tpce_status column_forward_sp(const LinearNames &nm, const void *const *X_chunks, const void *W, const float *b,
+                              int64_t T, int64_t n_in, int64_t n_out, int t, int dtype, void *Y, void *ws,
+                              size_t ws_bytes, void *stream) {
+    tpce_status st = check_linear_shape(T, n_in, n_out, t, TPCE_COLUMN_PARALLEL, dtype);
+    if (st != TPCE_OK || T == 0) return st;
+    Chunks xc{};
+    if ((st = check_chunks(X_chunks, T, t, xc)) != TPCE_OK) return st;
+    const LinSP sp{&xc, nullptr, nullptr};
+    return linear_forward(nm, nullptr, W, b, T, n_in, n_out, t, TPCE_COLUMN_PARALLEL, dtype, Y, ws, ws_bytes, stream,
+                          &sp);
+}
+
+tpce_status column_backward_sp(const LinearNames &nm, const void *dY, const void *const *X_chunks, const void *W,
+                               int64_t T, int64_t n_in, int64_t n_out, int t, int dtype, void *const *dX_chunks,
+                               void *dW, float *db, void *ws, size_t ws_bytes, void *stream) {
+    tpce_status st = check_linear_shape(T, n_in, n_out, t, TPCE_COLUMN_PARALLEL, dtype);
+    if (st != TPCE_OK) return st;
+    if (T == 0)
+        return linear_backward(nm, nullptr, nullptr, W, 0, n_in, n_out, t, TPCE_COLUMN_PARALLEL, dtype, nullptr, dW, db,
+                               ws, ws_bytes, stream);
+    Chunks xc{}, dxc{};
+    if ((st = check_chunks(X_chunks, T, t, xc)) != TPCE_OK) return st;
+    if ((st = check_chunks(reinterpret_cast<const void *const *>(dX_chunks), T, t, dxc)) != TPCE_OK) return st;
+    const LinSP sp{&xc, nullptr, &dxc};
+    return linear_backward(nm, dY, nullptr, W, T, n_in, n_out, t, TPCE_COLUMN_PARALLEL, dtype, nullptr, dW, db, ws,
+                           ws_bytes, stream, &sp);
+}
+
+tpce_status row_forward_sp(const LinearNames &nm, const void *X, const void *W, const float *b, int64_t T, int64_t n_in,
+                           int64_t n_out, int t, int dtype, void *const *Y_chunks, void *ws, size_t ws_bytes,
+                           void *stream) {
+    tpce_status st = check_linear_shape(T, n_in, n_out, t, TPCE_ROW_PARALLEL, dtype);
+    if (st != TPCE_OK || T == 0) return st;
+    Chunks yc{};
+    if ((st = check_chunks(reinterpret_cast<const void *const *>(Y_chunks), T, t, yc)) != TPCE_OK) return st;
+    const LinSP sp{nullptr, nullptr, &yc};
+    return linear_forward(nm, X, W, b, T, n_in, n_out, t, TPCE_ROW_PARALLEL, dtype, nullptr, ws, ws_bytes, stream, &sp);
+}
+
+tpce_status row_backward_sp(const LinearNames &nm, const void *const *dY_chunks, const void *X, const void *W,
+                            int64_t T, int64_t n_in, int64_t n_out, int t, int dtype, void *dX, void *dW, float *db,
+                            void *ws, size_t ws_bytes, void *stream) {
+    tpce_status st = check_linear_shape(T, n_in, n_out, t, TPCE_ROW_PARALLEL, dtype);
+    if (st != TPCE_OK) return st;
+    if (T == 0)
+        return linear_backward(nm, nullptr, nullptr, W, 0, n_in, n_out, t, TPCE_ROW_PARALLEL, dtype, nullptr, dW, db,
+                               ws, ws_bytes, stream);
+    Chunks dyc{};
+    if ((st = check_chunks(dY_chunks, T, t, dyc)) != TPCE_OK) return st;
+    const LinSP sp{nullptr, &dyc, nullptr};
+    return linear_backward(nm, nullptr, X, W, T, n_in, n_out, t, TPCE_ROW_PARALLEL, dtype, dX, dW, db, ws, ws_bytes,
+                           stream, &sp);
 }
 
 const LinearNames kColumnNames{"linear_column_fwd", "linear_column_bwd_dX_shard_sum", "linear_column_bwd_dW"};
@@ -290,4 +453,68 @@ extern "C" tpce_status tp_attn_out_backward(const void *dZ, const void *O, const
         return TPCE_ERR_SHAPE;
     return linear_backward(kOutNames, dZ, O, Wo, T, n_heads * head_dim, h, t, TPCE_ROW_PARALLEL, dtype, dO, dWo, dbo,
                            ws, ws_bytes, stream);
+}
+
+extern "C" tpce_status tp_column_linear_forward_sp(const void *const *X_chunks, const void *W, const float *b,
+                                                   int64_t T, int64_t n_in, int64_t n_out, int t, int dtype, void *Y,
+                                                   void *ws, size_t ws_bytes, void *stream) {
+    return column_forward_sp(kColumnNames, X_chunks, W, b, T, n_in, n_out, t, dtype, Y, ws, ws_bytes, stream);
+}
+
+extern "C" tpce_status tp_column_linear_backward_sp(const void *dY, const void *const *X_chunks, const void *W,
+                                                    int64_t T, int64_t n_in, int64_t n_out, int t, int dtype,
+                                                    void *const *dX_chunks, void *dW, float *db, void *ws,
+                                                    size_t ws_bytes, void *stream) {
+    return column_backward_sp(kColumnNames, dY, X_chunks, W, T, n_in, n_out, t, dtype, dX_chunks, dW, db, ws, ws_bytes,
+                              stream);
+}
+
+extern "C" tpce_status tp_row_linear_forward_sp(const void *X, const void *W, const float *b, int64_t T, int64_t n_in,
+                                                int64_t n_out, int t, int dtype, void *const *Y_chunks, void *ws,
+                                                size_t ws_bytes, void *stream) {
+    return row_forward_sp(kRowNames, X, W, b, T, n_in, n_out, t, dtype, Y_chunks, ws, ws_bytes, stream);
+}
+
+extern "C" tpce_status tp_row_linear_backward_sp(const void *const *dY_chunks, const void *X, const void *W, int64_t T,
+                                                 int64_t n_in, int64_t n_out, int t, int dtype, void *dX, void *dW,
+                                                 float *db, void *ws, size_t ws_bytes, void *stream) {
+    return row_backward_sp(kRowNames, dY_chunks, X, W, T, n_in, n_out, t, dtype, dX, dW, db, ws, ws_bytes, stream);
+}
+
+extern "C" tpce_status tp_attn_qkv_forward_sp(const void *const *X_chunks, const void *Wqkv, const float *bqkv,
+                                              int64_t T, int64_t h, int64_t n_heads, int64_t n_kv_heads,
+                                              int64_t head_dim, int t, int dtype, void *QKV, void *ws, size_t ws_bytes,
+                                              void *stream) {
+    tpce_status st = check_heads(n_heads, n_kv_heads, head_dim, t);
+    if (st != TPCE_OK) return st;
+    return column_forward_sp(kQkvNames, X_chunks, Wqkv, bqkv, T, h, (n_heads + 2 * n_kv_heads) * head_dim, t, dtype,
+                             QKV, ws, ws_bytes, stream);
+}
+
+extern "C" tpce_status tp_attn_qkv_backward_sp(const void *dQKV, const void *const *X_chunks, const void *Wqkv,
+                                               int64_t T, int64_t h, int64_t n_heads, int64_t n_kv_heads,
+                                               int64_t head_dim, int t, int dtype, void *const *dX_chunks,
+                                               void *dWqkv, float *dbqkv, void *ws, size_t ws_bytes, void *stream) {
+    tpce_status st = check_heads(n_heads, n_kv_heads, head_dim, t);
+    if (st != TPCE_OK) return st;
+    return column_backward_sp(kQkvNames, dQKV, X_chunks, Wqkv, T, h, (n_heads + 2 * n_kv_heads) * head_dim, t, dtype,
+                              dX_chunks, dWqkv, dbqkv, ws, ws_bytes, stream);
+}
+
+extern "C" tpce_status tp_attn_out_forward_sp(const void *O, const void *Wo, const float *bo, int64_t T, int64_t h,
+                                              int64_t n_heads, int64_t head_dim, int t, int dtype,
+                                              void *const *Z_chunks, void *ws, size_t ws_bytes, void *stream) {
+    if (n_heads < 1 || head_dim < 8 || head_dim % 8 != 0 || n_heads % t != 0 || n_heads > kMaxDim / head_dim)
+        return TPCE_ERR_SHAPE;
+    return row_forward_sp(kOutNames, O, Wo, bo, T, n_heads * head_dim, h, t, dtype, Z_chunks, ws, ws_bytes, stream);
+}
+
+extern "C" tpce_status tp_attn_out_backward_sp(const void *const *dZ_chunks, const void *O, const void *Wo, int64_t T,
+                                               int64_t h, int64_t n_heads, int64_t head_dim, int t, int dtype,
+                                               void *dO, void *dWo, float *dbo, void *ws, size_t ws_bytes,
+                                               void *stream) {
+    if (n_heads < 1 || head_dim < 8 || head_dim % 8 != 0 || n_heads % t != 0 || n_heads > kMaxDim / head_dim)
+        return TPCE_ERR_SHAPE;
+    return row_backward_sp(kOutNames, dZ_chunks, O, Wo, T, n_heads * head_dim, h, t, dtype, dO, dWo, dbo, ws, ws_bytes,
+                           stream);
 }
