@@ -139,7 +139,7 @@ tpce_status ce_forward(const CeArgs &a, const CeWs &L, void *ws, float *lse_buf,
     KernelTimer timer("ce_combine", s);
     ce_combine_kernel<<<static_cast<unsigned>((a.T + 255) / 256), 256, 0, s>>>(
         stats, tau, a.targets, a.T, a.t, static_cast<int>(L.n_tiles / a.t), vvi, a.loss, lse_buf, err);
-    return check_launch("ce_combine");
+    return check_launch("ce_combine", s);
 }
 
 tpce_status ce_backward_bf16(const CeArgs &a, const CeWs &L, void *ws, const float *lse_buf, cudaStream_t s) {

@@ -111,5 +111,5 @@ extern "C" tpce_status vocab_parallel_ce_loss_static(const void *H, const void *
     if (st != TPCE_OK) return st;
     ce_combine_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, s>>>(
         stats, tau, targets, T, t, static_cast<int>(n_tiles / t), vvi, loss, lse_buf, err);
-    return check_launch("ce_static_combine");
+    return check_launch("ce_static_combine", s);
 }

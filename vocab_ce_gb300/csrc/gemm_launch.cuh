@@ -211,7 +211,7 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
     const int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
     KernelTimer timer(timed ? name : nullptr, stream);
     kern<<<grid, 64 + 32 * Epi::kWarps, Cfg::kSmemBytes, stream>>>(ta, tb, tc[0], tc[1], tin, cs, s, ep, err);
-    return check_launch(name);
+    return check_launch(name, stream);
 }
 
 // The CTA-pair kernel (bf16 operands): a 256 x BN tile per cluster of two CTAs.
@@ -294,7 +294,7 @@ tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &
     const int grid = 2 * static_cast<int>(std::min<int64_t>(tiles, sms / 2));
     KernelTimer timer(timed ? name : nullptr, stream);
     kern<<<grid, 64 + 32 * Epi::kWarps, Cfg::kSmemBytes, stream>>>(ta, tb, tc[0], tc[1], tin, cs, s, ep, err);
-    return check_launch(name);
+    return check_launch(name, stream);
 }
 
 // launch_gemm with the tile width chosen by pick_bn among `Allowed`.

@@ -69,10 +69,12 @@ inline tpce_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TPCE_O
 // and return `st`.
 tpce_status fail(tpce_status st, const char *fmt, ...);
 tpce_status fail_cuda(cudaError_t e, const char *what);
-// cudaGetLastError after a launch, recorded under the kernel's name
-tpce_status check_launch(const char *name);
+// cudaGetLastError after a launch on stream s, recorded under the kernel's name
+tpce_status check_launch(const char *name, cudaStream_t s);
 // when the environment sets TPCE_SYNC_CHECK=1, every launch is followed by a
-// stream synchronisation so that a failing kernel is named by check_launch
+// device synchronisation so that a failing kernel is named by check_launch --
+// except while s is being captured into a CUDA graph, where synchronising is
+// not allowed
 bool sync_check_enabled();
 
 }  // namespace tpce

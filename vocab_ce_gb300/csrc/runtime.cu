@@ -77,12 +77,13 @@ bool sync_check_enabled() {
     return on == 1;
 }
 
-tpce_status check_launch(const char *name) {
+tpce_status check_launch(const char *name, cudaStream_t s) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail_cuda(e, name);
     if (sync_check_enabled()) {
-        e = cudaDeviceSynchronize();
-        if (e != cudaSuccess) return fail_cuda(e, name);
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if ((e = cudaStreamIsCapturing(s, &cs)) != cudaSuccess) return fail_cuda(e, name);
+        if (cs == cudaStreamCaptureStatusNone && (e = cudaDeviceSynchronize()) != cudaSuccess) return fail_cuda(e, name);
     }
     return TPCE_OK;
 }
@@ -281,12 +282,12 @@ static tpce_status colsum_impl(const Rows &rows_of, int64_t R, int64_t N, float 
         dim3 grid(static_cast<unsigned>((N + 255) / 256), static_cast<unsigned>(S));
         using T = typename std::remove_const<typename std::remove_pointer<decltype(rows_of.row(0))>::type>::type;
         colsum_stage1<T, Rows><<<grid, 256, 0, s>>>(rows_of, R, N, rows_per, partial);
-        if (check_launch("colsum_stage1") != TPCE_OK) return TPCE_ERR_CUDA;
+        if (check_launch("colsum_stage1", s) != TPCE_OK) return TPCE_ERR_CUDA;
     }
     {
         KernelTimer t("colsum_stage2", s);
         colsum_stage2<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(partial, S, N, out);
-        if (check_launch("colsum_stage2") != TPCE_OK) return TPCE_ERR_CUDA;
+        if (check_launch("colsum_stage2", s) != TPCE_OK) return TPCE_ERR_CUDA;
     }
     return TPCE_OK;
 }
@@ -338,7 +339,7 @@ tpce_status f32_to_bf16(const float *in, void *out, int64_t n, cudaStream_t s) {
     KernelTimer t("f32_to_bf16", s);
     f32_to_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(reinterpret_cast<const float4 *>(in),
                                                                      static_cast<uint4 *>(out), n8);
-    return check_launch("f32_to_bf16");
+    return check_launch("f32_to_bf16", s);
 }
 
 // ------------------------------------------------------------------ transpose
@@ -366,7 +367,7 @@ tpce_status transpose_f32(const float *in, int64_t R, int64_t C, int64_t ld_in, 
     KernelTimer t("transpose_f32", s);
     dim3 grid(static_cast<unsigned>((C + 31) / 32), static_cast<unsigned>((R + 31) / 32));
     transpose_f32_kernel<<<grid, dim3(32, 8), 0, s>>>(in, R, C, ld_in, out, ld_out);
-    return check_launch("transpose_f32");
+    return check_launch("transpose_f32", s);
 }
 
 }  // namespace tpce
