@@ -276,10 +276,10 @@ class Step:
         if w.sp:
             xc = [mi[f"X{r}"] for r in range(w.t)]
             return tp.tp_mlp_forward_sp(xc, mi["A"], mi["B"], w.t, mi["bA"], mi["bB"],
-                                        out={"Z": self.zc, "U": self.fo["U"], "Y": self.fo["Y"]})
+                                        out={"Z": self.zc, "U": self.fo["U"], "Y": self.fo["Y"]}, ws=self.mws)
         if self.glu:
-            return tp.tp_swiglu_forward(mi["X"], mi["W1"], mi["W2"], w.t, mi["b1"], mi["b2"], out=self.fo)
-        return tp.tp_mlp_forward(mi["X"], mi["A"], mi["B"], w.t, mi["bA"], mi["bB"], out=self.fo)
+            return tp.tp_swiglu_forward(mi["X"], mi["W1"], mi["W2"], w.t, mi["b1"], mi["b2"], out=self.fo, ws=self.mws)
+        return tp.tp_mlp_forward(mi["X"], mi["A"], mi["B"], w.t, mi["bA"], mi["bB"], out=self.fo, ws=self.mws)
 
     def mlp_bwd(self, mi=None, dZ=None):
         mi = mi or self.mi
@@ -304,9 +304,9 @@ class Step:
         ai = ai or self.ai
         tp, w = self.tp, self.w
         nq, nkv, d = w.n_heads, w.n_kv_heads, w.head_dim
-        tp.tp_attn_qkv_forward(ai["X"], ai["Wqkv"], nq, nkv, d, w.t, ai["bqkv"], out=self.ao["QKV"])
+        tp.tp_attn_qkv_forward(ai["X"], ai["Wqkv"], nq, nkv, d, w.t, ai["bqkv"], out=self.ao["QKV"], ws=self.aws)
         tp.tp_attn_qkv_backward(ai["dQKV"], ai["X"], ai["Wqkv"], nq, nkv, d, w.t, out=self.aq, ws=self.aws)
-        tp.tp_attn_out_forward(ai["O"], ai["Wo"], nq, d, w.t, ai["bo"], out=self.ao["Z"])
+        tp.tp_attn_out_forward(ai["O"], ai["Wo"], nq, d, w.t, ai["bo"], out=self.ao["Z"], ws=self.aws)
         tp.tp_attn_out_backward(ai["dZ"], ai["O"], ai["Wo"], nq, d, w.t, out=self.ag, ws=self.aws)
 
     def ce(self, ci=None, H=None):

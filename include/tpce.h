@@ -119,6 +119,15 @@ int64_t tpce_pad_vocab(int64_t v, int t, int divisor);
  * accumulator for dH. Returns 0 for invalid shapes.
  * ------------------------------------------------------------------------- */
 size_t tpce_mlp_workspace_bytes(int64_t T, int64_t h, int64_t f, int t, int dtype);
+/* The optional workspace of the bf16 forward calls (tp_mlp_forward,
+ * tp_swiglu_forward, tp_linear_forward, the attention forwards and their
+ * sequence-parallel forms): with ws_bytes >= this, a GEMM whose last wave of
+ * tiles is short splits those tiles along K over the idle SMs (each part's
+ * fp32 partial written to the workspace, the last part summing them in part
+ * order); with ws NULL the GEMMs run unsplit. Results differ only by the fp32
+ * summation order of those tiles and are deterministic either way. Every
+ * workspace query below includes this region at the start. */
+size_t tpce_tail_workspace_bytes(void);
 /* (the MLP query covers both calls of one dtype; TPCE_F32 adds transposed
  * copies of A, B, Y, dZ, X and dU) */
 size_t tpce_ce_workspace_bytes(int64_t T, int64_t h, int64_t v_pad, int t, int dtype,

@@ -67,15 +67,19 @@ def test_vocab_padding_rule(L):
 
 def test_workspace_sizes(L):
     import vocab_ce_gb300 as tp
+    # every workspace starts with the GEMMs' split-tail scratch: at most 64
+    # K parts of one CTA pair's 256 x 256 fp32 tile, plus their tickets
+    tail = tp.tail_workspace_bytes()
+    assert tail == 64 * 2 * 128 * 256 * 4 + 4096
     # MLP backward holds dU [T, f] in bf16 plus a small column-sum buffer
     for T, h, f in ((32, 64, 256), (4096, 8192, 32768)):
-        b = tp.mlp_workspace_bytes(T, h, f, 8 if f % 512 == 0 else 2)
+        b = tp.mlp_workspace_bytes(T, h, f, 8 if f % 512 == 0 else 2) - tail
         assert b >= T * f * 2 and b < T * f * 2 + 64 * max(f, h) * 4 + 4096
     # CE: the forward keeps statistics only; the backward scratch stays far
     # below the T x v_pad logits (the logits are never materialised)
     T, h, vp, t = 16384, 8192, 129024, 8
-    fwd = tp.ce_workspace_bytes(T, h, vp, t, grads=False)
-    bwd = tp.ce_workspace_bytes(T, h, vp, t, grads=True)
+    fwd = tp.ce_workspace_bytes(T, h, vp, t, grads=False) - tail
+    bwd = tp.ce_workspace_bytes(T, h, vp, t, grads=True) - tail
     assert fwd < 0.02 * T * vp * 2
     # the dl scratch holds at most half the vocabulary and at most 1 GiB
     assert bwd <= 2 ** 30 + T * h * 4 + fwd + 4096
@@ -135,7 +139,7 @@ def test_swiglu_validation_and_workspace(L):
     assert st == 4
     # the backward holds [dG | dUp] [T, 2f] in bf16 plus a small column-sum buffer
     T, h, f = 4096, 8192, 28672
-    b = tp.swiglu_workspace_bytes(T, h, f, 8)
+    b = tp.swiglu_workspace_bytes(T, h, f, 8) - tp.tail_workspace_bytes()
     assert T * 2 * f * 2 <= b < T * 2 * f * 2 + 64 * 2 * f * 4 + 4096
     # fp32: transposed W1 [2f, h], W2, Y, dZ, X and [dG | dUp]
     T, h, f = 32, 64, 256

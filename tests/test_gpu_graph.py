@@ -33,7 +33,7 @@ def test_block_and_loss_replay_from_a_cuda_graph():
     cws = torch.empty(tp.ce_workspace_bytes(T, h, w.v_pad, w.t), dtype=torch.uint8, device=dev)
 
     def step():
-        tp.tp_mlp_forward(mi["X"], mi["A"], mi["B"], w.t, mi["bA"], mi["bB"], out=fo)
+        tp.tp_mlp_forward(mi["X"], mi["A"], mi["B"], w.t, mi["bA"], mi["bB"], out=fo, ws=mws)
         tp.tp_mlp_backward(mi["dZ"], mi["X"], mi["A"], mi["B"], fo["U"], fo["Y"], w.t, out=bo, ws=mws)
         tp.vocab_parallel_ce(ci["H"], ci["E"], ci["targets"], w.v_valid, w.t, grad_scale=1.0 / T, out=co, ws=cws)
 

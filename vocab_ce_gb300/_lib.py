@@ -35,6 +35,7 @@ SIGNATURES = {
     "tpce_last_error": (ctypes.c_char_p, []),
     "tpce_pad_vocab": (_I64, [_I64, _I, _I]),
     "tpce_mlp_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I, _I]),
+    "tpce_tail_workspace_bytes": (_SZ, []),
     "tpce_ce_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I, _I, _I]),
     "tp_mlp_forward": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "tp_mlp_backward": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I,

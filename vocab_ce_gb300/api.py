@@ -46,6 +46,21 @@ def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]) -> Optional[torc
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 
+def tail_workspace_bytes() -> int:
+    """Workspace with which the bf16 forward calls split a short last wave of tiles."""
+    return int(lib().tpce_tail_workspace_bytes())
+
+
+def _fwd_workspace(dt, T: int, full_bytes, dev, ws: Optional[torch.Tensor]) -> Optional[torch.Tensor]:
+    """The forward's workspace: required on the fp32 path (transposed operands),
+    optional on the bf16 path, where it lets short last waves of tiles split."""
+    if T == 0:
+        return None
+    if dt == torch.float32:
+        return _workspace(full_bytes(), dev, ws)
+    return _workspace(tail_workspace_bytes(), dev, ws)
+
+
 def pad_vocab(v: int, t: int, divisor: int = 128) -> int:
     """Smallest multiple of divisor * t that is >= v (Megatron's vocabulary padding)."""
     r = lib().tpce_pad_vocab(v, t, divisor)
@@ -79,9 +94,7 @@ def tp_mlp_forward(X: torch.Tensor, A: torch.Tensor, B: torch.Tensor, t: int,
     Z = out.get("Z") if out.get("Z") is not None else torch.empty((T, h), dtype=dt, device=X.device)
     U = out.get("U") if out.get("U") is not None else torch.empty((T, f), dtype=dt, device=X.device)
     Y = out.get("Y") if out.get("Y") is not None else torch.empty((T, f), dtype=dt, device=X.device)
-    w = None
-    if dt == torch.float32 and T > 0:  # the tf32 path stages transposed operands
-        w = _workspace(mlp_workspace_bytes(T, h, f, t, dt), X.device, ws)
+    w = _fwd_workspace(dt, T, lambda: mlp_workspace_bytes(T, h, f, t, dt), X.device, ws)
     st = lib().tp_mlp_forward(_ptr(X), _ptr(A), _ptr(bA), _ptr(B), _ptr(bB), T, h, f, t, _DT[dt],
                               _ptr(Z), _ptr(U), _ptr(Y), _ptr(w),
                               0 if w is None else w.numel() * w.element_size(), _stream(stream))
@@ -143,9 +156,7 @@ def tp_swiglu_forward(X: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, t: in
     Z = out.get("Z") if out.get("Z") is not None else torch.empty((T, h), dtype=dt, device=X.device)
     GU = out.get("GU") if out.get("GU") is not None else torch.empty((T, 2 * f), dtype=dt, device=X.device)
     Y = out.get("Y") if out.get("Y") is not None else torch.empty((T, f), dtype=dt, device=X.device)
-    w = None
-    if dt == torch.float32 and T > 0:  # the tf32 path stages transposed operands
-        w = _workspace(swiglu_workspace_bytes(T, h, f, t, dt), X.device, ws)
+    w = _fwd_workspace(dt, T, lambda: swiglu_workspace_bytes(T, h, f, t, dt), X.device, ws)
     st = lib().tp_swiglu_forward(_ptr(X), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), T, h, f, t, _DT[dt],
                                  _ptr(Z), _ptr(GU), _ptr(Y), _ptr(w),
                                  0 if w is None else w.numel() * w.element_size(), _stream(stream))
@@ -220,10 +231,8 @@ def _mlp_sp(glu, X_chunks, W1, W2, t, b1, b2, out, ws, stream):
     ukey = "GU" if glu else "U"
     U = out.get(ukey) if out.get(ukey) is not None else torch.empty((T, fw), dtype=dt, device=dev)
     Y = out.get("Y") if out.get("Y") is not None else torch.empty((T, f), dtype=dt, device=dev)
-    w = None
-    if dt == torch.float32 and T > 0:
-        q = swiglu_workspace_bytes if glu else mlp_workspace_bytes
-        w = _workspace(q(T, h, f, t, dt), dev, ws)
+    q = swiglu_workspace_bytes if glu else mlp_workspace_bytes
+    w = _fwd_workspace(dt, T, lambda: q(T, h, f, t, dt), dev, ws)
     xp, zp = _ptr_list(X_chunks), _ptr_list(Zc)
     fn = lib().tp_swiglu_forward_sp if glu else lib().tp_mlp_forward_sp
     st = fn(xp, _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), T, h, f, t, _DT[dt], zp, _ptr(U), _ptr(Y), _ptr(w),
@@ -321,9 +330,7 @@ def tp_linear_forward(X: torch.Tensor, W: torch.Tensor, t: int, parallel: str = 
     if b is not None:
         _need(b, "b", torch.float32, (n_out,))
     Y = out if out is not None else torch.empty((T, n_out), dtype=dt, device=X.device)
-    w = None
-    if dt == torch.float32 and T > 0:
-        w = _workspace(linear_workspace_bytes(T, n_in, n_out, t, parallel, dt), X.device, ws)
+    w = _fwd_workspace(dt, T, lambda: linear_workspace_bytes(T, n_in, n_out, t, parallel, dt), X.device, ws)
     st = lib().tp_linear_forward(_ptr(X), _ptr(W), _ptr(b), T, n_in, n_out, t, _PAR[parallel], _DT[dt], _ptr(Y),
                                  _ptr(w), _wsize(w), _stream(stream))
     check(st, "tp_linear_forward")
@@ -373,9 +380,7 @@ def tp_attn_qkv_forward(X: torch.Tensor, Wqkv: torch.Tensor, n_heads: int, n_kv_
     if bqkv is not None:
         _need(bqkv, "bqkv", torch.float32, (n,))
     QKV = out if out is not None else torch.empty((T, n), dtype=dt, device=X.device)
-    w = None
-    if dt == torch.float32 and T > 0:
-        w = _workspace(attn_workspace_bytes(T, h, n_heads, n_kv_heads, head_dim, t, dt), X.device, ws)
+    w = _fwd_workspace(dt, T, lambda: attn_workspace_bytes(T, h, n_heads, n_kv_heads, head_dim, t, dt), X.device, ws)
     st = lib().tp_attn_qkv_forward(_ptr(X), _ptr(Wqkv), _ptr(bqkv), T, h, n_heads, n_kv_heads, head_dim, t, _DT[dt],
                                    _ptr(QKV), _ptr(w), _wsize(w), _stream(stream))
     check(st, "tp_attn_qkv_forward")
@@ -420,9 +425,7 @@ def tp_attn_out_forward(O: torch.Tensor, Wo: torch.Tensor, n_heads: int, head_di
     if bo is not None:
         _need(bo, "bo", torch.float32, (h,))
     Z = out if out is not None else torch.empty((T, h), dtype=dt, device=O.device)
-    w = None
-    if dt == torch.float32 and T > 0:
-        w = _workspace(linear_workspace_bytes(T, hq, h, t, "row", dt), O.device, ws)
+    w = _fwd_workspace(dt, T, lambda: linear_workspace_bytes(T, hq, h, t, "row", dt), O.device, ws)
     st = lib().tp_attn_out_forward(_ptr(O), _ptr(Wo), _ptr(bo), T, h, n_heads, head_dim, t, _DT[dt], _ptr(Z),
                                    _ptr(w), _wsize(w), _stream(stream))
     check(st, "tp_attn_out_forward")
@@ -470,6 +473,11 @@ def _wsz(T, n_in, n_out, t, parallel, dt, dev, ws, need):
     return w, (0 if w is None else w.numel() * w.element_size())
 
 
+def _wsz_fwd(T, n_in, n_out, t, parallel, dt, dev, ws):
+    w = _fwd_workspace(dt, T, lambda: linear_workspace_bytes(T, n_in, n_out, t, parallel, dt), dev, ws)
+    return w, (0 if w is None else w.numel() * w.element_size())
+
+
 def tp_column_linear_forward_sp(X_chunks, W: torch.Tensor, t: int, b: Optional[torch.Tensor] = None,
                                 out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
                                 stream=None) -> torch.Tensor:
@@ -482,7 +490,7 @@ def tp_column_linear_forward_sp(X_chunks, W: torch.Tensor, t: int, b: Optional[t
     if b is not None:
         _need(b, "b", torch.float32, (n_out,))
     Y = out if out is not None else torch.empty((T, n_out), dtype=dt, device=dev)
-    w, wb = _wsz(T, n_in, n_out, t, "column", dt, dev, ws, dt == torch.float32 and T > 0)
+    w, wb = _wsz_fwd(T, n_in, n_out, t, "column", dt, dev, ws)
     xp = _ptr_list(X_chunks)
     check(lib().tp_column_linear_forward_sp(xp, _ptr(W), _ptr(b), T, n_in, n_out, t, _DT[dt], _ptr(Y), _ptr(w), wb,
                                             _stream(stream)), "tp_column_linear_forward_sp")
@@ -526,7 +534,7 @@ def tp_row_linear_forward_sp(X: torch.Tensor, W: torch.Tensor, t: int, b: Option
     if T % t:
         raise ValueError("T must divide by t")
     Yc = _chunk_list({"Y": out} if out is not None else None, "Y", t, T // t, n_out, dt, dev)
-    w, wb = _wsz(T, n_in, n_out, t, "row", dt, dev, ws, dt == torch.float32 and T > 0)
+    w, wb = _wsz_fwd(T, n_in, n_out, t, "row", dt, dev, ws)
     yp = _ptr_list(Yc)
     check(lib().tp_row_linear_forward_sp(_ptr(X), _ptr(W), _ptr(b), T, n_in, n_out, t, _DT[dt], yp, _ptr(w), wb,
                                          _stream(stream)), "tp_row_linear_forward_sp")
@@ -569,7 +577,7 @@ def tp_attn_qkv_forward_sp(X_chunks, Wqkv: torch.Tensor, n_heads: int, n_kv_head
     if bqkv is not None:
         _need(bqkv, "bqkv", torch.float32, (n,))
     QKV = out if out is not None else torch.empty((T, n), dtype=dt, device=dev)
-    w, wb = _wsz(T, h, n, t, "column", dt, dev, ws, dt == torch.float32 and T > 0)
+    w, wb = _wsz_fwd(T, h, n, t, "column", dt, dev, ws)
     xp = _ptr_list(X_chunks)
     check(lib().tp_attn_qkv_forward_sp(xp, _ptr(Wqkv), _ptr(bqkv), T, h, n_heads, n_kv_heads, head_dim, t, _DT[dt],
                                        _ptr(QKV), _ptr(w), wb, _stream(stream)), "tp_attn_qkv_forward_sp")
@@ -616,7 +624,7 @@ def tp_attn_out_forward_sp(O: torch.Tensor, Wo: torch.Tensor, n_heads: int, head
     if T % t:
         raise ValueError("T must divide by t")
     Zc = _chunk_list({"Z": out} if out is not None else None, "Z", t, T // t, h, dt, dev)
-    w, wb = _wsz(T, hq, h, t, "row", dt, dev, ws, dt == torch.float32 and T > 0)
+    w, wb = _wsz_fwd(T, hq, h, t, "row", dt, dev, ws)
     zp = _ptr_list(Zc)
     check(lib().tp_attn_out_forward_sp(_ptr(O), _ptr(Wo), _ptr(bo), T, h, n_heads, head_dim, t, _DT[dt], zp, _ptr(w),
                                        wb, _stream(stream)), "tp_attn_out_forward_sp")

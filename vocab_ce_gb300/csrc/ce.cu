@@ -45,7 +45,7 @@ struct CeWs {
     int64_t n_tiles;     // v_pad / bn
     int64_t vc;          // vocabulary chunk width of the backward
     int64_t chunks;      // v_pad / vc
-    size_t stats, tau, lse, dl, acc, Ht, Et, dlt, total;
+    size_t tail, stats, tau, lse, dl, acc, Ht, Et, dlt, total;
 };
 
 CeWs ce_ws_layout(int64_t T, int64_t h, int64_t v_pad, int t, bool grads, int dtype) {
@@ -75,6 +75,7 @@ CeWs ce_ws_layout(int64_t T, int64_t h, int64_t v_pad, int t, bool grads, int dt
         off = round_up(off + bytes, 256);
         return at;
     };
+    L.tail = take(kTailScratchBytes);  // the GEMMs' split tails
     L.stats = take(static_cast<size_t>(L.n_tiles) * T * sizeof(float2));
     L.tau = take(static_cast<size_t>(T) * sizeof(float));
     L.lse = take(static_cast<size_t>(T) * sizeof(float));
@@ -120,11 +121,12 @@ tpce_status ce_forward(const CeArgs &a, const CeWs &L, void *ws, float *lse_buf,
     Operand A{a.H, a.T, a.h, a.h};          // K-major [T, h]
     Operand B{a.E, a.v_pad, a.h, a.h};      // K-major: N = v_pad rows, K = h columns
     EpiCeStats::Params ep{stats, tau, a.targets, a.T, vvi, 0, 0, L.bn};
+    const TailScratch tail{at<uint8_t>(ws, L.tail), kTailScratchBytes};
     tpce_status st;
     if constexpr (std::is_same<ElemT, __nv_bfloat16>::value && TPCE_PAIR_BN == 256) {
         if (L.bn == 256)
             st = launch_gemm_pair<256, false, false, EpiCeStats>("ce_fwd_logits_stats", A, B, nullptr, nullptr, Ti, vpi, hi,
-                                                                 0, 0, 0, 0, ep, s);
+                                                                 0, 0, 0, 0, ep, s, true, 0, nullptr, &tail);
         else
             st = launch_gemm<ElemT, 128, false, false, EpiCeStats>("ce_fwd_logits_stats", A, B, nullptr, nullptr, Ti, vpi,
                                                                    hi, 0, 0, 0, 0, ep, s);
@@ -146,6 +148,7 @@ tpce_status ce_backward_bf16(const CeArgs &a, const CeWs &L, void *ws, const flo
     using bf = __nv_bfloat16;
     bf *dl = at<bf>(ws, L.dl);
     float *acc = at<float>(ws, L.acc);
+    const TailScratch tail{at<uint8_t>(ws, L.tail), kTailScratchBytes};
     const int Ti = static_cast<int>(a.T), hi = static_cast<int>(a.h), vci = static_cast<int>(L.vc);
     const int vvi = static_cast<int>(a.v_valid);
     for (int64_t c = 0; c < L.chunks; ++c) {
@@ -158,7 +161,7 @@ tpce_status ce_backward_bf16(const CeArgs &a, const CeWs &L, void *ws, const flo
             const OutView o[1] = {{dl, a.T, L.vc, L.vc}};
             typename EpiCeDlogits<bf>::Params ep{lse_buf, a.targets, a.grad_scale, vvi, n_base};
             st = launch_gemm_auto<bf, false, false, EpiCeDlogits<bf>, kBN192 | kBN256>(
-                "ce_bwd_logits_dl", A, B, o, nullptr, Ti, vci, hi, 0, 0, n_base, 0, ep, s);
+                "ce_bwd_logits_dl", A, B, o, nullptr, Ti, vci, hi, 0, 0, n_base, 0, ep, s, 0, nullptr, &tail);
             if (st != TPCE_OK) return st;
         }
         // dE rows of this chunk = dl^T H (no exchange: the rows belong to one shard)
@@ -167,7 +170,8 @@ tpce_status ce_backward_bf16(const CeArgs &a, const CeWs &L, void *ws, const flo
             Operand B{a.H, a.T, a.h, a.h};   // MN-major: K = T rows, N = h columns
             const OutView o[1] = {{static_cast<bf *>(a.dE) + static_cast<int64_t>(n_base) * a.h, L.vc, a.h, a.h}};
             st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>("ce_bwd_dE", A, B, o, nullptr, vci, hi, Ti,
-                                                                                  0, 0, 0, 0, {nullptr}, s);
+                                                                                  0, 0, 0, 0, {nullptr}, s, 0, nullptr,
+                                                                                  &tail);
             if (st != TPCE_OK) return st;
         }
         // dH += dl E_chunk: the sum over shards (and chunks), in fp32, stored by
@@ -177,7 +181,8 @@ tpce_status ce_backward_bf16(const CeArgs &a, const CeWs &L, void *ws, const flo
             Operand B{a.E, a.v_pad, a.h, a.h};  // MN-major: K = v rows (from n_base), N = h columns
             const OutView o[1] = {{acc, a.T, a.h, a.h}};
             st = launch_gemm_auto<bf, false, true, EpiF32Accumulate, kBN192 | kBN256>(
-                "ce_bwd_dH_shard_sum", A, B, o, nullptr, Ti, hi, vci, 0, 0, 0, n_base, {c == 0 ? 0 : 1}, s);
+                "ce_bwd_dH_shard_sum", A, B, o, nullptr, Ti, hi, vci, 0, 0, 0, n_base, {c == 0 ? 0 : 1}, s, 0,
+                nullptr, &tail);
             if (st != TPCE_OK) return st;
         }
     }

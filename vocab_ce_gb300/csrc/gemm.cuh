@@ -75,7 +75,32 @@ struct GemmShape {
     int a_off_mn, a_off_k;     // coordinate offsets of the A operand inside its tensor map
     int b_off_mn, b_off_k;     // same for B
     int b_gate_off;            // gated tiles: B column (or row) offset of the second half, else 0
+    // Split tail (CTA-pair kernel): the first full_units work units are whole
+    // tiles; each of the last tail_tiles tiles is split along K into `split`
+    // units whose fp32 partials meet in `partial`, counted by `tickets`.
+    int full_units;            // whole-tile units (all tiles when the tail is not split)
+    int split;                 // K parts per tail tile (1: no split)
+    int tail_tiles;            // tiles split
+    float *partial;            // [tail_tiles * split][2 CTAs][128 rows][BN] fp32
+    uint32_t *tickets;         // [tail_tiles][2 CTAs], zero at launch
 };
+
+// Work unit u: its tile, its K-block range, and its part (-1: a whole tile).
+__device__ __forceinline__ void unit_coords(int u, const GemmShape &s, int &tile, int &kb0, int &kb1, int &part) {
+    if (u < s.full_units) {
+        tile = u;
+        kb0 = 0;
+        kb1 = s.k_blocks;
+        part = -1;
+    } else {
+        const int j = u - s.full_units;
+        const int tl = j / s.split;
+        part = j - tl * s.split;
+        tile = s.full_units + tl;
+        kb0 = part * s.k_blocks / s.split;
+        kb1 = (part + 1) * s.k_blocks / s.split;
+    }
+}
 
 __device__ __forceinline__ void tile_coords(int tile, const GemmShape &s, int &m_blk, int &n_blk) {
     const int per_group = s.group_m * s.tiles_n;
@@ -670,12 +695,38 @@ __device__ __forceinline__ void epi_drain_inputs(EpiWarp &w) {
     }
 }
 
+// Where an epilogue reads the accumulator from: tensor memory (one row per
+// thread, warp-collective loads), or -- for a split tail tile -- the sum of
+// the fp32 partials of its K parts, added in part order so that the result
+// does not depend on which part finished last.
+struct TmemAcc {
+    uint32_t taddr;  // this warp's lane quarter, column 0
+    __device__ __forceinline__ void load(int col, float (&v)[32]) const { ptx::tmem_ld32(taddr + col, v); }
+};
+// A partial is stored column-major, element (row, col) at col * 128 + row,
+// so that the 32 lanes of a warp (32 consecutive rows) touch one 128-byte
+// line per column.
+struct PartialAcc {
+    const float *row;     // this thread's row of part 0 (element (row, 0))
+    int64_t part_stride;  // floats between parts
+    int parts;
+    __device__ __forceinline__ void load(int col, float (&v)[32]) const {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+        for (int p = 0; p < parts; ++p) {
+            const float *src = row + p * part_stride + static_cast<int64_t>(col) * kBM;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += __ldcg(src + i * kBM);  // written by other SMs: not through L1
+        }
+    }
+};
+
 // One tile's epilogue for this warp: chunks [c0, c1) of its 32 rows starting
 // at row0, columns from n0. The input chunk c0 must already be issued. Gated
-// epilogues read the up half of chunk c at TMEM column up_col + 32 c.
+// epilogues read the up half of chunk c at accumulator column up_col + 32 c.
 // Returns false if a bounded wait gave up.
-template <class Epi, int kChunk>
-__device__ __forceinline__ bool epi_tile(const typename Epi::Params &ep, const GemmShape &shp, uint32_t taddr,
+template <class Epi, int kChunk, class Acc>
+__device__ __forceinline__ bool epi_tile(const typename Epi::Params &ep, const GemmShape &shp, const Acc &acc,
                                          uint32_t up_col, int row0, int n0, int c0, int c1, int lane, EpiWarp &w,
                                          const CUtensorMap *tmC0, const CUtensorMap *tmC1,
                                          const CUtensorMap *tmIn, const ChunkSet<kChunk> *cs,
@@ -695,9 +746,9 @@ __device__ __forceinline__ bool epi_tile(const typename Epi::Params &ep, const G
         const int n = n0 + c * 32;
         if (c + 1 < c1) epi_issue_input<Epi>(w, ep, tmIn, lane, n + 32, row0);
         float v[32];
-        ptx::tmem_ld32(taddr + c * 32, v);
+        acc.load(c * 32, v);
         float in[2][32];
-        if constexpr (Epi::kGated) ptx::tmem_ld32(taddr + up_col + c * 32, in[0]);
+        if constexpr (Epi::kGated) acc.load(static_cast<int>(up_col) + c * 32, in[0]);
         if constexpr (Epi::kIns > 0) {
             const uint32_t b = w.in_used & 1u;
             const bool ok = ptx::mbar_wait(&w.in_bar[b], (w.in_used >> 1) & 1u, abort_flag, err, 5);
@@ -987,8 +1038,8 @@ __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
-            if (!epi_tile<Epi, kChunk>(ep, shp, taddr, BN / 2, row0, n0, c0, c1, lane, w, &tmC0, &tmC1, &tmIn, &cs,
-                                       abort_flag, err))
+            if (!epi_tile<Epi, kChunk>(ep, shp, TmemAcc{taddr}, BN / 2, row0, n0, c0, c1, lane, w, &tmC0, &tmC1,
+                                       &tmIn, &cs, abort_flag, err))
                 break;
             ptx::tc_fence_before();
             __syncwarp();

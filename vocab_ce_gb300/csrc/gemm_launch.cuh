@@ -39,6 +39,54 @@ struct Chunks {
     int count;
 };
 
+// Scratch for the split tail of a CTA-pair launch (caller's workspace);
+// null or too small: the tail is not split.
+struct TailScratch {
+    void *ptr;
+    size_t bytes;
+};
+
+// Split-tail plan. With C clusters and tiles = W C + r, the last r tiles (a
+// partial wave, r <= C / 2) are each split along K into s parts, so the last
+// wave runs r s parts of 1/s the work on otherwise idle clusters. s is capped
+// so that every part has at least kTailMinKBlocks K blocks, r s <= C (one
+// part per cluster) and r s <= kTailMaxUnits (the scratch bound).
+// Measured on GB300 (A/B, two repetitions): 32 K blocks per part is best --
+// the 8.3B step's dH GEMM gains 10% and its GEMM2 / dX 7%, while splitting
+// the K = 3072 GEMMs (16-block parts) did not pay for the partials' round
+// trip through L2.
+#ifndef TPCE_TAIL_MIN_KBLOCKS
+#define TPCE_TAIL_MIN_KBLOCKS 32
+#endif
+#ifndef TPCE_TAIL_SPLIT
+#define TPCE_TAIL_SPLIT 1
+#endif
+constexpr int kTailMinKBlocks = TPCE_TAIL_MIN_KBLOCKS;  // build-time tuning knobs
+constexpr int kTailMaxSplit = 8;
+inline void plan_tail(GemmShape &s, int clusters, int bn, const TailScratch *ts, cudaStream_t stream, bool &memset_ok) {
+    const int tiles = s.tiles_m * s.tiles_n;
+    s.full_units = tiles;
+    s.split = 1;
+    s.tail_tiles = 0;
+    s.partial = nullptr;
+    s.tickets = nullptr;
+    memset_ok = true;
+    if (!TPCE_TAIL_SPLIT || !ts || !ts->ptr || clusters < 2 || tiles <= clusters) return;
+    const int r = tiles % clusters;
+    if (r == 0 || r > clusters / 2) return;
+    int sp = std::min({kTailMaxSplit, clusters / r, kTailMaxUnits / r, s.k_blocks / kTailMinKBlocks});
+    if (sp < 2) return;
+    const size_t part_bytes = sizeof(float) * 2 * kBM * static_cast<size_t>(bn);
+    const size_t need = part_bytes * r * sp + sizeof(uint32_t) * 2 * r;
+    if (ts->bytes < need) return;
+    s.full_units = tiles - r;
+    s.split = sp;
+    s.tail_tiles = r;
+    s.partial = static_cast<float *>(ts->ptr);
+    s.tickets = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ts->ptr) + part_bytes * r * sp);
+    memset_ok = cudaMemsetAsync(s.tickets, 0, sizeof(uint32_t) * 2 * r, stream) == cudaSuccess;
+}
+
 // Tensor maps of the chunks of one role, built like the role's own map.
 template <int kChunk, typename Build>
 inline bool build_chunk_maps(ChunkSet<kChunk> &cs, const Chunks *ch, Build build) {
@@ -198,6 +246,11 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
     s.b_off_mn = b_off_mn;
     s.b_off_k = b_off_k;
     s.b_gate_off = b_gate_off;
+    s.full_units = s.tiles_m * s.tiles_n;  // the one-CTA kernel never splits its tail
+    s.split = 1;
+    s.tail_tiles = 0;
+    s.partial = nullptr;
+    s.tickets = nullptr;
 
     auto kern = tc_gemm_kernel<ElemT, BN, A_MN, B_MN, Epi, kChunk>;
     static std::mutex attr_mu;
@@ -226,7 +279,7 @@ template <int BN, bool A_MN, bool B_MN, class Epi, int kChunk = kChunkNone>
 tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &b, const OutView *outs,
                              const OutView *ins, int M, int N, int K, int a_off_mn, int a_off_k, int b_off_mn,
                              int b_off_k, const typename Epi::Params &ep, cudaStream_t stream, bool timed = true,
-                             int b_gate_off = 0, const Chunks *chunks = nullptr) {
+                             int b_gate_off = 0, const Chunks *chunks = nullptr, const TailScratch *tail = nullptr) {
     using Cfg = PairCfg<BN, Epi>;
     constexpr int kTileN = Epi::kGated ? BN / 2 : BN;
     using OutT = typename Epi::Out;
@@ -291,7 +344,11 @@ tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &
     uint32_t *err = device_error_word();
     if (sms < 2 || err == nullptr) return fail(TPCE_ERR_CUDA, "device query failed (%s)", name);
     const int64_t tiles = static_cast<int64_t>(s.tiles_m) * s.tiles_n;
-    const int grid = 2 * static_cast<int>(std::min<int64_t>(tiles, sms / 2));
+    const int clusters = static_cast<int>(std::min<int64_t>(tiles, sms / 2));
+    bool memset_ok = true;
+    plan_tail(s, clusters, BN, tail, stream, memset_ok);
+    if (!memset_ok) return fail(TPCE_ERR_CUDA, "cudaMemsetAsync of the tail tickets (%s)", name);
+    const int grid = 2 * clusters;
     KernelTimer timer(timed ? name : nullptr, stream);
     kern<<<grid, 64 + 32 * Epi::kWarps, Cfg::kSmemBytes, stream>>>(ta, tb, tc[0], tc[1], tin, cs, s, ep, err);
     return check_launch(name, stream);
@@ -302,12 +359,12 @@ template <typename ElemT, bool A_MN, bool B_MN, class Epi, unsigned Allowed, int
 tpce_status launch_gemm_auto(const char *name, const Operand &a, const Operand &b, const OutView *outs,
                              const OutView *ins, int M, int N, int K, int a_off_mn, int a_off_k, int b_off_mn,
                              int b_off_k, const typename Epi::Params &ep, cudaStream_t stream, int b_gate_off = 0,
-                             const Chunks *chunks = nullptr) {
+                             const Chunks *chunks = nullptr, const TailScratch *tail = nullptr) {
     static_assert(!Epi::kGated || (Allowed & kBN192) == 0, "gated tiles are 128 or 256 wide");
     if constexpr (TPCE_PAIR_BN != 0 && std::is_same<ElemT, __nv_bfloat16>::value && Epi::kWarps == 4) {
         return launch_gemm_pair<TPCE_PAIR_BN, A_MN, B_MN, Epi, kChunk>(name, a, b, outs, ins, M, N, K, a_off_mn,
                                                                       a_off_k, b_off_mn, b_off_k, ep, stream, true,
-                                                                      b_gate_off, chunks);
+                                                                      b_gate_off, chunks, tail);
     } else {
         const int sms = num_sms();
         if (sms <= 0) return fail(TPCE_ERR_CUDA, "device query failed (%s)", name);

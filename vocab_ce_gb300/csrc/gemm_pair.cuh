@@ -16,6 +16,15 @@
 //   tfull[a]   in each CTA, arrived by the even CTA's MMA commit (multicast).
 //   tempty[a]  lives in the even CTA; the epilogue warps of both CTAs arrive.
 // The epilogue is the one-CTA kernel's, applied to each CTA's 128 rows.
+//
+// Split tail. When the last wave holds few tiles (host's choice, see
+// launch_gemm_pair), each of them is split along K into parts run by
+// otherwise idle clusters; a cluster runs at most one part. A part's
+// epilogue writes its fp32 partial (per CTA: 128 rows x BN) to global
+// scratch, and its four epilogue warps meet on a shared-memory barrier
+// (bounded waits) before one thread takes a ticket with an atomic add. The
+// part that draws the last ticket sums the partials in part order and runs
+// the ordinary epilogue on the sum; no CTA ever waits for another.
 #pragma once
 
 #include "gemm.cuh"
@@ -66,8 +75,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
     uint64_t *in_bars = drain + 1;  // 2 per epilogue warp
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(in_bars + 2 * Epi::kWarps);
+    uint64_t *tail_bar = in_bars + 2 * Epi::kWarps;  // the epilogue warps' partials are written
+    uint64_t *tail_done = tail_bar + 1;             // the ticket is drawn
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile uint32_t *tail_ticket = reinterpret_cast<volatile uint32_t *>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -84,6 +96,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
         }
         for (int i = 0; i < 2 * Epi::kWarps; ++i) ptx::mbar_init(&in_bars[i], 1);
         ptx::mbar_init(drain, 1);
+        ptx::mbar_init(tail_bar, Epi::kWarps);
+        ptx::mbar_init(tail_done, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -106,7 +120,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
     // both CTAs' barriers exist before either signals the other
     ptx::cluster_sync();
 
-    const int num_tiles = shp.tiles_m * shp.tiles_n;  // tiles of 256 x BN
+    const int num_units = shp.full_units + shp.tail_tiles * shp.split;  // tiles of 256 x BN, or their K parts
     const int cluster_id = blockIdx.x >> 1;
     const int clusters = gridDim.x >> 1;
 
@@ -117,7 +131,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
             uint32_t phase = 0;
             uint32_t issued = 0;
             uint32_t issued_parity = 0;
-            for (int tile = cluster_id; tile < num_tiles && !*abort_flag; tile += clusters) {
+            for (int u = cluster_id; u < num_units && !*abort_flag; u += clusters) {
+                int tile, kb0, kb1, part;
+                unit_coords(u, shp, tile, kb0, kb1, part);
                 int mb, nb;
                 tile_coords(tile, shp, mb, nb);
                 const int m0 = mb * (2 * kBM) + static_cast<int>(rank) * kBM;
@@ -126,9 +142,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
                 const int nh0 = Epi::kGated ? nb * kTileN + static_cast<int>(rank) * shp.b_gate_off
                                             : nb * BN + static_cast<int>(rank) * kHalfN;
                 ChunkCursor<kChunk> cur;
-                if constexpr (kChunk == kChunkA) cur.init(cs, A_MN ? shp.a_off_k : m0 + shp.a_off_mn);
-                if constexpr (kChunk == kChunkB) cur.init(cs, B_MN ? shp.b_off_k : nh0 + shp.b_off_mn);
-                for (int kb = 0; kb < shp.k_blocks; ++kb) {
+                if constexpr (kChunk == kChunkA) cur.init(cs, A_MN ? shp.a_off_k + kb0 * kBK : m0 + shp.a_off_mn);
+                if constexpr (kChunk == kChunkB) cur.init(cs, B_MN ? shp.b_off_k + kb0 * kBK : nh0 + shp.b_off_mn);
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!ptx::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, 1)) break;
                     const uint32_t bar = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
                     if (rank == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
@@ -184,12 +200,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            for (int tile = cluster_id; tile < num_tiles; tile += clusters) {
+            for (int u = cluster_id; u < num_units; u += clusters) {
+                int tile, kb0, kb1, part;
+                unit_coords(u, shp, tile, kb0, kb1, part);
                 if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, err, 2)) break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 bool ok = true;
-                for (int kb = 0; kb < shp.k_blocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!ptx::mbar_wait(&full[stage], phase, abort_flag, err, 3)) {
                         ok = false;
                         break;
@@ -203,7 +221,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
                                                  : ptx::sdesc_sw128(sa + kk * 32, 16, 1024);
                         const uint64_t bd = B_MN ? ptx::sdesc_sw128(sb + kk * (kUmmaK * kRowBytes), kMnBlockBytes, 1024)
                                                  : ptx::sdesc_sw128(sb + kk * 32, 16, 1024);
-                        ptx::mma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        ptx::mma_bf16_pair(d_tmem, ad, bd, kIdesc, ((kb - kb0) | kk) != 0 ? 1u : 0u);
                     }
                     ptx::mma_commit_pair(&empty[stage]);
                     if (++stage == S) {
@@ -226,19 +244,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
         EpiWarp w{staging + ew * EpiSmem<Epi>::kWarpBytes, in_bars + 2 * ew, 0, false, 0u, 0u};
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = cluster_id; tile < num_tiles; tile += clusters) {
+        for (int u = cluster_id; u < num_units; u += clusters) {
+            int tile, kb0, kb1, part;
+            unit_coords(u, shp, tile, kb0, kb1, part);
             int mb, nb;
             tile_coords(tile, shp, mb, nb);
             const int row0 = mb * (2 * kBM) + static_cast<int>(rank) * kBM + quarter * 32;
             const int n0 = nb * kTileN;
-            epi_issue_input<Epi>(w, ep, &tmIn, lane, n0, row0);
+            if (part < 0) epi_issue_input<Epi>(w, ep, &tmIn, lane, n0, row0);
             const bool ok = ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, err, 4);
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
-            if (!epi_tile<Epi, kChunk>(ep, shp, taddr, BN / 2, row0, n0, 0, kChunks, lane, w, &tmC0, &tmC1, &tmIn,
-                                       &cs, abort_flag, err))
-                break;
+            if (part < 0) {
+                if (!epi_tile<Epi, kChunk>(ep, shp, TmemAcc{taddr}, BN / 2, row0, n0, 0, kChunks, lane, w, &tmC0,
+                                           &tmC1, &tmIn, &cs, abort_flag, err))
+                    break;
+            } else {
+                // a K part of a tail tile: its partial to global scratch, all
+                // BN accumulator columns of this thread's row, column-major
+                // (a warp's 32 rows of one column are one 128-byte line)
+                const int tl = tile - shp.full_units;
+                const int64_t slot_floats = static_cast<int64_t>(kBM) * BN;
+                float *mine = shp.partial + (static_cast<int64_t>(tl * shp.split + part) * 2 + rank) * slot_floats +
+                              quarter * 32 + lane;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    ptx::tmem_ld32(taddr + c * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) mine[static_cast<int64_t>(c * 32 + i) * kBM] = v[i];
+                }
+                __threadfence();  // the partial is visible GPU-wide before the ticket below
+                // the accumulator is free again
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&tempty[acc]), 0));
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+                // the four epilogue warps' partials are written: draw the ticket
+                if (lane == 0) ptx::mbar_arrive(tail_bar);
+                if (ew == 0 && lane == 0) {
+                    uint32_t t = 0xffffffffu;
+                    if (ptx::mbar_wait(tail_bar, 0, abort_flag, err, 6)) {
+                        t = atomicAdd(&shp.tickets[tl * 2 + rank], 1u);
+                        __threadfence();
+                    }
+                    *tail_ticket = t;
+                    ptx::mbar_arrive(tail_done);
+                }
+                bool got = lane == 0 ? ptx::mbar_wait(tail_done, 0, abort_flag, err, 7) : true;
+                if (!__all_sync(0xffffffffu, got)) break;
+                const uint32_t ticket = __shfl_sync(0xffffffffu, lane == 0 ? *tail_ticket : 0u, 0);
+                if (ticket != static_cast<uint32_t>(shp.split - 1)) continue;  // another part finishes the tile
+                __threadfence();  // every part's partial is visible to this CTA
+                if (ew == 0 && lane == 0) shp.tickets[tl * 2 + rank] = 0;  // leave the ticket clear
+                const PartialAcc sum{shp.partial + (static_cast<int64_t>(tl * shp.split) * 2 + rank) * slot_floats +
+                                         quarter * 32 + lane,
+                                     2 * slot_floats, shp.split};
+                epi_issue_input<Epi>(w, ep, &tmIn, lane, n0, row0);
+                if (!epi_tile<Epi, kChunk>(ep, shp, sum, BN / 2, row0, n0, 0, kChunks, lane, w, &tmC0, &tmC1, &tmIn,
+                                           &cs, abort_flag, err))
+                    break;
+                continue;
+            }
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&tempty[acc]), 0));

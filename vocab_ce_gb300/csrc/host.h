@@ -49,6 +49,12 @@ tpce_status f32_to_bf16(const float *in, void *out, int64_t n, cudaStream_t s);
 size_t colsum_partial_floats(int64_t R, int64_t N);
 tpce_status colsum(int dt, const void *X, int64_t R, int64_t N, int64_t ld, float *out, float *partial,
                    cudaStream_t s);
+// Workspace the GEMMs use to split the last partial wave of tiles along K:
+// at most kTailMaxUnits parts of one CTA pair's 256 x 256 fp32 tile, plus
+// their tickets. Every workspace layout starts with this region.
+constexpr int kTailMaxUnits = 64;
+constexpr size_t kTailScratchBytes = static_cast<size_t>(kTailMaxUnits) * 2 * 128 * 256 * 4 + 4096;
+
 // The same over rows split into `count` buffers of `rows` rows each (row
 // pitch ld): the column sums of their concatenation. count <= kMaxRowChunks.
 constexpr int kMaxRowChunks = 16;

@@ -68,7 +68,7 @@ inline int64_t pad4(int64_t x) { return (x + 3) / 4 * 4; }
 // transposed operands of the tf32 path: W^T (forward), X^T and dY^T
 // (weight gradient), token-major ones with rows padded to a multiple of 4.
 struct LinWs {
-    size_t partial, Wt, Xt, dYt, total;
+    size_t tail, partial, Wt, Xt, dYt, total;
 };
 
 LinWs lin_ws_layout(int64_t T, int64_t n_in, int64_t n_out, int dtype) {
@@ -79,6 +79,7 @@ LinWs lin_ws_layout(int64_t T, int64_t n_in, int64_t n_out, int dtype) {
         off = round_up(off + bytes, 256);
         return at;
     };
+    L.tail = take(kTailScratchBytes);  // offset 0: all the bf16 forward needs
     L.partial = take(colsum_partial_floats(T, n_out) * sizeof(float));
     if (dtype == TPCE_F32) {
         const size_t Tp = static_cast<size_t>(pad4(T));
@@ -107,17 +108,17 @@ struct LinSP {
 // Y = X W (+ b) on the bf16 path, with X or Y chunked as sp says.
 template <typename ElemT>
 tpce_status gemm_fwd(const char *name, const Operand &a, const Operand &bw, const OutView *o, int Ti, int oi, int ii,
-                     const float *b, cudaStream_t s, const LinSP *sp) {
+                     const float *b, cudaStream_t s, const LinSP *sp, const TailScratch *ts) {
     constexpr bool kBf = std::is_same<ElemT, __nv_bfloat16>::value;
     if constexpr (kBf) {
         if (sp && sp->x)
             return launch_gemm_auto<ElemT, false, true, EpiStore<ElemT>, kBN192 | kBN256, kChunkA>(
-                name, a, bw, o, nullptr, Ti, oi, ii, 0, 0, 0, 0, {b}, s, 0, sp->x);
+                name, a, bw, o, nullptr, Ti, oi, ii, 0, 0, 0, 0, {b}, s, 0, sp->x, ts);
         if (sp && sp->out)
             return launch_gemm_auto<ElemT, false, true, EpiStore<ElemT>, kBN192 | kBN256, kChunkC>(
-                name, a, bw, o, nullptr, Ti, oi, ii, 0, 0, 0, 0, {b}, s, 0, sp->out);
+                name, a, bw, o, nullptr, Ti, oi, ii, 0, 0, 0, 0, {b}, s, 0, sp->out, ts);
         return launch_gemm_auto<ElemT, false, true, EpiStore<ElemT>, kBN192 | kBN256>(name, a, bw, o, nullptr, Ti, oi, ii,
-                                                                                   0, 0, 0, 0, {b}, s);
+                                                                                   0, 0, 0, 0, {b}, s, 0, nullptr, ts);
     } else {
         if (sp && sp->x)
             return launch_gemm<float, 128, false, false, EpiStore<float>, kChunkA>(name, a, bw, o, nullptr, Ti, oi, ii, 0,
@@ -133,17 +134,18 @@ tpce_status gemm_fwd(const char *name, const Operand &a, const Operand &bw, cons
 // dX = dY W^T, with dY (row exit) or dX (column entry) chunked as sp says.
 template <typename ElemT>
 tpce_status gemm_dx(const char *name, const Operand &a, const Operand &bw, const OutView *o, int Ti, int ii, int oi,
-                    cudaStream_t s, const LinSP *sp) {
+                    cudaStream_t s, const LinSP *sp, const TailScratch *ts) {
     constexpr bool kBf = std::is_same<ElemT, __nv_bfloat16>::value;
     if constexpr (kBf) {
         if (sp && sp->dy)
             return launch_gemm_auto<ElemT, false, false, EpiStore<ElemT>, kBN192 | kBN256, kChunkA>(
-                name, a, bw, o, nullptr, Ti, ii, oi, 0, 0, 0, 0, {nullptr}, s, 0, sp->dy);
+                name, a, bw, o, nullptr, Ti, ii, oi, 0, 0, 0, 0, {nullptr}, s, 0, sp->dy, ts);
         if (sp && sp->out)
             return launch_gemm_auto<ElemT, false, false, EpiStore<ElemT>, kBN192 | kBN256, kChunkC>(
-                name, a, bw, o, nullptr, Ti, ii, oi, 0, 0, 0, 0, {nullptr}, s, 0, sp->out);
+                name, a, bw, o, nullptr, Ti, ii, oi, 0, 0, 0, 0, {nullptr}, s, 0, sp->out, ts);
         return launch_gemm_auto<ElemT, false, false, EpiStore<ElemT>, kBN192 | kBN256>(name, a, bw, o, nullptr, Ti, ii,
-                                                                                    oi, 0, 0, 0, 0, {nullptr}, s);
+                                                                                    oi, 0, 0, 0, 0, {nullptr}, s, 0,
+                                                                                    nullptr, ts);
     } else {
         if (sp && sp->dy)
             return launch_gemm<float, 128, false, false, EpiStore<float>, kChunkA>(name, a, bw, o, nullptr, Ti, ii, oi, 0,
@@ -170,20 +172,20 @@ tpce_status transpose_rows(const float *in, const Chunks *ch, int64_t T, int64_t
 
 tpce_status forward_impl(const LinearNames &nm, const void *X, const void *W, const float *b, int64_t T, int64_t n_in,
                          int64_t n_out, int dtype, void *Y, void *ws, const LinWs &L, cudaStream_t s,
-                         const LinSP *sp) {
+                         const LinSP *sp, const TailScratch *ts) {
     const int Ti = static_cast<int>(T), ii = static_cast<int>(n_in), oi = static_cast<int>(n_out);
     const OutView o[1] = {{Y, T, n_out, n_out}};
     if (dtype == TPCE_BF16) {
         Operand a{X, T, n_in, n_in};      // K-major [T, n_in]
         Operand bw{W, n_in, n_out, n_out};  // MN-major: K = n_in rows, N = n_out columns
-        return gemm_fwd<__nv_bfloat16>(nm.fwd, a, bw, o, Ti, oi, ii, b, s, sp);
+        return gemm_fwd<__nv_bfloat16>(nm.fwd, a, bw, o, Ti, oi, ii, b, s, sp, ts);
     }
     float *Wt = at<float>(ws, L.Wt);
     tpce_status st = transpose_f32(static_cast<const float *>(W), n_in, n_out, n_out, Wt, n_in, s);  // W^T
     if (st != TPCE_OK) return st;
     Operand a{X, T, n_in, n_in};       // K-major [T, n_in]
     Operand bw{Wt, n_out, n_in, n_in};  // K-major: N = n_out rows, K = n_in columns
-    return gemm_fwd<float>(nm.fwd, a, bw, o, Ti, oi, ii, b, s, sp);
+    return gemm_fwd<float>(nm.fwd, a, bw, o, Ti, oi, ii, b, s, sp, nullptr);
 }
 
 tpce_status backward_impl(const LinearNames &nm, const void *dY, const void *X, const void *W, int64_t T, int64_t n_in,
@@ -191,6 +193,8 @@ tpce_status backward_impl(const LinearNames &nm, const void *dY, const void *X, 
                           cudaStream_t s, const LinSP *sp) {
     const int Ti = static_cast<int>(T), ii = static_cast<int>(n_in), oi = static_cast<int>(n_out);
     float *partial = at<float>(ws, L.partial);
+    const TailScratch tail{at<uint8_t>(ws, L.tail), kTailScratchBytes};
+    const TailScratch *ts = &tail;
     tpce_status st;
     if (dtype == TPCE_BF16) {
         using bf = __nv_bfloat16;
@@ -199,7 +203,7 @@ tpce_status backward_impl(const LinearNames &nm, const void *dY, const void *X, 
             Operand a{dY, T, n_out, n_out};   // K-major [T, n_out]
             Operand bw{W, n_in, n_out, n_out};  // K-major: N = n_in rows, K = n_out columns
             const OutView o[1] = {{dX, T, n_in, n_in}};
-            if ((st = gemm_dx<bf>(nm.dX, a, bw, o, Ti, ii, oi, s, sp)) != TPCE_OK) return st;
+            if ((st = gemm_dx<bf>(nm.dX, a, bw, o, Ti, ii, oi, s, sp, ts)) != TPCE_OK) return st;
         }
         // dW = X^T dY (each shard's own block of W)
         {
@@ -208,13 +212,14 @@ tpce_status backward_impl(const LinearNames &nm, const void *dY, const void *X, 
             const OutView o[1] = {{dW, n_in, n_out, n_out}};
             if (sp && sp->x)
                 st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256, kChunkA>(
-                    nm.dW, a, bw, o, nullptr, ii, oi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, sp->x);
+                    nm.dW, a, bw, o, nullptr, ii, oi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, sp->x, ts);
             else if (sp && sp->dy)
                 st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256, kChunkB>(
-                    nm.dW, a, bw, o, nullptr, ii, oi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, sp->dy);
+                    nm.dW, a, bw, o, nullptr, ii, oi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, sp->dy, ts);
             else
                 st = launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>(nm.dW, a, bw, o, nullptr, ii, oi,
-                                                                                      Ti, 0, 0, 0, 0, {nullptr}, s);
+                                                                                      Ti, 0, 0, 0, 0, {nullptr}, s, 0,
+                                                                                      nullptr, ts);
             if (st != TPCE_OK) return st;
         }
         if (db) {
@@ -231,7 +236,7 @@ tpce_status backward_impl(const LinearNames &nm, const void *dY, const void *X, 
         Operand a{dY, T, n_out, n_out};   // K-major [T, n_out]
         Operand bw{W, n_in, n_out, n_out};  // K-major: N = n_in rows, K = n_out columns
         const OutView o[1] = {{dX, T, n_in, n_in}};
-        if ((st = gemm_dx<float>(nm.dX, a, bw, o, Ti, ii, oi, s, sp)) != TPCE_OK) return st;
+        if ((st = gemm_dx<float>(nm.dX, a, bw, o, Ti, ii, oi, s, sp, nullptr)) != TPCE_OK) return st;
     }
     st = transpose_rows(static_cast<const float *>(X), sp ? sp->x : nullptr, T, n_in, Xt, Tp, s);
     if (st != TPCE_OK) return st;
@@ -267,7 +272,10 @@ tpce_status linear_forward(const LinearNames &nm, const void *X, const void *W, 
         if (!aligned16(p)) return TPCE_ERR_ALIGN;
     const LinWs L = lin_ws_layout(T, n_in, n_out, dtype);
     if (dtype == TPCE_F32 && (!ws || ws_bytes < L.total)) return TPCE_ERR_WORKSPACE;
-    return forward_impl(nm, X, W, b, T, n_in, n_out, dtype, Y, ws, L, static_cast<cudaStream_t>(stream), sp);
+    // the bf16 forward takes an optional workspace: its start splits the last wave's tiles
+    const TailScratch tail = (ws && ws_bytes >= kTailScratchBytes) ? TailScratch{ws, kTailScratchBytes}
+                                                                  : TailScratch{nullptr, 0};
+    return forward_impl(nm, X, W, b, T, n_in, n_out, dtype, Y, ws, L, static_cast<cudaStream_t>(stream), sp, &tail);
 }
 
 tpce_status linear_backward(const LinearNames &nm, const void *dY, const void *X, const void *W, int64_t T,

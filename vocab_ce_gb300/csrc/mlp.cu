@@ -75,12 +75,18 @@ struct SeqPar {
     const Chunks *out;  // the Z chunks (forward) or dX chunks (backward): output map 0
 };
 
+// The split-tail scratch at the start of a workspace of at least ws_bytes
+// (null when the workspace is missing or too small: tails run unsplit).
+inline TailScratch tail_of(void *ws, size_t ws_bytes) {
+    return (ws && ws_bytes >= kTailScratchBytes) ? TailScratch{ws, kTailScratchBytes} : TailScratch{nullptr, 0};
+}
+
 // Workspace layout. bf16: dU [T, fw] (fw = f, or 2f for SwiGLU: [dG | dUp])
 // and the column-sum partials. fp32 adds the transposed operands of the tf32
 // path: W1^T, W2^T (forward), Y^T, dZ^T, X^T, dU^T (backward), the
 // token-major ones with rows padded to a multiple of 4.
 struct MlpWs {
-    size_t dU, partial, At, Bt, Yt, dZt, Xt, dUt, total;
+    size_t tail, dU, partial, At, Bt, Yt, dZt, Xt, dUt, total;
 };
 
 MlpWs mlp_ws_layout(Act act, int64_t T, int64_t h, int64_t f, int dtype) {
@@ -93,6 +99,7 @@ MlpWs mlp_ws_layout(Act act, int64_t T, int64_t h, int64_t f, int dtype) {
         off = round_up(off + bytes, 256);
         return at;
     };
+    L.tail = take(kTailScratchBytes);  // offset 0: all the bf16 forward needs
     L.dU = take(static_cast<size_t>(T) * fw * esz);
     const size_t pf = std::max(colsum_partial_floats(T, fw), colsum_partial_floats(T, h));
     L.partial = take(pf * sizeof(float));
@@ -119,7 +126,7 @@ T *at(void *ws, size_t off) {
 // U_save = [G | Up] [T, 2f].
 tpce_status forward_bf16(Act act, const void *X, const void *A, const float *bA, const void *B, const float *bB,
                          int64_t T, int64_t h, int64_t f, void *Z, void *U, void *Y, cudaStream_t s,
-                         const SeqPar *sp) {
+                         const SeqPar *sp, const TailScratch *ts) {
     using bf = __nv_bfloat16;
     const int Ti = static_cast<int>(T), hi = static_cast<int>(h), fi = static_cast<int>(f);
     const int64_t fw = pre_width(act, f);
@@ -130,15 +137,16 @@ tpce_status forward_bf16(Act act, const void *X, const void *A, const float *bA,
     if (act == Act::GeLU) {
         // GEMM1 (column-parallel): U = X A + bA, Y = GeLU(U)
         st = sp ? launch_gemm_auto<bf, false, true, EpiBiasGelu<bf>, kBN192 | kBN256, kChunkA>(
-                      "mlp_fwd_gemm1_bias_gelu", a, b, o1, nullptr, Ti, fi, hi, 0, 0, 0, 0, {bA}, s, 0, sp->x)
+                      "mlp_fwd_gemm1_bias_gelu", a, b, o1, nullptr, Ti, fi, hi, 0, 0, 0, 0, {bA}, s, 0, sp->x, ts)
                 : launch_gemm_auto<bf, false, true, EpiBiasGelu<bf>, kBN192 | kBN256>(
-                      "mlp_fwd_gemm1_bias_gelu", a, b, o1, nullptr, Ti, fi, hi, 0, 0, 0, 0, {bA}, s);
+                      "mlp_fwd_gemm1_bias_gelu", a, b, o1, nullptr, Ti, fi, hi, 0, 0, 0, 0, {bA}, s, 0, nullptr, ts);
     } else {
         // GEMM1 (column-parallel, gated): [G | Up] = X W1 + b1, Y = Swish(G) Up
         st = sp ? launch_gemm_auto<bf, false, true, EpiSwiGlu<bf>, kBN128 | kBN256, kChunkA>(
-                      "swiglu_fwd_gemm1_gate_up", a, b, o1, nullptr, Ti, fi, hi, 0, 0, 0, 0, {bA, fi}, s, fi, sp->x)
+                      "swiglu_fwd_gemm1_gate_up", a, b, o1, nullptr, Ti, fi, hi, 0, 0, 0, 0, {bA, fi}, s, fi, sp->x, ts)
                 : launch_gemm_auto<bf, false, true, EpiSwiGlu<bf>, kBN128 | kBN256>(
-                      "swiglu_fwd_gemm1_gate_up", a, b, o1, nullptr, Ti, fi, hi, 0, 0, 0, 0, {bA, fi}, s, fi);
+                      "swiglu_fwd_gemm1_gate_up", a, b, o1, nullptr, Ti, fi, hi, 0, 0, 0, 0, {bA, fi}, s, fi, nullptr,
+                      ts);
     }
     if (st != TPCE_OK) return st;
     // GEMM2 (row-parallel) + g: Z = sum_i Y_i B_i + bB (sequence-parallel:
@@ -149,15 +157,17 @@ tpce_status forward_bf16(Act act, const void *X, const void *A, const float *bA,
     const char *n2 = act == Act::GeLU ? "mlp_fwd_gemm2_shard_sum" : "swiglu_fwd_gemm2_shard_sum";
     if (sp)
         return launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256, kChunkC>(
-            n2, a2, b2, o2, nullptr, Ti, hi, fi, 0, 0, 0, 0, {bB}, s, 0, sp->out);
+            n2, a2, b2, o2, nullptr, Ti, hi, fi, 0, 0, 0, 0, {bB}, s, 0, sp->out, ts);
     return launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256>(n2, a2, b2, o2, nullptr, Ti, hi, fi, 0, 0,
-                                                                             0, 0, {bB}, s);
+                                                                             0, 0, {bB}, s, 0, nullptr, ts);
 }
 
 tpce_status backward_bf16(Act act, const void *dZ, const void *X, const void *A, const void *B, const void *U,
                           const void *Y, int64_t T, int64_t h, int64_t f, void *dX, void *dA, float *dbA, void *dB,
                           float *dbB, void *ws, const MlpWs &L, cudaStream_t s, const SeqPar *sp) {
     using bf = __nv_bfloat16;
+    const TailScratch tail{at<uint8_t>(ws, L.tail), kTailScratchBytes};
+    const TailScratch *ts = &tail;
     bf *dU = at<bf>(ws, L.dU);
     float *partial = at<float>(ws, L.partial);
     const int64_t fw = pre_width(act, f);
@@ -175,14 +185,14 @@ tpce_status backward_bf16(Act act, const void *dZ, const void *X, const void *A,
         const OutView in[1] = {{const_cast<void *>(U), T, fw, fw}};  // read by TMA, never written
         if (!glu)
             st = sp ? launch_gemm_auto<bf, false, false, EpiGeluGrad<bf>, kBN192 | kBN256, kChunkA>(
-                          "mlp_bwd_dY_gelu_grad", a, b, o, in, Ti, fi, hi, 0, 0, 0, 0, {}, s, 0, sp->dz)
+                          "mlp_bwd_dY_gelu_grad", a, b, o, in, Ti, fi, hi, 0, 0, 0, 0, {}, s, 0, sp->dz, ts)
                     : launch_gemm_auto<bf, false, false, EpiGeluGrad<bf>, kBN192 | kBN256>(
-                          "mlp_bwd_dY_gelu_grad", a, b, o, in, Ti, fi, hi, 0, 0, 0, 0, {}, s);
+                          "mlp_bwd_dY_gelu_grad", a, b, o, in, Ti, fi, hi, 0, 0, 0, 0, {}, s, 0, nullptr, ts);
         else
             st = sp ? launch_gemm_auto<bf, false, false, EpiSwiGluGrad<bf>, kBN192 | kBN256, kChunkA>(
-                          "swiglu_bwd_dY_swiglu_grad", a, b, o, in, Ti, fi, hi, 0, 0, 0, 0, {fi}, s, 0, sp->dz)
+                          "swiglu_bwd_dY_swiglu_grad", a, b, o, in, Ti, fi, hi, 0, 0, 0, 0, {fi}, s, 0, sp->dz, ts)
                     : launch_gemm_auto<bf, false, false, EpiSwiGluGrad<bf>, kBN192 | kBN256>(
-                          "swiglu_bwd_dY_swiglu_grad", a, b, o, in, Ti, fi, hi, 0, 0, 0, 0, {fi}, s);
+                          "swiglu_bwd_dY_swiglu_grad", a, b, o, in, Ti, fi, hi, 0, 0, 0, 0, {fi}, s, 0, nullptr, ts);
         if (st != TPCE_OK) return st;
     }
     // dB_i = Y_i^T dZ
@@ -192,9 +202,9 @@ tpce_status backward_bf16(Act act, const void *dZ, const void *X, const void *A,
         const OutView o[1] = {{dB, f, h, h}};
         const char *nm = glu ? "swiglu_bwd_dW2" : "mlp_bwd_dB";
         st = sp ? launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256, kChunkB>(
-                      nm, a, b, o, nullptr, fi, hi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, sp->dz)
+                      nm, a, b, o, nullptr, fi, hi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, sp->dz, ts)
                 : launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>(nm, a, b, o, nullptr, fi, hi, Ti, 0, 0,
-                                                                                   0, 0, {nullptr}, s);
+                                                                                   0, 0, {nullptr}, s, 0, nullptr, ts);
         if (st != TPCE_OK) return st;
     }
     // dA_i = X^T dU_i
@@ -204,9 +214,9 @@ tpce_status backward_bf16(Act act, const void *dZ, const void *X, const void *A,
         const OutView o[1] = {{dA, h, fw, fw}};
         const char *nm = glu ? "swiglu_bwd_dW1" : "mlp_bwd_dA";
         st = sp ? launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256, kChunkA>(
-                      nm, a, b, o, nullptr, hi, fwi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, sp->x)
+                      nm, a, b, o, nullptr, hi, fwi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, sp->x, ts)
                 : launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>(nm, a, b, o, nullptr, hi, fwi, Ti, 0,
-                                                                                   0, 0, 0, {nullptr}, s);
+                                                                                   0, 0, 0, {nullptr}, s, 0, nullptr, ts);
         if (st != TPCE_OK) return st;
     }
     // f*: dX = sum_i dU_i A_i^T, the shard sum taken in the accumulator
@@ -216,9 +226,10 @@ tpce_status backward_bf16(Act act, const void *dZ, const void *X, const void *A,
         const OutView o[1] = {{dX, T, h, h}};
         const char *nm = glu ? "swiglu_bwd_dX_shard_sum" : "mlp_bwd_dX_shard_sum";
         st = sp ? launch_gemm_auto<bf, false, false, EpiStore<bf>, kBN192 | kBN256, kChunkC>(
-                      nm, a, b, o, nullptr, Ti, hi, fwi, 0, 0, 0, 0, {nullptr}, s, 0, sp->out)
+                      nm, a, b, o, nullptr, Ti, hi, fwi, 0, 0, 0, 0, {nullptr}, s, 0, sp->out, ts)
                 : launch_gemm_auto<bf, false, false, EpiStore<bf>, kBN192 | kBN256>(nm, a, b, o, nullptr, Ti, hi, fwi, 0,
-                                                                                     0, 0, 0, {nullptr}, s);
+                                                                                     0, 0, 0, {nullptr}, s, 0, nullptr,
+                                                                                     ts);
         if (st != TPCE_OK) return st;
     }
     if (dbA && (st = colsum(0, dU, T, fw, fw, dbA, partial, s)) != TPCE_OK) return st;
@@ -369,7 +380,10 @@ tpce_status forward(Act act, const void *X, const void *A, const float *bA, cons
                           static_cast<const void *>(ws)})
         if (!aligned16(p)) return TPCE_ERR_ALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (dtype == TPCE_BF16) return forward_bf16(act, X, A, bA, B, bB, T, h, f, Z, U, Y, s, sp);
+    if (dtype == TPCE_BF16) {
+        const TailScratch tail = tail_of(ws, ws_bytes);  // optional: splits the last wave's tiles
+        return forward_bf16(act, X, A, bA, B, bB, T, h, f, Z, U, Y, s, sp, &tail);
+    }
     const MlpWs L = mlp_ws_layout(act, T, h, f, dtype);
     if (!ws || ws_bytes < L.total) return TPCE_ERR_WORKSPACE;
     return forward_f32(act, static_cast<const float *>(X), static_cast<const float *>(A), bA,

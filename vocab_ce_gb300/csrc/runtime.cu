@@ -461,3 +461,5 @@ extern "C" tpce_status tpce_profile_get(int i, const char **name, int64_t *launc
     if (total_ms) *total_ms = g_agg[i].ms;
     return TPCE_OK;
 }
+
+extern "C" size_t tpce_tail_workspace_bytes(void) { return tpce::kTailScratchBytes; }
