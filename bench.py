@@ -76,6 +76,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, ws: int, device) -> float:
+    """The largest of every rank's value (each rank's elapsed time -> the job's)."""
+    if ws <= 1:
+        return value
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(ws: int, work_per_rank: float, seconds: float) -> float:
+    """Whole-job throughput: the work all ranks processed over the slowest rank's time."""
+    return ws * work_per_rank / seconds
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -488,16 +504,11 @@ def run_ours(args, w, name):
     clk = clocks.stop()
     assert tp.device_status() == 0, "device status after the timed region"
     elapsed_ms = t_start.elapsed_time(t_end)
-    if ws > 1:
-        import torch.distributed as dist
-
-        tmax = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tmax.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, ws, dev)
     ms_step = elapsed_ms / args.steps
     mlp_ms = sum(a.elapsed_time(b) for e in ev for part, a, b in e if part == "mlp") / args.steps
     ce_ms = sum(a.elapsed_time(b) for e in ev for part, a, b in e if part == "ce") / args.steps
-    value = ws * (mlp_fl + ce_fl) / (ms_step * 1e-3) / 1e12
+    value = job_rate(ws, mlp_fl + ce_fl, ms_step * 1e-3) / 1e12
 
     pk, pk_src = peaks()
     # ---------------- roofline of the dominant kernel
@@ -585,15 +596,10 @@ def run_ours(args, w, name):
         torch.cuda.synchronize()
         barrier()
         e_ms = a.elapsed_time(b)
-        if ws > 1:
-            import torch.distributed as dist
-
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_ms, ws, dev)
         h2d = sum(v.numel() * v.element_size() for v in host.values())
         d2h = (loss_host.numel() * 4) if w.v_pad else z_host.numel() * 2
-        e2e = {"value": ws * (mlp_fl + ce_fl) / (e_ms / args.steps * 1e-3) / 1e12, "unit": UNIT,
+        e2e = {"value": job_rate(ws, mlp_fl + ce_fl, e_ms / args.steps * 1e-3) / 1e12, "unit": UNIT,
                "ms_per_step": e_ms / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "path": "vocab_ce_gb300 Python API -> C ABI; every step's inputs copied from pinned host memory "
                        "(on a second stream, double-buffered: step i+1's copy overlaps step i's compute; the first "
