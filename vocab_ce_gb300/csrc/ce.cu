@@ -139,8 +139,8 @@ tpce_status ce_forward(const CeArgs &a, const CeWs &L, void *ws, float *lse_buf,
     if (st != TPCE_OK) return st;
     // exchange of the per-token statistics across shards
     KernelTimer timer("ce_combine", s);
-    ce_combine_kernel<<<static_cast<unsigned>((a.T + 255) / 256), 256, 0, s>>>(
-        stats, tau, a.targets, a.T, a.t, static_cast<int>(L.n_tiles / a.t), vvi, a.loss, lse_buf, err);
+    launch_ce_combine(stats, tau, a.targets, a.T, a.t, static_cast<int>(L.n_tiles / a.t), vvi, a.loss, lse_buf, err,
+                      s);
     return check_launch("ce_combine", s);
 }
 

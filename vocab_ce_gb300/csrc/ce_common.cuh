@@ -29,12 +29,56 @@ tpce_status check_ce_shape(int64_t T, int64_t h, int64_t v_pad, int64_t v_valid,
     return TPCE_OK;
 }
 
-// Per token: fold the tiles of each shard into (m_i, s_i), then fold the shards.
-__global__ void ce_combine_kernel(const float2 *__restrict__ stats, const float *__restrict__ tau,
-                                  const int32_t *__restrict__ targets, int64_t T, int t, int tiles_per_shard,
-                                  int v_valid, float *__restrict__ loss, float *__restrict__ lse, uint32_t *err) {
-    const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (r >= T) return;
+// (m, s) <- the log-sum-exp fold of (m, s) and (m2, s2): s e^{m - M} + s2 e^{m2 - M}
+// with M = max(m, m2). A part with s2 = 0 holds no real id and is skipped.
+__device__ __forceinline__ void lse_fold(float &m, float &s, float m2, float s2) {
+    if (s2 > 0.0f) {
+        const float nm = fmaxf(m, m2);
+        s = s * expf(m - nm) + s2 * expf(m2 - nm);
+        m = nm;
+    }
+}
+
+// Per token: fold the tiles of each shard into (m_i, s_i), then fold the
+// shards. A block takes 32 tokens, one per lane, so each tile's statistics
+// arrive as one coalesced 256-byte load per warp. Its warps take the shards
+// in turn (warp w: shards w, w + kCombineWarps, ...), and warp 0 folds the
+// warps' results: only (m_i, s_i) crosses shards. Loads are issued four tiles
+// at a time so that enough of this HBM-bound pass is in flight.
+constexpr int kCombineWarps = 8;
+__global__ void __launch_bounds__(32 * kCombineWarps)
+    ce_combine_kernel(const float2 *__restrict__ stats, const float *__restrict__ tau,
+                      const int32_t *__restrict__ targets, int64_t T, int t, int tiles_per_shard, int v_valid,
+                      float *__restrict__ loss, float *__restrict__ lse, uint32_t *err) {
+    __shared__ float2 part[kCombineWarps][32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+    const bool live = r < T;
+    float M = -INFINITY, S = 0.0f;
+    if (live) {
+        for (int i = warp; i < t; i += kCombineWarps) {
+            // shard i's own statistics, from its vocabulary tiles
+            const float2 *p = stats + static_cast<int64_t>(i) * tiles_per_shard * T + r;
+            float mi = -INFINITY, si = 0.0f;
+            int k = 0;
+            for (; k + 4 <= tiles_per_shard; k += 4) {
+                float2 st[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) st[j] = __ldg(p + static_cast<int64_t>(k + j) * T);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) lse_fold(mi, si, st[j].x, st[j].y);
+            }
+            for (; k < tiles_per_shard; ++k) {
+                const float2 st = __ldg(p + static_cast<int64_t>(k) * T);
+                lse_fold(mi, si, st.x, st.y);
+            }
+            lse_fold(M, S, mi, si);  // the exchange
+        }
+    }
+    part[warp][lane] = make_float2(M, S);
+    __syncthreads();
+    if (warp != 0 || !live) return;
+    for (int w = 1; w < kCombineWarps; ++w) lse_fold(M, S, part[w][lane].x, part[w][lane].y);
     const int y = targets[r];
     if (y < 0 || y >= v_valid) {
         ptx::record_error(err, kErrInvalid | (1u << 8));
@@ -42,28 +86,16 @@ __global__ void ce_combine_kernel(const float2 *__restrict__ stats, const float 
         lse[r] = NAN;
         return;
     }
-    float M = -INFINITY, S = 0.0f;
-    for (int i = 0; i < t; ++i) {
-        // shard i's own statistics, from its vocabulary tiles
-        float mi = -INFINITY, si = 0.0f;
-        for (int k = 0; k < tiles_per_shard; ++k) {
-            const float2 st = stats[static_cast<int64_t>(i * tiles_per_shard + k) * T + r];
-            if (st.y > 0.0f) {
-                const float nm = fmaxf(mi, st.x);
-                si = si * expf(mi - nm) + st.y * expf(st.x - nm);
-                mi = nm;
-            }
-        }
-        // the exchange: only (m_i, s_i) crosses shards
-        if (si > 0.0f) {
-            const float nm = fmaxf(M, mi);
-            S = S * expf(M - nm) + si * expf(mi - nm);
-            M = nm;
-        }
-    }
     const float L = M + logf(S);
     lse[r] = L;
     loss[r] = L - tau[r];
+}
+
+inline void launch_ce_combine(const float2 *stats, const float *tau, const int32_t *targets, int64_t T, int t,
+                              int tiles_per_shard, int v_valid, float *loss, float *lse, uint32_t *err,
+                              cudaStream_t s) {
+    ce_combine_kernel<<<static_cast<unsigned>((T + 31) / 32), 32 * kCombineWarps, 0, s>>>(
+        stats, tau, targets, T, t, tiles_per_shard, v_valid, loss, lse, err);
 }
 
 }  // namespace

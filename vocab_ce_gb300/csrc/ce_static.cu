@@ -109,7 +109,6 @@ extern "C" tpce_status vocab_parallel_ce_loss_static(const void *H, const void *
         st = launch_gemm<__nv_bfloat16, 128, false, false, EpiCeStats>("ce_static_logits_stats", a, b, nullptr, nullptr, Ti, vpi, hi,
                                                                        0, 0, 0, 0, ep, s, /*timed=*/false);
     if (st != TPCE_OK) return st;
-    ce_combine_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, s>>>(
-        stats, tau, targets, T, t, static_cast<int>(n_tiles / t), vvi, loss, lse_buf, err);
+    launch_ce_combine(stats, tau, targets, T, t, static_cast<int>(n_tiles / t), vvi, loss, lse_buf, err, s);
     return check_launch("ce_static_combine", s);
 }

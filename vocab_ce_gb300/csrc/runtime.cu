@@ -223,7 +223,9 @@ struct ChunkedRows {
 
 // Stage 1: block (x, y) sums rows [y*rows_per, (y+1)*rows_per) of 256 columns
 // starting at 256*x; each lane owns 8 adjacent columns (one vector load per
-// row), the 8 warps stride over the rows, and shared memory combines the warps.
+// row), the 8 warps stride over the rows four rows at a time (four loads in
+// flight per lane: the pass is HBM-bound), and shared memory combines the
+// warps.
 template <typename T, class Rows>
 __global__ void __launch_bounds__(256) colsum_stage1(const Rows rows_of, int64_t R, int64_t N, int64_t rows_per,
                                                      float *__restrict__ part) {
@@ -234,7 +236,18 @@ __global__ void __launch_bounds__(256) colsum_stage1(const Rows rows_of, int64_t
     const int64_t r1 = min(R, r0 + rows_per);
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (c0 < N) {
-        for (int64_t r = r0 + warp; r < r1; r += 8) add8(rows_of.row(r) + c0, acc);
+        int64_t r = r0 + warp;
+        for (; r + 24 < r1; r += 32) {
+            float a0[8] = {0, 0, 0, 0, 0, 0, 0, 0}, a1[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            float a2[8] = {0, 0, 0, 0, 0, 0, 0, 0}, a3[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            add8(rows_of.row(r) + c0, a0);
+            add8(rows_of.row(r + 8) + c0, a1);
+            add8(rows_of.row(r + 16) + c0, a2);
+            add8(rows_of.row(r + 24) + c0, a3);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] += (a0[i] + a1[i]) + (a2[i] + a3[i]);
+        }
+        for (; r < r1; r += 8) add8(rows_of.row(r) + c0, acc);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) red[warp][lane * 8 + i] = acc[i];
