@@ -554,7 +554,17 @@ struct EpiCeStats : EpiBase {
                                  const float (&)[2][32], float (&)[1][32]) {
         const int g0 = p.n_base + n;                 // vocabulary id of v[0]
         const int nvalid = min(32, p.v_valid - g0);  // ids < v_valid are real
-        if (nvalid > 0) {
+        if (nvalid == 32) {
+            float cm = v[0];
+#pragma unroll
+            for (int i = 1; i < 32; ++i) cm = fmaxf(cm, v[i]);
+            const float nm = fmaxf(r.m, cm);
+            float acc = r.sum * __expf(r.m - nm);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc += __expf(v[i] - nm);
+            r.sum = acc;
+            r.m = nm;
+        } else if (nvalid > 0) {  // the chunk that holds the last real ids
             float cm = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -584,7 +594,10 @@ struct EpiCeStats : EpiBase {
 };
 
 // CE pass 2, first GEMM: recomputed logits -> dl = g (exp(l - lse) - onehot),
-// zero on padded ids.
+// zero on padded ids. Per element only the exponential: for g > 0 the scale
+// is folded into it (g exp(l - lse) = exp(l - (lse - ln g))); the padding and
+// the target column are handled per 32-column chunk, in the rare chunks that
+// hold them.
 template <typename OutT>
 struct EpiCeDlogits : EpiBase {
     static constexpr int kWarps = kHeavyEpiWarps;
@@ -592,7 +605,8 @@ struct EpiCeDlogits : EpiBase {
     static constexpr int kIns = 0;
     using Out = OutT;
     struct Row {
-        float lse;
+        float c;    // exp(l - c) * mul = g softmax(l)
+        float mul;  // 1 when g > 0 (folded into c), else g
         int tgt;
     };
     struct Params {
@@ -604,16 +618,31 @@ struct EpiCeDlogits : EpiBase {
     };
     __device__ static int mode(const Params &) { return 0; }
     __device__ static Row begin(const Params &p, int row, bool live) {
-        return Row{live ? __ldg(p.lse + row) : 0.0f, live ? __ldg(p.targets + row) : -1};
+        const float lse = live ? __ldg(p.lse + row) : 0.0f;
+        const bool fold = p.grad_scale > 0.0f;
+        return Row{fold ? lse - logf(p.grad_scale) : lse, fold ? 1.0f : p.grad_scale,
+                   live ? __ldg(p.targets + row) : -1};
     }
     __device__ static void chunk(const Params &p, Row &r, int, int n, int, bool, float (&v)[32],
                                  const float (&in)[2][32], float (&o)[kOuts][32]) {
-        const int g0 = p.n_base + n;
+        const int g0 = p.n_base + n;  // vocabulary id of v[0]
+        if (r.mul == 1.0f) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int g = g0 + i;
-            const float pr = __expf(v[i] - r.lse);
-            o[0][i] = g < p.v_valid ? p.grad_scale * (pr - (g == r.tgt ? 1.0f : 0.0f)) : 0.0f;
+            for (int i = 0; i < 32; ++i) o[0][i] = __expf(v[i] - r.c);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[0][i] = r.mul * __expf(v[i] - r.c);
+        }
+        if (g0 + 32 > p.v_valid) {  // padded ids: zero gradient
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (g0 + i >= p.v_valid) o[0][i] = 0.0f;
+        }
+        const int tl = r.tgt - g0;
+        if (static_cast<unsigned>(tl) < 32u) {  // the target column: minus g
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i == tl) o[0][i] -= p.grad_scale;
         }
     }
     __device__ static void end(const Params &, Row &, int, int, bool) {}
