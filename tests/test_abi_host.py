@@ -247,3 +247,22 @@ def test_profile_api_without_launches(L):
     assert L.tpce_profile_enable(1) == 0
     assert L.tpce_profile_count() == 0
     assert L.tpce_profile_enable(0) == 0
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    # a process whose library build is missing gets an error at its first call,
+    # never a result from some other implementation
+    import subprocess
+    import sys
+    code = ("import vocab_ce_gb300 as tp\n"
+            "try:\n"
+            "    tp.pad_vocab(50257, 8)\n"
+            "except Exception as e:\n"
+            "    print('raised', type(e).__name__)\n"
+            "else:\n"
+            "    print('no error')\n")
+    env = dict(__import__("os").environ, TPCE_LIBRARY=str(tmp_path / "libtpce.so"))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=300,
+                       cwd=__import__("os").path.dirname(__import__("os").path.dirname(__file__)))
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.startswith("raised"), r.stdout
