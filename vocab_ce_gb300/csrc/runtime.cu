@@ -270,9 +270,10 @@ __global__ void colsum_stage2(const float *__restrict__ part, int S, int64_t N, 
     out[c] = s;
 }
 
-// Row splits of the column sum: enough blocks to cover the SMs about twice.
+// Row splits of the column sum: enough blocks to cover the SMs about four times
+// (with four row loads in flight per lane, enough bytes in flight to fill HBM).
 // Fixed (not queried from the device) so workspace sizes are known on the host.
-constexpr int64_t kColsumTargetBlocks = 2 * 152;
+constexpr int64_t kColsumTargetBlocks = 4 * 152;
 
 static int colsum_splits(int64_t R, int64_t N) {
     const int64_t col_blocks = (N + 255) / 256;
