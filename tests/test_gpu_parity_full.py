@@ -11,7 +11,13 @@ of dZ, recomputed in full. dE needs the softmax of every token,
 so it is checked in full on a run over the first tokens at the full h and v.
 The shard sweep checks that t = 1 and t = 16 give bit-identical outputs at
 full size.
+
+With TPCE_FULL_ORACLE=1 the 8.3B-shaped block is also compared element by
+element in full (every row and column of every output; a few minutes of
+host time for the oracle).
 """
+
+import os
 
 import numpy as np
 import pytest
@@ -83,6 +89,33 @@ def test_gpt8b_block_full_size():
     w = wl.WORKLOADS["gpt8b"]
     check_mlp_full(w, dev)
     check_ce_full(w, dev, de_tokens=128)
+
+
+@pytest.mark.skipif(os.environ.get("TPCE_FULL_ORACLE") != "1", reason="opt-in: TPCE_FULL_ORACLE=1")
+def test_gpt8b_block_full_oracle():
+    # every element of the 8.3B-shaped block's outputs against the fp64 oracle
+    dev = gpu_or_skip()
+    w = wl.WORKLOADS["gpt8b"]
+    mi = wl.mlp_inputs(w, seed=0, device=dev)
+    fwd = tp.tp_mlp_forward(mi["X"], mi["A"], mi["B"], w.t, mi["bA"], mi["bB"])
+    bwd = tp.tp_mlp_backward(mi["dZ"], mi["X"], mi["A"], mi["B"], fwd["U"], fwd["Y"], w.t)
+    ci = wl.ce_inputs(w, seed=0, device=dev)
+    gs = 1.0 / w.T
+    out = tp.vocab_parallel_ce(ci["H"], ci["E"], ci["targets"], w.v_valid, w.t, grad_scale=gs)
+    assert tp.device_status() == 0
+    X, A, B, dZ = (_host(mi[k]) for k in ("X", "A", "B", "dZ"))
+    bA, bB = _host(mi["bA"]), _host(mi["bB"])
+    of = oracle.mlp_forward(X, A, bA, B, bB)
+    for k in ("U", "Y", "Z"):
+        assert_rel(k, _host(fwd[k]), of[k])
+    ob = oracle.mlp_backward(X, A, bA, B, dZ)
+    for k in ("dX", "dA", "dbA", "dB", "dbB"):
+        assert_rel(k, _host(bwd[k]), ob[k])
+    ref = oracle.ce(_host(ci["H"]), _host(ci["E"]), _host(ci["targets"]).numpy(), w.v_valid, grad_scale=gs)
+    assert_loss("loss", _host(out["loss"]), ref["loss"])
+    assert_loss("lse", _host(out["lse"]), ref["lse"])
+    assert_rel("dH", _host(out["dH"]), ref["dH"])
+    assert_rel("dE", _host(out["dE"]), ref["dE"])
 
 
 def test_mlp70b_full_size():
