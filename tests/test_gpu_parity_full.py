@@ -74,6 +74,13 @@ def check_ce_full(w, dev, seed=0, de_tokens=48):
     assert_loss("lse", _host(out["lse"])[rows], ref["lse"])
     assert_rel("dH", _host(out["dH"])[rows], ref["dH"])
     assert torch.count_nonzero(out["dE"][w.v_valid:]).item() == 0
+    # sum_v dl_tv = 0 for every token, hence sum_v dE_v = 0 at full size, up to the
+    # bf16 rounding of dl and dE (each at most 2^-8 of the magnitudes summed)
+    dEf = out["dE"].float()
+    col_sum = dEf.sum(0).abs().max().item()
+    col_abs = dEf.abs().sum(0).max().item()
+    assert col_sum <= 1e-2 * col_abs, f"sum_v dE_v = {col_sum} against sum_v |dE_v| = {col_abs}"
+    del dEf
     # dE in full on the first de_tokens tokens, same h and vocabulary
     sub = tp.vocab_parallel_ce(ci["H"][:de_tokens].contiguous(), ci["E"], ci["targets"][:de_tokens].contiguous(),
                                w.v_valid, w.t, grad_scale=1.0)
