@@ -266,3 +266,20 @@ def test_missing_library_fails_loudly(tmp_path):
                        cwd=__import__("os").path.dirname(__import__("os").path.dirname(__file__)))
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.startswith("raised"), r.stdout
+
+
+def test_python_binding_rejects_bad_tensors_before_the_library():
+    # host tensors, wrong dtypes and non-contiguous views are refused in Python,
+    # before any pointer reaches the library (no GPU needed)
+    import torch
+    import vocab_ce_gb300 as tp
+    X = torch.zeros(32, 64, dtype=torch.bfloat16)
+    A = torch.zeros(64, 256, dtype=torch.bfloat16)
+    B = torch.zeros(256, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        tp.tp_mlp_forward(X, A, B, 2)
+    H = torch.zeros(32, 64, dtype=torch.bfloat16)
+    E = torch.zeros(512, 64, dtype=torch.bfloat16)
+    y = torch.zeros(32, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        tp.vocab_parallel_ce(H, E, y, 512, 2)

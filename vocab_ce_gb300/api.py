@@ -30,6 +30,9 @@ def _stream(stream) -> ctypes.c_void_p:
 def _need(x: torch.Tensor, name: str, dtype=None, shape=None):
     if not x.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if x.device.index != torch.cuda.current_device():
+        # the library launches on the current device's stream
+        raise ValueError(f"{name} is on {x.device}, not on the current device cuda:{torch.cuda.current_device()}")
     if not x.is_contiguous():
         raise ValueError(f"{name} must be contiguous (row-major)")
     if dtype is not None and x.dtype != dtype:
