@@ -40,6 +40,8 @@ MLP_CASES = {
     "ragged": (333, 200, 384, 2, "bf16"),
     "multi_tile": (640, 512, 1024, 4, "bf16"),
     "one_token": (1, 64, 128, 2, "bf16"),
+    "min_hidden": (5, 8, 128, 2, "bf16"),            # h = 8: one k-block, mostly zero-filled by TMA
+    "min_hidden_f32": (5, 8, 128, 2, "f32"),
     "wide_n_tiles": (1000, 1536, 3072, 8, "bf16"),   # picks 192-wide tiles
     "ragged_f32": (333, 200, 384, 2, "f32"),
     "multi_tile_f32": (300, 256, 512, 4, "f32"),
@@ -131,6 +133,7 @@ CE_CASES = {
     "ragged_bn128": (333, 200, 768, 700, 2, "bf16"),          # shard = 384 ids: 128-wide tiles
     "padded_shards": (130, 96, 2048, 1800, 16, "bf16"),       # shard 15 holds only padding
     "single_shard": (257, 128, 1024, 1000, 1, "bf16"),        # t = 1: the unsharded loss
+    "min_hidden": (7, 8, 256, 200, 2, "bf16"),                # h = 8: one mostly zero-filled k-block
     "multi_tile": (600, 320, 4096, 4000, 4, "bf16"),
     "wide_h": (700, 1536, 3072, 3000, 4, "bf16"),             # dE / dH pick 192-wide tiles
     "ragged_f32": (333, 200, 768, 700, 2, "f32"),
