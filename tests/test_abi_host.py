@@ -283,3 +283,13 @@ def test_python_binding_rejects_bad_tensors_before_the_library():
     y = torch.zeros(32, dtype=torch.int32)
     with pytest.raises(ValueError, match="CUDA tensor"):
         tp.vocab_parallel_ce(H, E, y, 512, 2)
+
+
+def test_dimensions_beyond_32_bit_coordinates_are_rejected(L):
+    # kernel coordinates are 32-bit: a dimension at or above 2^31 is a shape
+    # error, reported by the size queries before any call could be made
+    big = 1 << 31
+    assert L.tpce_mlp_workspace_bytes(big, 64, 256, 2, 0) == 0
+    assert L.tpce_mlp_workspace_bytes(64, big, 256, 2, 0) == 0
+    assert L.tpce_ce_workspace_bytes(big, 64, 512, 2, 0, 1) == 0
+    assert L.tpce_ce_workspace_bytes(64, 64, big, 2, 0, 1) == 0

@@ -197,6 +197,25 @@ def test_ce_closed_form_zero_embedding():
     assert torch.count_nonzero(out["dH"]).item() == 0
 
 
+def test_ce_single_real_id():
+    # v_valid = 1: the softmax over the one real id is exactly the one-hot target,
+    # so the loss is 0 and dl, dH, dE vanish exactly; shard 1 holds only padding
+    dev = gpu_or_skip()
+    T, h, v_pad, v_valid, t = 96, 64, 256, 1, 2
+    g = torch.Generator().manual_seed(21)
+    H = torch.randn(T, h, generator=g).to(torch.bfloat16).to(dev)
+    E = (0.5 * torch.randn(v_pad, h, generator=g)).to(torch.bfloat16).to(dev)
+    y = torch.zeros(T, dtype=torch.int32, device=dev)
+    out = tp.vocab_parallel_ce(H, E, y, v_valid, t)
+    assert tp.device_status() == 0
+    assert torch.count_nonzero(out["loss"]).item() == 0
+    assert torch.count_nonzero(out["dH"]).item() == 0
+    assert torch.count_nonzero(out["dE"]).item() == 0
+    # lse is the target logit itself
+    ref = oracle.ce(H.cpu(), E.cpu(), y.cpu().numpy(), v_valid, want_dE=False)
+    assert_loss("lse", out["lse"], ref["lse"])
+
+
 def test_empty_token_batch():
     dev = gpu_or_skip()
     h, f, t = 64, 256, 2
