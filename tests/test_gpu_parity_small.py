@@ -197,6 +197,26 @@ def test_ce_closed_form_zero_embedding():
     assert torch.count_nonzero(out["dH"]).item() == 0
 
 
+def test_ce_large_logits():
+    # logits with standard deviation ~30 (maxima near 100): exp without the running
+    # max would overflow fp32; loss, lse and gradients still match the fp64 oracle
+    dev = gpu_or_skip()
+    T, h, v_pad, v_valid, t = 96, 64, 1024, 1000, 4
+    g = torch.Generator().manual_seed(23)
+    H = torch.randn(T, h, generator=g).to(torch.bfloat16)
+    E = (3.75 * torch.randn(v_pad, h, generator=g)).to(torch.bfloat16)
+    y = torch.randint(0, v_valid, (T,), generator=g, dtype=torch.int64).to(torch.int32)
+    out = tp.vocab_parallel_ce(H.to(dev), E.to(dev), y.to(dev), v_valid, t, grad_scale=1.0 / T)
+    assert tp.device_status() == 0
+    assert torch.isfinite(out["loss"]).all() and torch.isfinite(out["dH"].float()).all()
+    ref = oracle.ce(H, E, y.numpy(), v_valid, grad_scale=1.0 / T)
+    assert float(np.abs(ref["lse"]).max()) > 60.0  # the case really has large logits
+    assert_loss("loss", out["loss"], ref["loss"])
+    assert_loss("lse", out["lse"], ref["lse"])
+    assert_rel("dH", out["dH"], ref["dH"])
+    assert_rel("dE", out["dE"], ref["dE"])
+
+
 def test_ce_single_real_id():
     # v_valid = 1: the softmax over the one real id is exactly the one-hot target,
     # so the loss is 0 and dl, dH, dE vanish exactly; shard 1 holds only padding
