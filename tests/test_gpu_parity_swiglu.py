@@ -94,6 +94,29 @@ def test_swish_and_derivative_evaluation_error_fp32():
     assert np.abs(db1[:f] - dsw).max() <= 2e-6
 
 
+def test_swish_saturated_gates_fp32():
+    # |G| up to 120: exp overflows inside the sigmoid, which must still give the
+    # limits Swish -> 0 (G << 0), G (G >> 0) and Swish' -> 0, 1, with no NaN
+    dev = gpu_or_skip()
+    h = f = 256
+    X = torch.linspace(-120.0, 120.0, h, dtype=torch.float32).reshape(1, h).to(dev)
+    I = torch.eye(h, dtype=torch.float32, device=dev)
+    W1 = torch.cat([I, torch.zeros_like(I)], dim=1).contiguous()
+    b1 = torch.cat([torch.zeros(f), torch.ones(f)]).float().to(dev)
+    fwd = tp.tp_swiglu_forward(X, W1, I, 2, b1)
+    bwd = tp.tp_swiglu_backward(torch.ones(1, h, device=dev), X, W1, I, fwd["GU"], fwd["Y"], 2)
+    assert tp.device_status() == 0
+    G = fwd["GU"].double().cpu().numpy()[0, :f]
+    Y = fwd["Y"].double().cpu().numpy()[0]
+    db1 = bwd["db1"].double().cpu().numpy()
+    assert np.isfinite(Y).all() and np.isfinite(db1).all()
+    sw = np.array([oracle.swish(g) for g in G])
+    dsw = np.array([oracle.swish_grad(g) for g in G])
+    assert np.abs(Y - sw).max() <= 2e-6 * np.abs(G).max()
+    assert np.abs(db1[f:] - sw).max() <= 2e-6 * np.abs(G).max()
+    assert np.abs(db1[:f] - dsw).max() <= 2e-6
+
+
 def test_swiglu_shard_count_does_not_change_results():
     dev = gpu_or_skip()
     base = None
