@@ -93,6 +93,26 @@ def test_gelu_and_derivative_evaluation_error_fp32():
     assert np.abs(dU - dgelu).max() <= 1e-6
 
 
+def test_gelu_far_tails_fp32():
+    # |u| up to 120: e^{-u^2/2} underflows to 0, and GeLU -> max(u, 0),
+    # GeLU' -> 1 or 0, with no NaN
+    dev = gpu_or_skip()
+    h = f = 256
+    X = torch.linspace(-120.0, 120.0, h, dtype=torch.float32).reshape(1, h).to(dev)
+    I = torch.eye(h, dtype=torch.float32, device=dev)
+    fwd = tp.tp_mlp_forward(X, I, I, 2)
+    bwd = tp.tp_mlp_backward(torch.ones(1, h, device=dev), X, I, I, fwd["U"], fwd["Y"], 2)
+    assert tp.device_status() == 0
+    U = fwd["U"].double().cpu().numpy()[0]
+    Y = fwd["Y"].double().cpu().numpy()[0]
+    dU = bwd["dbA"].double().cpu().numpy()
+    assert np.isfinite(Y).all() and np.isfinite(dU).all()
+    gelu = np.array([oracle.gelu(u) for u in U])
+    dgelu = np.array([oracle.gelu_grad(u) for u in U])
+    assert np.abs(Y - gelu).max() <= 1e-6 * np.abs(U).max()
+    assert np.abs(dU - dgelu).max() <= 1e-6
+
+
 @pytest.mark.parametrize("case", list(MLP_CASES))
 def test_mlp_matches_oracle(case):
     dev = gpu_or_skip()
