@@ -3,20 +3,31 @@
 vocabulary-parallel cross-entropy forward+backward, all t shards on one GPU.
 
 One step = one pass of the whole path over one batch of synthetic inputs
-resident in HBM: tp_mlp_forward, tp_mlp_backward, vocab_parallel_ce (loss,
-dH, dE). The default workload is the 8.3B-shaped block (T = 8192 tokens,
-h = 3072, f = 12288, vocabulary 50,257 padded to 51,200, t = 8).
+resident in HBM. The default workload, ``headline``, is the pair of
+configurations the targets are stated on, run back to back in every step:
+
+* the 70B-shaped GeLU MLP block forward+backward (T = 4096 tokens, h = 8192,
+  f = 32768, t = 8): tp_mlp_forward, tp_mlp_backward;
+* the fused vocabulary-parallel logit GEMM + cross-entropy forward+backward
+  over a 128,256-id vocabulary padded to 129,024 (T = 16,384, h = 8192,
+  t = 8): vocab_parallel_ce with loss, dH and dE.
 
 Printed (rank 0, one JSON line): whole-job TFLOP/s over the step (MLP
 12 T h f + CE 8 T h v_pad FLOPs, the CE count including the logit recompute
-that unmaterialised logits require), the MLP TFLOP/s and CE tokens/s parts,
-the end-to-end figure through the Python API from pinned host buffers, the
-roofline of the dominant kernel, SM clocks during the timed region, and the
-CPU oracle timed on a bounded sample on this host.
+that unmaterialised logits require), the MLP TFLOP/s and CE tokens/s parts
+with their fractions of the dense bf16 peak (2.25 PFLOP/s nominal, and the
+measured burst and sustained figures), the end-to-end figure through the
+Python API from pinned host buffers, the roofline of the dominant kernel,
+SM clocks during the timed region, and the CPU oracle timed on a bounded
+sample on this host.
+
+The headline timing runs with the library's kernel timer off; the per-kernel
+figures (and the dominant kernel's roofline) come from a second pass of the
+same steps with the timer on, right after.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W]
                        [--impl ours|reference]
-                       [--workload gpt8b|gpt8b_chain|mlp70b|mlp70b_sp|ce128k|ce128k_eval|
+                       [--workload headline|gpt8b|gpt8b_chain|mlp70b|mlp70b_sp|ce128k|ce128k_eval|
                                    swiglu70b|attn70b|sweep]
 Multi-GPU (one process per GPU under torchrun): every rank runs its own
 independent batch (data parallel, weak scaling); there is no collective on
@@ -47,26 +58,40 @@ METRIC = "TP-MLP fwd+bwd TFLOP/s and fused vocab-parallel CE tokens/s vs rooflin
 UNIT = "TFLOP/s"
 # fallbacks only if the generated MEASURED_PEAKS.json is absent
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# tokens the CPU oracle processes per timed sample
+# nominal dense bf16 tensor peak of a GB300, the figure the targets are stated against
+SPEC_BF16_TFLOPS = 2250.0
+# targets: MLP at >= 60% of the dense bf16 peak, fused CE at >= 50% of its roofline
+TARGETS = {"mlp_frac_of_spec_peak": 0.60, "ce_frac_of_spec_roofline": 0.50}
+# a timed region at least this long runs under the power cap: its kernels are
+# compared with the measured sustained peak, shorter ones with the burst peak
+SUSTAINED_REGION_S = 1.0
+
+# the workloads of each job, run back to back in one step
+JOBS = {"headline": ("mlp70b", "ce128k")}
+WORKLOAD_NAMES = ["headline", "gpt8b", "gpt8b_chain", "mlp70b", "mlp70b_sp", "ce128k", "ce128k_eval", "swiglu70b",
+                  "attn70b", "sweep"]
+# tokens of each workload the CPU oracle processes per timed sample
 CPU_SAMPLE_TOKENS = {"gpt8b": 512, "gpt8b_chain": 512, "mlp70b": 192, "mlp70b_sp": 192, "ce128k": 96, "ce128k_eval": 256,
                      "swiglu70b": 144, "attn70b": 512, "sweep": 512}
+CPU_SAMPLE_TOKENS_JOB = {"headline": {"mlp70b": 96, "ce128k": 48}}
 REF_STEP_TOKENS = {"gpt8b": 8, "gpt8b_chain": 8, "mlp70b": 4, "mlp70b_sp": 4, "ce128k": 2, "ce128k_eval": 4, "swiglu70b": 3,
                    "attn70b": 8, "sweep": 8}
+REF_STEP_TOKENS_JOB = {"headline": {"mlp70b": 1, "ce128k": 2}}
 
 
 # ---------------------------------------------------------------------- setup
-def parse_args():
+def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["gpt8b", "gpt8b_chain", "mlp70b", "mlp70b_sp", "ce128k", "ce128k_eval",
-                                          "swiglu70b", "attn70b", "sweep"], default="gpt8b")
+    p.add_argument("--workload", choices=WORKLOAD_NAMES, default="headline")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
-    return p.parse_args()
+    p.add_argument("--no-kernel-pass", action="store_true", help="skip the per-kernel timing pass")
+    return p.parse_args(argv)
 
 
 def dist_env():
@@ -101,7 +126,13 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def job_workloads(name):
+    """The workloads one step of job `name` runs, in launch order."""
+    return [wl.WORKLOADS[n] for n in JOBS.get(name, (name,))]
+
+
 def flops(w):
+    """(MLP-side, CE-side) FLOPs of one step of workload w, in the bench's convention."""
     # GeLU block: 4 T h f forward + 8 T h f backward; SwiGLU: GEMM1 is twice as
     # wide (6 T h f forward, 12 T h f backward)
     mlp = (18.0 if w.act == "swiglu" else 12.0) * w.T * w.h * w.f if w.f else 0.0
@@ -111,6 +142,19 @@ def flops(w):
     if w.n_heads:
         nqkv = (w.n_heads + 2 * w.n_kv_heads) * w.head_dim
         mlp += 6.0 * w.T * w.h * nqkv + 6.0 * w.T * (w.n_heads * w.head_dim) * w.h
+    return mlp, ce
+
+
+def ce_model_flops(w):
+    """CE model FLOPs over the real vocabulary without the backward's logit
+    recompute: 6 T h v_valid with gradients (logits, dH, dE), 2 T h v_valid
+    for the loss alone."""
+    return ((6.0 if w.ce_grads else 2.0) * w.T * w.h * w.v_valid) if w.v_pad else 0.0
+
+
+def job_flops(ws_):
+    mlp = sum(flops(w)[0] for w in ws_)
+    ce = sum(flops(w)[1] for w in ws_)
     return mlp, ce
 
 
@@ -136,6 +180,19 @@ def workload_config(w, name):
     if w.n_heads:
         cfg.update(n_heads=w.n_heads, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim)
     return cfg
+
+
+def job_config(name, ws_):
+    """The `config` of a job: one workload's, or for a composite job a
+    description naming every part and each part's own config."""
+    if len(ws_) == 1:
+        return workload_config(ws_[0], name)
+    parts = {w.name: workload_config(w, w.name) for w in ws_}
+    m, c = ws_
+    text = (f"70B-shaped MLP fwd+bwd (T={m.T}, h={m.h}, f={m.f}, GeLU, t={m.t}) then vocab-parallel fused logit GEMM "
+            f"+ CE fwd+bwd (T={c.T}, h={c.h}, vocabulary {c.v_valid:,} padded to {c.v_pad:,}, t={c.t}), each step")
+    return {"workload": text, "parts": parts, "seed": 0,
+            "inputs": "seeded synthetic (workloads.py recipe), resident in HBM"}
 
 
 # ---------------------------------------------------------------------- clocks
@@ -352,6 +409,24 @@ class Step:
             fn()
 
 
+class Job:
+    """The steps of every workload of a job, run back to back."""
+
+    def __init__(self, ws_, dev, seed):
+        self.steps = [Step(w, dev, seed) for w in ws_]
+
+    def segments(self, ins=None):
+        seg = []
+        for k, st in enumerate(self.steps):
+            mi, ci, ai = ins[k] if ins else (None, None, None)
+            seg += st.segments(mi, ci, ai)
+        return seg
+
+    def run(self, ins=None):
+        for _, fn in self.segments(ins):
+            fn()
+
+
 def input_bytes(step):
     b = 0
     for tag, d in (("m", step.mi), ("c", step.ci), ("a", step.ai)):
@@ -410,45 +485,50 @@ def oracle_step(w, s):
         oracle.ce(s["H"], s["E"], s["y"], w.v_valid, grad_scale=1.0, grads=w.ce_grads)
 
 
-def oracle_rate(w, s, n_tokens, reps=1):
-    """(TFLOP/s in the bench's FLOP convention, seconds per rep)."""
-    mlp, ce = flops(w)
-    work = (mlp + ce) / w.T * n_tokens
-    t0 = time.perf_counter()
-    for _ in range(reps):
-        oracle_step(w, s)
-    dt = (time.perf_counter() - t0) / reps
-    return work / dt / 1e12, dt
+def sample_work(ws_, tokens):
+    """FLOPs (bench convention) of processing tokens[w.name] tokens of each workload."""
+    return sum(sum(flops(w)) / w.T * tokens[w.name] for w in ws_)
+
+
+def sample_text(ws_, tokens):
+    return " + ".join(f"first {tokens[w.name]} of {w.T} tokens of {w.name}" for w in ws_)
 
 
 # ---------------------------------------------------------------------- arms
-def run_reference(args, w, name):
+def run_reference(args, ws_, name):
     import oracle
 
-    ws, rank, _ = dist_env()
+    _, rank, _ = dist_env()
     if rank != 0:
         return 0
     oracle.build()
-    n = REF_STEP_TOKENS[name]
-    mi = ((wl.swiglu_inputs if w.act == "swiglu" else wl.mlp_inputs)(w, seed=0)) if w.f else None
-    ci = wl.ce_inputs(w, seed=0) if w.v_pad else None
-    ai = wl.attn_inputs(w, seed=0) if w.n_heads else None
-    s = oracle_sample(w, mi, ci, n, ai)
+    tokens = REF_STEP_TOKENS_JOB.get(name) or {ws_[0].name: REF_STEP_TOKENS[name]}
+    samples = []
+    for w in ws_:
+        mi = ((wl.swiglu_inputs if w.act == "swiglu" else wl.mlp_inputs)(w, seed=0)) if w.f else None
+        ci = wl.ce_inputs(w, seed=0) if w.v_pad else None
+        ai = wl.attn_inputs(w, seed=0) if w.n_heads else None
+        samples.append((w, oracle_sample(w, mi, ci, tokens[w.name], ai)))
+        del mi, ci, ai
+
+    def step():
+        for w, s in samples:
+            oracle_step(w, s)
+
     for _ in range(args.warmup):
-        oracle_step(w, s)
+        step()
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle_step(w, s)
+        step()
         times.append(time.perf_counter() - t0)
     dt = sum(times) / len(times)
-    mlp, ce = flops(w)
-    value = (mlp + ce) / w.T * n / dt / 1e12
-    sample = f"first {n} of {w.T} tokens at full h, f, v per step (weights in full), fp64 oracle"
+    value = sample_work(ws_, tokens) / dt / 1e12
+    sample = f"{sample_text(ws_, tokens)} per step at full h, f, v (weights in full), fp64 oracle"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w, name),
+            "config": job_config(name, ws_),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -456,7 +536,80 @@ def run_reference(args, w, name):
     return 0
 
 
-def run_ours(args, w, name):
+def time_steps(job, steps, stream, profiled=False, clocks=None):
+    """Run `steps` steps between two events on `stream`; per-segment events
+    give the MLP and CE parts. Returns (elapsed ms, {part: ms}, kernels)."""
+    import vocab_ce_gb300 as tp
+
+    segs = job.segments()
+    ev = [[(part, torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for part, _ in segs]
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    if profiled:
+        tp.profile_enable(True)
+    sampler = clocks() if clocks else None
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(steps):
+        for (_, a, b), (_, fn) in zip(ev[i], segs):
+            a.record(stream)
+            fn()
+            b.record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = sampler.stop() if sampler else None
+    kernels = None
+    if profiled:
+        kernels = tp.profile_read()
+        tp.profile_enable(False)
+    parts = {}
+    for e in ev:
+        for part, a, b in e:
+            parts[part] = parts.get(part, 0.0) + a.elapsed_time(b)
+    return t_start.elapsed_time(t_end), {k: v / steps for k, v in parts.items()}, kernels, clk
+
+
+def fractions(ws_, mlp_ms, ce_ms, pk):
+    """The parts of a step and their fractions of the dense bf16 peak: the
+    nominal 2.25 PFLOP/s the targets are stated against, and the measured
+    burst and sustained figures."""
+    mlp_fl, ce_fl = job_flops(ws_)
+    out = {}
+    has_mlp = any(w.f for w in ws_)
+    has_attn = any(w.n_heads for w in ws_)
+    ce_ws = [w for w in ws_ if w.v_pad]
+    denoms = {"spec": SPEC_BF16_TFLOPS, "measured_burst": pk["bf16_tflops"],
+              "measured_sustained": pk["bf16_tflops_sustained"]}
+    if (has_mlp or has_attn) and mlp_ms:
+        r = mlp_fl / (mlp_ms * 1e-3) / 1e12
+        key = "mlp" if has_mlp else "attn_proj"
+        out[f"{key}_tflops"] = r
+        out[f"{key}_ms"] = mlp_ms
+        out[f"{key}_frac_of_spec_peak"] = r / denoms["spec"]
+        out[f"{key}_frac_of_measured_burst_peak"] = r / denoms["measured_burst"]
+        out[f"{key}_frac_of_measured_sustained_peak"] = r / denoms["measured_sustained"]
+    if ce_ws and ce_ms:
+        T = sum(w.T for w in ce_ws)
+        r = ce_fl / (ce_ms * 1e-3) / 1e12
+        tok = T / (ce_ms * 1e-3)
+        model = sum(ce_model_flops(w) for w in ce_ws) / (ce_ms * 1e-3) / 1e12
+        # the roofline in tokens/s: the peak over the FLOPs one token costs (8 h v_pad, or 2 h v_pad forward only)
+        per_tok = ce_fl / T
+        out.update(ce_tokens_per_s=tok, ce_ms=ce_ms, ce_tflops=r,
+                   ce_roofline_tokens_per_s_spec=denoms["spec"] * 1e12 / per_tok,
+                   ce_frac_of_spec_roofline=r / denoms["spec"],
+                   ce_frac_of_measured_burst_roofline=r / denoms["measured_burst"],
+                   ce_frac_of_measured_sustained_roofline=r / denoms["measured_sustained"],
+                   ce_model_tflops=model, ce_model_frac_of_spec_peak=model / denoms["spec"],
+                   ce_flop_convention=("8 T h v_pad with gradients (logits, their recompute in the backward, dE, dH; "
+                                       "padded ids count, they are computed), 2 T h v_pad forward only; the model "
+                                       "figure counts 6 T h v_valid (2 T h v_valid forward only): no recompute, "
+                                       "real ids only"))
+    return out
+
+
+def run_ours(args, ws_, name):
     ws, rank, local = dist_env()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -466,10 +619,10 @@ def run_ours(args, w, name):
         dist.init_process_group("nccl", device_id=dev)
     import vocab_ce_gb300 as tp
 
-    step = Step(w, dev, seed=rank)
+    job = Job(ws_, dev, seed=rank)
     stream = torch.cuda.current_stream()
     for _ in range(max(3, args.warmup)):
-        step.run()
+        job.run()
     torch.cuda.synchronize()
     assert tp.device_status() == 0, "device status after warm-up"
 
@@ -479,131 +632,61 @@ def run_ours(args, w, name):
 
             dist.barrier()
 
-    # ---------------- timed region (device-resident inputs)
-    mlp_fl, ce_fl = flops(w)
-    segs = step.segments()
-    ev = [[(part, torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for part, _ in segs]
-          for _ in range(args.steps)]
-    clocks = ClockSampler(dev, enabled=not args.no_clocks)
+    # ---------------- timed region (device-resident inputs, kernel timer off)
+    mlp_fl, ce_fl = job_flops(ws_)
     barrier()
-    torch.cuda.synchronize()
-    tp.profile_enable(True)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        for (_, a, b), (_, fn) in zip(ev[i], segs):
-            a.record(stream)
-            fn()
-            b.record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
+    elapsed_ms, parts_ms, _, clk = time_steps(
+        job, args.steps, stream, clocks=(lambda: ClockSampler(dev)) if not args.no_clocks else None)
     barrier()
-    kernels = tp.profile_read()
-    tp.profile_enable(False)
-    clk = clocks.stop()
     assert tp.device_status() == 0, "device status after the timed region"
-    elapsed_ms = t_start.elapsed_time(t_end)
     elapsed_ms = max_over_ranks(elapsed_ms, ws, dev)
     ms_step = elapsed_ms / args.steps
-    mlp_ms = sum(a.elapsed_time(b) for e in ev for part, a, b in e if part == "mlp") / args.steps
-    ce_ms = sum(a.elapsed_time(b) for e in ev for part, a, b in e if part == "ce") / args.steps
     value = job_rate(ws, mlp_fl + ce_fl, ms_step * 1e-3) / 1e12
+    region_s = elapsed_ms * 1e-3
 
     pk, pk_src = peaks()
-    # ---------------- roofline of the dominant kernel
-    dominant = max(kernels.items(), key=lambda kv: kv[1]["ms"]) if kernels else None
-    roof = None
-    if dominant:
-        kname, kd = dominant
-        kflops = kernel_flops_per_step(kname, w)
-        launches_per_step = kd["launches"] / args.steps
-        per_launch = kflops / launches_per_step if kflops and launches_per_step else None
-        avg_ms = kd["ms"] / kd["launches"]
-        if per_launch:
-            achieved = per_launch / (avg_ms * 1e-3) / 1e12
-            roof = {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": pk["bf16_tflops_sustained"],
-                    "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"],
-                    "peak_kind": f"{pk_src} sustained bf16 (kernel timed inside a long step)",
-                    "frac_of_burst_peak": achieved / pk["bf16_tflops"],
-                    "flops_per_launch": per_launch, "avg_launch_ms": avg_ms,
-                    "traffic": traffic_from_profiles(kname, name)}
-    gpu_launches = int(sum(k["launches"] for k in kernels.values()))
-    per_kernel = {k: {"launches": v["launches"], "ms_per_step": v["ms"] / args.steps,
-                      "tflops": (kernel_flops_per_step(k, w) / (v["ms"] / args.steps * 1e-3) / 1e12)
-                      if kernel_flops_per_step(k, w) else None}
-                  for k, v in sorted(kernels.items(), key=lambda kv: -kv[1]["ms"])}
+    sustained = region_s >= SUSTAINED_REGION_S
+    peak = pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]
+    peak_kind = (f"{pk_src} {'sustained' if sustained else 'burst'} bf16: the kernel runs inside a timed region of "
+                 f"{region_s:.2f} s of back-to-back steps ({'>=' if sustained else '<'} {SUSTAINED_REGION_S:.0f} s)")
+
+    # ---------------- per-kernel pass: the same steps with the library's kernel timer on
+    roof, per_kernel, gpu_launches = None, None, None
+    if not args.no_kernel_pass:
+        barrier()
+        _, _, kernels, _ = time_steps(job, args.steps, stream, profiled=True)
+        barrier()
+        assert tp.device_status() == 0, "device status after the kernel pass"
+        dominant = max(kernels.items(), key=lambda kv: kv[1]["ms"]) if kernels else None
+        if dominant:
+            kname, kd = dominant
+            kflops = kernel_flops_per_step(kname, ws_)
+            launches_per_step = kd["launches"] / args.steps
+            per_launch = kflops / launches_per_step if kflops and launches_per_step else None
+            avg_ms = kd["ms"] / kd["launches"]
+            if per_launch:
+                achieved = per_launch / (avg_ms * 1e-3) / 1e12
+                roof = {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                        "frac": achieved / peak, "peak_kind": peak_kind,
+                        "frac_of_measured_burst_peak": achieved / pk["bf16_tflops"],
+                        "frac_of_measured_sustained_peak": achieved / pk["bf16_tflops_sustained"],
+                        "frac_of_spec_peak": achieved / SPEC_BF16_TFLOPS,
+                        "flops_per_launch": per_launch, "avg_launch_ms": avg_ms,
+                        "timing": "CUDA events around each launch on its stream, in a second pass of the same "
+                                  "steps right after the headline timing",
+                        "traffic": traffic_from_profiles(kname, owner_workload(kname, ws_))}
+        # the kernel pass ran the same steps as the timed region, and every
+        # launch of a step is one of this library's kernels
+        gpu_launches = int(sum(k["launches"] for k in kernels.values()))
+        per_kernel = {k: {"launches_per_step": v["launches"] / args.steps, "ms_per_step": v["ms"] / args.steps,
+                          "tflops": (kernel_flops_per_step(k, ws_) / (v["ms"] / args.steps * 1e-3) / 1e12)
+                          if kernel_flops_per_step(k, ws_) else None}
+                      for k, v in sorted(kernels.items(), key=lambda kv: -kv[1]["ms"])}
 
     # ---------------- end to end: pinned host inputs -> device, the step, loss -> host
     e2e = None
     if not args.no_e2e:
-        host = {}
-        for tag, src in (("m", step.mi), ("c", step.ci), ("a", step.ai)):
-            if src:
-                for k, v in src.items():
-                    if (tag, k) not in step.unused:
-                        host[tag + k] = v.cpu().pin_memory()
-        # two device copies of the inputs: step i+1's inputs are copied on a
-        # second stream while step i computes from the other set
-        dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
-        loss_host = torch.empty(w.T, dtype=torch.float32).pin_memory() if w.v_pad else None
-        z_host = torch.empty((w.T, w.h), dtype=torch.bfloat16).pin_memory() if not w.v_pad else None
-        copy_stream = torch.cuda.Stream(device=dev)
-        copied = [torch.cuda.Event() for _ in range(2)]    # set s holds its step's inputs
-        consumed = [torch.cuda.Event() for _ in range(2)]  # the step that read set s has finished
-
-        def issue_copy(i):
-            s_ = i % 2
-            with torch.cuda.stream(copy_stream):
-                if i >= 2:
-                    copy_stream.wait_event(consumed[s_])
-                for k, v in host.items():
-                    dev_in[s_][k].copy_(v, non_blocking=True)
-                copied[s_].record(copy_stream)
-
-        def compute(i):
-            s_ = i % 2
-            d = dev_in[s_]
-            stream.wait_event(copied[s_])
-            mi = {k: d["m" + k] for k in step.mi if ("m", k) not in step.unused} if w.f else None
-            ci = {k: d["c" + k] for k in step.ci if ("c", k) not in step.unused} if w.v_pad else None
-            ai = {k: d["a" + k] for k in step.ai} if w.n_heads else None
-            step.run(mi, ci, ai)
-            consumed[s_].record(stream)
-            if w.v_pad:
-                loss_host.copy_(step.co["loss"], non_blocking=True)
-            else:
-                z_src = (torch.cat(step.zc) if w.sp else step.fo["Z"]) if w.f else step.ao["Z"]
-                z_host.copy_(z_src, non_blocking=True)
-
-        def e2e_run(n, start_event=None):
-            if start_event is not None:
-                copy_stream.wait_event(start_event)  # the first copy starts inside the timed region
-            issue_copy(0)
-            for i in range(n):
-                if i + 1 < n:
-                    issue_copy(i + 1)
-                compute(i)
-
-        e2e_run(2)
-        torch.cuda.synchronize()
-        barrier()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        e2e_run(args.steps, a)
-        b.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        e_ms = a.elapsed_time(b)
-        e_ms = max_over_ranks(e_ms, ws, dev)
-        h2d = sum(v.numel() * v.element_size() for v in host.values())
-        d2h = (loss_host.numel() * 4) if w.v_pad else z_host.numel() * 2
-        e2e = {"value": job_rate(ws, mlp_fl + ce_fl, e_ms / args.steps * 1e-3) / 1e12, "unit": UNIT,
-               "ms_per_step": e_ms / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "path": "vocab_ce_gb300 Python API -> C ABI; every step's inputs copied from pinned host memory "
-                       "(on a second stream, double-buffered: step i+1's copy overlaps step i's compute; the first "
-                       "copy and the last result read are inside the timed region)"}
+        e2e = run_e2e(args, job, ws_, dev, stream, barrier, ws, mlp_fl + ce_fl)
 
     # ---------------- CPU oracle baseline (rank 0 at N = 1 only)
     cpu = None
@@ -611,32 +694,34 @@ def run_ours(args, w, name):
         import oracle
 
         oracle.build()
-        n = CPU_SAMPLE_TOKENS[name]
-        s = oracle_sample(w, step.mi, step.ci, n, step.ai)
-        rate, sec = oracle_rate(w, s, n)
-        cpu = {"value": rate, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-               "sample": f"first {n} of {w.T} tokens through the full step ({workload_config(w, name)['workload'].split(':')[0]}) "
-                         f"at full widths; {sec:.1f} s; same FLOP-per-token convention as value"}
+        tokens = CPU_SAMPLE_TOKENS_JOB.get(name) or {ws_[0].name: CPU_SAMPLE_TOKENS[name]}
+        samples = [(w, oracle_sample(w, st.mi, st.ci, tokens[w.name], st.ai)) for w, st in zip(ws_, job.steps)]
+        t0 = time.perf_counter()
+        for w, s in samples:
+            oracle_step(w, s)
+        sec = time.perf_counter() - t0
+        cpu = {"value": sample_work(ws_, tokens) / sec / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
+               "kind": "oracle",
+               "sample": f"{sample_text(ws_, tokens)} through the full step at full widths; {sec:.1f} s; "
+                         f"same FLOP-per-token convention as value"}
 
     if rank != 0:
         return 0
-    ws_bytes = input_bytes(step)
+    in_bytes = sum(input_bytes(st) for st in job.steps)
+    parts = fractions(ws_, parts_ms.get("mlp"), parts_ms.get("ce"), pk)
+    parts["targets"] = {k: v for k, v in TARGETS.items()
+                        if (k.startswith("mlp") and "mlp_tflops" in parts) or (k.startswith("ce") and "ce_tflops" in parts)}
+    mhz = clk.get("sm_mhz") if clk else None
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {**workload_config(w, name), "parallelism": f"t={w.t} shards on each GPU; dp{ws} (independent batches)",
-                       "l2": f"no flush: inputs alone are {ws_bytes / 1e9:.2f} GB per step, > 129 MB L2"},
-            "parts": {"mlp_tflops": (mlp_fl / (mlp_ms * 1e-3) / 1e12) if w.f else None, "mlp_ms": mlp_ms if w.f else None,
-                      "attn_proj_tflops": (mlp_fl / (mlp_ms * 1e-3) / 1e12) if w.n_heads else None,
-                      "attn_proj_ms": mlp_ms if w.n_heads else None,
-                      "attn_proj_frac_of_peak": ((mlp_fl / (mlp_ms * 1e-3) / 1e12) / pk["bf16_tflops_sustained"])
-                      if w.n_heads else None,
-                      "ce_tokens_per_s": (w.T / (ce_ms * 1e-3)) if w.v_pad else None,
-                      "ce_tflops": (ce_fl / (ce_ms * 1e-3) / 1e12) if w.v_pad else None, "ce_ms": ce_ms if w.v_pad else None,
-                      "mlp_frac_of_peak": ((mlp_fl / (mlp_ms * 1e-3) / 1e12) / pk["bf16_tflops_sustained"]) if w.f else None,
-                      "ce_frac_of_roofline": ((ce_fl / (ce_ms * 1e-3) / 1e12) / pk["bf16_tflops_sustained"]) if w.v_pad else None},
-            "roofline": roof, "kernels": per_kernel, "gpu_launches": gpu_launches,
-            "e2e": e2e, "cpu_baseline": cpu, "clocks": clk}
+            "config": {**job_config(name, ws_), "parallelism": f"t={ws_[0].t} shards on each GPU; dp{ws} "
+                                                               f"(independent batches)",
+                       "l2": f"no flush: inputs alone are {in_bytes / 1e9:.2f} GB per step, > 129 MB L2"},
+            "timed_region_s": region_s,
+            "parts": parts, "roofline": roof, "kernels": per_kernel, "gpu_launches": gpu_launches,
+            "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
+            "clock_normalised": {"sm_mhz_median": mhz, "tflops_per_ghz": value / (mhz * 1e-3)} if mhz else None}
     print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
@@ -645,18 +730,101 @@ def run_ours(args, w, name):
     return 0
 
 
-def kernel_flops_per_step(name, w):
+def run_e2e(args, job, ws_, dev, stream, barrier, ws, work):
+    """The same steps through the Python API with every step's inputs copied
+    from pinned host memory (a second stream, double-buffered: step i+1's copy
+    overlaps step i's compute) and the step's result read back."""
+    host = {}
+    for j, st in enumerate(job.steps):
+        for tag, src in (("m", st.mi), ("c", st.ci), ("a", st.ai)):
+            if src:
+                for k, v in src.items():
+                    if (tag, k) not in st.unused:
+                        host[(j, tag, k)] = v.cpu().pin_memory()
+    dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
+    # the result read back: the loss where the step has one, else the last block's output
+    ce_steps = [st for st in job.steps if st.w.v_pad]
+    res_host = torch.empty(ce_steps[-1].w.T, dtype=torch.float32).pin_memory() if ce_steps else None
+    last = job.steps[-1]
+    if res_host is None:
+        res_host = torch.empty((last.w.T, last.w.h), dtype=torch.bfloat16).pin_memory()
+    copy_stream = torch.cuda.Stream(device=dev)
+    copied = [torch.cuda.Event() for _ in range(2)]    # set s holds its step's inputs
+    consumed = [torch.cuda.Event() for _ in range(2)]  # the step that read set s has finished
+
+    def issue_copy(i):
+        s_ = i % 2
+        with torch.cuda.stream(copy_stream):
+            if i >= 2:
+                copy_stream.wait_event(consumed[s_])
+            for k, v in host.items():
+                dev_in[s_][k].copy_(v, non_blocking=True)
+            copied[s_].record(copy_stream)
+
+    def compute(i):
+        s_ = i % 2
+        d = dev_in[s_]
+        stream.wait_event(copied[s_])
+        ins = []
+        for j, st in enumerate(job.steps):
+            w = st.w
+            mi = {k: d[(j, "m", k)] for k in st.mi if ("m", k) not in st.unused} if w.f else None
+            ci = {k: d[(j, "c", k)] for k in st.ci if ("c", k) not in st.unused} if w.v_pad else None
+            ai = {k: d[(j, "a", k)] for k in st.ai} if w.n_heads else None
+            ins.append((mi, ci, ai))
+        job.run(ins)
+        consumed[s_].record(stream)
+        if ce_steps:
+            res_host.copy_(ce_steps[-1].co["loss"], non_blocking=True)
+        else:
+            z_src = (torch.cat(last.zc) if last.w.sp else last.fo["Z"]) if last.w.f else last.ao["Z"]
+            res_host.copy_(z_src, non_blocking=True)
+
+    def e2e_run(n, start_event=None):
+        if start_event is not None:
+            copy_stream.wait_event(start_event)  # the first copy starts inside the timed region
+        issue_copy(0)
+        for i in range(n):
+            if i + 1 < n:
+                issue_copy(i + 1)
+            compute(i)
+
+    e2e_run(2)
+    torch.cuda.synchronize()
+    barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    e2e_run(args.steps, a)
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e_ms = max_over_ranks(a.elapsed_time(b), ws, dev)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = res_host.numel() * res_host.element_size()
+    return {"value": job_rate(ws, work, e_ms / args.steps * 1e-3) / 1e12, "unit": UNIT,
+            "ms_per_step": e_ms / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": "vocab_ce_gb300 Python API -> C ABI; every step's inputs copied from pinned host memory "
+                    "(on a second stream, double-buffered: step i+1's copy overlaps step i's compute; the first "
+                    "copy and the last result read are inside the timed region)"}
+
+
+def kernel_flops_one(name, w):
     T, h, f, vp = w.T, w.h, w.f, w.v_pad
-    table = {
-        "mlp_fwd_gemm1_bias_gelu": 2.0 * T * h * f, "mlp_fwd_gemm2_shard_sum": 2.0 * T * f * h,
-        "mlp_bwd_dY_gelu_grad": 2.0 * T * h * f, "mlp_bwd_dB": 2.0 * T * f * h, "mlp_bwd_dA": 2.0 * T * h * f,
-        "mlp_bwd_dX_shard_sum": 2.0 * T * f * h,
-        "swiglu_fwd_gemm1_gate_up": 4.0 * T * h * f, "swiglu_fwd_gemm2_shard_sum": 2.0 * T * f * h,
-        "swiglu_bwd_dY_swiglu_grad": 2.0 * T * h * f, "swiglu_bwd_dW2": 2.0 * T * f * h,
-        "swiglu_bwd_dW1": 4.0 * T * h * f, "swiglu_bwd_dX_shard_sum": 4.0 * T * f * h,
-        "ce_fwd_logits_stats": 2.0 * T * h * vp, "ce_bwd_logits_dl": 2.0 * T * h * vp,
-        "ce_bwd_dE": 2.0 * T * h * vp, "ce_bwd_dH_shard_sum": 2.0 * T * h * vp,
-    }
+    table = {}
+    if f and w.act == "swiglu":
+        table.update({"swiglu_fwd_gemm1_gate_up": 4.0 * T * h * f, "swiglu_fwd_gemm2_shard_sum": 2.0 * T * f * h,
+                      "swiglu_bwd_dY_swiglu_grad": 2.0 * T * h * f, "swiglu_bwd_dW2": 2.0 * T * f * h,
+                      "swiglu_bwd_dW1": 4.0 * T * h * f, "swiglu_bwd_dX_shard_sum": 4.0 * T * f * h})
+    elif f:
+        table.update({"mlp_fwd_gemm1_bias_gelu": 2.0 * T * h * f, "mlp_fwd_gemm2_shard_sum": 2.0 * T * f * h,
+                      "mlp_bwd_dY_gelu_grad": 2.0 * T * h * f, "mlp_bwd_dB": 2.0 * T * f * h,
+                      "mlp_bwd_dA": 2.0 * T * h * f, "mlp_bwd_dX_shard_sum": 2.0 * T * f * h})
+    if vp:
+        table.update({"ce_fwd_logits_stats": 2.0 * T * h * vp})
+        if w.ce_grads:
+            table.update({"ce_bwd_logits_dl": 2.0 * T * h * vp, "ce_bwd_dE": 2.0 * T * h * vp,
+                          "ce_bwd_dH_shard_sum": 2.0 * T * h * vp})
     if w.n_heads:
         nqkv = (w.n_heads + 2 * w.n_kv_heads) * w.head_dim
         hq = w.n_heads * w.head_dim
@@ -667,16 +835,28 @@ def kernel_flops_per_step(name, w):
     return table.get(name)
 
 
-def main():
-    args = parse_args()
+def owner_workload(name, ws_):
+    """The name of the workload of a job whose step launches kernel `name`."""
+    return next((w.name for w in ws_ if kernel_flops_one(name, w)), ws_[0].name)
+
+
+def kernel_flops_per_step(name, ws_):
+    """FLOPs one step spends in the kernel `name` (None for the side kernels)."""
+    vals = [kernel_flops_one(name, w) for w in ws_]
+    vals = [v for v in vals if v]
+    return sum(vals) if vals else None
+
+
+def main(argv=None):
+    args = parse_args(argv)
     name = args.workload
+    arm = run_reference if args.impl == "reference" else run_ours
     if name == "sweep":
         rc = 0
         for t in wl.SWEEP_T:
-            rc |= (run_reference if args.impl == "reference" else run_ours)(args, wl.sweep_workload(t), name)
+            rc |= arm(args, [wl.sweep_workload(t)], name)
         return rc
-    w = wl.WORKLOADS[name]
-    return run_reference(args, w, name) if args.impl == "reference" else run_ours(args, w, name)
+    return arm(args, job_workloads(name), name)
 
 
 if __name__ == "__main__":
