@@ -1,8 +1,32 @@
 """Shared comparison helpers for the GPU parity tests.
 
 Tolerances (fp32 accumulation, bf16 storage):
-  * GEMM outputs and gradients: per tensor, max|gpu - oracle| / max|oracle| <= 1e-2.
+  * GEMM outputs and gradients, the contract: per tensor,
+    max|gpu - oracle| / max|oracle| <= 1e-2.
   * Per-token loss (and lse): max|gpu - oracle| <= 2e-3 absolute.
+
+Every tensor comparison also takes the element-wise figure
+    max over elements of |gpu - oracle| / (|oracle| + 1e-2 rms(oracle))
+and asserts it against ELEM_TOL. Where that bound comes from: a bf16 output
+g is the fp32 result x rounded once, |g - x| <= u |x| with u = 2^-8, and x
+differs from the exact value o by delta, the fp32-accumulated effect of the
+bf16 roundings of the intermediate operands the path stores (Y before GEMM2,
+dU before dA and dX, dl before dE and dH, Z and dH between chained stages).
+delta does not shrink with |o|: it is a sum of many rounding errors, each
+relative to one product term, so its size follows rms(o), |delta| <=
+kappa u rms(o). Then
+
+    |g - o| / (|o| + f rms(o)) <= u + (1 + u) kappa u / f,   f = 1e-2,
+
+which for the element-wise floor f = 1e-2 is dominated by the near-zero
+elements. kappa: one rounded intermediate contributes a zero-mean sum of
+independent roundings, each uniform within +-u of its term, whose standard
+deviation is at most u rms(o) / sqrt(3); a path rounds at most two
+intermediates on the way to one output (U, then dU, on the dA path), and the
+largest of up to 10^8 Gaussian samples lies within 6.1 standard deviations,
+so kappa = 6.1 * 2 / sqrt(3) = 7.0 and ELEM_TOL = u (1 + 1.0039 * 700) = 2.75.
+fp32 (tf32) cases are held to the same figure. Each test run prints the worst
+element-wise figure of every comparison in its terminal summary.
 """
 
 import numpy as np
@@ -10,6 +34,13 @@ import torch
 
 REL_TOL = 1e-2
 LOSS_ABS_TOL = 2e-3
+ELEM_FLOOR = 1e-2
+_U_BF16 = 2.0 ** -8
+_KAPPA = 7.0
+ELEM_TOL = _U_BF16 * (1.0 + (1.0 + _U_BF16) * _KAPPA / ELEM_FLOOR)
+
+# (test-visible name, per-tensor figure, element-wise figure) of every comparison made
+RECORD = []
 
 
 def as_f64(x):
@@ -22,20 +53,37 @@ def rel_err(gpu, ref) -> float:
     g, r = as_f64(gpu), as_f64(ref)
     assert g.shape == r.shape, (g.shape, r.shape)
     assert np.all(np.isfinite(g)), "non-finite GPU output"
-    denom = np.abs(r).max()
-    return float(np.abs(g - r).max() / max(denom, 1e-30))
+    denom = np.abs(r).max() if r.size else 0.0
+    return float(np.abs(g - r).max() / max(denom, 1e-30)) if r.size else 0.0
 
 
-def assert_rel(name, gpu, ref, tol=REL_TOL):
+def elem_err(gpu, ref, floor=ELEM_FLOOR) -> float:
+    """max |g - o| / (|o| + floor rms(o)) over the elements (0 for an empty or all-zero pair)."""
+    g, r = as_f64(gpu), as_f64(ref)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    if r.size == 0:
+        return 0.0
+    d = np.abs(g - r)
+    den = np.abs(r) + floor * float(np.sqrt(np.mean(r * r)))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(d == 0.0, 0.0, d / np.where(den > 0.0, den, 1e-300))
+    return float(q.max())
+
+
+def assert_rel(name, gpu, ref, tol=REL_TOL, elem_tol=ELEM_TOL):
     e = rel_err(gpu, ref)
+    el = elem_err(gpu, ref)
+    RECORD.append((name, e, el))
     assert e <= tol, f"{name}: max rel err {e:.3e} > {tol}"
+    assert el <= elem_tol, f"{name}: element-wise err {el:.3e} > {elem_tol:.3f} (per-tensor {e:.3e})"
     return e
 
 
 def assert_loss(name, gpu, ref, tol=LOSS_ABS_TOL):
     g, r = as_f64(gpu), as_f64(ref)
     assert np.all(np.isfinite(g)), f"{name}: non-finite"
-    e = float(np.abs(g - r).max())
+    e = float(np.abs(g - r).max()) if r.size else 0.0
+    RECORD.append((name, e, None))
     assert e <= tol, f"{name}: max abs err {e:.3e} > {tol}"
     return e
 
