@@ -445,8 +445,12 @@ tpce_status vocab_parallel_ce(const void *H, const void *E, const int32_t *targe
  * multiple of 256 and v_pad / 128 otherwise; larger requests return
  * TPCE_ERR_WORKSPACE with the sizes in tpce_last_error(), before any launch.
  * The first call on a device, with that device current, looks up the array's
- * device address (cudaGetSymbolAddress) and caches it; make that first call
- * before any stream capture. All calls share the one array and it keeps the
+ * device address (cudaGetSymbolAddress) and caches it. Under CUDA's default
+ * lazy module loading that first call is also when the array's memory is
+ * committed on the device (under eager loading: when the library loads), a
+ * one-time implicit allocation that fails if the device is full. Make the
+ * first call per device before a memory planner reserves the device and
+ * before any stream capture; later calls allocate nothing. All calls share the one array and it keeps the
  * last call's contents (nothing in it needs clearing: a call writes every
  * entry it reads); calls whose kernels overlap on the GPU race on it, so
  * order them on one stream or with events.
@@ -467,6 +471,25 @@ tpce_status vocab_parallel_ce_loss_static(const void *H, const void *E, const in
  * receives the raw word.
  * ------------------------------------------------------------------------- */
 tpce_status tpce_device_status(void *stream, int clear, uint32_t *detail);
+
+/* ---------------------------------------------------------------------------
+ * Failure-path test knob (not for production use). The pages' in-depth
+ * Megatron-LM page ("Megatron-LM, in depth", "Failure modes") treats a hung
+ * collective as a failure to be detected rather than waited out; here every
+ * wait inside a kernel is bounded, and this call lets a test make one wait
+ * run out on purpose. tpce_debug_withhold_next_load(1) arms it: the next
+ * bf16 GEMM launch on the CTA-pair kernel (any entry point) then arms the
+ * full-barrier of its first pipeline stage in cluster 0 but issues none of
+ * that stage's TMA loads, so the MMA thread's wait for it can never complete.
+ * After its bound (2 s) that wait records TPCE_ERR_TIMEOUT (detail: which
+ * wait, bits 8..) in the device status word and raises the CTA's abort flag;
+ * the kernel's other waits then give up too (each bounded), in-flight loads
+ * and stores land, tensor memory is freed and the kernel returns, leaving the
+ * context usable. That launch's outputs are undefined. The arming is used up
+ * by that one launch; tpce_debug_withhold_next_load(0) disarms it unused.
+ * Process-wide; returns TPCE_OK.
+ * ------------------------------------------------------------------------- */
+tpce_status tpce_debug_withhold_next_load(int on);
 
 /* ---------------------------------------------------------------------------
  * Kernel timing. While enabled, every kernel the library launches is

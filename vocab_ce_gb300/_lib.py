@@ -70,6 +70,7 @@ SIGNATURES = {
                                _P, _P, _P, _P, _P, _SZ, _P]),
     "vocab_parallel_ce_loss_static": (_I, [_P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _P, _P, _P]),
     "tpce_device_status": (_I, [_P, _I, ctypes.POINTER(ctypes.c_uint32)]),
+    "tpce_debug_withhold_next_load": (_I, [_I]),
     "tpce_profile_enable": (_I, [_I]),
     "tpce_profile_count": (_I, []),
     "tpce_profile_get": (_I, [_I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(_I64),

@@ -14,11 +14,17 @@
 // Host code cannot use the array's name as a device address (on the host it
 // names a host-side stand-in), so the first call on each device, with that
 // device current, asks the runtime for the array's device address with
-// cudaGetSymbolAddress and caches it; that first call should therefore come
-// before any stream capture. All calls share the one array: two calls whose
-// kernels overlap on the GPU (different streams, no ordering) race on it.
-// Nothing in it needs clearing between calls: every statistic the combine
-// kernel reads is written earlier in the same call.
+// cudaGetSymbolAddress and caches it. Under CUDA's default lazy module
+// loading that lookup is also where this file's module -- and with it the
+// array's memory -- is loaded onto the device (under eager loading it happens
+// when the library's modules load), so the first call per device commits the
+// array once, an implicit device allocation that can fail when the device is
+// already full. Make that first call before a memory planner reserves the
+// device, and before any stream capture; later calls allocate nothing. All
+// calls share the one array: two calls whose kernels overlap on the GPU
+// (different streams, no ordering) race on it. Nothing in it needs clearing
+// between calls: every statistic the combine kernel reads is written earlier
+// in the same call.
 #include <cuda_runtime.h>
 
 #include <mutex>

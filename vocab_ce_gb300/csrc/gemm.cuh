@@ -83,6 +83,10 @@ struct GemmShape {
     int tail_tiles;            // tiles split
     float *partial;            // [tail_tiles * split][2 CTAs][128 rows][BN] fp32
     uint32_t *tickets;         // [tail_tiles][2 CTAs], zero at launch
+    // Failure-path test knob, 0 in every ordinary launch. 1 (CTA-pair kernel
+    // only): cluster 0 arms the full barrier of its first k-block but loads
+    // nothing into it, so the MMA thread's bounded wait on it runs out.
+    int debug_withhold;
 };
 
 // Work unit u: its tile, its K-block range, and its part (-1: a whole tile).

@@ -251,6 +251,7 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
     s.tail_tiles = 0;
     s.partial = nullptr;
     s.tickets = nullptr;
+    s.debug_withhold = 0;
 
     auto kern = tc_gemm_kernel<ElemT, BN, A_MN, B_MN, Epi, kChunk>;
     static std::mutex attr_mu;
@@ -335,6 +336,7 @@ tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &
     s.b_off_mn = b_off_mn;
     s.b_off_k = b_off_k;
     s.b_gate_off = b_gate_off;
+    s.debug_withhold = take_debug_withhold();
     auto kern = tc_gemm_pair_kernel<BN, A_MN, B_MN, Epi, kChunk>;
     static std::mutex attr_mu;
     static bool attr_done[64] = {};

@@ -144,6 +144,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
                 ChunkCursor<kChunk> cur;
                 if constexpr (kChunk == kChunkA) cur.init(cs, A_MN ? shp.a_off_k + kb0 * kBK : m0 + shp.a_off_mn);
                 if constexpr (kChunk == kChunkB) cur.init(cs, B_MN ? shp.b_off_k + kb0 * kBK : nh0 + shp.b_off_mn);
+                // failure-path test knob (off in every ordinary launch): cluster
+                // 0's first unit leaves its first k-block's stage unloaded
+                const int kb_skip = (shp.debug_withhold != 0 && u == 0) ? kb0 : -1;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!ptx::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, 1)) break;
                     const uint32_t bar = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
@@ -167,19 +170,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
                         yb = cur.y;
                     }
                     if constexpr ((kChunk == kChunkA && A_MN) || (kChunk == kChunkB && B_MN)) cur.advance(cs, kBK);
-                    if (!A_MN) {
-                        ptx::tma_load_2d_pair(sa, ma, bar, k0 + shp.a_off_k, ya);
-                    } else {
+                    if (kb != kb_skip) {
+                        if (!A_MN) {
+                            ptx::tma_load_2d_pair(sa, ma, bar, k0 + shp.a_off_k, ya);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < kBM / 64; ++j)
-                            ptx::tma_load_2d_pair(sa + j * kMnBlockBytes, ma, bar, m0 + shp.a_off_mn + 64 * j, ya);
-                    }
-                    if (!B_MN) {
-                        ptx::tma_load_2d_pair(sb, mb, bar, k0 + shp.b_off_k, yb);
-                    } else {
+                            for (int j = 0; j < kBM / 64; ++j)
+                                ptx::tma_load_2d_pair(sa + j * kMnBlockBytes, ma, bar, m0 + shp.a_off_mn + 64 * j, ya);
+                        }
+                        if (!B_MN) {
+                            ptx::tma_load_2d_pair(sb, mb, bar, k0 + shp.b_off_k, yb);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < kHalfN / 64; ++j)
-                            ptx::tma_load_2d_pair(sb + j * kMnBlockBytes, mb, bar, nh0 + shp.b_off_mn + 64 * j, yb);
+                            for (int j = 0; j < kHalfN / 64; ++j)
+                                ptx::tma_load_2d_pair(sb + j * kMnBlockBytes, mb, bar, nh0 + shp.b_off_mn + 64 * j,
+                                                      yb);
+                        }
                     }
                     if (++stage == S) {
                         stage = 0;

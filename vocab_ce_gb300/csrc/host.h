@@ -17,6 +17,9 @@ namespace tpce {
 uint32_t *device_error_word();
 // number of SMs of the current device (0 on failure)
 int num_sms();
+// 1 once after tpce_debug_withhold_next_load(1) armed it (the arming is used
+// up by the CTA-pair GEMM launch that reads it), else 0.
+int take_debug_withhold();
 
 // RAII kernel timer: when profiling is on, records an event pair around the
 // launches made during its lifetime on `stream` and files them under `name`.

@@ -7,6 +7,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -50,6 +51,13 @@ int num_sms() {
     }
     return count[dev];
 }
+
+// ------------------------------------------------------------------ failure-path test knob
+namespace {
+std::atomic<int> g_debug_withhold{0};
+}
+
+int take_debug_withhold() { return g_debug_withhold.exchange(0); }
 
 // ------------------------------------------------------------------ error text
 namespace {
@@ -423,6 +431,11 @@ extern "C" tpce_status tpce_device_status(void *stream, int clear, uint32_t *det
     if (detail) *detail = v;
     const uint32_t code = v & 0xffu;
     return code <= TPCE_ERR_UNSUPPORTED ? static_cast<tpce_status>(code) : TPCE_ERR_INVALID;
+}
+
+extern "C" tpce_status tpce_debug_withhold_next_load(int on) {
+    g_debug_withhold.store(on ? 1 : 0);
+    return TPCE_OK;
 }
 
 extern "C" tpce_status tpce_profile_enable(int on) {
