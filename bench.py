@@ -91,6 +91,9 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--no-kernel-pass", action="store_true", help="skip the per-kernel timing pass")
+    p.add_argument("--tokens", type=int, default=0,
+                   help="run every workload of the job on this many tokens instead of its own T (a smaller "
+                        "case of the same kernels, for profiler captures); the line then names the reduced T")
     return p.parse_args(argv)
 
 
@@ -126,9 +129,13 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def job_workloads(name):
-    """The workloads one step of job `name` runs, in launch order."""
-    return [wl.WORKLOADS[n] for n in JOBS.get(name, (name,))]
+def job_workloads(name, tokens=0):
+    """The workloads one step of job `name` runs, in launch order (on `tokens`
+    tokens each when given, else at their own T)."""
+    import dataclasses
+
+    ws_ = [wl.WORKLOADS[n] for n in JOBS.get(name, (name,))]
+    return [dataclasses.replace(w, T=tokens, b=1, s=tokens) for w in ws_] if tokens else ws_
 
 
 def flops(w):
@@ -238,16 +245,22 @@ class ClockSampler:
             if len(parts) < 9:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                power = float(parts[3])
+            except ValueError:
+                power = None
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9], power))
             except ValueError:
                 continue
         os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower().startswith("active")})
+        reasons = sorted({names[i] for _, _, r, _ in rows for i in range(4) if r[i].lower().startswith("active")})
+        watts = [r[3] for r in rows if r[3] is not None]
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows),
+                "power_w_median": statistics.median(watts) if watts else None}
 
 
 # ---------------------------------------------------------------------- traffic from committed ncu summaries
@@ -852,11 +865,16 @@ def main(argv=None):
     name = args.workload
     arm = run_reference if args.impl == "reference" else run_ours
     if name == "sweep":
+        import dataclasses
+
         rc = 0
         for t in wl.SWEEP_T:
-            rc |= arm(args, [wl.sweep_workload(t)], name)
+            w = wl.sweep_workload(t)
+            if args.tokens:
+                w = dataclasses.replace(w, T=args.tokens, b=1, s=args.tokens)
+            rc |= arm(args, [w], name)
         return rc
-    return arm(args, job_workloads(name), name)
+    return arm(args, job_workloads(name, args.tokens), name)
 
 
 if __name__ == "__main__":

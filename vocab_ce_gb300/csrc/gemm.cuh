@@ -83,6 +83,11 @@ struct GemmShape {
     int tail_tiles;            // tiles split
     float *partial;            // [tail_tiles * split][2 CTAs][128 rows][BN] fp32
     uint32_t *tickets;         // [tail_tiles][2 CTAs], zero at launch
+    // L2 eviction priorities of the operand loads (CTA-pair kernel): 0 none;
+    // 1 A's lines evict_last and B's evict_first, for launches whose group of
+    // A panels fits in L2 and is reused by every column block the group walks
+    // while B streams through once per group.
+    int l2_hint;
     // Failure-path test knob, 0 in every ordinary launch. 1 (CTA-pair kernel
     // only): cluster 0 arms the full barrier of its first k-block but loads
     // nothing into it, so the MMA thread's bounded wait on it runs out.

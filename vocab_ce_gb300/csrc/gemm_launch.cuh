@@ -127,6 +127,26 @@ inline int pick_group_m(int tiles_m, int64_t rows_per_block, int64_t K, int64_t 
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles_m, g)));
 }
 
+// L2 eviction priorities of a CTA-pair launch. The group's A panels (group_m
+// row-blocks x K) are read once per column block the group walks; B's panels
+// once per group. With TPCE_L2_HINT=1, when the A panels fit the budget and B
+// is too large to stay in L2 anyway, A's lines are loaded evict_last and B's
+// evict_first. Off by default: measured on GB300 (the 70B MLP + 129K CE step,
+// A/B twice in one session) it was 2% slower, and the 129K logit-statistics
+// GEMM read 77 GB from DRAM instead of 64 GB -- the kept A panels crowd out B
+// lines that the other row-blocks of the same wave were still to read.
+#ifndef TPCE_L2_HINT
+#define TPCE_L2_HINT 0
+#endif
+#ifndef TPCE_L2_KEEP_BYTES
+#define TPCE_L2_KEEP_BYTES (64ll << 20)
+#endif
+inline int pick_l2_hint(int group_m, int tiles_n, int64_t rows_per_block, int64_t bn, int64_t K, int64_t elem_bytes) {
+    const int64_t a_group = group_m * rows_per_block * K * elem_bytes;
+    const int64_t b_all = tiles_n * bn * K * elem_bytes;
+    return (TPCE_L2_HINT && tiles_n > 1 && a_group <= TPCE_L2_KEEP_BYTES && b_all > TPCE_L2_KEEP_BYTES) ? 1 : 0;
+}
+
 // Tile widths a launch may use.
 enum : unsigned { kBN128 = 1u, kBN192 = 2u, kBN256 = 4u };
 // Build-time tuning knob: the tile widths launch_gemm_auto may choose from.
@@ -251,6 +271,7 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
     s.tail_tiles = 0;
     s.partial = nullptr;
     s.tickets = nullptr;
+    s.l2_hint = 0;
     s.debug_withhold = 0;
 
     auto kern = tc_gemm_kernel<ElemT, BN, A_MN, B_MN, Epi, kChunk>;
@@ -336,6 +357,7 @@ tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &
     s.b_off_mn = b_off_mn;
     s.b_off_k = b_off_k;
     s.b_gate_off = b_gate_off;
+    s.l2_hint = pick_l2_hint(s.group_m, s.tiles_n, 2 * kBM, BN, K, 2);
     s.debug_withhold = take_debug_withhold();
     auto kern = tc_gemm_pair_kernel<BN, A_MN, B_MN, Epi, kChunk>;
     static std::mutex attr_mu;

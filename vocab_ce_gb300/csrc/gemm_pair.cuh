@@ -131,6 +131,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
             uint32_t phase = 0;
             uint32_t issued = 0;
             uint32_t issued_parity = 0;
+            const bool hint = shp.l2_hint != 0;
+            const uint64_t pol_a = hint ? ptx::l2_policy_evict_last() : 0;
+            const uint64_t pol_b = hint ? ptx::l2_policy_evict_first() : 0;
+            auto load = [&](void *dst, const CUtensorMap *m, uint32_t bar, int c0, int c1, uint64_t pol) {
+                if (hint)
+                    ptx::tma_load_2d_pair_hint(dst, m, bar, c0, c1, pol);
+                else
+                    ptx::tma_load_2d_pair(dst, m, bar, c0, c1);
+            };
             for (int u = cluster_id; u < num_units && !*abort_flag; u += clusters) {
                 int tile, kb0, kb1, part;
                 unit_coords(u, shp, tile, kb0, kb1, part);
@@ -172,19 +181,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
                     if constexpr ((kChunk == kChunkA && A_MN) || (kChunk == kChunkB && B_MN)) cur.advance(cs, kBK);
                     if (kb != kb_skip) {
                         if (!A_MN) {
-                            ptx::tma_load_2d_pair(sa, ma, bar, k0 + shp.a_off_k, ya);
+                            load(sa, ma, bar, k0 + shp.a_off_k, ya, pol_a);
                         } else {
 #pragma unroll
                             for (int j = 0; j < kBM / 64; ++j)
-                                ptx::tma_load_2d_pair(sa + j * kMnBlockBytes, ma, bar, m0 + shp.a_off_mn + 64 * j, ya);
+                                load(sa + j * kMnBlockBytes, ma, bar, m0 + shp.a_off_mn + 64 * j, ya, pol_a);
                         }
                         if (!B_MN) {
-                            ptx::tma_load_2d_pair(sb, mb, bar, k0 + shp.b_off_k, yb);
+                            load(sb, mb, bar, k0 + shp.b_off_k, yb, pol_b);
                         } else {
 #pragma unroll
                             for (int j = 0; j < kHalfN / 64; ++j)
-                                ptx::tma_load_2d_pair(sb + j * kMnBlockBytes, mb, bar, nh0 + shp.b_off_mn + 64 * j,
-                                                      yb);
+                                load(sb + j * kMnBlockBytes, mb, bar, nh0 + shp.b_off_mn + 64 * j, yb, pol_b);
                         }
                     }
                     if (++stage == S) {
