@@ -156,6 +156,10 @@ CE_CASES = {
     "min_hidden": (7, 8, 256, 200, 2, "bf16"),                # h = 8: one mostly zero-filled k-block
     "multi_tile": (600, 320, 4096, 4000, 4, "bf16"),
     "wide_h": (700, 1536, 3072, 3000, 4, "bf16"),             # dE / dH pick 192-wide tiles
+    # 25 row-blocks x 4 shards: each shard's 6 tiles are cut into 3 runs of 2
+    # (300 work units, 4 rounds over the CTA pairs), so the combine folds 3
+    # partial statistics per shard
+    "runs_split_shards": (6400, 64, 6144, 6000, 4, "bf16"),
     "ragged_f32": (333, 200, 768, 700, 2, "f32"),
     "padded_shards_f32": (130, 96, 2048, 1800, 16, "f32"),
 }

@@ -17,7 +17,8 @@ parity tests:
 * the device's free memory (cudaMemGetInfo) is the same before and after a
   call, once the first call has committed the array;
 * an fp32 (tf32) case, and one call through the Python wrapper;
-* one case is also checked against the CPU oracle.
+* one case is also checked against the CPU oracle;
+* the 129K-vocabulary config (16,384 tokens) fits the array and matches.
 
 The host test checks that a request larger than the static scratch is
 refused before anything is launched. This file is named to be collected last.
@@ -130,11 +131,29 @@ def test_static_scratch_fp32_and_python_wrapper():
     _check(tp, "static via the Python wrapper", cb, v_valid, t, loss, lse)
 
 
+@pytest.mark.gpu
+def test_static_scratch_serves_the_129k_vocabulary_config():
+    # 16,384 tokens over 129,024 padded ids (t = 8): 72 statistics parts per
+    # token, 9.6 MB of the 16 MiB array
+    dev = gpu_or_skip()
+    import vocab_ce_gb300 as tp
+
+    w = wl.WORKLOADS["ce128k"]
+    ci = wl.ce_inputs(w, seed=0, device=dev)
+    loss = torch.full((w.T,), float("nan"), dtype=torch.float32, device=dev)
+    lse = torch.full((w.T,), float("nan"), dtype=torch.float32, device=dev)
+    assert _call_static(ci["H"], ci["E"], ci["targets"], w.v_valid, w.t, loss, lse) == 0, lib().tpce_last_error()
+    torch.cuda.synchronize()
+    assert tp.device_status() == 0
+    _check(tp, "static at the 129K config", ci, w.v_valid, w.t, loss, lse)
+
+
 def test_static_scratch_refuses_oversize_request_before_launch():
-    # 16,384 tokens x 504 vocabulary tiles need 66 MB of statistics: refused on
-    # the host (pointers are never dereferenced on this path)
+    # 300,000 tokens over 129,024 ids: one part per shard already needs
+    # 8 x 300,000 x 8 bytes = 19.2 MB of statistics: refused on the host
+    # (pointers are never dereferenced on this path)
     fake = P(1 << 20)
-    st = lib().vocab_parallel_ce_loss_static(fake, fake, fake, 16384, 8192, 129024, 128256, 8, 0, fake, fake, None)
+    st = lib().vocab_parallel_ce_loss_static(fake, fake, fake, 300000, 8192, 129024, 128256, 8, 0, fake, fake, None)
     assert st == 4  # TPCE_ERR_WORKSPACE
     msg = lib().tpce_last_error().decode()
     assert "static scratch" in msg and str(16 << 20) in msg

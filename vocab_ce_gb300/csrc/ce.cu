@@ -7,11 +7,13 @@
 // not b*s*v logits; the vocabulary is padded so that each shard is a multiple
 // of 128 ids.
 //
-// Forward: one persistent GEMM over all vocabulary tiles of all shards; each
-// tile's epilogue reduces its fp32 logits, per token, to (max, sum exp) over
-// the real ids and picks up the target logit. A combine kernel folds the
-// tiles of a shard into that shard's (m_i, s_i), then folds the shards:
-// m = max m_i, S = sum s_i exp(m_i - m), lse = m + ln S, loss = lse - tau.
+// Forward: one persistent GEMM over all vocabulary tiles of all shards; its
+// epilogue reduces the fp32 logits of a run of tiles of one shard, per token,
+// to (max, sum exp) over the real ids, carried from tile to tile, and picks up
+// the target logit (each shard leaves a few such parts per token, see
+// ce_stats_plan). A combine kernel folds the parts of a shard into that
+// shard's (m_i, s_i), then folds the shards: m = max m_i,
+// S = sum s_i exp(m_i - m), lse = m + ln S, loss = lse - tau.
 //
 // Backward (the gradient of softmax cross-entropy, dl = g (p - onehot)): the
 // vocabulary is walked in chunks of whole shards (or parts of one shard). For each chunk
@@ -41,8 +43,7 @@ constexpr size_t kDlScratchBound = size_t(1) << 30;
 inline int64_t pad4(int64_t x) { return (x + 3) / 4 * 4; }  // fp32 rows padded to 16 bytes
 
 struct CeWs {
-    int bn;              // vocabulary tile width of the statistics GEMM
-    int64_t n_tiles;     // v_pad / bn
+    CeStatsPlan plan;    // pass 1's tiles, runs and statistics parts
     int64_t vc;          // vocabulary chunk width of the backward
     int64_t chunks;      // v_pad / vc
     size_t tail, stats, tau, lse, dl, acc, Ht, Et, dlt, total;
@@ -53,8 +54,7 @@ CeWs ce_ws_layout(int64_t T, int64_t h, int64_t v_pad, int t, bool grads, int dt
     const bool f32 = dtype == TPCE_F32;
     const size_t esz = f32 ? 4 : 2;
     const int64_t vs = v_pad / t;
-    L.bn = (!f32 && vs % 256 == 0) ? 256 : 128;  // a tile never straddles two shards
-    L.n_tiles = v_pad / L.bn;
+    L.plan = ce_stats_plan(T, v_pad, t, dtype, TPCE_PAIR_BN == 256);  // a tile never straddles two shards
     // chunk = g whole shards: the largest g dividing t with g <= t / 2 (so the
     // whole vocabulary's dl is never resident) whose scratch fits the bound.
     // Fewer, wider chunks mean fewer fp32 passes over the dH accumulator
@@ -76,7 +76,7 @@ CeWs ce_ws_layout(int64_t T, int64_t h, int64_t v_pad, int t, bool grads, int dt
         return at;
     };
     L.tail = take(kTailScratchBytes);  // the GEMMs' split tails
-    L.stats = take(static_cast<size_t>(L.n_tiles) * T * sizeof(float2));
+    L.stats = take(static_cast<size_t>(L.plan.parts) * T * sizeof(float2));
     L.tau = take(static_cast<size_t>(T) * sizeof(float));
     L.lse = take(static_cast<size_t>(T) * sizeof(float));
     if (grads) {
@@ -120,17 +120,18 @@ tpce_status ce_forward(const CeArgs &a, const CeWs &L, void *ws, float *lse_buf,
     const int vvi = static_cast<int>(a.v_valid);
     Operand A{a.H, a.T, a.h, a.h};          // K-major [T, h]
     Operand B{a.E, a.v_pad, a.h, a.h};      // K-major: N = v_pad rows, K = h columns
-    EpiCeStats::Params ep{stats, tau, a.targets, a.T, vvi, 0, 0, L.bn};
+    const CeStatsPlan &P = L.plan;
+    EpiCeStats::Params ep{stats, tau, a.targets, a.T, vvi, 0, 0, P.bn, P.run_len};
     const TailScratch tail{at<uint8_t>(ws, L.tail), kTailScratchBytes};
     tpce_status st;
     if constexpr (std::is_same<ElemT, __nv_bfloat16>::value && TPCE_PAIR_BN == 256) {
-        if (L.bn == 256)
+        if (P.pair)
             st = launch_gemm_pair<256, false, false, EpiCeStats>("ce_fwd_logits_stats", A, B, nullptr, nullptr, Ti, vpi, hi,
-                                                                 0, 0, 0, 0, ep, s, true, 0, nullptr, &tail);
+                                                                 0, 0, 0, 0, ep, s, true, 0, nullptr, &tail, P.run_len);
         else
             st = launch_gemm<ElemT, 128, false, false, EpiCeStats>("ce_fwd_logits_stats", A, B, nullptr, nullptr, Ti, vpi,
                                                                    hi, 0, 0, 0, 0, ep, s);
-    } else if (L.bn == 256)
+    } else if (P.bn == 256)
         st = launch_gemm<ElemT, 256, false, false, EpiCeStats>("ce_fwd_logits_stats", A, B, nullptr, nullptr, Ti, vpi, hi, 0,
                                                                0, 0, 0, ep, s);
     else
@@ -139,8 +140,7 @@ tpce_status ce_forward(const CeArgs &a, const CeWs &L, void *ws, float *lse_buf,
     if (st != TPCE_OK) return st;
     // exchange of the per-token statistics across shards
     KernelTimer timer("ce_combine", s);
-    launch_ce_combine(stats, tau, a.targets, a.T, a.t, static_cast<int>(L.n_tiles / a.t), vvi, a.loss, lse_buf, err,
-                      s);
+    launch_ce_combine(stats, tau, a.targets, a.T, a.t, P.parts_per_shard, vvi, a.loss, lse_buf, err, s);
     return check_launch("ce_combine", s);
 }
 

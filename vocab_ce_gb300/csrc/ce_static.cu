@@ -24,7 +24,9 @@
 // calls share the one array: two calls whose kernels overlap on the GPU
 // (different streams, no ordering) race on it. Nothing in it needs clearing
 // between calls: every statistic the combine kernel reads is written earlier
-// in the same call.
+// in the same call. The statistics are vocab_parallel_ce's: a few (max,
+// sumexp) parts per shard and token, so the 129K-vocabulary config (16,384
+// tokens, 72 parts) needs 9.6 MB of the array.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -75,20 +77,19 @@ extern "C" tpce_status vocab_parallel_ce_loss_static(const void *H, const void *
                           static_cast<const void *>(lse)})
         if (reinterpret_cast<uintptr_t>(p) & 3u) return TPCE_ERR_ALIGN;
 
-    // scratch layout: per-tile (max, sumexp) [n_tiles][T], target logit [T], lse [T] if not an output
-    const int64_t vs = v_pad / t;
+    // scratch layout: per-part (max, sumexp) [parts][T] (the same parts as
+    // vocab_parallel_ce's), target logit [T], lse [T] if not an output
     const bool f32 = dtype == TPCE_F32;
-    const int bn = (!f32 && vs % 256 == 0) ? 256 : 128;  // a tile never straddles two shards
-    const int64_t n_tiles = v_pad / bn;
-    const size_t stats_bytes = round_up(static_cast<size_t>(n_tiles) * T * sizeof(float2), 256);
+    const CeStatsPlan P = ce_stats_plan(T, v_pad, t, dtype, TPCE_PAIR_BN == 256);
+    const size_t stats_bytes = round_up(static_cast<size_t>(P.parts) * T * sizeof(float2), 256);
     const size_t tau_bytes = round_up(static_cast<size_t>(T) * sizeof(float), 256);
     const size_t lse_bytes = lse ? 0 : tau_bytes;
     const size_t need = stats_bytes + tau_bytes + lse_bytes;
     if (need > TPCE_CE_STATIC_SCRATCH_BYTES)
         return fail(TPCE_ERR_WORKSPACE,
-                    "vocab_parallel_ce_loss_static: T=%lld and %lld vocabulary tiles need %zu bytes of scratch; "
-                    "the static scratch holds %u",
-                    static_cast<long long>(T), static_cast<long long>(n_tiles), need,
+                    "vocab_parallel_ce_loss_static: T=%lld and %lld statistics parts per token need %zu bytes of "
+                    "scratch; the static scratch holds %u",
+                    static_cast<long long>(T), static_cast<long long>(P.parts), need,
                     static_cast<unsigned>(TPCE_CE_STATIC_SCRATCH_BYTES));
     uint8_t *base = nullptr;
     st = static_scratch_address(&base);
@@ -104,17 +105,21 @@ extern "C" tpce_status vocab_parallel_ce_loss_static(const void *H, const void *
 
     Operand a{H, T, h, h};      // K-major [T, h]
     Operand b{E, v_pad, h, h};  // K-major: N = v_pad rows, K = h columns
-    EpiCeStats::Params ep{stats, tau, targets, T, vvi, 0, 0, bn};
+    EpiCeStats::Params ep{stats, tau, targets, T, vvi, 0, 0, P.bn, P.run_len};
     if (f32)
         st = launch_gemm<float, 128, false, false, EpiCeStats>("ce_static_logits_stats", a, b, nullptr, nullptr, Ti, vpi, hi, 0, 0, 0,
                                                                0, ep, s, /*timed=*/false);
-    else if (bn == 256)
+    else if (P.pair)  // no tail scratch: the CTA pairs never split a tile here
+        st = launch_gemm_pair<256, false, false, EpiCeStats>("ce_static_logits_stats", a, b, nullptr, nullptr, Ti, vpi, hi,
+                                                             0, 0, 0, 0, ep, s, /*timed=*/false, 0, nullptr, nullptr,
+                                                             P.run_len);
+    else if (P.bn == 256)
         st = launch_gemm<__nv_bfloat16, 256, false, false, EpiCeStats>("ce_static_logits_stats", a, b, nullptr, nullptr, Ti,
                                                                        vpi, hi, 0, 0, 0, 0, ep, s, /*timed=*/false);
     else
         st = launch_gemm<__nv_bfloat16, 128, false, false, EpiCeStats>("ce_static_logits_stats", a, b, nullptr, nullptr, Ti, vpi, hi,
                                                                        0, 0, 0, 0, ep, s, /*timed=*/false);
     if (st != TPCE_OK) return st;
-    launch_ce_combine(stats, tau, targets, T, t, static_cast<int>(n_tiles / t), vvi, loss, lse_buf, err, s);
+    launch_ce_combine(stats, tau, targets, T, t, P.parts_per_shard, vvi, loss, lse_buf, err, s);
     return check_launch("ce_static_combine", s);
 }

@@ -72,6 +72,11 @@ struct GemmShape {
     int tiles_m, tiles_n;      // ceil(M / 128), ceil(N / BN)
     int k_blocks;              // ceil(K / BK)
     int group_m;               // rasterisation: tiles_m are walked in groups of this many
+    // Runs (CTA-pair kernel): a work unit is run_len consecutive column tiles
+    // of one row-block, walked in order, the epilogue's row state carried
+    // from tile to tile; unit_cols = tiles_n / run_len units per row-block.
+    int run_len;
+    int unit_cols;
     int a_off_mn, a_off_k;     // coordinate offsets of the A operand inside its tensor map
     int b_off_mn, b_off_k;     // same for B
     int b_gate_off;            // gated tiles: B column (or row) offset of the second half, else 0
@@ -111,8 +116,9 @@ __device__ __forceinline__ void unit_coords(int u, const GemmShape &s, int &tile
     }
 }
 
+// Row-block and unit column of work unit `tile` (the column block when run_len = 1).
 __device__ __forceinline__ void tile_coords(int tile, const GemmShape &s, int &m_blk, int &n_blk) {
-    const int per_group = s.group_m * s.tiles_n;
+    const int per_group = s.group_m * s.unit_cols;
     const int g = tile / per_group;
     const int first_m = g * s.group_m;
     const int gsz = min(s.tiles_m - first_m, s.group_m);
@@ -531,10 +537,13 @@ struct EpiSwiGluGrad : EpiBase {
     __device__ static void end(const Params &, Row &, int, int, bool) {}
 };
 
-// CE pass 1: logits of one vocabulary tile, reduced per token to (max, sum of
-// exp(l - max)) over the real ids, plus the target logit where the target
-// falls in this tile. The logits never leave the registers. One warp per TMEM
-// lane quarter, so each thread sees its token's whole tile row.
+// CE pass 1: logits of a run of vocabulary tiles (one tile on the one-CTA
+// kernel), reduced per token to (max, sum of exp(l - max)) over the real ids,
+// plus the target logit where the target falls in the run. The running
+// (max, sum) is carried from tile to tile of the run in registers and stored
+// once, for the run's part of its shard. The logits never leave the
+// registers. One warp per TMEM lane quarter, so each thread sees its token's
+// whole tile row.
 struct EpiCeStats : EpiBase {
     static constexpr int kWarps = 4;
     static constexpr int kOuts = 0;
@@ -546,14 +555,15 @@ struct EpiCeStats : EpiBase {
         bool has_tau;
     };
     struct Params {
-        float2 *stats;          // [n_tiles_total][T]: (max, sumexp) per tile and token
+        float2 *stats;          // [n_parts][T]: (max, sumexp) per part and token
         float *tau;             // [T] target logit
         const int32_t *targets; // [T]
         int64_t T;
         int v_valid;
         int n_base;             // vocabulary id of GEMM column 0
-        int tile_base;          // global tile index of GEMM tile column 0
+        int tile_base;          // global part index of GEMM tile column 0
         int bn;                 // tile width
+        int run_len;            // tiles per part: a part is one work unit's run of tiles
     };
     __device__ static int mode(const Params &) { return 0; }
     __device__ static Row begin(const Params &p, int row, bool live) {
@@ -594,10 +604,11 @@ struct EpiCeStats : EpiBase {
             r.has_tau = true;
         }
     }
+    // n0: the first column of the run's last tile
     __device__ static void end(const Params &p, Row &r, int row, int n0, bool live) {
         if (!live) return;
-        const int tile = p.tile_base + n0 / p.bn;
-        p.stats[static_cast<int64_t>(tile) * p.T + row] = make_float2(r.m, r.sum);
+        const int part = p.tile_base + (n0 / p.bn) / p.run_len;
+        p.stats[static_cast<int64_t>(part) * p.T + row] = make_float2(r.m, r.sum);
         if (r.has_tau) p.tau[row] = r.tau;
     }
 };
@@ -762,10 +773,12 @@ struct PartialAcc {
 // One tile's epilogue for this warp: chunks [c0, c1) of its 32 rows starting
 // at row0, columns from n0. The input chunk c0 must already be issued. Gated
 // epilogues read the up half of chunk c at accumulator column up_col + 32 c.
-// Returns false if a bounded wait gave up.
+// The row state rs is begun on the first tile of a run and ended on its last
+// (both for a lone tile). Returns false if a bounded wait gave up.
 template <class Epi, int kChunk, class Acc>
 __device__ __forceinline__ bool epi_tile(const typename Epi::Params &ep, const GemmShape &shp, const Acc &acc,
                                          uint32_t up_col, int row0, int n0, int c0, int c1, int lane, EpiWarp &w,
+                                         typename Epi::Row &rs, bool first, bool last,
                                          const CUtensorMap *tmC0, const CUtensorMap *tmC1,
                                          const CUtensorMap *tmIn, const ChunkSet<kChunk> *cs,
                                          volatile int *abort_flag, uint32_t *err) {
@@ -778,7 +791,7 @@ __device__ __forceinline__ bool epi_tile(const typename Epi::Params &ep, const G
     const CUtensorMap *tm0 = tmC0;
     int y0 = row0;
     if constexpr (kChunk == kChunkC) tm0 = chunk_map(*cs, y0);
-    typename Epi::Row rs = Epi::begin(ep, row, row < shp.M);
+    if (first) rs = Epi::begin(ep, row, row < shp.M);
 #pragma unroll 1
     for (int c = c0; c < c1; ++c) {
         const int n = n0 + c * 32;
@@ -833,7 +846,7 @@ __device__ __forceinline__ bool epi_tile(const typename Epi::Params &ep, const G
             ++w.chunk_ctr;
         }
     }
-    Epi::end(ep, rs, row, n0, row < shp.M);
+    if (last) Epi::end(ep, rs, row, n0, row < shp.M);
     return true;
 }
 
@@ -1076,7 +1089,9 @@ __global__ void __launch_bounds__(64 + 32 * Epi::kWarps, 1)
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
-            if (!epi_tile<Epi, kChunk>(ep, shp, TmemAcc{taddr}, BN / 2, row0, n0, c0, c1, lane, w, &tmC0, &tmC1,
+            typename Epi::Row rs;
+            if (!epi_tile<Epi, kChunk>(ep, shp, TmemAcc{taddr}, BN / 2, row0, n0, c0, c1, lane, w, rs, true, true,
+                                       &tmC0, &tmC1,
                                        &tmIn, &cs, abort_flag, err))
                 break;
             ptx::tc_fence_before();

@@ -64,14 +64,14 @@ struct TailScratch {
 constexpr int kTailMinKBlocks = TPCE_TAIL_MIN_KBLOCKS;  // build-time tuning knobs
 constexpr int kTailMaxSplit = 8;
 inline void plan_tail(GemmShape &s, int clusters, int bn, const TailScratch *ts, cudaStream_t stream, bool &memset_ok) {
-    const int tiles = s.tiles_m * s.tiles_n;
+    const int tiles = s.tiles_m * s.unit_cols;  // work units: tiles, or runs of tiles
     s.full_units = tiles;
     s.split = 1;
     s.tail_tiles = 0;
     s.partial = nullptr;
     s.tickets = nullptr;
     memset_ok = true;
-    if (!TPCE_TAIL_SPLIT || !ts || !ts->ptr || clusters < 2 || tiles <= clusters) return;
+    if (!TPCE_TAIL_SPLIT || s.run_len != 1 || !ts || !ts->ptr || clusters < 2 || tiles <= clusters) return;
     const int r = tiles % clusters;
     if (r == 0 || r > clusters / 2) return;
     int sp = std::min({kTailMaxSplit, clusters / r, kTailMaxUnits / r, s.k_blocks / kTailMinKBlocks});
@@ -261,6 +261,8 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
     s.tiles_n = (N + kTileN - 1) / kTileN;
     s.k_blocks = (K + static_cast<int>(kBoxK) - 1) / static_cast<int>(kBoxK);
     s.group_m = pick_group_m(s.tiles_m, kBM, K, sizeof(ElemT));
+    s.run_len = 1;  // the one-CTA kernel walks single tiles
+    s.unit_cols = s.tiles_n;
     s.a_off_mn = a_off_mn;
     s.a_off_k = a_off_k;
     s.b_off_mn = b_off_mn;
@@ -297,11 +299,14 @@ tpce_status launch_gemm(const char *name, const Operand &a, const Operand &b, co
 #define TPCE_PAIR_BN 256
 #endif
 
+// run_len > 1: each work unit is that many consecutive column tiles of one
+// row-block (tiles_n must be a multiple of it; no split tail).
 template <int BN, bool A_MN, bool B_MN, class Epi, int kChunk = kChunkNone>
 tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &b, const OutView *outs,
                              const OutView *ins, int M, int N, int K, int a_off_mn, int a_off_k, int b_off_mn,
                              int b_off_k, const typename Epi::Params &ep, cudaStream_t stream, bool timed = true,
-                             int b_gate_off = 0, const Chunks *chunks = nullptr, const TailScratch *tail = nullptr) {
+                             int b_gate_off = 0, const Chunks *chunks = nullptr, const TailScratch *tail = nullptr,
+                             int run_len = 1) {
     using Cfg = PairCfg<BN, Epi>;
     constexpr int kTileN = Epi::kGated ? BN / 2 : BN;
     using OutT = typename Epi::Out;
@@ -352,6 +357,9 @@ tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &
     s.tiles_n = (N + kTileN - 1) / kTileN;
     s.k_blocks = (K + 63) / 64;
     s.group_m = pick_group_m(s.tiles_m, 2 * kBM, K, 2);
+    if (run_len < 1 || s.tiles_n % run_len != 0) return fail(TPCE_ERR_INVALID, "run of %d tiles for %s", run_len, name);
+    s.run_len = run_len;
+    s.unit_cols = s.tiles_n / run_len;
     s.a_off_mn = a_off_mn;
     s.a_off_k = a_off_k;
     s.b_off_mn = b_off_mn;
@@ -367,8 +375,8 @@ tpce_status launch_gemm_pair(const char *name, const Operand &a, const Operand &
     const int sms = num_sms();
     uint32_t *err = device_error_word();
     if (sms < 2 || err == nullptr) return fail(TPCE_ERR_CUDA, "device query failed (%s)", name);
-    const int64_t tiles = static_cast<int64_t>(s.tiles_m) * s.tiles_n;
-    const int clusters = static_cast<int>(std::min<int64_t>(tiles, sms / 2));
+    const int64_t units = static_cast<int64_t>(s.tiles_m) * s.unit_cols;
+    const int clusters = static_cast<int>(std::min<int64_t>(units, sms / 2));
     bool memset_ok = true;
     plan_tail(s, clusters, BN, tail, stream, memset_ok);
     if (!memset_ok) return fail(TPCE_ERR_CUDA, "cudaMemsetAsync of the tail tickets (%s)", name);

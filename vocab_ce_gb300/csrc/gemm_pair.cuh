@@ -143,61 +143,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
             for (int u = cluster_id; u < num_units && !*abort_flag; u += clusters) {
                 int tile, kb0, kb1, part;
                 unit_coords(u, shp, tile, kb0, kb1, part);
-                int mb, nb;
-                tile_coords(tile, shp, mb, nb);
+                int mb, rb;
+                tile_coords(tile, shp, mb, rb);
                 const int m0 = mb * (2 * kBM) + static_cast<int>(rank) * kBM;
-                // this CTA's half of the B tile; gated tiles: the even CTA loads
-                // the gate columns, the odd CTA the same columns of the up half
-                const int nh0 = Epi::kGated ? nb * kTileN + static_cast<int>(rank) * shp.b_gate_off
-                                            : nb * BN + static_cast<int>(rank) * kHalfN;
-                ChunkCursor<kChunk> cur;
-                if constexpr (kChunk == kChunkA) cur.init(cs, A_MN ? shp.a_off_k + kb0 * kBK : m0 + shp.a_off_mn);
-                if constexpr (kChunk == kChunkB) cur.init(cs, B_MN ? shp.b_off_k + kb0 * kBK : nh0 + shp.b_off_mn);
-                // failure-path test knob (off in every ordinary launch): cluster
-                // 0's first unit leaves its first k-block's stage unloaded
-                const int kb_skip = (shp.debug_withhold != 0 && u == 0) ? kb0 : -1;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!ptx::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, 1)) break;
-                    const uint32_t bar = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
-                    if (rank == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
-                    issued |= 1u << stage;
-                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                    uint8_t *sa = smem + stage * C::kStageBytes;
-                    uint8_t *sb = sa + C::kABytes;
-                    const int k0 = kb * kBK;
-                    // outer coordinates: A's M (K-major) or K (MN-major), likewise B's N or K
-                    int ya = A_MN ? k0 + shp.a_off_k : m0 + shp.a_off_mn;
-                    int yb = B_MN ? k0 + shp.b_off_k : nh0 + shp.b_off_mn;
-                    const CUtensorMap *ma = &tmA;
-                    const CUtensorMap *mb = &tmB;
-                    if constexpr (kChunk == kChunkA) {
-                        ma = cur.map;
-                        ya = cur.y;
-                    }
-                    if constexpr (kChunk == kChunkB) {
-                        mb = cur.map;
-                        yb = cur.y;
-                    }
-                    if constexpr ((kChunk == kChunkA && A_MN) || (kChunk == kChunkB && B_MN)) cur.advance(cs, kBK);
-                    if (kb != kb_skip) {
-                        if (!A_MN) {
-                            load(sa, ma, bar, k0 + shp.a_off_k, ya, pol_a);
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < kBM / 64; ++j)
-                                load(sa + j * kMnBlockBytes, ma, bar, m0 + shp.a_off_mn + 64 * j, ya, pol_a);
+                for (int i = 0; i < shp.run_len && !*abort_flag; ++i) {
+                    const int nb = rb * shp.run_len + i;
+                    // this CTA's half of the B tile; gated tiles: the even CTA loads
+                    // the gate columns, the odd CTA the same columns of the up half
+                    const int nh0 = Epi::kGated ? nb * kTileN + static_cast<int>(rank) * shp.b_gate_off
+                                                : nb * BN + static_cast<int>(rank) * kHalfN;
+                    ChunkCursor<kChunk> cur;
+                    if constexpr (kChunk == kChunkA) cur.init(cs, A_MN ? shp.a_off_k + kb0 * kBK : m0 + shp.a_off_mn);
+                    if constexpr (kChunk == kChunkB) cur.init(cs, B_MN ? shp.b_off_k + kb0 * kBK : nh0 + shp.b_off_mn);
+                    // failure-path test knob (off in every ordinary launch): cluster
+                    // 0's first tile leaves its first k-block's stage unloaded
+                    const int kb_skip = (shp.debug_withhold != 0 && u == 0 && i == 0) ? kb0 : -1;
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!ptx::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, 1)) break;
+                        const uint32_t bar = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
+                        if (rank == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
+                        issued |= 1u << stage;
+                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                        uint8_t *sa = smem + stage * C::kStageBytes;
+                        uint8_t *sb = sa + C::kABytes;
+                        const int k0 = kb * kBK;
+                        // outer coordinates: A's M (K-major) or K (MN-major), likewise B's N or K
+                        int ya = A_MN ? k0 + shp.a_off_k : m0 + shp.a_off_mn;
+                        int yb = B_MN ? k0 + shp.b_off_k : nh0 + shp.b_off_mn;
+                        const CUtensorMap *ma = &tmA;
+                        const CUtensorMap *mb_ = &tmB;
+                        if constexpr (kChunk == kChunkA) {
+                            ma = cur.map;
+                            ya = cur.y;
                         }
-                        if (!B_MN) {
-                            load(sb, mb, bar, k0 + shp.b_off_k, yb, pol_b);
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < kHalfN / 64; ++j)
-                                load(sb + j * kMnBlockBytes, mb, bar, nh0 + shp.b_off_mn + 64 * j, yb, pol_b);
+                        if constexpr (kChunk == kChunkB) {
+                            mb_ = cur.map;
+                            yb = cur.y;
                         }
-                    }
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1;
+                        if constexpr ((kChunk == kChunkA && A_MN) || (kChunk == kChunkB && B_MN)) cur.advance(cs, kBK);
+                        if (kb != kb_skip) {
+                            if (!A_MN) {
+                                load(sa, ma, bar, k0 + shp.a_off_k, ya, pol_a);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < kBM / 64; ++j)
+                                    load(sa + j * kMnBlockBytes, ma, bar, m0 + shp.a_off_mn + 64 * j, ya, pol_a);
+                            }
+                            if (!B_MN) {
+                                load(sb, mb_, bar, k0 + shp.b_off_k, yb, pol_b);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < kHalfN / 64; ++j)
+                                    load(sb + j * kMnBlockBytes, mb_, bar, nh0 + shp.b_off_mn + 64 * j, yb, pol_b);
+                            }
+                        }
+                        if (++stage == S) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
                     }
                 }
             }
@@ -214,39 +217,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            for (int u = cluster_id; u < num_units; u += clusters) {
+            bool ok = true;
+            for (int u = cluster_id; u < num_units && ok; u += clusters) {
                 int tile, kb0, kb1, part;
                 unit_coords(u, shp, tile, kb0, kb1, part);
-                if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, err, 2)) break;
-                ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN;
-                bool ok = true;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!ptx::mbar_wait(&full[stage], phase, abort_flag, err, 3)) {
+                for (int i = 0; i < shp.run_len; ++i) {
+                    if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, err, 2)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t sa = ptx::smem_u32(smem + stage * C::kStageBytes);
-                    const uint32_t sb = sa + C::kABytes;
+                    const uint32_t d_tmem = tmem_base + acc * BN;
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!ptx::mbar_wait(&full[stage], phase, abort_flag, err, 3)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const uint32_t sa = ptx::smem_u32(smem + stage * C::kStageBytes);
+                        const uint32_t sb = sa + C::kABytes;
 #pragma unroll
-                    for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                        const uint64_t ad = A_MN ? ptx::sdesc_sw128(sa + kk * (kUmmaK * kRowBytes), kMnBlockBytes, 1024)
-                                                 : ptx::sdesc_sw128(sa + kk * 32, 16, 1024);
-                        const uint64_t bd = B_MN ? ptx::sdesc_sw128(sb + kk * (kUmmaK * kRowBytes), kMnBlockBytes, 1024)
-                                                 : ptx::sdesc_sw128(sb + kk * 32, 16, 1024);
-                        ptx::mma_bf16_pair(d_tmem, ad, bd, kIdesc, ((kb - kb0) | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                            const uint64_t ad = A_MN ? ptx::sdesc_sw128(sa + kk * (kUmmaK * kRowBytes), kMnBlockBytes, 1024)
+                                                     : ptx::sdesc_sw128(sa + kk * 32, 16, 1024);
+                            const uint64_t bd = B_MN ? ptx::sdesc_sw128(sb + kk * (kUmmaK * kRowBytes), kMnBlockBytes, 1024)
+                                                     : ptx::sdesc_sw128(sb + kk * 32, 16, 1024);
+                            ptx::mma_bf16_pair(d_tmem, ad, bd, kIdesc, ((kb - kb0) | kk) != 0 ? 1u : 0u);
+                        }
+                        ptx::mma_commit_pair(&empty[stage]);
+                        if (++stage == S) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
                     }
-                    ptx::mma_commit_pair(&empty[stage]);
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
+                    if (!ok) break;
+                    ptx::mma_commit_pair(&tfull[acc]);
+                    acc ^= 1;
+                    if (acc == 0) acc_phase ^= 1;
                 }
-                if (!ok) break;
-                ptx::mma_commit_pair(&tfull[acc]);
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1;
             }
             ptx::mma_commit_pair(drain);
             ptx::mbar_wait_drain(drain, 0);
@@ -258,75 +266,91 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * Epi::kWarp
         EpiWarp w{staging + ew * EpiSmem<Epi>::kWarpBytes, in_bars + 2 * ew, 0, false, 0u, 0u};
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int u = cluster_id; u < num_units; u += clusters) {
+        bool alive = true;
+        for (int u = cluster_id; u < num_units && alive; u += clusters) {
             int tile, kb0, kb1, part;
             unit_coords(u, shp, tile, kb0, kb1, part);
-            int mb, nb;
-            tile_coords(tile, shp, mb, nb);
+            int mb, rb;
+            tile_coords(tile, shp, mb, rb);
             const int row0 = mb * (2 * kBM) + static_cast<int>(rank) * kBM + quarter * 32;
-            const int n0 = nb * kTileN;
-            if (part < 0) epi_issue_input<Epi>(w, ep, &tmIn, lane, n0, row0);
-            const bool ok = ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, err, 4);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            ptx::tc_fence_after();
-            const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
-            if (part < 0) {
-                if (!epi_tile<Epi, kChunk>(ep, shp, TmemAcc{taddr}, BN / 2, row0, n0, 0, kChunks, lane, w, &tmC0,
-                                           &tmC1, &tmIn, &cs, abort_flag, err))
+            typename Epi::Row rs;  // this thread's row state, carried along the unit's run of tiles
+            for (int i = 0; i < shp.run_len; ++i) {
+                const int n0 = (rb * shp.run_len + i) * kTileN;
+                if (part < 0) epi_issue_input<Epi>(w, ep, &tmIn, lane, n0, row0);
+                const bool ok = ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, err, 4);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    alive = false;
                     break;
-            } else {
-                // a K part of a tail tile: its partial to global scratch, all
-                // BN accumulator columns of this thread's row, column-major
-                // (a warp's 32 rows of one column are one 128-byte line)
-                const int tl = tile - shp.full_units;
-                const int64_t slot_floats = static_cast<int64_t>(kBM) * BN;
-                float *mine = shp.partial + (static_cast<int64_t>(tl * shp.split + part) * 2 + rank) * slot_floats +
-                              quarter * 32 + lane;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v[32];
-                    ptx::tmem_ld32(taddr + c * 32, v);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) mine[static_cast<int64_t>(c * 32 + i) * kBM] = v[i];
                 }
-                __threadfence();  // the partial is visible GPU-wide before the ticket below
-                // the accumulator is free again
+                ptx::tc_fence_after();
+                const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+                if (part < 0) {
+                    if (!epi_tile<Epi, kChunk>(ep, shp, TmemAcc{taddr}, BN / 2, row0, n0, 0, kChunks, lane, w, rs,
+                                               i == 0, i == shp.run_len - 1, &tmC0, &tmC1, &tmIn, &cs, abort_flag,
+                                               err)) {
+                        alive = false;
+                        break;
+                    }
+                } else {
+                    // a K part of a tail tile (runs of one tile only): its partial
+                    // to global scratch, all BN accumulator columns of this
+                    // thread's row, column-major (a warp's 32 rows of one column
+                    // are one 128-byte line)
+                    const int tl = tile - shp.full_units;
+                    const int64_t slot_floats = static_cast<int64_t>(kBM) * BN;
+                    float *mine = shp.partial + (static_cast<int64_t>(tl * shp.split + part) * 2 + rank) * slot_floats +
+                                  quarter * 32 + lane;
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
+                        float v[32];
+                        ptx::tmem_ld32(taddr + c * 32, v);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) mine[static_cast<int64_t>(c * 32 + e) * kBM] = v[e];
+                    }
+                    __threadfence();  // the partial is visible GPU-wide before the ticket below
+                    // the accumulator is free again
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&tempty[acc]), 0));
+                    acc ^= 1;
+                    if (acc == 0) acc_phase ^= 1;
+                    // the four epilogue warps' partials are written: draw the ticket
+                    if (lane == 0) ptx::mbar_arrive(tail_bar);
+                    if (ew == 0 && lane == 0) {
+                        uint32_t t = 0xffffffffu;
+                        if (ptx::mbar_wait(tail_bar, 0, abort_flag, err, 6)) {
+                            t = atomicAdd(&shp.tickets[tl * 2 + rank], 1u);
+                            __threadfence();
+                        }
+                        *tail_ticket = t;
+                        ptx::mbar_arrive(tail_done);
+                    }
+                    bool got = lane == 0 ? ptx::mbar_wait(tail_done, 0, abort_flag, err, 7) : true;
+                    if (!__all_sync(0xffffffffu, got)) {
+                        alive = false;
+                        break;
+                    }
+                    const uint32_t ticket = __shfl_sync(0xffffffffu, lane == 0 ? *tail_ticket : 0u, 0);
+                    if (ticket != static_cast<uint32_t>(shp.split - 1)) continue;  // another part finishes the tile
+                    __threadfence();  // every part's partial is visible to this CTA
+                    if (ew == 0 && lane == 0) shp.tickets[tl * 2 + rank] = 0;  // leave the ticket clear
+                    const PartialAcc sum{shp.partial + (static_cast<int64_t>(tl * shp.split) * 2 + rank) * slot_floats +
+                                             quarter * 32 + lane,
+                                         2 * slot_floats, shp.split};
+                    epi_issue_input<Epi>(w, ep, &tmIn, lane, n0, row0);
+                    if (!epi_tile<Epi, kChunk>(ep, shp, sum, BN / 2, row0, n0, 0, kChunks, lane, w, rs, true, true,
+                                               &tmC0, &tmC1, &tmIn, &cs, abort_flag, err)) {
+                        alive = false;
+                        break;
+                    }
+                    continue;
+                }
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&tempty[acc]), 0));
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1;
-                // the four epilogue warps' partials are written: draw the ticket
-                if (lane == 0) ptx::mbar_arrive(tail_bar);
-                if (ew == 0 && lane == 0) {
-                    uint32_t t = 0xffffffffu;
-                    if (ptx::mbar_wait(tail_bar, 0, abort_flag, err, 6)) {
-                        t = atomicAdd(&shp.tickets[tl * 2 + rank], 1u);
-                        __threadfence();
-                    }
-                    *tail_ticket = t;
-                    ptx::mbar_arrive(tail_done);
-                }
-                bool got = lane == 0 ? ptx::mbar_wait(tail_done, 0, abort_flag, err, 7) : true;
-                if (!__all_sync(0xffffffffu, got)) break;
-                const uint32_t ticket = __shfl_sync(0xffffffffu, lane == 0 ? *tail_ticket : 0u, 0);
-                if (ticket != static_cast<uint32_t>(shp.split - 1)) continue;  // another part finishes the tile
-                __threadfence();  // every part's partial is visible to this CTA
-                if (ew == 0 && lane == 0) shp.tickets[tl * 2 + rank] = 0;  // leave the ticket clear
-                const PartialAcc sum{shp.partial + (static_cast<int64_t>(tl * shp.split) * 2 + rank) * slot_floats +
-                                         quarter * 32 + lane,
-                                     2 * slot_floats, shp.split};
-                epi_issue_input<Epi>(w, ep, &tmIn, lane, n0, row0);
-                if (!epi_tile<Epi, kChunk>(ep, shp, sum, BN / 2, row0, n0, 0, kChunks, lane, w, &tmC0, &tmC1, &tmIn,
-                                           &cs, abort_flag, err))
-                    break;
-                continue;
             }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&tempty[acc]), 0));
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1;
         }
         if (kOuts > 0 && lane == 0) ptx::bulk_wait_all();
         epi_drain_inputs<Epi>(w);
