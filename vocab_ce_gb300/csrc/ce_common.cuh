@@ -48,7 +48,10 @@ tpce_status check_ce_shape(int64_t T, int64_t h, int64_t v_pad, int64_t v_valid,
 // The one-CTA kernel (fp32, or shards that are not whole 256-id tiles) stores
 // one part per tile.
 constexpr int64_t kCePairClusters = 76;  // CTA pairs of a 152-SM GB300 (fixed, so sizes are known on the host)
-constexpr double kCeMinBusy = 0.985;
+#ifndef TPCE_CE_MIN_BUSY
+#define TPCE_CE_MIN_BUSY 0.985
+#endif
+constexpr double kCeMinBusy = TPCE_CE_MIN_BUSY;  // build-time tuning knob
 
 struct CeStatsPlan {
     bool pair;            // pass 1 runs on the CTA-pair kernel
