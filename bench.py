@@ -66,6 +66,12 @@ TARGETS = {"mlp_frac_of_spec_peak": 0.60, "ce_frac_of_spec_roofline": 0.50}
 # compared with the measured sustained peak, shorter ones with the burst peak
 SUSTAINED_REGION_S = 1.0
 
+# the pages' own figures, quoted beside the line as context (other hardware, whole-model
+# training on clusters; none is a figure for this path on one GPU)
+PAGES_CONTEXT = ("8.3B-parameter GPT-2-style model, 8-way tensor parallel x data parallel on 512 GPUs: 15.1 PFLOP/s "
+                 "aggregate, 76% scaling efficiency against a 39 TFLOP/s single-GPU baseline; 1T-parameter model with "
+                 "tensor + pipeline + data parallelism on 3,072 A100s: 502 PFLOP/s (52% of peak)")
+
 # the workloads of each job, run back to back in one step
 JOBS = {"headline": ("mlp70b", "ce128k")}
 WORKLOAD_NAMES = ["headline", "gpt8b", "gpt8b_chain", "mlp70b", "mlp70b_sp", "ce128k", "ce128k_eval", "swiglu70b",
@@ -734,7 +740,8 @@ def run_ours(args, ws_, name):
             "timed_region_s": region_s,
             "parts": parts, "roofline": roof, "kernels": per_kernel, "gpu_launches": gpu_launches,
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
-            "clock_normalised": {"sm_mhz_median": mhz, "tflops_per_ghz": value / (mhz * 1e-3)} if mhz else None}
+            "clock_normalised": {"sm_mhz_median": mhz, "tflops_per_ghz": value / (mhz * 1e-3)} if mhz else None,
+            "context": PAGES_CONTEXT}
     print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
