@@ -557,7 +557,9 @@ def run_reference(args, ws_, name):
 
 def time_steps(job, steps, stream, profiled=False, clocks=None):
     """Run `steps` steps between two events on `stream`; per-segment events
-    give the MLP and CE parts. Returns (elapsed ms, {part: ms}, kernels)."""
+    give the MLP and CE parts. Returns (elapsed ms, {part: ms per step},
+    per-kernel timer records when `profiled`, else None, and the clock record
+    when a sampler factory is given, else None)."""
     import vocab_ce_gb300 as tp
 
     segs = job.segments()
