@@ -407,11 +407,13 @@ tpce_status tp_attn_out_backward_sp(const void *const *dZ_chunks, const void *O,
  * Only (m_i, s_i) and tau are combined across shards:
  *   m = max_i m_i,  S = sum_i s_i exp(m_i - m),  lse = m + ln S,
  *   loss = lse - tau.
- * The logit GEMM leaves each shard's (m_i, s_i) as p_i partial pairs per
- * token, each the fold over one run of consecutive vocabulary tiles, which
- * the combine folds first: p_i = 1 when the GEMM's work units fill the GPU
- * in one round, else the fewest equal parts that keep it evenly busy (9 for
- * 16,384 tokens over 129,024 ids and t = 8; one per 128-id tile for fp32).
+ * The logit GEMM reaches each shard's (m_i, s_i) through p_i partial pairs
+ * per token, each the fold over one run of consecutive vocabulary tiles;
+ * where p_i > 1 the epilogue that finishes a shard's last run folds them, so
+ * the combine reads exactly one pair per shard and token. p_i = 1 when the
+ * GEMM's work units fill the GPU in one round, else the fewest equal parts
+ * that keep it evenly busy (9 for 16,384 tokens over 129,024 ids and t = 8;
+ * one per 128-id tile for fp32).
  * Backward (dH and/or dE requested), with dl = grad_scale * (softmax - onehot)
  * on real ids and 0 on padded ids, recomputing the logits chunk by chunk:
  *   dE_i = dl_i^T H   (each shard's own rows, no exchange; padded rows = 0)
@@ -442,14 +444,15 @@ tpce_status vocab_parallel_ce(const void *H, const void *E, const int32_t *targe
  * allocations it did not plan, or a latency-critical path that must not risk
  * the implicit device synchronisation of an allocation.
  * The caller passes inputs and outputs exactly as for vocab_parallel_ce with
- * dH = dE = NULL. The per-token statistics (vocab_parallel_ce's partial
- * (max, sumexp) pairs, sum_i p_i of them) live instead in a static device
+ * dH = dE = NULL. The per-token statistics live instead in a static device
  * array of TPCE_CE_STATIC_SCRATCH_BYTES bytes inside the library, which every
- * GPU that loads the library holds until the process exits. It must hold
- * (sum_i p_i) * T * 8 bytes plus T * 4 (plus another T * 4 when lse is NULL),
- * rounded up to 256 each -- 9.6 MB for 16,384 tokens over 129,024 ids at
- * t = 8; larger requests return TPCE_ERR_WORKSPACE with the sizes in
- * tpce_last_error(), before any launch.
+ * GPU that loads the library holds until the process exits. It must hold the
+ * shards' pairs, t * T * 8 bytes; where shards are cut into parts (p_i > 1)
+ * also the parts' pairs, (sum_i p_i) * T * 8 bytes, and ceil(T / 32) * t * 4
+ * bytes of tickets; and T * 4 bytes of target logits (plus another T * 4 when
+ * lse is NULL), each rounded up to 256 -- 10.6 MB for 16,384 tokens over
+ * 129,024 ids at t = 8. Larger requests return TPCE_ERR_WORKSPACE with the
+ * sizes in tpce_last_error(), before any launch.
  * The first call on a device, with that device current, looks up the array's
  * device address (cudaGetSymbolAddress) and caches it. Under CUDA's default
  * lazy module loading that first call is also when the array's memory is
@@ -457,9 +460,9 @@ tpce_status vocab_parallel_ce(const void *H, const void *E, const int32_t *targe
  * one-time implicit allocation that fails if the device is full. Make the
  * first call per device before a memory planner reserves the device and
  * before any stream capture; later calls allocate nothing. All calls share the one array and it keeps the
- * last call's contents (nothing in it needs clearing: a call writes every
- * entry it reads); calls whose kernels overlap on the GPU race on it, so
- * order them on one stream or with events.
+ * last call's contents: a call writes every statistic it reads and clears
+ * the tickets (a memset on its stream) before using them; calls whose kernels
+ * overlap on the GPU race on it, so order them on one stream or with events.
  * Errors as vocab_parallel_ce.
  * ------------------------------------------------------------------------- */
 #define TPCE_CE_STATIC_SCRATCH_BYTES (16u << 20)

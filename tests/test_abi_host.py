@@ -84,21 +84,27 @@ def test_workspace_sizes(L):
     # the dl scratch holds at most half the vocabulary and at most 1 GiB
     assert bwd <= 2 ** 30 + T * h * 4 + fwd + 4096
     assert bwd < 0.5 * T * vp * 2
-    # pass 1 leaves a few (max, sumexp) parts per shard and token: at the 129K
-    # config each shard's 63 tiles are cut into 9 runs of 7 (4608 work units
-    # keep the 76 CTA pairs 99.4% busy), at the 8.3B config 25 tiles into 5
-    # runs of 5, and one run per shard wherever the units fit in one round;
-    # the one-CTA kernel (fp32) keeps one part per 128-id tile
+    # pass 1 hands the combine one (max, sumexp) pair per shard and token; a
+    # shard cut into several runs ("parts") also needs the parts' pairs and a
+    # ticket per 32-token slab and shard for the fold. At the 129K config
+    # each shard's 63 tiles are cut into 9 runs of 7 (4608 work units keep the
+    # 76 CTA pairs 99.4% busy), at the 8.3B config 25 tiles into 5 runs of 5,
+    # and one run per shard wherever the units fit in one round; the one-CTA
+    # kernel (fp32) makes one part per 128-id tile
     def rup(x):
         return (x + 255) // 256 * 256
 
     def fwd_ws(T, h, vp, t, dt=None):
         kw = {} if dt is None else {"dtype": dt}
         return tp.ce_workspace_bytes(T, h, vp, t, grads=False, **kw) - tail
+
+    def expect(T, t, parts):
+        fold = rup(parts * T * 8) + rup((T + 31) // 32 * t * 4) if parts > t else 0
+        return rup(t * T * 8) + fold + 2 * rup(T * 4)
     for (Tq, hq, vq, tq, parts) in ((16384, 8192, 129024, 8, 72), (8192, 3072, 51200, 8, 40),
                                     (1000, 256, 4096, 8, 8), (6400, 64, 6144, 4, 12)):
-        assert fwd_ws(Tq, hq, vq, tq) == rup(parts * Tq * 8) + 2 * rup(Tq * 4), (Tq, vq, tq)
-    assert fwd_ws(100, 64, 512, 2, dt=__import__("torch").float32) == rup(4 * 100 * 8) + 2 * rup(400)
+        assert fwd_ws(Tq, hq, vq, tq) == expect(Tq, tq, parts), (Tq, vq, tq)
+    assert fwd_ws(100, 64, 512, 2, dt=__import__("torch").float32) == expect(100, 2, 4)
     # the 8.3B block: 4 of 8 shards per chunk
     T2, h2, vp2 = 8192, 3072, 51200
     b2 = tp.ce_workspace_bytes(T2, h2, vp2, 8, grads=True) - tp.ce_workspace_bytes(T2, h2, vp2, 8, grads=False)

@@ -10,9 +10,9 @@
 // Forward: one persistent GEMM over all vocabulary tiles of all shards; its
 // epilogue reduces the fp32 logits of a run of tiles of one shard, per token,
 // to (max, sum exp) over the real ids, carried from tile to tile, and picks up
-// the target logit (each shard leaves a few such parts per token, see
-// ce_stats_plan). A combine kernel folds the parts of a shard into that
-// shard's (m_i, s_i), then folds the shards: m = max m_i,
+// the target logit; a shard covered by several runs has their pairs folded by
+// the epilogue that finishes last (see ce_stats_plan, EpiCeStats). A combine
+// kernel then folds the shards' (m_i, s_i): m = max m_i,
 // S = sum s_i exp(m_i - m), lse = m + ln S, loss = lse - tau.
 //
 // Backward (the gradient of softmax cross-entropy, dl = g (p - onehot)): the
@@ -46,7 +46,7 @@ struct CeWs {
     CeStatsPlan plan;    // pass 1's tiles, runs and statistics parts
     int64_t vc;          // vocabulary chunk width of the backward
     int64_t chunks;      // v_pad / vc
-    size_t tail, stats, tau, lse, dl, acc, Ht, Et, dlt, total;
+    size_t tail, stats, parts, tickets, tau, lse, dl, acc, Ht, Et, dlt, total;
 };
 
 CeWs ce_ws_layout(int64_t T, int64_t h, int64_t v_pad, int t, bool grads, int dtype) {
@@ -76,7 +76,9 @@ CeWs ce_ws_layout(int64_t T, int64_t h, int64_t v_pad, int t, bool grads, int dt
         return at;
     };
     L.tail = take(kTailScratchBytes);  // the GEMMs' split tails
-    L.stats = take(static_cast<size_t>(L.plan.parts) * T * sizeof(float2));
+    L.stats = take(static_cast<size_t>(t) * T * sizeof(float2));
+    L.parts = take(ce_parts_bytes(L.plan, T));
+    L.tickets = take(ce_ticket_bytes(L.plan, T, t));
     L.tau = take(static_cast<size_t>(T) * sizeof(float));
     L.lse = take(static_cast<size_t>(T) * sizeof(float));
     if (grads) {
@@ -121,7 +123,12 @@ tpce_status ce_forward(const CeArgs &a, const CeWs &L, void *ws, float *lse_buf,
     Operand A{a.H, a.T, a.h, a.h};          // K-major [T, h]
     Operand B{a.E, a.v_pad, a.h, a.h};      // K-major: N = v_pad rows, K = h columns
     const CeStatsPlan &P = L.plan;
-    EpiCeStats::Params ep{stats, tau, a.targets, a.T, vvi, 0, 0, P.bn, P.run_len};
+    uint32_t *tickets = at<uint32_t>(ws, L.tickets);
+    const size_t tb = ce_ticket_bytes(P, a.T, a.t);
+    if (tb && cudaMemsetAsync(tickets, 0, tb, s) != cudaSuccess)
+        return fail(TPCE_ERR_CUDA, "vocab_parallel_ce: cudaMemsetAsync of the statistics tickets");
+    EpiCeStats::Params ep{stats, at<float2>(ws, L.parts), tickets, tau, a.targets, a.T, vvi, 0, 0, P.bn, P.run_len,
+                          P.parts_per_shard, a.t};
     const TailScratch tail{at<uint8_t>(ws, L.tail), kTailScratchBytes};
     tpce_status st;
     if constexpr (std::is_same<ElemT, __nv_bfloat16>::value && TPCE_PAIR_BN == 256) {
@@ -140,7 +147,7 @@ tpce_status ce_forward(const CeArgs &a, const CeWs &L, void *ws, float *lse_buf,
     if (st != TPCE_OK) return st;
     // exchange of the per-token statistics across shards
     KernelTimer timer("ce_combine", s);
-    launch_ce_combine(stats, tau, a.targets, a.T, a.t, P.parts_per_shard, vvi, a.loss, lse_buf, err, s);
+    launch_ce_combine(stats, tau, a.targets, a.T, a.t, 1, vvi, a.loss, lse_buf, err, s);
     return check_launch("ce_combine", s);
 }
 

@@ -30,8 +30,9 @@ tpce_status check_ce_shape(int64_t T, int64_t h, int64_t v_pad, int64_t v_valid,
     return TPCE_OK;
 }
 
-// The per-token statistics pass 1 leaves for the combine: `parts` (max,
-// sumexp) pairs per token, parts_per_shard of them per shard, in shard order.
+// The per-token statistics of pass 1. The combine receives one (max, sumexp)
+// pair per shard and token, [t][T]; the logit GEMM may reach a shard's pair
+// through parts_per_shard partial pairs, which its epilogue folds (EpiCeStats).
 //
 // On the CTA-pair kernel (bf16 operands, shards of whole 256-id tiles) a work
 // unit of the logit GEMM is a run of consecutive vocabulary tiles of one
@@ -45,8 +46,10 @@ tpce_status check_ce_shape(int64_t T, int64_t h, int64_t v_pad, int64_t v_valid,
 // parts (a divisor of its tile count) that keep the pairs at least 98.5% busy:
 // 9 parts at that config (runs of 7 tiles, 61 rounds of 4608 units), 5 at the
 // 8.3B config, 1 wherever the units fit in one round.
-// The one-CTA kernel (fp32, or shards that are not whole 256-id tiles) stores
+// The one-CTA kernel (fp32, or shards that are not whole 256-id tiles) makes
 // one part per tile.
+// Scratch: the shards' pairs [t][T]; with several parts per shard also the
+// parts' pairs [parts][T] and one ticket per 32-token slab and shard.
 constexpr int64_t kCePairClusters = 76;  // CTA pairs of a 152-SM GB300 (fixed, so sizes are known on the host)
 #ifndef TPCE_CE_MIN_BUSY
 #define TPCE_CE_MIN_BUSY 0.985
@@ -88,6 +91,15 @@ inline CeStatsPlan ce_stats_plan(int64_t T, int64_t v_pad, int t, int dtype, boo
     return P;
 }
 
+// Bytes of the fold's scratch beside the shards' pairs: the parts' pairs and
+// the tickets (none with one part per shard).
+inline size_t ce_parts_bytes(const CeStatsPlan &P, int64_t T) {
+    return P.parts_per_shard > 1 ? static_cast<size_t>(P.parts) * T * 8 : 0;
+}
+inline size_t ce_ticket_bytes(const CeStatsPlan &P, int64_t T, int t) {
+    return P.parts_per_shard > 1 ? static_cast<size_t>((T + 31) / 32) * t * 4 : 0;
+}
+
 // (m, s) <- the log-sum-exp fold of (m, s) and (m2, s2): s e^{m - M} + s2 e^{m2 - M}
 // with M = max(m, m2). A part with s2 = 0 holds no real id and is skipped.
 __device__ __forceinline__ void lse_fold(float &m, float &s, float m2, float s2) {
@@ -98,12 +110,11 @@ __device__ __forceinline__ void lse_fold(float &m, float &s, float m2, float s2)
     }
 }
 
-// Per token: fold the parts of each shard into (m_i, s_i), then fold the
-// shards. A block takes 32 tokens, one per lane, so each part's statistics
-// arrive as one coalesced 256-byte load per warp. Its warps take the shards
-// in turn (warp w: shards w, w + kCombineWarps, ...), and warp 0 folds the
-// warps' results: only (m_i, s_i) crosses shards. Loads are issued four parts
-// at a time so that enough of this HBM-bound pass is in flight.
+// Per token: fold the shards' (m_i, s_i). A block takes 32 tokens, one per
+// lane, so each shard's statistics arrive as one coalesced 256-byte load per
+// warp. Its warps take the shards in turn (warp w: shards w, w + kCombineWarps,
+// ...), and warp 0 folds the warps' results. (The kernel also folds several
+// pairs per shard, parts_per_shard > 1, which the library no longer passes.)
 constexpr int kCombineWarps = 8;
 __global__ void __launch_bounds__(32 * kCombineWarps)
     ce_combine_kernel(const float2 *__restrict__ stats, const float *__restrict__ tau,

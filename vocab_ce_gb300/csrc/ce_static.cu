@@ -22,11 +22,14 @@
 // already full. Make that first call before a memory planner reserves the
 // device, and before any stream capture; later calls allocate nothing. All
 // calls share the one array: two calls whose kernels overlap on the GPU
-// (different streams, no ordering) race on it. Nothing in it needs clearing
-// between calls: every statistic the combine kernel reads is written earlier
-// in the same call. The statistics are vocab_parallel_ce's: a few (max,
-// sumexp) parts per shard and token, so the 129K-vocabulary config (16,384
-// tokens, 72 parts) needs 9.6 MB of the array.
+// (different streams, no ordering) race on it. The array keeps the last
+// call's contents. Every statistic the combine kernel reads is written earlier
+// in the same call; the one thing that must start at zero, the tickets of the
+// fold of a shard's partial statistics, is cleared by each call (a memset on
+// its stream) before its logit GEMM. The statistics are vocab_parallel_ce's:
+// one (max, sumexp) pair per shard and token, reached through a few partial
+// pairs per shard where the shard is cut into parts, so the 129K-vocabulary
+// config (16,384 tokens, t = 8, 9 parts per shard) needs 10.6 MB of the array.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -77,14 +80,17 @@ extern "C" tpce_status vocab_parallel_ce_loss_static(const void *H, const void *
                           static_cast<const void *>(lse)})
         if (reinterpret_cast<uintptr_t>(p) & 3u) return TPCE_ERR_ALIGN;
 
-    // scratch layout: per-part (max, sumexp) [parts][T] (the same parts as
-    // vocab_parallel_ce's), target logit [T], lse [T] if not an output
+    // scratch layout (vocab_parallel_ce's): the shards' (max, sumexp) [t][T],
+    // the parts' pairs and tickets when shards are cut into parts, target
+    // logit [T], lse [T] if not an output
     const bool f32 = dtype == TPCE_F32;
     const CeStatsPlan P = ce_stats_plan(T, v_pad, t, dtype, TPCE_PAIR_BN == 256);
-    const size_t stats_bytes = round_up(static_cast<size_t>(P.parts) * T * sizeof(float2), 256);
+    const size_t stats_bytes = round_up(static_cast<size_t>(t) * T * sizeof(float2), 256);
+    const size_t parts_bytes = round_up(ce_parts_bytes(P, T), 256);
+    const size_t ticket_bytes = ce_ticket_bytes(P, T, t);
     const size_t tau_bytes = round_up(static_cast<size_t>(T) * sizeof(float), 256);
     const size_t lse_bytes = lse ? 0 : tau_bytes;
-    const size_t need = stats_bytes + tau_bytes + lse_bytes;
+    const size_t need = stats_bytes + parts_bytes + round_up(ticket_bytes, 256) + tau_bytes + lse_bytes;
     if (need > TPCE_CE_STATIC_SCRATCH_BYTES)
         return fail(TPCE_ERR_WORKSPACE,
                     "vocab_parallel_ce_loss_static: T=%lld and %lld statistics parts per token need %zu bytes of "
@@ -95,8 +101,11 @@ extern "C" tpce_status vocab_parallel_ce_loss_static(const void *H, const void *
     st = static_scratch_address(&base);
     if (st != TPCE_OK) return st;
     float2 *stats = reinterpret_cast<float2 *>(base);
-    float *tau = reinterpret_cast<float *>(base + stats_bytes);
-    float *lse_buf = lse ? lse : reinterpret_cast<float *>(base + stats_bytes + tau_bytes);
+    float2 *parts = reinterpret_cast<float2 *>(base + stats_bytes);
+    uint32_t *tickets = reinterpret_cast<uint32_t *>(base + stats_bytes + parts_bytes);
+    uint8_t *rest = base + stats_bytes + parts_bytes + round_up(ticket_bytes, 256);
+    float *tau = reinterpret_cast<float *>(rest);
+    float *lse_buf = lse ? lse : reinterpret_cast<float *>(rest + tau_bytes);
     uint32_t *err = device_error_word();
     if (!err) return fail(TPCE_ERR_CUDA, "vocab_parallel_ce_loss_static: device status word");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -105,7 +114,10 @@ extern "C" tpce_status vocab_parallel_ce_loss_static(const void *H, const void *
 
     Operand a{H, T, h, h};      // K-major [T, h]
     Operand b{E, v_pad, h, h};  // K-major: N = v_pad rows, K = h columns
-    EpiCeStats::Params ep{stats, tau, targets, T, vvi, 0, 0, P.bn, P.run_len};
+    // the tickets keep the last call's contents: clear them (a memset, not an allocation)
+    if (ticket_bytes && cudaMemsetAsync(tickets, 0, ticket_bytes, s) != cudaSuccess)
+        return fail(TPCE_ERR_CUDA, "vocab_parallel_ce_loss_static: cudaMemsetAsync of the statistics tickets");
+    EpiCeStats::Params ep{stats, parts, tickets, tau, targets, T, vvi, 0, 0, P.bn, P.run_len, P.parts_per_shard, t};
     if (f32)
         st = launch_gemm<float, 128, false, false, EpiCeStats>("ce_static_logits_stats", a, b, nullptr, nullptr, Ti, vpi, hi, 0, 0, 0,
                                                                0, ep, s, /*timed=*/false);
@@ -120,6 +132,6 @@ extern "C" tpce_status vocab_parallel_ce_loss_static(const void *H, const void *
         st = launch_gemm<__nv_bfloat16, 128, false, false, EpiCeStats>("ce_static_logits_stats", a, b, nullptr, nullptr, Ti, vpi, hi,
                                                                        0, 0, 0, 0, ep, s, /*timed=*/false);
     if (st != TPCE_OK) return st;
-    launch_ce_combine(stats, tau, targets, T, t, P.parts_per_shard, vvi, loss, lse_buf, err, s);
+    launch_ce_combine(stats, tau, targets, T, t, 1, vvi, loss, lse_buf, err, s);
     return check_launch("ce_static_combine", s);
 }

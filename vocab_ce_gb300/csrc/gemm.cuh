@@ -540,10 +540,16 @@ struct EpiSwiGluGrad : EpiBase {
 // CE pass 1: logits of a run of vocabulary tiles (one tile on the one-CTA
 // kernel), reduced per token to (max, sum of exp(l - max)) over the real ids,
 // plus the target logit where the target falls in the run. The running
-// (max, sum) is carried from tile to tile of the run in registers and stored
-// once, for the run's part of its shard. The logits never leave the
-// registers. One warp per TMEM lane quarter, so each thread sees its token's
-// whole tile row.
+// (max, sum) is carried from tile to tile of the run in registers. The logits
+// never leave the registers. One warp per TMEM lane quarter, so each thread
+// sees its token's whole tile row.
+//
+// A shard covered by one run stores its (max, sum) straight into the shard's
+// statistics. A shard cut into several runs ("parts") stores each part's pair;
+// then, per 32-row slab, the warp that finishes the shard's last part -- known
+// from an atomic ticket per (slab, shard), with no waiting -- folds the parts
+// in part order into the shard's pair. Either way the exchange across shards
+// sees exactly one (max, sum) per shard and token.
 struct EpiCeStats : EpiBase {
     static constexpr int kWarps = 4;
     static constexpr int kOuts = 0;
@@ -555,7 +561,9 @@ struct EpiCeStats : EpiBase {
         bool has_tau;
     };
     struct Params {
-        float2 *stats;          // [n_parts][T]: (max, sumexp) per part and token
+        float2 *stats;          // [t][T]: each shard's (max, sumexp) per token
+        float2 *parts;          // [t * parts_per_shard][T]: the parts' pairs (unused with one part per shard)
+        uint32_t *tickets;      // [ceil(T / 32)][t]: parts finished per slab and shard, zero at launch
         float *tau;             // [T] target logit
         const int32_t *targets; // [T]
         int64_t T;
@@ -564,6 +572,8 @@ struct EpiCeStats : EpiBase {
         int tile_base;          // global part index of GEMM tile column 0
         int bn;                 // tile width
         int run_len;            // tiles per part: a part is one work unit's run of tiles
+        int parts_per_shard;
+        int shards;             // t
     };
     __device__ static int mode(const Params &) { return 0; }
     __device__ static Row begin(const Params &p, int row, bool live) {
@@ -604,12 +614,44 @@ struct EpiCeStats : EpiBase {
             r.has_tau = true;
         }
     }
-    // n0: the first column of the run's last tile
+    // Called by all 32 lanes of a warp together, lane l on row row0 + l; n0 is
+    // the first column of the run's last tile.
     __device__ static void end(const Params &p, Row &r, int row, int n0, bool live) {
-        if (!live) return;
         const int part = p.tile_base + (n0 / p.bn) / p.run_len;
-        p.stats[static_cast<int64_t>(part) * p.T + row] = make_float2(r.m, r.sum);
+        const int shard = part / p.parts_per_shard;
         if (r.has_tau) p.tau[row] = r.tau;
+        if (p.parts_per_shard == 1) {
+            if (live) p.stats[static_cast<int64_t>(shard) * p.T + row] = make_float2(r.m, r.sum);
+            return;
+        }
+        if (live) p.parts[static_cast<int64_t>(part) * p.T + row] = make_float2(r.m, r.sum);
+        const int lane = static_cast<int>(threadIdx.x & 31u);
+        const int row0 = row - lane;
+        if (row0 >= p.T) return;  // no real rows in this slab (the same for every part)
+        __threadfence();          // this part's pairs are visible GPU-wide before the ticket
+        __syncwarp();
+        uint32_t *ticket = p.tickets + static_cast<int64_t>(row0 / 32) * p.shards + shard;
+        uint32_t t = 0;
+        if (lane == 0) t = atomicAdd(ticket, 1u);
+        t = __shfl_sync(0xffffffffu, t, 0);
+        if (t != static_cast<uint32_t>(p.parts_per_shard - 1)) return;  // another part folds
+        __threadfence();  // every part's pairs are visible to this warp
+        if (live) {
+            // the fold of the combine: parts with no real id (sum 0) are skipped
+            float m = -INFINITY, sum = 0.0f;
+            const float2 *src = p.parts + static_cast<int64_t>(shard) * p.parts_per_shard * p.T + row;
+            for (int k = 0; k < p.parts_per_shard; ++k) {
+                const float2 q = __ldcg(src + static_cast<int64_t>(k) * p.T);  // written by other SMs
+                if (q.y > 0.0f) {
+                    const float nm = fmaxf(m, q.x);
+                    sum = sum * expf(m - nm) + q.y * expf(q.x - nm);
+                    m = nm;
+                }
+            }
+            p.stats[static_cast<int64_t>(shard) * p.T + row] = make_float2(m, sum);
+        }
+        __syncwarp();
+        if (lane == 0) *ticket = 0u;  // every part has counted: leave the ticket clear
     }
 };
 
