@@ -190,6 +190,38 @@ def test_ce_matches_oracle(case):
     assert_loss("loss vs sharded oracle", out["loss"], sh["loss"])
 
 
+def test_ce_partial_statistics_fold_is_repeatable_on_a_dirty_workspace():
+    # A shard cut into several runs has its partial (max, sumexp) pairs folded
+    # by the epilogue that draws the last ticket. The tickets live in the
+    # caller's workspace, which may hold anything: each call clears them.
+    # Two calls on a workspace filled with 0xff bytes, then a third after a
+    # call of another shape, give the same losses bit for bit, matching the
+    # oracle.
+    dev = gpu_or_skip()
+    T, h, v_pad, v_valid, t, _ = CE_CASES["runs_split_shards"]
+    w = wl.custom("fold", T=T, h=h, f=0, v_valid=v_valid, v_pad=v_pad, t=t)
+    ci = wl.ce_inputs(w, seed=3)
+    g = {k: v.to(dev) for k, v in ci.items()}
+    nbytes = tp.ce_workspace_bytes(T, h, v_pad, t, grads=False)
+    ws = torch.full((nbytes,), 255, dtype=torch.uint8, device=dev)
+    runs = []
+    for _ in range(2):
+        out = tp.vocab_parallel_ce(g["H"], g["E"], g["targets"], v_valid, t, grads=False, ws=ws)
+        assert tp.device_status() == 0
+        runs.append(out["loss"].clone())
+    # a call of another shape through the same workspace, then the first again
+    w2 = wl.custom("fold2", T=1000, h=h, f=0, v_valid=3900, v_pad=4096, t=8)
+    c2 = {k: v.to(dev) for k, v in wl.ce_inputs(w2, seed=4).items()}
+    ws.fill_(255)
+    tp.vocab_parallel_ce(c2["H"], c2["E"], c2["targets"], 3900, 8, grads=False, ws=ws)
+    out = tp.vocab_parallel_ce(g["H"], g["E"], g["targets"], v_valid, t, grads=False, ws=ws)
+    assert tp.device_status() == 0
+    runs.append(out["loss"].clone())
+    assert torch.equal(runs[0], runs[1]) and torch.equal(runs[0], runs[2])
+    ref = oracle.ce(ci["H"], ci["E"], ci["targets"].numpy(), v_valid, grads=False)
+    assert_loss("loss after the fold", runs[2], ref["loss"])
+
+
 def test_ce_forward_only_and_single_gradients():
     dev = gpu_or_skip()
     T, h, v_pad, v_valid, t = 200, 128, 1024, 1000, 4
