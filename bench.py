@@ -271,10 +271,14 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------- traffic from committed ncu summaries
 def kernel_source_hash():
+    """A hash over every CUDA source of the library: recorded traffic is only
+    trusted for the sources it was captured with."""
     h = hashlib.sha256()
-    for f in ("gemm.cuh", "gemm_pair.cuh", "gemm_launch.cuh", "ptx.cuh"):
-        with open(os.path.join(ROOT, "vocab_ce_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    d = os.path.join(ROOT, "vocab_ce_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
     return h.hexdigest()[:16]
 
 

@@ -160,6 +160,8 @@ CE_CASES = {
     # (300 work units, 4 rounds over the CTA pairs), so the combine folds 3
     # partial statistics per shard
     "runs_split_shards": (6400, 64, 6144, 6000, 4, "bf16"),
+    # h >= 6144: dE reads a transposed copy of dl (rows padded from 300 to 304 tokens)
+    "wide_h_transposed_dl": (300, 6144, 1024, 1000, 4, "bf16"),
     "ragged_f32": (333, 200, 768, 700, 2, "f32"),
     "padded_shards_f32": (130, 96, 2048, 1800, 16, "f32"),
 }

@@ -37,8 +37,24 @@
 namespace tpce {
 namespace {
 
-// upper bound of the dl scratch of one vocabulary chunk
-constexpr size_t kDlScratchBound = size_t(1) << 30;
+// upper bound of the dl scratch of one vocabulary chunk (dl, and its
+// transposed copy where dE reads one), build-time tuning knob
+#ifndef TPCE_DL_SCRATCH_BOUND
+#define TPCE_DL_SCRATCH_BOUND (1ll << 30)
+#endif
+constexpr size_t kDlScratchBound = static_cast<size_t>(TPCE_DL_SCRATCH_BOUND);
+
+// dE = dl^T H contracts over tokens, and with dl stored [T, vc] its A operand
+// is MN-major, which costs the tensor core about 11% against a K-major A
+// (measured on GB300). From this hidden width on, dl is first transposed into
+// a [vc, T] copy (an HBM-bound pass, 4 T vc bytes) so that dE reads A K-major:
+// the pass costs 4 T vc bytes at HBM speed, the saving is 11% of 2 T vc h
+// FLOPs at tensor speed, which pays for h above about 4,500 on GB300.
+#ifndef TPCE_DE_KMAJOR_MIN_H
+#define TPCE_DE_KMAJOR_MIN_H 6144
+#endif
+inline bool de_kmajor(int64_t h, int dtype) { return dtype == TPCE_BF16 && h >= TPCE_DE_KMAJOR_MIN_H; }
+inline int64_t pad8(int64_t x) { return (x + 7) / 8 * 8; }  // bf16 rows padded to 16 bytes
 
 inline int64_t pad4(int64_t x) { return (x + 3) / 4 * 4; }  // fp32 rows padded to 16 bytes
 
@@ -46,7 +62,7 @@ struct CeWs {
     CeStatsPlan plan;    // pass 1's tiles, runs and statistics parts
     int64_t vc;          // vocabulary chunk width of the backward
     int64_t chunks;      // v_pad / vc
-    size_t tail, stats, parts, tickets, tau, lse, dl, acc, Ht, Et, dlt, total;
+    size_t tail, stats, parts, tickets, tau, lse, dl, dlT, acc, Ht, Et, dlt, total;
 };
 
 CeWs ce_ws_layout(int64_t T, int64_t h, int64_t v_pad, int t, bool grads, int dtype) {
@@ -61,12 +77,15 @@ CeWs ce_ws_layout(int64_t T, int64_t h, int64_t v_pad, int t, bool grads, int dt
     // (measured: 1457 -> 1517 TFLOP/s for the 8.3B block going from 1 to 4
     // shards per chunk). When one shard alone is too large, it is split into d
     // equal 128-multiples until the scratch fits.
+    // With the transposed copy for dE the scratch holds dl twice.
+    const size_t copies = (grads && de_kmajor(h, dtype)) ? 2 : 1;
+    const size_t row_bytes = copies * static_cast<size_t>(pad8(T)) * esz;  // per vocabulary id of a chunk
     int64_t g = 1;
     for (int64_t c = 2; c <= t / 2; ++c)
-        if (t % c == 0 && static_cast<size_t>(T) * (c * vs) * esz <= kDlScratchBound) g = c;
+        if (t % c == 0 && row_bytes * (c * vs) <= kDlScratchBound) g = c;
     const int64_t q = vs / 128;
     int64_t d = 1;
-    while (d < q && (q % d != 0 || static_cast<size_t>(T) * (vs / d) * esz > kDlScratchBound)) ++d;
+    while (d < q && (q % d != 0 || row_bytes * (vs / d) > kDlScratchBound)) ++d;
     L.vc = g > 1 ? g * vs : vs / d;
     L.chunks = v_pad / L.vc;
     size_t off = 0;
@@ -83,6 +102,8 @@ CeWs ce_ws_layout(int64_t T, int64_t h, int64_t v_pad, int t, bool grads, int dt
     L.lse = take(static_cast<size_t>(T) * sizeof(float));
     if (grads) {
         L.dl = take(static_cast<size_t>(T) * L.vc * esz);
+        // the chunk's dl^T [vc, T] (rows padded to 8 tokens) for a K-major dE
+        if (de_kmajor(h, dtype)) L.dlT = take(static_cast<size_t>(L.vc) * pad8(T) * esz);
         // bf16: dH accumulates in fp32 over the chunks, then is converted once
         if (!f32) L.acc = take(static_cast<size_t>(T) * h * sizeof(float));
         if (f32) {
@@ -172,7 +193,18 @@ tpce_status ce_backward_bf16(const CeArgs &a, const CeWs &L, void *ws, const flo
             if (st != TPCE_OK) return st;
         }
         // dE rows of this chunk = dl^T H (no exchange: the rows belong to one shard)
-        if (a.dE) {
+        if (a.dE && de_kmajor(a.h, TPCE_BF16)) {
+            bf *dlT = at<bf>(ws, L.dlT);
+            const int64_t Tp = pad8(a.T);
+            if ((st = transpose_bf16(dl, a.T, L.vc, L.vc, dlT, Tp, s)) != TPCE_OK) return st;
+            Operand A{dlT, L.vc, a.T, Tp};  // K-major: M = vc rows, K = T columns
+            Operand B{a.H, a.T, a.h, a.h};  // MN-major: K = T rows, N = h columns
+            const OutView o[1] = {{static_cast<bf *>(a.dE) + static_cast<int64_t>(n_base) * a.h, L.vc, a.h, a.h}};
+            st = launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256>("ce_bwd_dE", A, B, o, nullptr, vci, hi,
+                                                                                   Ti, 0, 0, 0, 0, {nullptr}, s, 0, nullptr,
+                                                                                   &tail);
+            if (st != TPCE_OK) return st;
+        } else if (a.dE) {
             Operand A{dl, a.T, L.vc, L.vc};  // MN-major: K = T rows, M = vc columns
             Operand B{a.H, a.T, a.h, a.h};   // MN-major: K = T rows, N = h columns
             const OutView o[1] = {{static_cast<bf *>(a.dE) + static_cast<int64_t>(n_base) * a.h, L.vc, a.h, a.h}};

@@ -64,6 +64,11 @@ constexpr int kMaxRowChunks = 16;
 tpce_status colsum_chunks(int dt, const void *const *chunks, int count, int64_t rows, int64_t N, int64_t ld,
                           float *out, float *partial, cudaStream_t s);
 
+// out[c, r] = in[r, c] for a bf16 [R, C] matrix (row pitches ld_in, ld_out,
+// in elements): C, ld_in and ld_out multiples of 8, ld_out >= R, 16-byte
+// aligned pointers; columns R .. ld_out of the output are written as zeros.
+tpce_status transpose_bf16(const void *in, int64_t R, int64_t C, int64_t ld_in, void *out, int64_t ld_out,
+                           cudaStream_t s);
 // out[c, r] = in[r, c] for an fp32 [R, C] matrix (row pitches ld_in, ld_out).
 tpce_status transpose_f32(const float *in, int64_t R, int64_t C, int64_t ld_in, float *out, int64_t ld_out,
                           cudaStream_t s);

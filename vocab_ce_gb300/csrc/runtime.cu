@@ -383,6 +383,60 @@ __global__ void __launch_bounds__(256) transpose_f32_kernel(const float *__restr
     }
 }
 
+// bf16 transpose out[c, r] = in[r, c] through 64 x 64 tiles in shared memory,
+// 16-byte loads and stores on both sides so that every global access is a
+// whole 128-byte row of the tile. In shared memory the 16-byte pieces of tile
+// row r are permuted by (r >> 3) & 7, so that the 8 threads that gather one
+// 16-byte output piece from 8 tile rows j*8 + e (one per j) read 8 different
+// bank groups. Input rows r >= R read as zeros; the output is written up to
+// the 8-aligned ld_out, so its padding holds zeros.
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint4 *__restrict__ in, int64_t R, int64_t C,
+                                                             int64_t ld_in8, uint4 *__restrict__ out, int64_t ld_out,
+                                                             int64_t ld_out8) {
+    __shared__ __align__(16) uint8_t tile[64 * 128];
+    const int t = threadIdx.x;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 64;
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const int row = p * 32 + (t >> 3), ch = t & 7;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r0 + row < R && c0 + ch * 8 < C) v = __ldg(in + (r0 + row) * ld_in8 + (c0 >> 3) + ch);
+        *reinterpret_cast<uint4 *>(tile + row * 128 + ((ch ^ ((row >> 3) & 7)) << 4)) = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const int oc = p * 32 + (t >> 3), j = t & 7;  // output row c0 + oc, its 16-byte piece j
+        if (c0 + oc >= C || r0 + j * 8 >= ld_out) continue;
+        uint16_t h[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int row = j * 8 + e;  // (row >> 3) & 7 == j
+            h[e] = *reinterpret_cast<const uint16_t *>(tile + row * 128 + ((((oc >> 3) ^ j)) << 4) + ((oc & 7) << 1));
+        }
+        uint4 v;
+        v.x = h[0] | (static_cast<uint32_t>(h[1]) << 16);
+        v.y = h[2] | (static_cast<uint32_t>(h[3]) << 16);
+        v.z = h[4] | (static_cast<uint32_t>(h[5]) << 16);
+        v.w = h[6] | (static_cast<uint32_t>(h[7]) << 16);
+        out[(c0 + oc) * ld_out8 + (r0 >> 3) + j] = v;
+    }
+}
+
+tpce_status transpose_bf16(const void *in, int64_t R, int64_t C, int64_t ld_in, void *out, int64_t ld_out,
+                           cudaStream_t s) {
+    if (R <= 0 || C <= 0) return TPCE_OK;
+    if (C % 8 || ld_in % 8 || ld_out % 8 || ld_out < R || !aligned16(in) || !aligned16(out))
+        return fail(TPCE_ERR_INVALID, "transpose_bf16: rows of 8-element multiples, 16-byte aligned");
+    KernelTimer t("transpose_bf16", s);
+    dim3 grid(static_cast<unsigned>((C + 63) / 64), static_cast<unsigned>((R + 63) / 64));
+    if (grid.y > 65535) return fail(TPCE_ERR_SHAPE, "transpose_bf16: %lld rows", static_cast<long long>(R));
+    transpose_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4 *>(in), R, C, ld_in / 8,
+                                               static_cast<uint4 *>(out), ld_out, ld_out / 8);
+    return check_launch("transpose_bf16", s);
+}
+
 tpce_status transpose_f32(const float *in, int64_t R, int64_t C, int64_t ld_in, float *out, int64_t ld_out,
                           cudaStream_t s) {
     if (R <= 0 || C <= 0) return TPCE_OK;
