@@ -71,10 +71,17 @@ def test_workspace_sizes(L):
     # K parts of one CTA pair's 256 x 256 fp32 tile, plus their tickets
     tail = tp.tail_workspace_bytes()
     assert tail == 64 * 2 * 128 * 256 * 4 + 4096
-    # MLP backward holds dU [T, f] in bf16 plus a small column-sum buffer
-    for T, h, f in ((32, 64, 256), (4096, 8192, 32768)):
+    # MLP backward holds dU [T, f] in bf16 plus a small column-sum buffer; from
+    # widths of 6144 on, the weight gradients read K-major copies: X^T [h, T]
+    # (for dA, when f >= 6144) and Y^T [f, T] (for dB, when h >= 6144), rows
+    # padded to 8 tokens
+    def copies(T, h, fw, f):
+        Tp = (T + 7) // 8 * 8
+        return (h * Tp * 2 if fw >= 6144 else 0) + (f * Tp * 2 if h >= 6144 else 0)
+    for T, h, f in ((32, 64, 256), (4096, 8192, 32768), (8192, 3072, 12288), (300, 6144, 6144)):
         b = tp.mlp_workspace_bytes(T, h, f, 8 if f % 512 == 0 else 2) - tail
-        assert b >= T * f * 2 and b < T * f * 2 + 64 * max(f, h) * 4 + 4096
+        base = T * f * 2 + copies(T, h, f, f)
+        assert b >= base and b < base + 64 * max(f, h) * 4 + 4096, (T, h, f)
     # CE: the forward keeps statistics only; the backward scratch stays far
     # below the T x v_pad logits (the logits are never materialised)
     T, h, vp, t = 16384, 8192, 129024, 8
@@ -161,7 +168,9 @@ def test_swiglu_validation_and_workspace(L):
     # the backward holds [dG | dUp] [T, 2f] in bf16 plus a small column-sum buffer
     T, h, f = 4096, 8192, 28672
     b = tp.swiglu_workspace_bytes(T, h, f, 8) - tp.tail_workspace_bytes()
-    assert T * 2 * f * 2 <= b < T * 2 * f * 2 + 64 * 2 * f * 4 + 4096
+    Tp = (T + 7) // 8 * 8
+    cp = (h * Tp * 2 if 2 * f >= 6144 else 0) + (f * Tp * 2 if h >= 6144 else 0)  # X^T, Y^T
+    assert T * 2 * f * 2 + cp <= b < T * 2 * f * 2 + cp + 64 * 2 * f * 4 + 4096
     # fp32: transposed W1 [2f, h], W2, Y, dZ, X and [dG | dUp]
     T, h, f = 32, 64, 256
     b32 = tp.swiglu_workspace_bytes(T, h, f, 2, dtype=torch.float32)

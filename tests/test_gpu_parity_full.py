@@ -159,6 +159,16 @@ def check_swiglu_full(w, dev, seed=0):
     assert_rel("db2", _host(bwd["db2"]), oracle.bias_grad(dZ))
 
 
+def test_transposed_weight_gradient_operands_at_width_6144():
+    # from widths of 6144 on, dA / dW1 read X^T and dB / dW2 read Y^T from
+    # transposed copies (K-major); a ragged T of 300 pads their rows to 304.
+    # The same sampled checks as the full-size configs, both MLP variants.
+    dev = gpu_or_skip()
+    check_mlp_full(wl.custom("xt_yt", T=300, h=6144, f=6144, v_valid=0, v_pad=0, t=2), dev, seed=5)
+    check_swiglu_full(wl.custom("xt_yt_glu", T=300, h=6144, f=3072, v_valid=0, v_pad=0, t=2, act="swiglu"), dev,
+                      seed=6)
+
+
 def test_swiglu70b_full_size():
     dev = gpu_or_skip()
     check_swiglu_full(wl.WORKLOADS["swiglu70b"], dev)

@@ -67,6 +67,21 @@ tpce_status check_mlp_shape(Act act, int64_t T, int64_t h, int64_t f, int t, int
 }
 
 inline int64_t pad4(int64_t x) { return (x + 3) / 4 * 4; }  // fp32 rows padded to 16 bytes
+inline int64_t pad8(int64_t x) { return (x + 7) / 8 * 8; }  // bf16 rows padded to 16 bytes
+
+// The weight gradients dB = Y^T dZ and dA = X^T dU contract over tokens, and
+// with Y and X stored token-major their A operand is MN-major, which costs the
+// tensor core about 11% against a K-major A (measured on GB300). A transposed
+// copy (an HBM-bound pass of 4 T n bytes for an [T, n] operand) pays when the
+// GEMM's other width is large: dA = X^T dU does 2 T h fw FLOPs over X's
+// 4 T h bytes, dB = Y^T dZ 2 T f h over Y's 4 T f bytes, and the copy wins for
+// that other width above about 4,500 on GB300. Dense bf16 calls only (the
+// sequence-parallel forms read X and dZ from their chunks).
+#ifndef TPCE_WGRAD_KMAJOR_MIN
+#define TPCE_WGRAD_KMAJOR_MIN 6144
+#endif
+inline bool xt_copy(int64_t fw, int dtype) { return dtype == TPCE_BF16 && fw >= TPCE_WGRAD_KMAJOR_MIN; }
+inline bool yt_copy(int64_t h, int dtype) { return dtype == TPCE_BF16 && h >= TPCE_WGRAD_KMAJOR_MIN; }
 
 // Sequence-chunked activations (null members: dense tensors).
 struct SeqPar {
@@ -81,12 +96,14 @@ inline TailScratch tail_of(void *ws, size_t ws_bytes) {
     return (ws && ws_bytes >= kTailScratchBytes) ? TailScratch{ws, kTailScratchBytes} : TailScratch{nullptr, 0};
 }
 
-// Workspace layout. bf16: dU [T, fw] (fw = f, or 2f for SwiGLU: [dG | dUp])
-// and the column-sum partials. fp32 adds the transposed operands of the tf32
-// path: W1^T, W2^T (forward), Y^T, dZ^T, X^T, dU^T (backward), the
-// token-major ones with rows padded to a multiple of 4.
+// Workspace layout. bf16: dU [T, fw] (fw = f, or 2f for SwiGLU: [dG | dUp]),
+// the column-sum partials, and where they pay the transposed copies X^T
+// [h, T] and Y^T [f, T] (rows padded to a multiple of 8) for K-major weight
+// gradients. fp32 adds the transposed operands of the tf32 path: W1^T, W2^T
+// (forward), Y^T, dZ^T, X^T, dU^T (backward), the token-major ones with rows
+// padded to a multiple of 4.
 struct MlpWs {
-    size_t tail, dU, partial, At, Bt, Yt, dZt, Xt, dUt, total;
+    size_t tail, dU, partial, At, Bt, Yt, dZt, Xt, dUt, XtB, YtB, total;
 };
 
 MlpWs mlp_ws_layout(Act act, int64_t T, int64_t h, int64_t f, int dtype) {
@@ -103,6 +120,8 @@ MlpWs mlp_ws_layout(Act act, int64_t T, int64_t h, int64_t f, int dtype) {
     L.dU = take(static_cast<size_t>(T) * fw * esz);
     const size_t pf = std::max(colsum_partial_floats(T, fw), colsum_partial_floats(T, h));
     L.partial = take(pf * sizeof(float));
+    if (xt_copy(fw, dtype)) L.XtB = take(static_cast<size_t>(h) * pad8(T) * 2);
+    if (yt_copy(h, dtype)) L.YtB = take(static_cast<size_t>(f) * pad8(T) * 2);
     if (dtype == TPCE_F32) {
         const size_t Tp = static_cast<size_t>(pad4(T));
         L.At = take(static_cast<size_t>(fw) * h * 4);
@@ -195,28 +214,45 @@ tpce_status backward_bf16(Act act, const void *dZ, const void *X, const void *A,
                           "swiglu_bwd_dY_swiglu_grad", a, b, o, in, Ti, fi, hi, 0, 0, 0, 0, {fi}, s, 0, nullptr, ts);
         if (st != TPCE_OK) return st;
     }
+    const int64_t Tp = pad8(T);
     // dB_i = Y_i^T dZ
     {
-        Operand a{Y, T, f, f};   // MN-major: K = T rows, M = f columns
+        const char *nm = glu ? "swiglu_bwd_dW2" : "mlp_bwd_dB";
         Operand b{dZ, T, h, h};  // MN-major: K = T rows, N = h columns
         const OutView o[1] = {{dB, f, h, h}};
-        const char *nm = glu ? "swiglu_bwd_dW2" : "mlp_bwd_dB";
-        st = sp ? launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256, kChunkB>(
-                      nm, a, b, o, nullptr, fi, hi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, sp->dz, ts)
-                : launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>(nm, a, b, o, nullptr, fi, hi, Ti, 0, 0,
+        if (!sp && yt_copy(h, TPCE_BF16)) {
+            bf *Yt = at<bf>(ws, L.YtB);
+            if ((st = transpose_bf16(Y, T, f, f, Yt, Tp, s)) != TPCE_OK) return st;
+            Operand a{Yt, f, T, Tp};  // K-major: M = f rows, K = T columns
+            st = launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256>(nm, a, b, o, nullptr, fi, hi, Ti, 0, 0,
                                                                                    0, 0, {nullptr}, s, 0, nullptr, ts);
+        } else {
+            Operand a{Y, T, f, f};  // MN-major: K = T rows, M = f columns
+            st = sp ? launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256, kChunkB>(
+                          nm, a, b, o, nullptr, fi, hi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, sp->dz, ts)
+                    : launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>(
+                          nm, a, b, o, nullptr, fi, hi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, nullptr, ts);
+        }
         if (st != TPCE_OK) return st;
     }
     // dA_i = X^T dU_i
     {
-        Operand a{X, T, h, h};     // MN-major: K = T rows, M = h columns
+        const char *nm = glu ? "swiglu_bwd_dW1" : "mlp_bwd_dA";
         Operand b{dU, T, fw, fw};  // MN-major: K = T rows, N = fw columns
         const OutView o[1] = {{dA, h, fw, fw}};
-        const char *nm = glu ? "swiglu_bwd_dW1" : "mlp_bwd_dA";
-        st = sp ? launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256, kChunkA>(
-                      nm, a, b, o, nullptr, hi, fwi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, sp->x, ts)
-                : launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>(nm, a, b, o, nullptr, hi, fwi, Ti, 0,
+        if (!sp && xt_copy(fw, TPCE_BF16)) {
+            bf *Xt = at<bf>(ws, L.XtB);
+            if ((st = transpose_bf16(X, T, h, h, Xt, Tp, s)) != TPCE_OK) return st;
+            Operand a{Xt, h, T, Tp};  // K-major: M = h rows, K = T columns
+            st = launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256>(nm, a, b, o, nullptr, hi, fwi, Ti, 0,
                                                                                    0, 0, 0, {nullptr}, s, 0, nullptr, ts);
+        } else {
+            Operand a{X, T, h, h};  // MN-major: K = T rows, M = h columns
+            st = sp ? launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256, kChunkA>(
+                          nm, a, b, o, nullptr, hi, fwi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, sp->x, ts)
+                    : launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256>(
+                          nm, a, b, o, nullptr, hi, fwi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, nullptr, ts);
+        }
         if (st != TPCE_OK) return st;
     }
     // f*: dX = sum_i dU_i A_i^T, the shard sum taken in the accumulator
