@@ -25,6 +25,9 @@ LINEAR_CASES = {
     "row_ragged": (333, 384, 200, 2, "row", "bf16"),
     "column_multi_tile": (700, 512, 1536, 4, "column", "bf16"),
     "row_multi_tile": (700, 1536, 512, 4, "row", "bf16"),
+    # n_out >= 6144: dW reads a transposed copy of X (rows padded from 301 to 304 tokens)
+    "column_wide_out": (301, 256, 6144, 4, "column", "bf16"),
+    "row_wide_out": (301, 512, 6144, 2, "row", "bf16"),
     "column_f32": (130, 96, 256, 4, "column", "f32"),
     "row_f32": (130, 256, 96, 4, "row", "f32"),
 }

@@ -63,12 +63,24 @@ tpce_status check_linear_shape(int64_t T, int64_t n_in, int64_t n_out, int t, in
 }
 
 inline int64_t pad4(int64_t x) { return (x + 3) / 4 * 4; }
+inline int64_t pad8(int64_t x) { return (x + 7) / 8 * 8; }
 
-// Workspace: the column-sum partials (bias gradient); fp32 adds the
-// transposed operands of the tf32 path: W^T (forward), X^T and dY^T
-// (weight gradient), token-major ones with rows padded to a multiple of 4.
+// dW = X^T dY contracts over tokens with X's rows as its A operand, MN-major
+// as X is stored: that costs the tensor core about 11% against a K-major A
+// (measured on GB300). From an output width of 6144 on, X is first transposed
+// into a K-major copy (4 T n_in bytes at HBM speed against 11% of 2 T n_in
+// n_out FLOPs). Dense bf16 calls only.
+#ifndef TPCE_WGRAD_KMAJOR_MIN
+#define TPCE_WGRAD_KMAJOR_MIN 6144
+#endif
+inline bool xt_copy(int64_t n_out, int dtype) { return dtype == TPCE_BF16 && n_out >= TPCE_WGRAD_KMAJOR_MIN; }
+
+// Workspace: the column-sum partials (bias gradient), and where it pays the
+// bf16 copy X^T [n_in, T] (rows padded to a multiple of 8); fp32 adds the
+// transposed operands of the tf32 path: W^T (forward), X^T and dY^T (weight
+// gradient), token-major ones with rows padded to a multiple of 4.
 struct LinWs {
-    size_t tail, partial, Wt, Xt, dYt, total;
+    size_t tail, partial, Wt, Xt, dYt, XtB, total;
 };
 
 LinWs lin_ws_layout(int64_t T, int64_t n_in, int64_t n_out, int dtype) {
@@ -81,6 +93,7 @@ LinWs lin_ws_layout(int64_t T, int64_t n_in, int64_t n_out, int dtype) {
     };
     L.tail = take(kTailScratchBytes);  // offset 0: all the bf16 forward needs
     L.partial = take(colsum_partial_floats(T, n_out) * sizeof(float));
+    if (xt_copy(n_out, dtype)) L.XtB = take(static_cast<size_t>(n_in) * pad8(T) * 2);
     if (dtype == TPCE_F32) {
         const size_t Tp = static_cast<size_t>(pad4(T));
         L.Wt = take(static_cast<size_t>(n_out) * n_in * 4);
@@ -206,7 +219,18 @@ tpce_status backward_impl(const LinearNames &nm, const void *dY, const void *X, 
             if ((st = gemm_dx<bf>(nm.dX, a, bw, o, Ti, ii, oi, s, sp, ts)) != TPCE_OK) return st;
         }
         // dW = X^T dY (each shard's own block of W)
-        {
+        if (!sp && xt_copy(n_out, dtype)) {
+            bf *Xt = at<bf>(ws, L.XtB);
+            const int64_t Tp = pad8(T);
+            if ((st = transpose_bf16(X, T, n_in, n_in, Xt, Tp, s)) != TPCE_OK) return st;
+            Operand a{Xt, n_in, T, Tp};       // K-major: M = n_in rows, K = T columns
+            Operand bw{dY, T, n_out, n_out};  // MN-major: K = T rows, N = n_out columns
+            const OutView o[1] = {{dW, n_in, n_out, n_out}};
+            st = launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256>(nm.dW, a, bw, o, nullptr, ii, oi, Ti,
+                                                                                   0, 0, 0, 0, {nullptr}, s, 0, nullptr,
+                                                                                   ts);
+            if (st != TPCE_OK) return st;
+        } else {
             Operand a{X, T, n_in, n_in};     // MN-major: K = T rows, M = n_in columns
             Operand bw{dY, T, n_out, n_out};  // MN-major: K = T rows, N = n_out columns
             const OutView o[1] = {{dW, n_in, n_out, n_out}};
