@@ -65,8 +65,10 @@ tpce_status colsum_chunks(int dt, const void *const *chunks, int count, int64_t 
                           float *out, float *partial, cudaStream_t s);
 
 // out[c, r] = in[r, c] for a bf16 [R, C] matrix (row pitches ld_in, ld_out,
-// in elements): C, ld_in and ld_out multiples of 8, ld_out >= R, 16-byte
-// aligned pointers; columns R .. ld_out of the output are written as zeros.
+// in elements): C, ld_in and ld_out multiples of 8, 16-byte aligned pointers,
+// ld_out >= R8 = R rounded up to 8. Output columns R .. R8 are written as
+// zeros; columns from R8 on are not touched (so an output block may sit inside
+// a wider matrix).
 tpce_status transpose_bf16(const void *in, int64_t R, int64_t C, int64_t ld_in, void *out, int64_t ld_out,
                            cudaStream_t s);
 // out[c, r] = in[r, c] for an fp32 [R, C] matrix (row pitches ld_in, ld_out).

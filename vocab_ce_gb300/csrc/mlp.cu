@@ -75,8 +75,9 @@ inline int64_t pad8(int64_t x) { return (x + 7) / 8 * 8; }  // bf16 rows padded 
 // copy (an HBM-bound pass of 4 T n bytes for an [T, n] operand) pays when the
 // GEMM's other width is large: dA = X^T dU does 2 T h fw FLOPs over X's
 // 4 T h bytes, dB = Y^T dZ 2 T f h over Y's 4 T f bytes, and the copy wins for
-// that other width above about 4,500 on GB300. Dense bf16 calls only (the
-// sequence-parallel forms read X and dZ from their chunks).
+// that other width above about 4,500 on GB300. bf16 only; the
+// sequence-parallel forms transpose X chunk by chunk into the column blocks of
+// one X^T, and keep reading dZ (the B operand) from its chunks.
 #ifndef TPCE_WGRAD_KMAJOR_MIN
 #define TPCE_WGRAD_KMAJOR_MIN 6144
 #endif
@@ -220,12 +221,14 @@ tpce_status backward_bf16(Act act, const void *dZ, const void *X, const void *A,
         const char *nm = glu ? "swiglu_bwd_dW2" : "mlp_bwd_dB";
         Operand b{dZ, T, h, h};  // MN-major: K = T rows, N = h columns
         const OutView o[1] = {{dB, f, h, h}};
-        if (!sp && yt_copy(h, TPCE_BF16)) {
+        if (yt_copy(h, TPCE_BF16)) {
             bf *Yt = at<bf>(ws, L.YtB);
             if ((st = transpose_bf16(Y, T, f, f, Yt, Tp, s)) != TPCE_OK) return st;
             Operand a{Yt, f, T, Tp};  // K-major: M = f rows, K = T columns
-            st = launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256>(nm, a, b, o, nullptr, fi, hi, Ti, 0, 0,
-                                                                                   0, 0, {nullptr}, s, 0, nullptr, ts);
+            st = sp ? launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256, kChunkB>(
+                          nm, a, b, o, nullptr, fi, hi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, sp->dz, ts)
+                    : launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256>(
+                          nm, a, b, o, nullptr, fi, hi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, nullptr, ts);
         } else {
             Operand a{Y, T, f, f};  // MN-major: K = T rows, M = f columns
             st = sp ? launch_gemm_auto<bf, true, true, EpiStore<bf>, kBN192 | kBN256, kChunkB>(
@@ -240,9 +243,18 @@ tpce_status backward_bf16(Act act, const void *dZ, const void *X, const void *A,
         const char *nm = glu ? "swiglu_bwd_dW1" : "mlp_bwd_dA";
         Operand b{dU, T, fw, fw};  // MN-major: K = T rows, N = fw columns
         const OutView o[1] = {{dA, h, fw, fw}};
-        if (!sp && xt_copy(fw, TPCE_BF16)) {
+        if (xt_copy(fw, TPCE_BF16)) {
             bf *Xt = at<bf>(ws, L.XtB);
-            if ((st = transpose_bf16(X, T, h, h, Xt, Tp, s)) != TPCE_OK) return st;
+            if (sp) {
+                // the gathered X^T, one sequence chunk (a column block of X^T) at a time
+                for (int c = 0; c < sp->x->count; ++c) {
+                    const int64_t r0 = c * sp->x->rows;
+                    st = transpose_bf16(sp->x->ptrs[c], sp->x->rows, h, h, Xt + r0, Tp, s);
+                    if (st != TPCE_OK) return st;
+                }
+            } else if ((st = transpose_bf16(X, T, h, h, Xt, Tp, s)) != TPCE_OK) {
+                return st;
+            }
             Operand a{Xt, h, T, Tp};  // K-major: M = h rows, K = T columns
             st = launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256>(nm, a, b, o, nullptr, hi, fwi, Ti, 0,
                                                                                    0, 0, 0, {nullptr}, s, 0, nullptr, ts);

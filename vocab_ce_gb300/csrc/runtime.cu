@@ -388,10 +388,10 @@ __global__ void __launch_bounds__(256) transpose_f32_kernel(const float *__restr
 // whole 128-byte row of the tile. In shared memory the 16-byte pieces of tile
 // row r are permuted by (r >> 3) & 7, so that the 8 threads that gather one
 // 16-byte output piece from 8 tile rows j*8 + e (one per j) read 8 different
-// bank groups. Input rows r >= R read as zeros; the output is written up to
-// the 8-aligned ld_out, so its padding holds zeros.
+// bank groups. Input rows r >= R read as zeros; each output row is written up
+// to column out_cols = R rounded up to 8, so that padding holds zeros.
 __global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint4 *__restrict__ in, int64_t R, int64_t C,
-                                                             int64_t ld_in8, uint4 *__restrict__ out, int64_t ld_out,
+                                                             int64_t ld_in8, uint4 *__restrict__ out, int64_t out_cols,
                                                              int64_t ld_out8) {
     __shared__ __align__(16) uint8_t tile[64 * 128];
     const int t = threadIdx.x;
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint4 *__rest
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
         const int oc = p * 32 + (t >> 3), j = t & 7;  // output row c0 + oc, its 16-byte piece j
-        if (c0 + oc >= C || r0 + j * 8 >= ld_out) continue;
+        if (c0 + oc >= C || r0 + j * 8 >= out_cols) continue;
         uint16_t h[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -427,13 +427,14 @@ __global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint4 *__rest
 tpce_status transpose_bf16(const void *in, int64_t R, int64_t C, int64_t ld_in, void *out, int64_t ld_out,
                            cudaStream_t s) {
     if (R <= 0 || C <= 0) return TPCE_OK;
-    if (C % 8 || ld_in % 8 || ld_out % 8 || ld_out < R || !aligned16(in) || !aligned16(out))
+    const int64_t out_cols = (R + 7) / 8 * 8;
+    if (C % 8 || ld_in % 8 || ld_out % 8 || ld_out < out_cols || !aligned16(in) || !aligned16(out))
         return fail(TPCE_ERR_INVALID, "transpose_bf16: rows of 8-element multiples, 16-byte aligned");
     KernelTimer t("transpose_bf16", s);
     dim3 grid(static_cast<unsigned>((C + 63) / 64), static_cast<unsigned>((R + 63) / 64));
     if (grid.y > 65535) return fail(TPCE_ERR_SHAPE, "transpose_bf16: %lld rows", static_cast<long long>(R));
     transpose_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4 *>(in), R, C, ld_in / 8,
-                                               static_cast<uint4 *>(out), ld_out, ld_out / 8);
+                                               static_cast<uint4 *>(out), out_cols, ld_out / 8);
     return check_launch("transpose_bf16", s);
 }
 
