@@ -270,13 +270,22 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------- traffic from committed ncu summaries
-def kernel_source_hash():
-    """A hash over every CUDA source of the library: recorded traffic is only
-    trusted for the sources it was captured with."""
-    h = hashlib.sha256()
+# The translation unit each kernel's launch is compiled in (by name prefix).
+KERNEL_UNITS = (("ce_static_", "ce_static.cu"), ("ce_", "ce.cu"), ("mlp_", "mlp.cu"), ("swiglu_", "mlp.cu"),
+                ("linear_", "linear.cu"), ("attn_", "linear.cu"), ("transpose_", "runtime.cu"),
+                ("colsum_", "runtime.cu"), ("f32_to_bf16", "runtime.cu"))
+
+
+def kernel_source_hash(kernel=None):
+    """A hash over the sources a kernel is built from: its translation unit and
+    every shared header of the library (every CUDA source when the kernel is
+    not known). Recorded traffic is only trusted for the sources it was
+    captured with."""
     d = os.path.join(ROOT, "vocab_ce_gb300", "csrc")
+    unit = next((u for p, u in KERNEL_UNITS if kernel and kernel.startswith(p)), None)
+    h = hashlib.sha256()
     for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")):
+        if f.endswith((".cuh", ".h")) or (f.endswith(".cu") and unit in (None, f)):
             with open(os.path.join(d, f), "rb") as fh:
                 h.update(fh.read())
     return h.hexdigest()[:16]
@@ -284,11 +293,11 @@ def kernel_source_hash():
 
 def traffic_from_profiles(kernel, workload):
     """dram bytes per launch recorded in profiles/ for this kernel and workload,
-    if the GEMM source has not changed since the capture; else None."""
+    if the kernel's sources have not changed since the capture; else None."""
     d = os.path.join(ROOT, "profiles")
     if not os.path.isdir(d):
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash(kernel)
     for fn in sorted(os.listdir(d)):
         if not fn.endswith((".md", ".txt")):
             continue

@@ -59,3 +59,24 @@ def test_fractions_of_the_peaks():
 
 def test_whole_job_rate_counts_every_rank():
     assert bench.job_rate(4, 2.0, 0.5) == 16.0
+
+
+def test_traffic_is_keyed_to_each_kernels_sources(tmp_path, monkeypatch):
+    # every kernel of the library maps to the translation unit its launch is compiled in
+    csrc = os.path.join(ROOT, "vocab_ce_gb300", "csrc")
+    units = {u for _, u in bench.KERNEL_UNITS}
+    assert units <= set(os.listdir(csrc))
+    ce, mlp = bench.kernel_source_hash("ce_bwd_logits_dl"), bench.kernel_source_hash("mlp_bwd_dA")
+    assert ce == bench.kernel_source_hash("ce_fwd_logits_stats") and ce != mlp
+    assert bench.kernel_source_hash("transpose_bf16") not in (ce, mlp)
+    assert len({ce, mlp, bench.kernel_source_hash()}) == 3
+    # a recorded line is used only while its kernel's sources are unchanged
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "t.md").write_text(f"    traffic_per_launch kernel=ce_bwd_logits_dl workload=ce128k bytes=1234 source={ce}\n"
+                               f"    traffic_per_launch kernel=mlp_bwd_dA workload=mlp70b bytes=99 source=0000\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "vocab_ce_gb300").symlink_to(os.path.join(ROOT, "vocab_ce_gb300"))
+    assert bench.traffic_from_profiles("ce_bwd_logits_dl", "ce128k") == 1234
+    assert bench.traffic_from_profiles("ce_bwd_logits_dl", "gpt8b") is None
+    assert bench.traffic_from_profiles("mlp_bwd_dA", "mlp70b") is None
