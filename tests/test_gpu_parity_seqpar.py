@@ -125,6 +125,8 @@ LIN_SP_CASES = {
     # both partitions valid: n_out / t (column) and n_in / t (row) are whole 64-wide blocks
     "bf16": (512, 512, 256, 4, "bf16"),
     "bf16_wide": (1024, 512, 1024, 8, "bf16"),
+    # output width 6144: dW reads the K-major copy of X (made chunk by chunk for the column form)
+    "bf16_wide_out": (512, 256, 6144, 4, "bf16"),
     "f32": (256, 128, 256, 2, "f32"),
 }
 

@@ -69,7 +69,8 @@ inline int64_t pad8(int64_t x) { return (x + 7) / 8 * 8; }
 // as X is stored: that costs the tensor core about 11% against a K-major A
 // (measured on GB300). From an output width of 6144 on, X is first transposed
 // into a K-major copy (4 T n_in bytes at HBM speed against 11% of 2 T n_in
-// n_out FLOPs). Dense bf16 calls only.
+// n_out FLOPs); with sequence-parallel X the copy is made chunk by chunk.
+// bf16 calls only.
 #ifndef TPCE_WGRAD_KMAJOR_MIN
 #define TPCE_WGRAD_KMAJOR_MIN 6144
 #endif
@@ -219,16 +220,25 @@ tpce_status backward_impl(const LinearNames &nm, const void *dY, const void *X, 
             if ((st = gemm_dx<bf>(nm.dX, a, bw, o, Ti, ii, oi, s, sp, ts)) != TPCE_OK) return st;
         }
         // dW = X^T dY (each shard's own block of W)
-        if (!sp && xt_copy(n_out, dtype)) {
+        if (xt_copy(n_out, dtype)) {
             bf *Xt = at<bf>(ws, L.XtB);
             const int64_t Tp = pad8(T);
-            if ((st = transpose_bf16(X, T, n_in, n_in, Xt, Tp, s)) != TPCE_OK) return st;
+            if (sp && sp->x) {
+                // the gathered X^T, one sequence chunk (a column block of X^T) at a time
+                for (int c = 0; c < sp->x->count; ++c) {
+                    st = transpose_bf16(sp->x->ptrs[c], sp->x->rows, n_in, n_in, Xt + c * sp->x->rows, Tp, s);
+                    if (st != TPCE_OK) return st;
+                }
+            } else if ((st = transpose_bf16(X, T, n_in, n_in, Xt, Tp, s)) != TPCE_OK) {
+                return st;
+            }
             Operand a{Xt, n_in, T, Tp};       // K-major: M = n_in rows, K = T columns
-            Operand bw{dY, T, n_out, n_out};  // MN-major: K = T rows, N = n_out columns
+            Operand bw{dY, T, n_out, n_out};  // MN-major: K = T rows, N = n_out columns (or the dY chunks)
             const OutView o[1] = {{dW, n_in, n_out, n_out}};
-            st = launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256>(nm.dW, a, bw, o, nullptr, ii, oi, Ti,
-                                                                                   0, 0, 0, 0, {nullptr}, s, 0, nullptr,
-                                                                                   ts);
+            st = (sp && sp->dy) ? launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256, kChunkB>(
+                                      nm.dW, a, bw, o, nullptr, ii, oi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, sp->dy, ts)
+                                : launch_gemm_auto<bf, false, true, EpiStore<bf>, kBN192 | kBN256>(
+                                      nm.dW, a, bw, o, nullptr, ii, oi, Ti, 0, 0, 0, 0, {nullptr}, s, 0, nullptr, ts);
             if (st != TPCE_OK) return st;
         } else {
             Operand a{X, T, n_in, n_in};     // MN-major: K = T rows, M = n_in columns
