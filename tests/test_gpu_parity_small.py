@@ -192,6 +192,27 @@ def test_ce_matches_oracle(case):
     assert_loss("loss vs sharded oracle", out["loss"], sh["loss"])
 
 
+@pytest.mark.parametrize("gs,dtype", [(0.0, "bf16"), (-0.75, "bf16"), (1.0e4, "bf16"), (-0.75, "f32")])
+def test_ce_grad_scale_zero_negative_and_large(gs, dtype):
+    # The dl epilogue folds a positive grad_scale into the exponent,
+    # exp(l - (lse - ln g)), and multiplies by it otherwise: a zero scale gives
+    # zero gradients, a negative one flips their sign, a large one stays finite.
+    dev = gpu_or_skip()
+    T, h, v_pad, v_valid, t = 200, 128, 1024, 1000, 4
+    w = wl.custom("grad_scale", T=T, h=h, f=0, v_valid=v_valid, v_pad=v_pad, t=t, dtype=dtype)
+    ci = wl.ce_inputs(w, seed=3)
+    g = {k: v.to(dev) for k, v in ci.items()}
+    out = tp.vocab_parallel_ce(g["H"], g["E"], g["targets"], v_valid, t, grad_scale=gs)
+    assert tp.device_status() == 0
+    ref = oracle.ce(ci["H"], ci["E"], ci["targets"].numpy(), v_valid, grad_scale=gs)
+    assert_loss("loss", out["loss"], ref["loss"])
+    if gs == 0.0:
+        assert torch.count_nonzero(out["dH"]).item() == 0 and torch.count_nonzero(out["dE"]).item() == 0
+    else:
+        assert_rel(f"dH (grad_scale {gs}, {dtype})", out["dH"], ref["dH"])
+        assert_rel(f"dE (grad_scale {gs}, {dtype})", out["dE"], ref["dE"])
+
+
 def test_ce_partial_statistics_fold_is_repeatable_on_a_dirty_workspace():
     # A shard cut into several runs has its partial (max, sumexp) pairs folded
     # by the epilogue that draws the last ticket. The tickets live in the
