@@ -127,12 +127,30 @@ def test_gpt8b_block_full_oracle():
 
 def test_mlp70b_full_size():
     dev = gpu_or_skip()
-    check_mlp_full(wl.WORKLOADS["mlp70b"], dev)
+    w = wl.WORKLOADS["mlp70b"]
+    mi, fwd, bwd = check_mlp_full(w, dev)
+    # the same call again gives the same bits (no atomics decide a sum's order)
+    fwd2 = tp.tp_mlp_forward(mi["X"], mi["A"], mi["B"], w.t, mi["bA"], mi["bB"])
+    bwd2 = tp.tp_mlp_backward(mi["dZ"], mi["X"], mi["A"], mi["B"], fwd2["U"], fwd2["Y"], w.t)
+    for k in ("Z", "U", "Y"):
+        assert torch.equal(fwd[k], fwd2[k]), k
+    for k in ("dX", "dA", "dbA", "dB", "dbB"):
+        assert torch.equal(bwd[k], bwd2[k]), k
 
 
 def test_ce128k_full_size():
     dev = gpu_or_skip()
-    check_ce_full(wl.WORKLOADS["ce128k"], dev, de_tokens=32)
+    w = wl.WORKLOADS["ce128k"]
+    out = check_ce_full(w, dev, de_tokens=32)
+    # the same call again gives the same bits: the statistics parts fold in run
+    # order, dH adds its vocabulary chunks in chunk order
+    ci = wl.ce_inputs(w, seed=0, device=dev)
+    ci["targets"][0] = 0
+    ci["targets"][1] = w.v_valid - 1
+    again = tp.vocab_parallel_ce(ci["H"], ci["E"], ci["targets"], w.v_valid, w.t, grad_scale=1.0 / w.T)
+    assert tp.device_status() == 0
+    for k in ("loss", "lse", "dH", "dE"):
+        assert torch.equal(out[k], again[k]), k
 
 
 def check_swiglu_full(w, dev, seed=0):

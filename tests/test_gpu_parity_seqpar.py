@@ -33,6 +33,9 @@ SP_CASES = {
     "ragged_last_pair_tile": (640, 136, 640, 5, "bf16"),      # T/128 odd: the last tile's second CTA is past T
     "sixteen_chunks": (2048, 128, 1024, 16, "bf16"),
     "fp32": (256, 128, 256, 2, "f32"),
+    # widths from 6144 on: dA reads X^T built chunk by chunk, dB reads Y^T with the dZ chunks as B
+    "wide_f_x_copy": (512, 256, 6144, 4, "bf16"),
+    "wide_h_y_copy": (512, 6144, 512, 4, "bf16"),
 }
 
 
@@ -66,10 +69,20 @@ def test_mlp_seq_parallel_matches_oracle(case):
         assert torch.equal(bwd[k], dbw[k]), k
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_swiglu_seq_parallel_matches_oracle(dtype):
+SWIGLU_SP_CASES = {
+    # name: (T, h, f, t, dtype)
+    "bf16": (512, 192, 512, 4, "bf16"),
+    "f32": (512, 192, 512, 4, "f32"),
+    # 2f = 6144: dW1 reads X^T built chunk by chunk; h = 6144: dW2 reads Y^T
+    "wide_f_x_copy": (256, 128, 3072, 2, "bf16"),
+    "wide_h_y_copy": (256, 6144, 256, 2, "bf16"),
+}
+
+
+@pytest.mark.parametrize("case", list(SWIGLU_SP_CASES))
+def test_swiglu_seq_parallel_matches_oracle(case):
     dev = gpu_or_skip()
-    T, h, f, t = 512, 192, 512, 4
+    T, h, f, t, dtype = SWIGLU_SP_CASES[case]
     w = wl.custom("sp_swiglu", T=T, h=h, f=f, v_valid=0, v_pad=0, t=t, dtype=dtype, act="swiglu")
     si = wl.swiglu_inputs(w, seed=0)
     si["b1"], si["b2"] = _biases(2 * f, h, 1)
