@@ -720,7 +720,8 @@ def run_ours(args, ws_, name):
     # ---------------- end to end: pinned host inputs -> device, the step, loss -> host
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, job, ws_, dev, stream, barrier, ws, mlp_fl + ce_fl)
+        e2e = run_e2e(args, job, ws_, dev, stream, barrier, ws, mlp_fl + ce_fl,
+                      clocks=(lambda: ClockSampler(dev)) if not args.no_clocks else None)
 
     # ---------------- CPU oracle baseline (rank 0 at N = 1 only)
     cpu = None
@@ -765,7 +766,7 @@ def run_ours(args, ws_, name):
     return 0
 
 
-def run_e2e(args, job, ws_, dev, stream, barrier, ws, work):
+def run_e2e(args, job, ws_, dev, stream, barrier, ws, work, clocks=None):
     """The same steps through the Python API with every step's inputs copied
     from pinned host memory (a second stream, double-buffered: step i+1's copy
     overlaps step i's compute) and the step's result read back."""
@@ -829,16 +830,19 @@ def run_e2e(args, job, ws_, dev, stream, barrier, ws, work):
     barrier()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
+    sampler = clocks() if clocks else None
     a.record(stream)
     e2e_run(args.steps, a)
     b.record(stream)
     torch.cuda.synchronize()
+    clk = sampler.stop() if sampler else None
     barrier()
     e_ms = max_over_ranks(a.elapsed_time(b), ws, dev)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = res_host.numel() * res_host.element_size()
     return {"value": job_rate(ws, work, e_ms / args.steps * 1e-3) / 1e12, "unit": UNIT,
             "ms_per_step": e_ms / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "clocks": clk,
             "path": "vocab_ce_gb300 Python API -> C ABI; every step's inputs copied from pinned host memory "
                     "(on a second stream, double-buffered: step i+1's copy overlaps step i's compute; the first "
                     "copy and the last result read are inside the timed region)"}
