@@ -21,9 +21,10 @@
 // dE_chunk = dl^T H (the shard's own rows) and dH += dl E_chunk (the sum over
 // shards, accumulated in fp32 across chunks) follow as two more GEMMs.
 //
-// bf16 tensors read the transposed operands (dl^T, H as the dE GEMM's N
-// operand, E as the dH GEMM's N operand) in place; the fp32 (tf32) path
-// transposes them into the workspace first.
+// bf16 tensors read H as the dE GEMM's N operand and E as the dH GEMM's N
+// operand in place, and dl^T either in place (MN-major) or, from the hidden
+// width below on, from a [vc, T] copy that the dl GEMM's epilogue writes beside
+// dl; the fp32 (tf32) path transposes them into the workspace first.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -46,10 +47,12 @@ constexpr size_t kDlScratchBound = static_cast<size_t>(TPCE_DL_SCRATCH_BOUND);
 
 // dE = dl^T H contracts over tokens, and with dl stored [T, vc] its A operand
 // is MN-major, which costs the tensor core about 11% against a K-major A
-// (measured on GB300). From this hidden width on, dl is first transposed into
-// a [vc, T] copy (an HBM-bound pass, 4 T vc bytes) so that dE reads A K-major:
-// the pass costs 4 T vc bytes at HBM speed, the saving is 11% of 2 T vc h
-// FLOPs at tensor speed, which pays for h above about 4,500 on GB300.
+// (measured on GB300). From this hidden width on, the dl GEMM's epilogue also
+// stores each dl tile transposed into a [vc, T] copy (a second TMA store of
+// the same values, 2 T vc bytes) so that dE reads A K-major. At the 129K
+// config that made the dl GEMM about 0.5% slower and took dE from 22.7 to
+// about 21 ms per step; a separate transpose pass (4 T vc bytes at HBM speed,
+// 1.4 ms per step there) did the same job before.
 #ifndef TPCE_DE_KMAJOR_MIN_H
 #define TPCE_DE_KMAJOR_MIN_H 6144
 #endif
@@ -183,20 +186,27 @@ tpce_status ce_backward_bf16(const CeArgs &a, const CeWs &L, void *ws, const flo
         const int n_base = static_cast<int>(c * L.vc);
         tpce_status st;
         // recompute this chunk's logits -> dl = g (softmax - onehot)
+        // at widths where dE reads dl^T, the dl epilogue writes it beside dl
+        const bool with_t = a.dE && de_kmajor(a.h, TPCE_BF16);
         {
             Operand A{a.H, a.T, a.h, a.h};
             Operand B{a.E, a.v_pad, a.h, a.h};  // K-major rows n_base .. n_base + vc
-            const OutView o[1] = {{dl, a.T, L.vc, L.vc}};
             typename EpiCeDlogits<bf>::Params ep{lse_buf, a.targets, a.grad_scale, vvi, n_base};
-            st = launch_gemm_auto<bf, false, false, EpiCeDlogits<bf>, kBN192 | kBN256>(
-                "ce_bwd_logits_dl", A, B, o, nullptr, Ti, vci, hi, 0, 0, n_base, 0, ep, s, 0, nullptr, &tail);
+            if (with_t) {
+                const OutView o[2] = {{dl, a.T, L.vc, L.vc}, {at<bf>(ws, L.dlT), L.vc, a.T, pad8(a.T)}};
+                st = launch_gemm_auto<bf, false, false, EpiCeDlogitsT, kBN192 | kBN256>(
+                    "ce_bwd_logits_dl", A, B, o, nullptr, Ti, vci, hi, 0, 0, n_base, 0, ep, s, 0, nullptr, &tail);
+            } else {
+                const OutView o[1] = {{dl, a.T, L.vc, L.vc}};
+                st = launch_gemm_auto<bf, false, false, EpiCeDlogits<bf>, kBN192 | kBN256>(
+                    "ce_bwd_logits_dl", A, B, o, nullptr, Ti, vci, hi, 0, 0, n_base, 0, ep, s, 0, nullptr, &tail);
+            }
             if (st != TPCE_OK) return st;
         }
         // dE rows of this chunk = dl^T H (no exchange: the rows belong to one shard)
-        if (a.dE && de_kmajor(a.h, TPCE_BF16)) {
+        if (with_t) {
             bf *dlT = at<bf>(ws, L.dlT);
             const int64_t Tp = pad8(a.T);
-            if ((st = transpose_bf16(dl, a.T, L.vc, L.vc, dlT, Tp, s)) != TPCE_OK) return st;
             Operand A{dlT, L.vc, a.T, Tp};  // K-major: M = vc rows, K = T columns
             Operand B{a.H, a.T, a.h, a.h};  // MN-major: K = T rows, N = h columns
             const OutView o[1] = {{static_cast<bf *>(a.dE) + static_cast<int64_t>(n_base) * a.h, L.vc, a.h, a.h}};

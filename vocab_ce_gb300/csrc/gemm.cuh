@@ -336,6 +336,20 @@ struct Stage<__nv_bfloat16> {
         }
     }
 };
+// The same 32 x 32 bf16 chunk staged transposed, for a TMA store into the
+// transposed output (rows: the chunk's columns, columns: its rows): lane r
+// writes its row's 32 values down column r. Element (c, r) of the staged box
+// lives in row c, 16-byte piece (r / 8) ^ ((c >> 1) & 3), slot r % 8; for
+// each c the warp's 32 two-byte writes fill one 64-byte row.
+struct StageT {
+    __device__ static void write(uint8_t *buf, int r, const float *v) {
+        const int piece = r >> 3, slot = (r & 7) * 2;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+            *reinterpret_cast<__nv_bfloat16 *>(buf + c * 64 + ((piece ^ ((c >> 1) & 3)) << 4) + slot) =
+                __float2bfloat16_rn(v[c]);
+    }
+};
 template <>
 struct Stage<float> {
     static constexpr uint32_t kBytes = 32 * 128;
@@ -385,6 +399,9 @@ struct NoRow {};
 
 struct EpiBase {
     static constexpr bool kGated = false;
+    // output 1 is the transpose of output 0's tile ([N, M], bf16): staged by
+    // StageT and stored at (row, column) = (n, m)
+    static constexpr bool kTransOut1 = false;
     __host__ __device__ static constexpr int out_map(int k) { return k; }
     template <class P>
     __device__ static int out_col(const P &, int) { return 0; }
@@ -710,6 +727,19 @@ struct EpiCeDlogits : EpiBase {
     __device__ static void end(const Params &, Row &, int, int, bool) {}
 };
 
+// The same dl tile stored twice: dl [T, vc] and its transpose dl^T [vc, T]
+// (the K-major A operand of dE = dl^T H).
+struct EpiCeDlogitsT : EpiCeDlogits<__nv_bfloat16> {
+    using Base = EpiCeDlogits<__nv_bfloat16>;
+    static constexpr int kOuts = 2;
+    static constexpr bool kTransOut1 = true;
+    // fills o[0]; the transposed output is staged from o[0] as well
+    __device__ static void chunk(const Params &p, Row &r, int row, int n, int N, bool live, float (&v)[32],
+                                 const float (&in)[2][32], float (&o)[kOuts][32]) {
+        Base::chunk(p, r, row, n, N, live, v, in, reinterpret_cast<float(&)[1][32]>(o));
+    }
+};
+
 // fp32 output stored (mode 0) or added element-wise into global memory by the
 // TMA reduction (mode 1): dH summed over vocabulary chunks, in chunk order.
 struct EpiF32Accumulate : EpiBase {
@@ -828,6 +858,9 @@ __device__ __forceinline__ bool epi_tile(const typename Epi::Params &ep, const G
     constexpr int kOuts = Epi::kOuts;
     constexpr uint32_t kB = EpiSmem<Epi>::kChunkBytes;
     static_assert(Epi::kIns <= 2 && !(Epi::kGated && Epi::kIns > 0), "epilogue inputs");
+    static_assert(!Epi::kTransOut1 || (Epi::kOuts == 2 && kChunk != kChunkC &&
+                                       std::is_same<OutT, __nv_bfloat16>::value),
+                  "a transposed second output: bf16, unchunked");
     const int row = row0 + lane;
     // output map 0 and the row coordinate in it (a sequence chunk, if chunked)
     const CUtensorMap *tm0 = tmC0;
@@ -866,7 +899,12 @@ __device__ __forceinline__ bool epi_tile(const typename Epi::Params &ep, const G
             }
             __syncwarp();
 #pragma unroll
-            for (int k = 0; k < kOuts; ++k) Stage<OutT>::write(w.stage + (2 * k + buf) * kB, lane, o[k]);
+            for (int k = 0; k < kOuts; ++k) {
+                if (Epi::kTransOut1 && k == 1)
+                    StageT::write(w.stage + (2 * k + buf) * kB, lane, o[0]);
+                else
+                    Stage<OutT>::write(w.stage + (2 * k + buf) * kB, lane, o[k]);
+            }
             ptx::fence_proxy_async_smem();
             __syncwarp();
             const bool do_store = col_live && row0 < shp.M;
@@ -875,8 +913,9 @@ __device__ __forceinline__ bool epi_tile(const typename Epi::Params &ep, const G
                 for (int k = 0; k < kOuts; ++k) {
                     const uint8_t *src = w.stage + (2 * k + buf) * kB;
                     const CUtensorMap *tm = Epi::out_map(k) == 0 ? tm0 : tmC1;
-                    const int col = n + Epi::out_col(ep, k);
-                    const int y = Epi::out_map(k) == 0 ? y0 : row0;
+                    const bool trans = Epi::kTransOut1 && k == 1;
+                    const int col = trans ? row0 : n + Epi::out_col(ep, k);
+                    const int y = trans ? n : (Epi::out_map(k) == 0 ? y0 : row0);
                     if (Epi::mode(ep) == 1)
                         ptx::tma_reduce_add_2d(tm, src, col, y);
                     else
