@@ -411,7 +411,7 @@ tpce_status tp_attn_out_backward_sp(const void *const *dZ_chunks, const void *O,
  * per token, each the fold over one run of consecutive vocabulary tiles;
  * where p_i > 1 the epilogue that finishes a shard's last run folds them, so
  * the combine reads exactly one pair per shard and token. p_i = 1 when the
- * GEMM's work units fill the GPU in one round, else the fewest equal parts
+ * GEMM's work units fill the GPU in one wave, else the fewest equal parts
  * that keep it evenly busy (9 for 16,384 tokens over 129,024 ids and t = 8;
  * one per 128-id tile for fp32).
  * Backward (dH and/or dE requested), with dl = grad_scale * (softmax - onehot)

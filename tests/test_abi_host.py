@@ -96,7 +96,7 @@ def test_workspace_sizes(L):
     # ticket per 32-token slab and shard for the fold. At the 129K config
     # each shard's 63 tiles are cut into 9 runs of 7 (4608 work units keep the
     # 76 CTA pairs 99.4% busy), at the 8.3B config 25 tiles into 5 runs of 5,
-    # and one run per shard wherever the units fit in one round; the one-CTA
+    # and one run per shard wherever the units fit in one wave; the one-CTA
     # kernel (fp32) makes one part per 128-id tile
     def rup(x):
         return (x + 255) // 256 * 256

@@ -157,7 +157,7 @@ CE_CASES = {
     "multi_tile": (600, 320, 4096, 4000, 4, "bf16"),
     "wide_h": (700, 1536, 3072, 3000, 4, "bf16"),             # dE / dH pick 192-wide tiles
     # 25 row-blocks x 4 shards: each shard's 6 tiles are cut into 3 runs of 2
-    # (300 work units, 4 rounds over the CTA pairs), so the combine folds 3
+    # (300 work units, 4 waves over the CTA pairs), so the combine folds 3
     # partial statistics per shard
     "runs_split_shards": (6400, 64, 6144, 6000, 4, "bf16"),
     # h >= 6144: dE reads a transposed copy of dl (rows padded from 300 to 304 tokens)
