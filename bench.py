@@ -788,13 +788,21 @@ def run_e2e(args, job, ws_, dev, stream, barrier, ws, work, clocks=None):
     copied = [torch.cuda.Event() for _ in range(2)]    # set s holds its step's inputs
     consumed = [torch.cuda.Event() for _ in range(2)]  # the step that read set s has finished
 
-    def issue_copy(i):
+    copy_events = []  # (start, end) of each step's copies in the timed run
+
+    def issue_copy(i, timed=False):
         s_ = i % 2
         with torch.cuda.stream(copy_stream):
             if i >= 2:
                 copy_stream.wait_event(consumed[s_])
+            if timed:
+                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ev[0].record(copy_stream)
             for k, v in host.items():
                 dev_in[s_][k].copy_(v, non_blocking=True)
+            if timed:
+                ev[1].record(copy_stream)
+                copy_events.append(ev)
             copied[s_].record(copy_stream)
 
     def compute(i):
@@ -817,12 +825,13 @@ def run_e2e(args, job, ws_, dev, stream, barrier, ws, work, clocks=None):
             res_host.copy_(z_src, non_blocking=True)
 
     def e2e_run(n, start_event=None):
-        if start_event is not None:
+        timed = start_event is not None
+        if timed:
             copy_stream.wait_event(start_event)  # the first copy starts inside the timed region
-        issue_copy(0)
+        issue_copy(0, timed)
         for i in range(n):
             if i + 1 < n:
-                issue_copy(i + 1)
+                issue_copy(i + 1, timed)
             compute(i)
 
     e2e_run(2)
@@ -840,9 +849,12 @@ def run_e2e(args, job, ws_, dev, stream, barrier, ws, work, clocks=None):
     e_ms = max_over_ranks(a.elapsed_time(b), ws, dev)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = res_host.numel() * res_host.element_size()
+    copy_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in copy_events) if copy_events else None
     return {"value": job_rate(ws, work, e_ms / args.steps * 1e-3) / 1e12, "unit": UNIT,
             "ms_per_step": e_ms / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "clocks": clk,
+            "h2d_ms_per_step": copy_ms,
+            "h2d_gb_per_s": h2d / copy_ms / 1e6 if copy_ms else None,
             "path": "vocab_ce_gb300 Python API -> C ABI; every step's inputs copied from pinned host memory "
                     "(on a second stream, double-buffered: step i+1's copy overlaps step i's compute; the first "
                     "copy and the last result read are inside the timed region)"}
