@@ -116,6 +116,11 @@ def test_workspace_sizes(L):
     T2, h2, vp2 = 8192, 3072, 51200
     b2 = tp.ce_workspace_bytes(T2, h2, vp2, 8, grads=True) - tp.ce_workspace_bytes(T2, h2, vp2, 8, grads=False)
     assert b2 <= T2 * (vp2 // 2) * 2 + T2 * h2 * 4 + 1024
+    # 66,000 tokens: one 8,192-id shard (1.08 GB of dl) exceeds the 1 GiB bound,
+    # so each shard is cut into two 4,096-id chunks
+    T3, h3, vp3 = 66000, 16, 16384
+    b3 = tp.ce_workspace_bytes(T3, h3, vp3, 2, grads=True) - tp.ce_workspace_bytes(T3, h3, vp3, 2, grads=False)
+    assert T3 * 4096 * 2 <= b3 <= T3 * 4096 * 2 + T3 * h3 * 4 + 4096
     # fp32 adds transposed operand copies: A^T, B^T, Y^T, dZ^T, X^T, dU^T
     T, h, f = 32, 64, 256
     assert tp.mlp_workspace_bytes(T, h, f, 2, dtype=__import__("torch").float32) >= 4 * (T * f + 2 * f * h + 2 * f * T + 2 * h * T)

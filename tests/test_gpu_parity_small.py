@@ -213,6 +213,25 @@ def test_ce_grad_scale_zero_negative_and_large(gs, dtype):
         assert_rel(f"dE (grad_scale {gs}, {dtype})", out["dE"], ref["dE"])
 
 
+def test_ce_backward_with_shards_split_into_chunks():
+    # The dl scratch of one vocabulary chunk is bounded (1 GiB): at 66,000
+    # tokens one 8,192-id shard alone would need 1.08 GB, so each shard is cut
+    # into two 4,096-id chunks and dH adds four chunks in fp32. Every output
+    # against the oracle (h = 16 keeps the oracle's full softmax to seconds).
+    dev = gpu_or_skip()
+    T, h, v_pad, v_valid, t = 66000, 16, 16384, 16000, 2
+    w = wl.custom("split_shards", T=T, h=h, f=0, v_valid=v_valid, v_pad=v_pad, t=t)
+    ci = wl.ce_inputs(w, seed=4)
+    g = {k: v.to(dev) for k, v in ci.items()}
+    out = tp.vocab_parallel_ce(g["H"], g["E"], g["targets"], v_valid, t, grad_scale=1.0 / T)
+    assert tp.device_status() == 0
+    ref = oracle.ce(ci["H"], ci["E"], ci["targets"].numpy(), v_valid, grad_scale=1.0 / T)
+    assert_loss("loss", out["loss"], ref["loss"])
+    assert_rel("dH", out["dH"], ref["dH"])
+    assert_rel("dE", out["dE"], ref["dE"])
+    assert torch.count_nonzero(out["dE"][v_valid:]).item() == 0
+
+
 def test_ce_partial_statistics_fold_is_repeatable_on_a_dirty_workspace():
     # A shard cut into several runs has its partial (max, sumexp) pairs folded
     # by the epilogue that draws the last ticket. The tickets live in the
