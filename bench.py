@@ -276,18 +276,26 @@ KERNEL_UNITS = (("ce_static_", "ce_static.cu"), ("ce_", "ce.cu"), ("mlp_", "mlp.
                 ("colsum_", "runtime.cu"), ("f32_to_bf16", "runtime.cu"))
 
 
+def _code_only(text):
+    """A CUDA source without its comments and with whitespace runs collapsed:
+    what the compiler sees, so that editing a comment keeps the hash."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(kernel=None):
-    """A hash over the sources a kernel is built from: its translation unit and
+    """A hash over the code a kernel is built from: its translation unit and
     every shared header of the library (every CUDA source when the kernel is
-    not known). Recorded traffic is only trusted for the sources it was
-    captured with."""
+    not known), comments left out. Recorded traffic is only trusted for the
+    code it was captured with."""
     d = os.path.join(ROOT, "vocab_ce_gb300", "csrc")
     unit = next((u for p, u in KERNEL_UNITS if kernel and kernel.startswith(p)), None)
     h = hashlib.sha256()
     for f in sorted(os.listdir(d)):
         if f.endswith((".cuh", ".h")) or (f.endswith(".cu") and unit in (None, f)):
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+            with open(os.path.join(d, f), encoding="utf-8") as fh:
+                h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

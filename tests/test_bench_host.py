@@ -80,3 +80,9 @@ def test_traffic_is_keyed_to_each_kernels_sources(tmp_path, monkeypatch):
     assert bench.traffic_from_profiles("ce_bwd_logits_dl", "ce128k") == 1234
     assert bench.traffic_from_profiles("ce_bwd_logits_dl", "gpt8b") is None
     assert bench.traffic_from_profiles("mlp_bwd_dA", "mlp70b") is None
+
+
+def test_source_hash_ignores_comments_only():
+    code = "int f(int x) { return x + 1; }  // one\n/* two\n three */ int g;"
+    assert bench._code_only(code) == bench._code_only("int f(int x) {\n  return x + 1;\n}\n// other words\nint g;")
+    assert bench._code_only(code) != bench._code_only(code.replace("x + 1", "x + 2"))

@@ -18,8 +18,10 @@
 //
 // bf16 operands can be K-major (the contraction dimension contiguous) or
 // MN-major (the output dimension contiguous): the transposed operands of the
-// backward GEMMs (Y^T dZ, X^T dU, dl^T H) are read in place, no transpose pass.
-// tf32 operands are K-major.
+// backward GEMMs (Y^T dZ, X^T dU, dl^T H) can be read in place. An MN-major A
+// costs the tensor core about 11%, so at large widths the callers give these
+// GEMMs a K-major copy of A instead (made by a transpose pass, or for dl^T
+// stored by the dl GEMM's own epilogue). tf32 operands are K-major.
 //
 // The tile grid's N coordinate of the column-parallel GEMMs is the
 // concatenation of the t shards' column ranges, and the K loop of the
