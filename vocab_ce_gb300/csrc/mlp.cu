@@ -32,7 +32,8 @@
 // all-gathered dZ from its chunks.
 //
 // bf16 tensors use the bf16 tensor-core path with operands read in place in
-// either major order. fp32 tensors use the tf32 path, whose operands are
+// either major order, except the A operands of the weight gradients at large
+// widths (X^T, Y^T copies, below). fp32 tensors use the tf32 path, whose operands are
 // K-major: the operands stored the other way (the weights in the forward; Y,
 // dZ, X and the pre-activation gradient in the weight gradients) are first
 // transposed into the workspace.
