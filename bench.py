@@ -849,7 +849,9 @@ def run_e2e(args, job, ws_, dev, stream, barrier, ws, work, clocks=None):
     b = torch.cuda.Event(enable_timing=True)
     sampler = clocks() if clocks else None
     a.record(stream)
+    t_host = time.perf_counter()
     e2e_run(args.steps, a)
+    host_ms = (time.perf_counter() - t_host) * 1e3  # the host's time to enqueue every step
     b.record(stream)
     torch.cuda.synchronize()
     clk = sampler.stop() if sampler else None
@@ -862,6 +864,8 @@ def run_e2e(args, job, ws_, dev, stream, barrier, ws, work, clocks=None):
             "ms_per_step": e_ms / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "clocks": clk,
             "h2d_ms_per_step": copy_ms,
+            "host_enqueue_ms_per_step": host_ms / args.steps,
+            "pinned": all(v.is_pinned() for v in host.values()),
             "h2d_gb_per_s": h2d / copy_ms / 1e6 if copy_ms else None,
             "path": "vocab_ce_gb300 Python API -> C ABI; every step's inputs copied from pinned host memory "
                     "(on a second stream, double-buffered: step i+1's copy overlaps step i's compute; the first "
